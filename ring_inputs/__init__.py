@@ -1,0 +1,271 @@
+"""Seeded synthetic inputs for the ring-attention workloads (no attention math).
+
+The generator itself lives in ``gen.c`` (SplitMix64 counter stream followed by
+Box-Muller, rounded to bf16 with round-to-nearest-even); this module builds it
+with gcc, loads it with ctypes, and describes the workloads:
+
+* the shapes of the five workloads in the mKernel pages' Ring Attention setting
+  (sequence-parallel attention over P shards; arxivdaily abstract and the
+  pwwt.cn analysis, Table 3 "Ring Attention" row),
+* the element order (Q, then K, then V, each in [B][H][S][d] order),
+* the power-of-two multipliers (x2 for the sharper-softmax GQA workload, x8 for
+  the 1 % outlier K rows of the long-sequence workload),
+* the fixed row samples used where the oracle cannot compute every row.
+
+Both the fp64 oracle and the GPU library consume the bytes produced here and
+nothing else is shared between them.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gen.c")
+_LIB_PATH = os.path.join(_HERE, "_gen.so")
+_lib = None
+_lock = threading.Lock()
+
+GAMMA = 0x9E3779B97F4A7C15
+OUTLIER_STREAM = 0x5EED0000  # added to the seed to draw the outlier-row mask
+
+
+def build(force: bool = False) -> str:
+    """Compile gen.c into _gen.so (gcc, no machine-specific flags)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", _SRC, "-o", tmp, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.ri_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64, ctypes.c_float,
+                                           ctypes.c_void_p, ctypes.c_int]
+            lib.ri_normal_bf16.restype = ctypes.c_int
+            lib.ri_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+            lib.ri_splitmix64.restype = ctypes.c_uint64
+            lib.ri_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+            lib.ri_uniform.restype = ctypes.c_double
+            _lib = lib
+    return _lib
+
+
+def n_threads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+# ----------------------------------------------------------------------------------------------
+# Low-level stream access
+# ----------------------------------------------------------------------------------------------
+
+def splitmix64(seed: int, n: int) -> int:
+    return int(_load().ri_splitmix64(seed & (2**64 - 1), n))
+
+
+def normal_bf16_into(addr: int, seed: int, first: int, count: int, mult: float = 1.0) -> None:
+    """Write `count` bf16 bit patterns (uint16) of stream elements [first, first+count) to `addr`."""
+    rc = _load().ri_normal_bf16(seed & (2**64 - 1), first, count, float(mult), ctypes.c_void_p(addr), n_threads())
+    if rc != 0:
+        raise RuntimeError("ri_normal_bf16 failed")
+
+
+def normal_bf16(seed: int, first: int, count: int, mult: float = 1.0) -> np.ndarray:
+    out = np.empty(count, dtype=np.uint16)
+    if count:
+        normal_bf16_into(out.ctypes.data, seed, first, count, mult)
+    return out
+
+
+def normal_bf16_numpy(seed: int, first: int, count: int, mult: float = 1.0) -> np.ndarray:
+    """Slow pure-numpy restatement of the same stream (used to cross-check gen.c)."""
+    n = np.arange(first, first + count, dtype=np.uint64)
+    p = n >> np.uint64(1)
+
+    def mix(idx):
+        with np.errstate(over="ignore"):
+            z = np.uint64(seed) + (idx + np.uint64(1)) * np.uint64(GAMMA)
+            z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+            z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        return z ^ (z >> np.uint64(31))
+
+    x1 = mix(np.uint64(2) * p)
+    x2 = mix(np.uint64(2) * p + np.uint64(1))
+    u1 = ((x1 >> np.uint64(11)) + np.uint64(1)).astype(np.float64) * 2.0**-53
+    u2 = (x2 >> np.uint64(11)).astype(np.float64) * 2.0**-53
+    r = np.sqrt(-2.0 * np.log(u1))
+    th = 2.0 * np.pi * u2
+    val = np.where((n & np.uint64(1)) == 1, r * np.sin(th), r * np.cos(th)).astype(np.float32)
+    b = f32_to_bf16_bits(val)
+    if mult != 1.0:
+        b = f32_to_bf16_bits(bf16_bits_to_f32(b) * np.float32(mult))
+    return b
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))
+    return (u >> np.uint64(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return bf16_bits_to_f32(b).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------------------------
+# Workloads
+# ----------------------------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    S: int
+    P: int
+    d: int
+    causal: bool
+    seed: int
+    qmul: float = 1.0
+    kmul: float = 1.0
+    vmul: float = 1.0
+    outlier_frac: float = 0.0   # fraction of K rows multiplied by outlier_mul
+    outlier_mul: float = 8.0
+
+    @property
+    def L(self) -> int:
+        return self.S // self.P
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.d))
+
+    @property
+    def n_q(self) -> int:
+        return self.B * self.Hq * self.S * self.d
+
+    @property
+    def n_kv(self) -> int:
+        return self.B * self.Hkv * self.S * self.d
+
+    def flops(self) -> float:
+        """Algorithmic flops: 4*d per unmasked (query, key) pair, times B*Hq."""
+        pairs = self.S * (self.S + 1) // 2 if self.causal else self.S * self.S
+        return 4.0 * self.d * pairs * self.B * self.Hq
+
+    def staging_transfers(self) -> int:
+        """(shard, chunk) transfers the ring performs: the local chunk is never moved."""
+        return self.P * (self.P - 1) // 2 if self.causal else self.P * (self.P - 1)
+
+    def staging_bytes(self) -> int:
+        """Bytes written into ring slots (K and V); the same amount is read from home."""
+        return self.staging_transfers() * 2 * self.L * self.d * 2 * self.B * self.Hkv
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+def _cfg5(d: int, P: int) -> Workload:
+    return Workload(f"sweep_d{d}_P{P}", 1, 16, 16, 16384, P, d, False, seed=500 + d)
+
+
+WORKLOADS = {
+    # B1 H2 S1024 P4 d64, non-causal: the small case the oracle computes in full
+    "small": Workload("small", 1, 2, 2, 1024, 4, 64, False, seed=1),
+    # B1 H32 S32768 P16 d128, non-causal and causal: the headline throughput case
+    "h32_s32k_nc": Workload("h32_s32k_nc", 1, 32, 32, 32768, 16, 128, False, seed=2),
+    "h32_s32k_c": Workload("h32_s32k_c", 1, 32, 32, 32768, 16, 128, True, seed=2),
+    # GQA, causal, B2 Hq32 Hkv8 S65536 P16 d128, Q and K x2
+    "gqa_s64k_c": Workload("gqa_s64k_c", 2, 32, 8, 65536, 16, 128, True, seed=3, qmul=2.0, kmul=2.0),
+    # long sequence, causal, B1 H8 S131072 P32 d128, 1 % of K rows x8
+    "long_s128k_c": Workload("long_s128k_c", 1, 8, 8, 131072, 32, 128, True, seed=4, outlier_frac=0.01),
+}
+for _d in (64, 128):
+    for _P in (2, 4, 8, 16, 32, 64):
+        WORKLOADS[f"sweep_d{_d}_P{_P}"] = _cfg5(_d, _P)
+
+
+def outlier_rows(w: Workload) -> np.ndarray:
+    """Boolean mask [B][Hkv][S]: K rows multiplied by w.outlier_mul (drawn from a separate stream)."""
+    n = w.B * w.Hkv * w.S
+    if w.outlier_frac <= 0:
+        return np.zeros(n, dtype=bool).reshape(w.B, w.Hkv, w.S)
+    seed = (w.seed + OUTLIER_STREAM) & (2**64 - 1)
+    idx = np.arange(n, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed) + (idx + np.uint64(1)) * np.uint64(GAMMA)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+    z = z ^ (z >> np.uint64(31))
+    u = (z >> np.uint64(11)).astype(np.float64) * 2.0**-53
+    return (u < w.outlier_frac).reshape(w.B, w.Hkv, w.S)
+
+
+def generate(w: Workload, q_addr: int | None = None, k_addr: int | None = None, v_addr: int | None = None):
+    """Produce Q, K, V as uint16 bf16 bit patterns in [B][H][S][d] order.
+
+    If addresses are given (e.g. pinned host buffers), the values are written
+    there and None is returned for that tensor; otherwise numpy arrays are made.
+    """
+    out = []
+    first = 0
+    for name, count, mult, addr, shape in (
+        ("q", w.n_q, w.qmul, q_addr, (w.B, w.Hq, w.S, w.d)),
+        ("k", w.n_kv, w.kmul, k_addr, (w.B, w.Hkv, w.S, w.d)),
+        ("v", w.n_kv, w.vmul, v_addr, (w.B, w.Hkv, w.S, w.d)),
+    ):
+        if addr is None:
+            arr = normal_bf16(w.seed, first, count, mult).reshape(shape)
+            out.append(arr)
+            addr_used = arr.ctypes.data
+        else:
+            normal_bf16_into(addr, w.seed, first, count, mult)
+            out.append(None)
+            addr_used = addr
+        if name == "k" and w.outlier_frac > 0:
+            mask = outlier_rows(w).reshape(-1)
+            kview = np.ctypeslib.as_array(ctypes.cast(addr_used, ctypes.POINTER(ctypes.c_uint16)), shape=(count,))
+            kview = kview.reshape(-1, w.d)
+            rows = np.nonzero(mask)[0]
+            kview[rows] = f32_to_bf16_bits(bf16_bits_to_f32(kview[rows]) * np.float32(w.outlier_mul))
+        first += count
+    return tuple(out)
+
+
+def sample_rows(w: Workload, n_random: int = 4096) -> np.ndarray:
+    """Fixed row sample: flat row ids ((b*Hq + hq)*S + i), sorted and unique.
+
+    For every (b, hq): rows 0, 1, 127, 128, each shard's first and last row and
+    S-1; then uniformly drawn rows (seeded) until at least `n_random` rows in total.
+    """
+    base = {0, 1, 127, 128, w.S - 1}
+    for r in range(w.P):
+        base.add(r * w.L)
+        base.add((r + 1) * w.L - 1)
+    base = sorted(i for i in base if 0 <= i < w.S)
+    ids = []
+    for bh in range(w.B * w.Hq):
+        ids.extend(bh * w.S + i for i in base)
+    ids = set(ids)
+    seed = (w.seed * 7919 + 17) & (2**64 - 1)
+    n = 0
+    total = w.B * w.Hq * w.S
+    while len(ids) < n_random:
+        ids.add(splitmix64(seed, n) % total)
+        n += 1
+    return np.array(sorted(ids), dtype=np.int64)
