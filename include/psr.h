@@ -1,0 +1,149 @@
+/*
+ * persistent_sm_ring_gb300 -- Ring Attention forward on one GB300 (sm_103a).
+ *
+ * C ABI of libpsr.so.  Plain pointers and sizes only; every call returns a
+ * status code (PSR_OK = 0) and never throws or exits.
+ *
+ * The operation (mKernel pages: arxivdaily abstract; dataforcee and chathome
+ * "five fused kernels" tables, Ring Attention row; pwwt.cn analysis §2.6,
+ * Table 3, Ring Attention row): sequence-parallel attention in which P ring
+ * ranks each hold one shard of L = S/P query rows; at ring step t the rank of
+ * shard r consumes KV chunk (r - t) mod P while the next chunk is moved into
+ * its receive buffer, and the per-chunk partial results are merged exactly
+ * through the running max and log-sum-exp.  Here the P ranks are P shards in
+ * one GPU's HBM: "staging" CTAs copy each chunk into a double-buffered ring
+ * slot with TMA and publish a readiness flag (pwwt.cn §2.2 Figure 2 readiness
+ * flag; §2.5: the flag names the completed payload), "compute" CTAs run the
+ * FlashAttention pass on tcgen05 tensor cores, and an on-GPU controller
+ * re-splits CTAs between the two roles with the pwwt.cn §2.4 rule
+ *     n_s* = N * (R_s*C_s) / (R_p*C_p + R_s*C_s).
+ *
+ * Result: O = softmax(scale * Q K^T [+ causal mask over global positions]) V,
+ * rounded to bf16, and LSE = natural-log log-sum-exp of the scaled scores per
+ * query row, fp32.  Query head hq reads KV head hq / (Hq/Hkv).
+ */
+#ifndef PSR_H
+#define PSR_H
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PSR_API __attribute__((visibility("default")))
+#else
+#define PSR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------------------- */
+#define PSR_OK 0
+#define PSR_ERR_ARG 1         /* null pointer, bad value, workspace too small */
+#define PSR_ERR_UNSUPPORTED 2 /* shape outside the supported set, or not an sm_103 device */
+#define PSR_ERR_CUDA 3        /* a CUDA runtime call failed (launch, memset, copy) */
+#define PSR_ERR_TIMEOUT 4     /* a bounded device wait expired (reported by psr_get_stats) */
+
+/* ---- partition modes --------------------------------------------------------------------------- */
+#define PSR_STATIC 0   /* n_staging CTAs stage for the whole launch, the rest compute */
+#define PSR_ADAPTIVE 1 /* the on-GPU controller re-splits CTAs at task boundaries */
+
+/* Fault-injection codes (psr_partition.fault); 0 in normal use.  They act on
+ * the host-visible protocol only and never fault the GPU: a dropped flag makes
+ * the consumers' bounded waits expire and the launch report PSR_ERR_TIMEOUT. */
+#define PSR_FAULT_NONE 0
+#define PSR_FAULT_DROP_FIRST_FLAG 1 /* the first staged chunk never publishes its readiness flag */
+#define PSR_FAULT_SLOW_STAGING 2    /* every staging task sleeps ~20 us before copying */
+
+typedef struct {
+  int B;        /* batch */
+  int Hq;       /* query heads */
+  int Hkv;      /* key/value heads; Hq % Hkv == 0 */
+  int S;        /* global sequence length */
+  int P;        /* ring size (number of shards); S % P == 0 */
+  int d;        /* head dim: 64 or 128 */
+  int causal;   /* 0 or 1: mask k_pos > q_pos over global positions */
+  float scale;  /* <= 0 selects 1/sqrt(d) */
+} psr_shape;
+
+typedef struct {
+  int mode;       /* PSR_STATIC or PSR_ADAPTIVE */
+  int n_staging;  /* static: staging CTA count; adaptive: initial count (<= 0: automatic) */
+  int n_min;      /* adaptive clamp, lower (<= 0: 1) */
+  int n_max;      /* adaptive clamp, upper (<= 0: automatic) */
+  int fault;      /* PSR_FAULT_* */
+  int timeout_ms; /* bound on every device wait (<= 0: 2000 ms) */
+} psr_partition;
+
+typedef struct {
+  int status;                     /* PSR_OK or PSR_ERR_TIMEOUT */
+  int error_site;                 /* which wait gave up (0 = none) */
+  int n_cta;                      /* persistent CTAs launched */
+  int n_s_initial, n_s_final;     /* controller target at start / end */
+  int n_s_min, n_s_max;           /* range of the target over the launch */
+  int traj_len;                   /* entries in the target trajectory log */
+  unsigned long long staging_cycles, compute_cycles; /* SM cycles spent inside tasks */
+  unsigned long long staging_tasks, compute_items, compute_tiles;
+  unsigned long long staging_bytes;                  /* bytes written into ring slots */
+  unsigned long long role_switches;
+  unsigned long long idle_polls;                     /* task-boundary polls that found no work */
+} psr_stats;
+
+/* Bytes of device workspace psr_ring_attn_fwd needs for this shape: the
+ * control block, readiness flags, consumption counters, the staging ready
+ * queue, the trajectory log and the two ring slots for K and V
+ * (2 x [n_groups][L][d] bf16 each).  Returns 0 for an invalid shape. */
+PSR_API size_t psr_workspace_bytes(const psr_shape* shape);
+
+/* Ring Attention forward.
+ *   q:  device, bf16, [B][Hq][S][d] contiguous      (read)
+ *   k,v: device, bf16, [B][Hkv][S][d] contiguous    (read)
+ *   o:  device, bf16, [B][Hq][S][d] contiguous      (written)
+ *   lse: device, fp32, [B][Hq][S]                   (written)
+ *   workspace: device, >= psr_workspace_bytes(shape) bytes, 256-byte aligned,
+ *              owned by the caller; must not be used by another launch in flight.
+ *   part: partition policy (NULL = adaptive, automatic).
+ *   stream: a cudaStream_t (NULL = legacy default stream).
+ * Asynchronous: enqueues a flag reset and one persistent launch on `stream`
+ * and returns.  The library allocates no device memory.  A device-side
+ * timeout is reported by psr_get_stats, not here.
+ * Supported: d in {64, 128}; S % P == 0; L = S/P a multiple of 256;
+ * Hq % Hkv == 0; sm_103 device.  Otherwise PSR_ERR_UNSUPPORTED. */
+PSR_API int psr_ring_attn_fwd(const psr_shape* shape, const void* q, const void* k, const void* v, void* o, float* lse,
+                      void* workspace, size_t workspace_bytes, const psr_partition* part, void* stream);
+
+/* Same operation with HOST buffers: copies q, k, v (host, ideally pinned) to
+ * the caller's device buffers dq, dk, dv on `stream`, runs psr_ring_attn_fwd,
+ * copies O and LSE back to o_host / lse_host, and synchronises the stream.
+ * Returns the launch status, or PSR_ERR_TIMEOUT if the device reported one. */
+PSR_API int psr_ring_attn_fwd_host(const psr_shape* shape, const void* q_host, const void* k_host, const void* v_host,
+                           void* o_host, float* lse_host, void* dq, void* dk, void* dv, void* d_o, float* d_lse,
+                           void* workspace, size_t workspace_bytes, const psr_partition* part, void* stream);
+
+/* Synchronises `stream`, reads the control block of the last launch that used
+ * `workspace` and fills *out.  Returns out->status (PSR_OK or
+ * PSR_ERR_TIMEOUT), or PSR_ERR_ARG / PSR_ERR_CUDA. */
+PSR_API int psr_get_stats(const void* workspace, psr_stats* out, void* stream);
+
+/* Copies up to max_entries (time_us, n_s) pairs of the controller's target
+ * trajectory (device workspace -> host); synchronises `stream`.  Returns the
+ * number of pairs written, or a negative status. */
+PSR_API int psr_get_trajectory(const void* workspace, uint32_t* out_pairs, int max_entries, void* stream);
+
+/* The controller rule evaluated on the host, as the device evaluates it:
+ * n = round(n_cta * R_s*C_s / (R_p*C_p + R_s*C_s)), clamped to
+ * [max(n_min,1), min(n_max, n_cta-1)] while both roles have work; 0 when
+ * R_s == 0; n_max when R_p == 0 and R_s > 0.  For tests and tooling. */
+PSR_API int psr_controller_target(int n_cta, double R_s, double C_s, double R_p, double C_p, int n_min, int n_max);
+
+/* Human-readable name of a status code (static string). */
+PSR_API const char* psr_status_string(int status);
+
+/* Number of persistent CTAs a launch on the current device uses (one per SM),
+ * or a negative status. */
+PSR_API int psr_num_ctas(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PSR_H */

@@ -1,0 +1,226 @@
+"""persistent_sm_ring_gb300: Ring Attention forward on one GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libpsr.so`` (declared in
+``include/psr.h``).  It only marshals arguments: every step of the ring
+(staging, readiness flags, the tcgen05 FlashAttention pass, the LSE-exact
+merge, the on-GPU partition controller) runs in the library's CUDA kernel.
+PyTorch supplies device memory and streams.  There is no fallback: if the
+library is missing or the device is not an sm_103 GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB, build as _build
+
+__all__ = ["build", "load", "Shape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host", "workspace_bytes",
+           "get_stats", "get_trajectory", "controller_target", "num_ctas", "status_string", "PsrError",
+           "STATIC", "ADAPTIVE", "FAULT_NONE", "FAULT_DROP_FIRST_FLAG", "FAULT_SLOW_STAGING"]
+
+OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+STATIC, ADAPTIVE = 0, 1
+FAULT_NONE, FAULT_DROP_FIRST_FLAG, FAULT_SLOW_STAGING = 0, 1, 2
+
+EXPORTED = ("psr_workspace_bytes", "psr_ring_attn_fwd", "psr_ring_attn_fwd_host", "psr_get_stats",
+            "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("S", ctypes.c_int),
+                ("P", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+class Partition(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("n_staging", ctypes.c_int), ("n_min", ctypes.c_int),
+                ("n_max", ctypes.c_int), ("fault", ctypes.c_int), ("timeout_ms", ctypes.c_int)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_int), ("error_site", ctypes.c_int), ("n_cta", ctypes.c_int),
+                ("n_s_initial", ctypes.c_int), ("n_s_final", ctypes.c_int), ("n_s_min", ctypes.c_int),
+                ("n_s_max", ctypes.c_int), ("traj_len", ctypes.c_int),
+                ("staging_cycles", ctypes.c_ulonglong), ("compute_cycles", ctypes.c_ulonglong),
+                ("staging_tasks", ctypes.c_ulonglong), ("compute_items", ctypes.c_ulonglong),
+                ("compute_tiles", ctypes.c_ulonglong), ("staging_bytes", ctypes.c_ulonglong),
+                ("role_switches", ctypes.c_ulonglong), ("idle_polls", ctypes.c_ulonglong)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class PsrError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile libpsr.so in-tree for sm_103a."""
+    return _build(force=force)
+
+
+def load() -> ctypes.CDLL:
+    """Load libpsr.so; raises if it has not been built (no fallback path exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: run persistent_sm_ring_gb300.build() (nvcc, sm_103a) first")
+        lib = ctypes.CDLL(LIB)
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        P_shape, P_part = ctypes.POINTER(Shape), ctypes.POINTER(Partition)
+        lib.psr_workspace_bytes.argtypes = [P_shape]
+        lib.psr_workspace_bytes.restype = sz
+        lib.psr_ring_attn_fwd.argtypes = [P_shape, vp, vp, vp, vp, vp, vp, sz, P_part, vp]
+        lib.psr_ring_attn_fwd.restype = ctypes.c_int
+        lib.psr_ring_attn_fwd_host.argtypes = [P_shape, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, P_part, vp]
+        lib.psr_ring_attn_fwd_host.restype = ctypes.c_int
+        lib.psr_get_stats.argtypes = [vp, ctypes.POINTER(Stats), vp]
+        lib.psr_get_stats.restype = ctypes.c_int
+        lib.psr_get_trajectory.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, vp]
+        lib.psr_get_trajectory.restype = ctypes.c_int
+        lib.psr_controller_target.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                              ctypes.c_double, ctypes.c_int, ctypes.c_int]
+        lib.psr_controller_target.restype = ctypes.c_int
+        lib.psr_status_string.argtypes = [ctypes.c_int]
+        lib.psr_status_string.restype = ctypes.c_char_p
+        lib.psr_num_ctas.argtypes = []
+        lib.psr_num_ctas.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().psr_status_string(int(status)).decode()
+
+
+def make_shape(B, Hq, Hkv, S, P, d, causal, scale=None) -> Shape:
+    return Shape(int(B), int(Hq), int(Hkv), int(S), int(P), int(d), int(bool(causal)),
+                 float(scale) if scale is not None else 0.0)
+
+
+def make_partition(mode=ADAPTIVE, n_staging=0, n_min=0, n_max=0, fault=FAULT_NONE, timeout_ms=0) -> Partition:
+    return Partition(int(mode), int(n_staging), int(n_min), int(n_max), int(fault), int(timeout_ms))
+
+
+def workspace_bytes(shape: Shape) -> int:
+    n = load().psr_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise PsrError(ERR_UNSUPPORTED, "psr_workspace_bytes")
+    return int(n)
+
+
+def controller_target(n_cta, R_s, C_s, R_p, C_p, n_min=1, n_max=1 << 30) -> int:
+    return int(load().psr_controller_target(int(n_cta), float(R_s), float(C_s), float(R_p), float(C_p), int(n_min),
+                                            int(n_max)))
+
+
+def num_ctas() -> int:
+    n = load().psr_num_ctas()
+    if n < 0:
+        raise PsrError(-n, "psr_num_ctas")
+    return n
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensor(t, name, shape, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ring_attn_fwd(q, k, v, *, P, causal, scale=None, partition=None, workspace=None, out=None, lse=None,
+                  stream=None):
+    """Ring Attention forward over P shards held on this GPU.
+
+    q: [B, Hq, S, d] bf16; k, v: [B, Hkv, S, d] bf16 (CUDA, contiguous).
+    Returns (o [B, Hq, S, d] bf16, lse [B, Hq, S] fp32, workspace).  The call is
+    asynchronous on `stream`; use get_stats(workspace) to read the device
+    status (timeouts) and the controller's statistics.
+    """
+    import torch
+    lib = load()
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be 4-d [B, H, S, d]")
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    _check_tensor(q, "q", (B, Hq, S, d), torch.bfloat16)
+    _check_tensor(k, "k", (B, Hkv, S, d), torch.bfloat16)
+    _check_tensor(v, "v", (B, Hkv, S, d), torch.bfloat16)
+    shape = make_shape(B, Hq, Hkv, S, P, d, causal, scale)
+    need = workspace_bytes(shape)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace too small: need {need} bytes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_tensor(out, "out", (B, Hq, S, d), torch.bfloat16)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    else:
+        _check_tensor(lse, "lse", (B, Hq, S), torch.float32)
+    part = partition if partition is not None else make_partition()
+    rc = lib.psr_ring_attn_fwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), workspace.data_ptr(), need, ctypes.byref(part),
+                               _stream_handle(stream))
+    if rc != OK:
+        raise PsrError(rc, "psr_ring_attn_fwd")
+    return out, lse, workspace
+
+
+def ring_attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, dq, dk, dv, d_o, d_lse, *, P, causal, scale=None,
+                       partition=None, workspace=None, stream=None):
+    """Host-buffer variant: copies in, runs, copies out and synchronises (one C call)."""
+    import torch
+    lib = load()
+    B, Hq, S, d = q_host.shape
+    Hkv = k_host.shape[1]
+    shape = make_shape(B, Hq, Hkv, S, P, d, causal, scale)
+    need = workspace_bytes(shape)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dq.device)
+    part = partition if partition is not None else make_partition()
+    rc = lib.psr_ring_attn_fwd_host(ctypes.byref(shape), q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
+                                    o_host.data_ptr(), lse_host.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), d_o.data_ptr(), d_lse.data_ptr(), workspace.data_ptr(), need,
+                                    ctypes.byref(part), _stream_handle(stream))
+    if rc != OK:
+        raise PsrError(rc, "psr_ring_attn_fwd_host")
+    return workspace
+
+
+def get_stats(workspace, stream=None) -> dict:
+    st = Stats()
+    rc = load().psr_get_stats(ctypes.c_void_p(workspace.data_ptr()), ctypes.byref(st), _stream_handle(stream))
+    if rc not in (OK, ERR_TIMEOUT):
+        raise PsrError(rc, "psr_get_stats")
+    return st.as_dict()
+
+
+def get_trajectory(workspace, max_entries=4096, stream=None):
+    buf = (ctypes.c_uint32 * (2 * max_entries))()
+    n = load().psr_get_trajectory(ctypes.c_void_p(workspace.data_ptr()), buf, max_entries, _stream_handle(stream))
+    if n < 0:
+        raise PsrError(-n, "psr_get_trajectory")
+    return [(int(buf[2 * i]), int(buf[2 * i + 1])) for i in range(n)]

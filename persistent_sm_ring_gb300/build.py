@@ -1,0 +1,50 @@
+"""Builds libpsr.so in-tree with nvcc for sm_103a (no cmake, no torch extension machinery)."""
+from __future__ import annotations
+
+import os
+import subprocess
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+LIB = os.path.join(HERE, "libpsr.so")
+SOURCES = [os.path.join(CSRC, "psr_ring_attn.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("psr_device.cuh", "psr_schedule.h")] + [
+    os.path.join(ROOT, "include", "psr.h")]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+_lock = threading.Lock()
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
+        if cand and (os.path.sep not in cand or os.path.exists(cand)):
+            return cand
+    return "nvcc"
+
+
+def needs_build() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    return any(os.path.getmtime(f) > t for f in DEPS)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA sources into persistent_sm_ring_gb300/libpsr.so."""
+    with _lock:
+        if not force and not needs_build():
+            return LIB
+        tmp = LIB + f".{os.getpid()}.tmp"
+        cmd = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
+               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"),
+               *SOURCES, "-o", tmp]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
+        if verbose:
+            print(res.stderr)
+        os.replace(tmp, LIB)
+        return LIB

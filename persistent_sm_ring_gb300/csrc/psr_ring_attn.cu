@@ -1,0 +1,1082 @@
+// Ring Attention forward as one persistent kernel on sm_103a.
+//
+// The mKernel pages (pwwt.cn analysis §2.2 Figure 2, §2.4, §2.6 Table 3;
+// dataforcee/chathome kernel tables) describe a persistent kernel per GPU whose
+// CTAs take specialised roles, move data at tile granularity, publish
+// readiness flags that name completed payloads, and are re-split between roles
+// by an on-GPU controller.  For Ring Attention the communication is a ring KV
+// exchange in 128-row tiles ("TMA store KV") and the computation a local
+// FlashAttention pass over the chunk received at the previous step.
+//
+// On one GPU the P ring ranks are P shards held in HBM:
+//  * staging CTAs copy chunk (r - t) mod P of K and V into the ring slot
+//    (t & 1) of shard r with TMA bulk loads/stores through shared memory and
+//    publish, per chunk, the count of completed 128-row tiles with a
+//    gpu-scope release after the bulk stores have completed;
+//  * compute CTAs process 256-query-row items across all ring steps of their
+//    shard: step 0 reads the shard's own chunk in place, later steps read
+//    the slot after acquiring its flag; QK^T and PV run on tcgen05 with the
+//    accumulators in tensor memory, the online softmax runs in two
+//    128-thread warpgroups, and the exact merge across chunks is the running
+//    max / sum of the online softmax itself;
+//  * the controller re-evaluates n_s* = N*(R_s*C_s)/(R_p*C_p + R_s*C_s) at task
+//    boundaries from cycle-counter costs and remaining-work counters.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/psr.h"
+#include "psr_device.cuh"
+#include "psr_schedule.h"
+
+namespace psr {
+
+// ------------------------------------------------------------------------------------------------
+// Workspace: control block + protocol arrays + ring slots (all caller-owned device memory)
+// ------------------------------------------------------------------------------------------------
+constexpr int kTrajMax = 4096;
+
+struct Ctrl {
+  uint32_t item_next;     // compute items dispensed
+  uint32_t init_next;     // static staging list dispensed (steps 1 and 2 of every group)
+  uint32_t q_head;        // dynamic ready queue: next entry to take
+  uint32_t q_tail;        // dynamic ready queue: next entry to fill
+  uint32_t target_ns;     // controller target + 1 (0 = not yet set)
+  uint32_t error;         // first error site (0 = none)
+  uint32_t abort;         // set on any error: every CTA drains and exits
+  uint32_t ticks;         // completed tasks (controller period counter)
+  uint32_t traj_len;
+  uint32_t ns_min_inv, ns_max;  // 0xFFFF - min target, max target
+  uint32_t ns_initial;
+  uint32_t fault_count;
+  uint32_t pad0[3];
+  unsigned long long t0_ns;  // launch start (first CTA)
+  unsigned long long stage_cycles, compute_cycles;
+  unsigned long long stage_done, compute_items, compute_tiles;
+  unsigned long long stage_bytes;
+  unsigned long long role_switches, idle_polls;
+  unsigned long long pad1[6];
+};
+static_assert(sizeof(Ctrl) <= 256, "control block");
+
+struct WsLayout {
+  size_t ctrl, flags, consumed, queue, traj, slot_k, slot_v, total, reset_bytes;
+};
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static WsLayout ws_layout(const Geometry& G) {
+  WsLayout w;
+  const size_t n_fc = (size_t)G.n_groups * G.P;
+  size_t off = 0;
+  w.ctrl = off; off += 256;
+  w.traj = off; off = align_up(off + (size_t)kTrajMax * 8, 256);  // fixed offset: read without the shape
+  w.flags = off; off = align_up(off + n_fc * 4, 256);
+  w.consumed = off; off = align_up(off + n_fc * 4, 256);
+  w.queue = off; off = align_up(off + (size_t)(dynamic_staging_tasks(G) + 1) * 4, 256);
+  w.reset_bytes = off;  // everything above is zeroed before each launch
+  const size_t slot_elems = (size_t)2 * G.n_groups * G.L * G.d;
+  w.slot_k = off; off = align_up(off + slot_elems * 2, 256);
+  w.slot_v = off; off = align_up(off + slot_elems * 2, 256);
+  w.total = off;
+  return w;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Kernel parameters and per-D configuration
+// ------------------------------------------------------------------------------------------------
+struct KParams {
+  Geometry geo;
+  float scale_log2;  // scale * log2(e)
+  const uint16_t* k;
+  const uint16_t* v;
+  uint16_t* slot_k;
+  uint16_t* slot_v;
+  uint16_t* o;
+  float* lse;
+  Ctrl* ctrl;
+  uint32_t* flags;
+  uint32_t* consumed;
+  uint32_t* queue;
+  uint32_t* traj;
+  unsigned long long timeout_ns;
+  unsigned long long n_tiles_total;
+  unsigned long long n_stage_total;
+  int n_dyn;          // dynamic staging tasks
+  int n_init;         // static staging list length (2 per group)
+  int mode;           // PSR_STATIC / PSR_ADAPTIVE
+  int n_s_init;
+  int n_min, n_max;   // effective clamp
+  int fault;
+  int lookahead;      // static list: groups ahead of the dispense frontier
+  int ctrl_period;    // tasks between controller evaluations
+  float c_s0, c_p0;   // prior costs (cycles per staging task / per tile) before measurements exist
+};
+
+constexpr int kWarps = 10;
+constexpr int kThreads = kWarps * 32;  // warp 0 producer, 1 MMA, 2-5 softmax tile 0, 6-9 softmax tile 1
+
+template <int D>
+struct Cfg {
+  static constexpr int QT = kTileRows * D * 2;  // bytes of one 128-row bf16 tile
+  static constexpr int NSTAGE = D == 128 ? 5 : 12;
+  static constexpr int NB = D == 128 ? 3 : 7;  // staging buffers of one K tile + one V tile
+  static constexpr int SMEM = 1024 + 2 * QT + NSTAGE * QT;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  static_assert(NB * 2 * QT <= 2 * QT + NSTAGE * QT, "staging buffers must fit in the compute region");
+  static_assert(SMEM <= 232448 - 512, "shared memory");
+};
+
+enum : int { CMD_EXIT = 0, CMD_COMPUTE = 1, CMD_STAGE = 2, CMD_IDLE = 3 };
+
+// error sites
+enum : uint32_t {
+  SITE_NONE = 0, SITE_FLAG = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_S_FULL = 4, SITE_P_FULL = 5,
+  SITE_O_FULL = 6, SITE_Q_FULL = 7, SITE_STAGE_LOAD = 8, SITE_DRAIN = 9, SITE_QUEUE = 10, SITE_IDLE = 11
+};
+
+struct SmemCtl {
+  uint64_t q_full[2];
+  uint64_t kv_full[16];
+  uint64_t kv_empty[16];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t stg[8];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int cmd, arg;
+  volatile uint32_t abort;
+};
+
+__device__ __forceinline__ void raise_error(const KParams& p, uint32_t site) {
+  atomicCAS(&p.ctrl->error, 0u, site);
+  st_release(&p.ctrl->abort, 1u);
+}
+
+// Bounded mbarrier wait: false on timeout or abort.
+__device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KParams& p, SmemCtl* sc, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++it & 15u) == 0) {
+      if (sc->abort) return false;
+      if (ld_relaxed(&p.ctrl->abort)) { sc->abort = 1; return false; }
+      if (globaltimer_ns() - t0 > p.timeout_ns) { raise_error(p, site); sc->abort = 1; return false; }
+    }
+  }
+}
+
+// Bounded wait until *flag >= want (gpu-scope acquire).
+__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t want, uint32_t& seen, const KParams& p, SmemCtl* sc) {
+  seen = ld_acquire(flag);
+  if (seen >= want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (true) {
+    nanosleep_ns(64);
+    seen = ld_acquire(flag);
+    if (seen >= want) return true;
+    if ((++it & 15u) == 0) {
+      if (sc->abort) return false;
+      if (ld_relaxed(&p.ctrl->abort)) { sc->abort = 1; return false; }
+      if (globaltimer_ns() - t0 > p.timeout_ns) { raise_error(p, SITE_FLAG); sc->abort = 1; return false; }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Controller (one thread, at task boundaries)
+// ------------------------------------------------------------------------------------------------
+__device__ int current_target(const KParams& p) {
+  if (p.mode == PSR_STATIC) return p.n_s_init;
+  const uint32_t t = ld_relaxed(&p.ctrl->target_ns);
+  return t ? (int)(t - 1) : p.n_s_init;
+}
+
+__device__ void controller_update(const KParams& p) {
+  Ctrl* c = p.ctrl;
+  const unsigned long long sd = atomicAdd(&c->stage_done, 0ull);
+  const unsigned long long td = atomicAdd(&c->compute_tiles, 0ull);
+  const unsigned long long scy = atomicAdd(&c->stage_cycles, 0ull);
+  const unsigned long long ccy = atomicAdd(&c->compute_cycles, 0ull);
+  const double R_s = (double)(p.n_stage_total > sd ? p.n_stage_total - sd : 0);
+  const double R_p = (double)(p.n_tiles_total > td ? p.n_tiles_total - td : 0);
+  // measured cost per unit, blended with the prior until a few units are measured
+  const double C_s = (scy + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
+  const double C_p = (ccy + (double)p.c_p0 * 64.0) / ((double)td + 64.0);
+  int n = controller_rule((int)gridDim.x, R_s, C_s, R_p, C_p, p.n_min, p.n_max);
+  const int cur = current_target(p);
+  // hysteresis: move only by a margin unless the staging work is finished
+  const int margin = 1 + cur / 16;
+  if (n != 0 && n > cur - margin && n < cur + margin) return;
+  if (n == cur) return;
+  st_relaxed(&c->target_ns, (uint32_t)n + 1u);
+  atomicMax(&c->ns_min_inv, 0xFFFFu - (uint32_t)n);
+  atomicMax(&c->ns_max, (uint32_t)n);
+  const uint32_t k = atomicAdd(&c->traj_len, 1u);
+  if (k < (uint32_t)kTrajMax) {
+    const unsigned long long now = globaltimer_ns();
+    const unsigned long long t0 = c->t0_ns;
+    p.traj[2 * k] = (uint32_t)((now > t0 ? now - t0 : 0) / 1000ull);
+    p.traj[2 * k + 1] = (uint32_t)n;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Task selection (thread 0 of the CTA)
+// ------------------------------------------------------------------------------------------------
+// Claim a staging task without ever blocking: a ready entry of the dynamic
+// queue first, else the next static (group, step 1|2) entry if its group is
+// within the lookahead window of the compute dispense frontier.
+// Returns task id g*P + step, or -1 if none is claimable now.
+__device__ int try_claim_staging(const KParams& p) {
+  Ctrl* c = p.ctrl;
+  const Geometry& G = p.geo;
+  for (int attempt = 0; attempt < 4; ++attempt) {
+    const uint32_t h = ld_relaxed(&c->q_head);
+    if (h < (uint32_t)p.n_dyn) {
+      const uint32_t e = ld_acquire(&p.queue[h]);
+      if (e != 0) {
+        if (atom_cas_acq_rel(&c->q_head, h, h + 1) == h) return (int)(e - 1);
+        continue;
+      }
+    }
+    const uint32_t i = ld_relaxed(&c->init_next);
+    if (i >= (uint32_t)p.n_init) return -1;
+    const int g = (int)(i / 2), step = 1 + (int)(i % 2);
+    const uint32_t disp = ld_relaxed(&c->item_next);
+    const int frontier = (int)(disp / (uint32_t)G.Gs);
+    if (g > frontier + p.lookahead) return -1;
+    if (atom_cas_acq_rel(&c->init_next, i, i + 1) == i) {
+      if (step < group_steps(G, g)) return g * G.P + step;
+      // shard with fewer steps: entry is a no-op, count it as done
+      attempt = -1;  // keep looking
+      continue;
+    }
+  }
+  return -1;
+}
+
+__device__ bool staging_all_claimed(const KParams& p) {
+  return ld_relaxed(&p.ctrl->init_next) >= (uint32_t)p.n_init && ld_relaxed(&p.ctrl->q_head) >= (uint32_t)p.n_dyn;
+}
+
+__device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging) {
+  Ctrl* c = p.ctrl;
+  if (sc->abort || ld_relaxed(&c->abort)) { sc->cmd = CMD_EXIT; return; }
+  const int n_s = current_target(p);
+  const bool staging_role = (int)blockIdx.x < n_s;
+  if (staging_role != was_staging) {
+    atomicAdd(&c->role_switches, 1ull);
+    was_staging = staging_role;
+  }
+  if (staging_role) {
+    const int t = try_claim_staging(p);
+    if (t >= 0) { sc->cmd = CMD_STAGE; sc->arg = t; return; }
+    if (staging_all_claimed(p)) {
+      if (p.mode == PSR_STATIC) { sc->cmd = CMD_EXIT; return; }
+      // adaptive: nothing left to stage; fall through to compute
+    } else {
+      sc->cmd = CMD_IDLE; return;
+    }
+  }
+  if (ld_relaxed(&c->item_next) < (uint32_t)p.geo.n_items) {
+    const uint32_t n = atomicAdd(&c->item_next, 1u);
+    if (n < (uint32_t)p.geo.n_items) { sc->cmd = CMD_COMPUTE; sc->arg = (int)n; return; }
+  }
+  // no compute left
+  if (p.mode == PSR_STATIC || staging_all_claimed(p)) { sc->cmd = CMD_EXIT; return; }
+  const int t = try_claim_staging(p);
+  if (t >= 0) { sc->cmd = CMD_STAGE; sc->arg = t; return; }
+  sc->cmd = CMD_IDLE;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Staging task (thread 0): chunk (r - step) mod P of K and V -> slot (step & 1) of group g
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, int task, uint32_t (&stg_phase)[8]) {
+  using C = Cfg<D>;
+  const Geometry& G = p.geo;
+  const int g = task / G.P, step = task % G.P;
+  int r, b, kvh, sub;
+  group_coord(G, g, r, b, kvh, sub);
+  const int j = ((r - step) % G.P + G.P) % G.P;
+  const size_t tile_elems = (size_t)kTileRows * D;
+  const uint16_t* src_k = p.k + ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L) * D;
+  const uint16_t* src_v = p.v + ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L) * D;
+  const size_t slot_off = ((size_t)(step & 1) * G.n_groups + g) * (size_t)G.L * D;
+  uint16_t* dst_k = p.slot_k + slot_off;
+  uint16_t* dst_v = p.slot_v + slot_off;
+  uint32_t* flag = p.flags + (size_t)g * G.P + step;
+  const int n_kt = G.kv_tiles;
+  const bool drop = (p.fault == PSR_FAULT_DROP_FIRST_FLAG) && (atomicAdd(&p.ctrl->fault_count, 1u) == 0u);
+  if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
+  // staging "acquire": queue entries were published with release after the slot's
+  // previous contents were consumed; order those async-proxy reads before our writes
+  fence_proxy_async_global();
+
+  constexpr int NB = C::NB;
+  constexpr uint32_t BUF = 2 * C::QT;
+  auto issue_load = [&](int kt) {
+    const int bi = kt % NB;
+    uint64_t* bar = &sc->stg[bi];
+    mbar_expect_tx(bar, BUF);
+    bulk_load(smem_base + bi * BUF, src_k + (size_t)kt * tile_elems, C::QT, bar);
+    bulk_load(smem_base + bi * BUF + C::QT, src_v + (size_t)kt * tile_elems, C::QT, bar);
+  };
+  const int pre = n_kt < NB - 1 ? n_kt : NB - 1;
+  for (int kt = 0; kt < pre; ++kt) issue_load(kt);
+  int issued = pre;
+  bool ok = true;
+  for (int kt = 0; kt < n_kt; ++kt) {
+    const int bi = kt % NB;
+    if (kt >= issued) break;  // aborted: no more loads were issued
+    if (ok && !wait_bar(&sc->stg[bi], stg_phase[bi] & 1u, p, sc, SITE_STAGE_LOAD)) ok = false;
+    if (!ok) {
+      // drain this load (bounded) so that no bulk copy targets shared memory after we leave
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&sc->stg[bi], stg_phase[bi] & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+    stg_phase[bi]++;
+    if (ok) {
+      bulk_store(dst_k + (size_t)kt * tile_elems, smem_base + bi * BUF, C::QT);
+      bulk_store(dst_v + (size_t)kt * tile_elems, smem_base + bi * BUF + C::QT, C::QT);
+    }
+    bulk_commit();
+    const int nk = kt + NB - 1;
+    if (nk < n_kt && ok) {
+      bulk_wait_read<1>();  // the store that used buffer nk % NB (tile kt-1) has read shared memory
+      issue_load(nk);
+      issued = nk + 1;
+    }
+    if (kt >= 2 && ok && !drop) {
+      bulk_wait<2>();  // stores of tiles <= kt-2 are complete
+      fence_proxy_async_global();
+      st_release(flag, (uint32_t)(kt - 1));
+    }
+  }
+  bulk_wait<0>();
+  if (ok && !drop) {
+    fence_proxy_async_global();
+    st_release(flag, (uint32_t)n_kt);
+  }
+  atomicAdd(&p.ctrl->stage_bytes, (unsigned long long)n_kt * 2ull * C::QT);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Compute item: producer warp (TMA), MMA warp (tcgen05), two softmax warpgroups
+// ------------------------------------------------------------------------------------------------
+// Running counts over the CTA's lifetime; every thread keeps its own copy and
+// advances it identically, so mbarrier phases agree across roles.
+struct Counters {
+  uint32_t kv;     // K/V tile loads (producer issues them, MMA consumes them)
+  uint32_t items;  // items processed
+  uint32_t tiles;  // KV tiles processed before the current item (S, P and O barrier phases)
+};
+
+template <int D>
+__device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, uint32_t dst, int row, uint64_t* bar) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * 16384, tm, 64 * h, row, bar);
+}
+
+template <int D>
+__device__ void producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it,
+                         const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                         const CUtensorMap* tm_sk, const CUtensorMap* tm_sv, Counters& cnt) {
+  using C = Cfg<D>;
+  const Geometry& G = p.geo;
+  const uint32_t sQ = smem_base, sStage = smem_base + 2 * C::QT;
+  // Q tiles (the barrier phase of q_full is the item count)
+  const int q_row = (it.b * G.Hq + it.hq) * G.S + it.r * G.L + it.qp * kItemRows;
+  for (int i = 0; i < 2; ++i) {
+    mbar_expect_tx(&sc->q_full[i], C::QT);
+    load_kv_tile<D>(tm_q, sQ + i * C::QT, q_row + i * kTileRows, &sc->q_full[i]);
+  }
+  // pending "slot consumed" notifications: (step, load index of the step's last tile)
+  int pend_step[4] = {0, 0, 0, 0};
+  uint32_t pend_load[4] = {0, 0, 0, 0};
+  int pend_n = 0;
+  auto resolve_one = [&](bool blocking) -> bool {
+    const uint32_t c = pend_load[0];
+    const uint32_t stage = c % C::NSTAGE, par = (c / C::NSTAGE) & 1u;
+    if (blocking) {
+      if (!wait_bar(&sc->kv_full[stage], par, p, sc, SITE_KV_FULL)) return false;
+    } else if (!mbar_test_wait(&sc->kv_full[stage], par)) {
+      return false;
+    }
+    const int t = pend_step[0];
+    fence_proxy_async_global();
+    const uint32_t old = atom_add_acq_rel(p.consumed + (size_t)it.g * G.P + t, 1u);
+    if (old + 1 == (uint32_t)G.Gs && t + 2 < it.n_steps) {
+      const uint32_t k = atomicAdd(&p.ctrl->q_tail, 1u);
+      if (k < (uint32_t)p.n_dyn) st_release(p.queue + k, (uint32_t)(it.g * G.P + t + 2) + 1u);
+      else raise_error(p, SITE_QUEUE);
+    }
+    for (int i = 1; i < pend_n; ++i) { pend_step[i - 1] = pend_step[i]; pend_load[i - 1] = pend_load[i]; }
+    --pend_n;
+    return true;
+  };
+  bool ok = true;
+  for (int t = 0; t < it.n_steps && ok; ++t) {
+    const int j = ((it.r - t) % G.P + G.P) % G.P;
+    const int n_kt = tiles_at_step(G, it, t);
+    const CUtensorMap* mk = t == 0 ? tm_k : tm_sk;
+    const CUtensorMap* mv = t == 0 ? tm_v : tm_sv;
+    const int row0 = t == 0 ? (it.b * G.Hkv + it.kvh) * G.S + j * G.L
+                            : ((t & 1) * G.n_groups + it.g) * G.L;
+    const uint32_t* flag = p.flags + (size_t)it.g * G.P + t;
+    uint32_t seen = 0;
+    for (int kt = 0; kt < n_kt && ok; ++kt) {
+      if (t > 0 && seen < (uint32_t)(kt + 1)) {
+        if (!wait_flag(flag, (uint32_t)(kt + 1), seen, p, sc)) { ok = false; break; }
+        fence_proxy_async_global();  // acquire (generic) before the async-proxy reads of the slot
+      }
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint32_t c = cnt.kv;
+        const uint32_t stage = c % C::NSTAGE, fill = c / C::NSTAGE;
+        // notifications whose stage is about to be refilled must be sent first
+        while (pend_n > 0 && pend_load[0] + C::NSTAGE <= c) {
+          if (!resolve_one(true)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (pend_n > 0) resolve_one(false);
+        if (fill > 0 && !wait_bar(&sc->kv_empty[stage], (fill - 1) & 1u, p, sc, SITE_KV_EMPTY)) { ok = false; break; }
+        mbar_expect_tx(&sc->kv_full[stage], C::QT);
+        load_kv_tile<D>(kv == 0 ? mk : mv, sStage + stage * C::QT, row0 + kt * kTileRows, &sc->kv_full[stage]);
+        cnt.kv++;
+      }
+    }
+    if (ok && t > 0) {
+      if (pend_n == 4 && !resolve_one(true)) ok = false;
+      pend_step[pend_n] = t;
+      pend_load[pend_n] = cnt.kv - 1;
+      ++pend_n;
+    }
+  }
+  while (ok && pend_n > 0)
+    if (!resolve_one(true)) ok = false;
+  if (!ok) sc->abort = 1;
+}
+
+template <int D>
+__device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, Counters& cnt) {
+  using C = Cfg<D>;
+  const Geometry& G = p.geo;
+  const uint32_t tb = sc->tmem_base;
+  const uint32_t sQ = smem_base, sStage = smem_base + 2 * C::QT;
+  constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false);
+  constexpr uint32_t IPV = idesc_bf16_f32(128, D, true);
+  long long n = item_tiles(G, it);
+  const uint32_t qpar = cnt.items & 1u;
+  if (!wait_bar(&sc->q_full[0], qpar, p, sc, SITE_Q_FULL) || !wait_bar(&sc->q_full[1], qpar, p, sc, SITE_Q_FULL)) {
+    sc->abort = 1;
+    return;
+  }
+  tc_fence_after();
+  auto issue_s = [&](int i, uint32_t kstage) {
+    const uint32_t a0 = sQ + i * C::QT, b0 = sStage + kstage * C::QT;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+      mma_ss(tb + (i ? C::COL_S1 : C::COL_S0), sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), IQK,
+             kk > 0 ? 1u : 0u);
+    }
+    mma_commit(&sc->s_full[i]);
+  };
+  auto issue_pv = [&](int i, uint32_t vstage, bool first) {
+    const uint32_t b0 = sStage + vstage * C::QT;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      mma_ts(tb + (i ? C::COL_O1 : C::COL_O0), tb + (i ? C::COL_S1 : C::COL_S0) + kk * 8,
+             sdesc_sw128(b0 + kk * 2048, 16384, 1024), IPV, (first && kk == 0) ? 0u : 1u);
+    }
+    mma_commit(&sc->o_full[i]);
+  };
+  auto stage_of = [](uint32_t c) { return c % C::NSTAGE; };
+  auto par_of = [](uint32_t c) { return (c / C::NSTAGE) & 1u; };
+  // prologue: S0_0, S1_0
+  uint32_t ck = cnt.kv;  // load index of K_0
+  if (!wait_bar(&sc->kv_full[stage_of(ck)], par_of(ck), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
+  tc_fence_after();
+  issue_s(0, stage_of(ck));
+  issue_s(1, stage_of(ck));
+  mma_commit(&sc->kv_empty[stage_of(ck)]);
+  for (long long jt = 0; jt < n; ++jt) {
+    const uint32_t cv = ck + 1;      // V_j
+    const uint32_t cn = ck + 2;      // K_{j+1}
+    const bool more = jt + 1 < n;
+    if (!wait_bar(&sc->kv_full[stage_of(cv)], par_of(cv), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
+    // P0_j ready
+    if (!wait_bar(&sc->p_full[0], (cnt.tiles + (uint32_t)jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
+    tc_fence_after();
+    issue_pv(0, stage_of(cv), jt == 0);
+    if (more) {
+      if (!wait_bar(&sc->kv_full[stage_of(cn)], par_of(cn), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
+      tc_fence_after();
+      issue_s(0, stage_of(cn));
+    }
+    if (!wait_bar(&sc->p_full[1], (cnt.tiles + (uint32_t)jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
+    tc_fence_after();
+    issue_pv(1, stage_of(cv), jt == 0);
+    mma_commit(&sc->kv_empty[stage_of(cv)]);
+    if (more) {
+      issue_s(1, stage_of(cn));
+      mma_commit(&sc->kv_empty[stage_of(cn)]);
+    }
+    ck = cn;
+  }
+  cnt.kv += (uint32_t)(2 * n);
+}
+
+template <int D>
+__device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, int i, Counters& cnt) {
+  using C = Cfg<D>;
+  const Geometry& G = p.geo;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quarter = warp % 4;
+  const int row = quarter * 32 + lane;                         // TMEM lane = tile row
+  const int q_local = it.qp * kItemRows + i * kTileRows + row;  // position within the shard
+  const uint32_t lane_base = sc->tmem_base + ((uint32_t)(quarter * 32) << 16);
+  const uint32_t tS = lane_base + (i ? C::COL_S1 : C::COL_S0);
+  const uint32_t tO = lane_base + (i ? C::COL_O1 : C::COL_O0);
+  const float sl2 = p.scale_log2;
+  float m_run = -INFINITY;  // running max in the log2-scaled domain
+  float l_run = 0.0f;
+  uint32_t jglob = 0;
+  bool ok = true;
+  for (int t = 0; t < it.n_steps && ok; ++t) {
+    const int n_kt = tiles_at_step(G, it, t);
+    for (int kt = 0; kt < n_kt; ++kt, ++jglob) {
+      if (!wait_bar(&sc->s_full[i], (cnt.tiles + jglob) & 1u, p, sc, SITE_S_FULL)) { ok = false; break; }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+      }
+      // causal mask on the shard's own chunk: key position kt*128 + c > q_local
+      if (G.causal && t == 0) {
+        const int lim = q_local - kt * kTileRows;
+        if (lim < 127) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * sl2;
+      // rescale only when the max grows by more than 2^8 (values below stay in range)
+      const bool need = (jglob == 0) || (m_tile > m_run + 8.0f);
+      float m_new = need ? fmaxf(m_run, m_tile) : m_run;
+      if (jglob > 0 && __any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+        if (!wait_bar(&sc->o_full[i], (cnt.tiles + jglob - 1) & 1u, p, sc, SITE_O_FULL)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(tO + c * 32, r);
+        }
+        tmem_st_wait();
+        l_run *= alpha;
+      }
+      m_run = m_new;
+      const float m_use = m_run == -INFINITY ? 0.0f : m_run;
+      float sum = 0.0f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * e], sl2, -m_use));
+          const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * e + 1], sl2, -m_use));
+          sum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + h * 32, pk);
+      }
+      tmem_st_wait();
+      l_run += sum;
+      tc_fence_before();
+      mbar_arrive(&sc->p_full[i]);
+    }
+  }
+  const uint32_t n = jglob;
+  if (ok) {
+    // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
+    if (!wait_bar(&sc->o_full[i], (cnt.tiles + n - 1) & 1u, p, sc, SITE_O_FULL)) ok = false;
+  }
+  if (ok) {
+    tc_fence_after();
+    const float inv_l = 1.0f / l_run;
+    const size_t row_id = (size_t)(it.b * G.Hq + it.hq) * G.S + (size_t)it.r * G.L + q_local;
+    uint16_t* orow = p.o + row_id * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tO + c * 32, r);
+      tmem_ld_wait();
+      uint4 v4[4];
+      uint32_t* w = reinterpret_cast<uint32_t*>(v4);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+      uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[e] = v4[e];
+    }
+    p.lse[row_id] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
+  } else {
+    sc->abort = 1;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// The persistent kernel
+// ------------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_sk, const __grid_constant__ CUtensorMap tm_sv) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ SmemCtl sc;
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sc.q_full[i], 1);
+      mbar_init(&sc.s_full[i], 1);
+      mbar_init(&sc.p_full[i], 128);
+      mbar_init(&sc.o_full[i], 1);
+    }
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&sc.kv_full[s], 1);
+      mbar_init(&sc.kv_empty[s], 1);
+    }
+    for (int s = 0; s < C::NB; ++s) mbar_init(&sc.stg[s], 1);
+    mbar_init(&sc.drain, 1);
+    sc.abort = 0;
+    fence_barrier_init();
+    if (blockIdx.x == 0) {
+      unsigned long long z = 0;
+      atomicCAS(&p.ctrl->t0_ns, z, (unsigned long long)globaltimer_ns());
+      p.ctrl->ns_initial = (uint32_t)p.n_s_init;
+      atomicMax(&p.ctrl->ns_max, (uint32_t)p.n_s_init);
+      atomicMax(&p.ctrl->ns_min_inv, 0xFFFFu - (uint32_t)p.n_s_init);
+    }
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_sk);
+    prefetch_tmap(&tm_sv);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sc.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  Counters cnt{0, 0, 0};
+  uint32_t stg_phase[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  bool was_staging = false;
+  long long t_task = 0;
+  uint64_t idle_since = 0;  // first idle poll of the current idle stretch (0 = not idle)
+  while (true) {
+    if (threadIdx.x == 0) {
+      decide(p, &sc, was_staging);
+      t_task = clock64();
+    }
+    __syncthreads();
+    const int cmd = sc.cmd, arg = sc.arg;
+    if (cmd == CMD_EXIT) break;
+    if (cmd == CMD_STAGE) {
+      if (threadIdx.x == 0) run_staging<D>(p, &sc, smem_base, arg, stg_phase);
+    } else if (cmd == CMD_COMPUTE) {
+      const ItemCoord it = item_coord(p.geo, arg);
+      if (warp == 0) {
+        if (lane == 0) producer<D>(p, &sc, smem_base, it, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
+      } else if (warp == 1) {
+        if (lane == 0) mma_issuer<D>(p, &sc, smem_base, it, cnt);
+      } else {
+        softmax_wg<D>(p, &sc, it, warp < 6 ? 0 : 1, cnt);
+      }
+      cnt.items++;
+      cnt.tiles += (uint32_t)item_tiles(p.geo, it);
+    } else {
+      if (threadIdx.x == 0) {
+        atomicAdd(&p.ctrl->idle_polls, 1ull);
+        // a CTA that finds no claimable work for longer than the wait bound reports it
+        const uint64_t now = globaltimer_ns();
+        if (idle_since == 0) idle_since = now;
+        else if (now - idle_since > p.timeout_ns) raise_error(p, SITE_IDLE);
+        nanosleep_ns(500);
+      }
+    }
+    if (threadIdx.x == 0 && cmd != CMD_IDLE) idle_since = 0;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0 && cmd != CMD_IDLE) {
+      const unsigned long long dt = (unsigned long long)(clock64() - t_task);
+      if (cmd == CMD_STAGE) {
+        atomicAdd(&p.ctrl->stage_cycles, dt);
+        atomicAdd(&p.ctrl->stage_done, 1ull);
+      } else {
+        const ItemCoord it = item_coord(p.geo, arg);
+        atomicAdd(&p.ctrl->compute_cycles, dt);
+        atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles(p.geo, it));
+        atomicAdd(&p.ctrl->compute_items, 1ull);
+      }
+      const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
+      if (p.mode == PSR_ADAPTIVE && (tick % (uint32_t)p.ctrl_period) == 0) controller_update(p);
+    }
+  }
+  // drain: every tcgen05 op issued by this CTA has completed before TMEM is released
+  if (threadIdx.x == 32) {
+    mma_commit(&sc.drain);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&sc.drain, 0)) {
+      if (globaltimer_ns() - t0 > 100000000ull) break;
+    }
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait<0>();
+    // every TMA load this CTA issued has landed (normally already true)
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t s = 0; s < (uint32_t)C::NSTAGE && s < cnt.kv; ++s) {
+      const uint32_t fills = (cnt.kv - s + C::NSTAGE - 1) / C::NSTAGE;  // loads that used stage s
+      while (!mbar_try_wait(&sc.kv_full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(sc.tmem_base, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------------
+struct DeviceInfo {
+  int device = -1, n_sm = 0, cc_major = 0, cc_minor = 0;
+};
+
+static bool device_info(DeviceInfo& di) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev >= 0 && dev < 64 && cache[dev].device == dev) { di = cache[dev]; return true; }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return false;
+  di.device = dev;
+  di.n_sm = prop.multiProcessorCount;
+  di.cc_major = prop.major;
+  di.cc_minor = prop.minor;
+  if (dev >= 0 && dev < 64) cache[dev] = di;
+  return true;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [rows][d] bf16, box = 64 columns x 128 rows, 128-byte swizzle
+static bool make_tmap(CUtensorMap* m, const void* base, long long rows, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int max_group_items(int n_cta) {
+  // the compute CTAs must be able to hold a whole group at once; leave room for
+  // at least a quarter of the CTAs to stage
+  int m = n_cta - n_cta / 4 - 1;
+  return m < 1 ? 1 : m;
+}
+
+static int shape_geometry(const psr_shape* sh, Geometry& G, int n_cta) {
+  if (!sh) return PSR_ERR_ARG;
+  if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->P < 1) return PSR_ERR_ARG;
+  if (sh->Hq % sh->Hkv != 0 || sh->S % sh->P != 0) return PSR_ERR_UNSUPPORTED;
+  if (sh->d != 64 && sh->d != 128) return PSR_ERR_UNSUPPORTED;
+  if (sh->causal != 0 && sh->causal != 1) return PSR_ERR_ARG;
+  if (!(sh->scale == sh->scale)) return PSR_ERR_ARG;  // NaN
+  const long long rows_q = (long long)sh->B * sh->Hq * sh->S;
+  if (rows_q >= (1LL << 31) || rows_q * sh->d >= (1LL << 40)) return PSR_ERR_UNSUPPORTED;
+  const int rc = geometry_init(G, sh->B, sh->Hq, sh->Hkv, sh->S, sh->P, sh->d, sh->causal, max_group_items(n_cta));
+  if (rc == 1) return PSR_ERR_ARG;
+  if (rc != 0) return PSR_ERR_UNSUPPORTED;
+  if (2LL * G.n_groups * G.L >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;  // slot rows index with int32
+  return PSR_OK;
+}
+
+template <int D>
+static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(ring_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_cta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: they wait on each other
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ring_attn_kernel<D>, kp, maps[0], maps[1], maps[2], maps[3], maps[4]);
+}
+
+}  // namespace psr
+
+using namespace psr;
+
+extern "C" {
+
+const char* psr_status_string(int s) {
+  switch (s) {
+    case PSR_OK: return "ok";
+    case PSR_ERR_ARG: return "invalid argument";
+    case PSR_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case PSR_ERR_CUDA: return "CUDA runtime error";
+    case PSR_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int psr_controller_target(int n_cta, double R_s, double C_s, double R_p, double C_p, int n_min, int n_max) {
+  return controller_rule(n_cta, R_s, C_s, R_p, C_p, n_min, n_max);
+}
+
+int psr_num_ctas(void) {
+  DeviceInfo di;
+  if (!device_info(di)) return -PSR_ERR_CUDA;
+  return di.n_sm;
+}
+
+static int ncta_for_sizing() {
+  DeviceInfo di;
+  if (device_info(di) && di.n_sm > 0) return di.n_sm;
+  return 152;  // sizing without a device: the GB300's SM count
+}
+
+size_t psr_workspace_bytes(const psr_shape* sh) {
+  Geometry G;
+  if (shape_geometry(sh, G, ncta_for_sizing()) != PSR_OK) return 0;
+  return ws_layout(G).total;
+}
+
+int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const void* v, void* o, float* lse,
+                      void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
+  if (!sh || !q || !k || !v || !o || !lse || !workspace) return PSR_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PSR_ERR_ARG;
+  for (const void* ptr : {q, k, v, (const void*)o, (const void*)lse})
+    if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return PSR_ERR_ARG;
+  DeviceInfo di;
+  if (!device_info(di)) return PSR_ERR_CUDA;
+  if (di.cc_major != 10 || di.cc_minor != 3) return PSR_ERR_UNSUPPORTED;
+  const int n_cta = di.n_sm;
+  Geometry G;
+  int rc = shape_geometry(sh, G, n_cta);
+  if (rc != PSR_OK) return rc;
+  const WsLayout L = ws_layout(G);
+  if (ws_bytes < L.total) return PSR_ERR_ARG;
+
+  psr_partition pt;
+  if (part) pt = *part;
+  else { pt.mode = PSR_ADAPTIVE; pt.n_staging = 0; pt.n_min = 0; pt.n_max = 0; pt.fault = 0; pt.timeout_ms = 0; }
+  if (pt.mode != PSR_STATIC && pt.mode != PSR_ADAPTIVE) return PSR_ERR_ARG;
+  if (pt.fault < 0 || pt.fault > PSR_FAULT_SLOW_STAGING) return PSR_ERR_ARG;
+
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.geo = G;
+  const double scale = sh->scale > 0.0f ? (double)sh->scale : 1.0 / std::sqrt((double)sh->d);
+  kp.scale_log2 = (float)(scale * 1.4426950408889634);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  kp.k = static_cast<const uint16_t*>(k);
+  kp.v = static_cast<const uint16_t*>(v);
+  kp.slot_k = reinterpret_cast<uint16_t*>(ws + L.slot_k);
+  kp.slot_v = reinterpret_cast<uint16_t*>(ws + L.slot_v);
+  kp.o = static_cast<uint16_t*>(o);
+  kp.lse = lse;
+  kp.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  kp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+  kp.consumed = reinterpret_cast<uint32_t*>(ws + L.consumed);
+  kp.queue = reinterpret_cast<uint32_t*>(ws + L.queue);
+  kp.traj = reinterpret_cast<uint32_t*>(ws + L.traj);
+  kp.timeout_ns = (unsigned long long)(pt.timeout_ms > 0 ? pt.timeout_ms : 2000) * 1000000ull;
+  kp.n_tiles_total = (unsigned long long)total_tiles(G);
+  kp.n_stage_total = (unsigned long long)total_staging_tasks(G);
+  kp.n_dyn = (int)dynamic_staging_tasks(G);
+  kp.n_init = 2 * G.n_groups;
+  kp.mode = pt.mode;
+  kp.fault = pt.fault;
+  // clamps: at least one stager while staging remains; enough compute CTAs to hold a group
+  const int hard_max = n_cta - G.Gs - 1 < 1 ? 1 : n_cta - G.Gs - 1;
+  int n_max = pt.n_max > 0 ? pt.n_max : hard_max;
+  if (n_max > hard_max) n_max = hard_max;
+  int n_min = pt.n_min > 0 ? pt.n_min : 1;
+  if (n_min > n_max) n_min = n_max;
+  kp.n_min = n_min;
+  kp.n_max = n_max;
+  const bool any_staging = kp.n_stage_total > 0;
+  // costs before any measurement: a staging task moves 2*L*d*2 bytes at ~100 GB/s per SM;
+  // a compute tile pair is 4*128*128*d flops at ~60 % of an SM's dense bf16 rate (8192 flop/clk)
+  kp.c_s0 = (float)((2.0 * G.L * G.d * 2.0) / 100e9 * 1.9e9);
+  kp.c_p0 = (float)(4.0 * 128.0 * 128.0 * G.d / (0.6 * 8192.0));
+  int n_s;
+  if (pt.mode == PSR_STATIC) {
+    n_s = pt.n_staging;
+    if (!any_staging) n_s = 0;
+    else if (n_s < 1 || n_s > n_cta - 1) return PSR_ERR_ARG;
+    if (any_staging && n_cta - n_s < G.Gs) return PSR_ERR_ARG;  // a group could never be fully resident
+  } else {
+    n_s = pt.n_staging > 0 ? pt.n_staging
+                           : controller_rule(n_cta, (double)kp.n_stage_total, kp.c_s0, (double)kp.n_tiles_total,
+                                             kp.c_p0, n_min, n_max);
+    if (!any_staging) n_s = 0;
+    else {
+      if (n_s < n_min) n_s = n_min;
+      if (n_s > n_max) n_s = n_max;
+    }
+  }
+  kp.n_s_init = n_s;
+  kp.lookahead = n_cta / G.Gs + 2;
+  kp.ctrl_period = n_cta / 8 > 1 ? n_cta / 8 : 1;
+
+  CUtensorMap maps[5];
+  const long long rows_q = (long long)G.B * G.Hq * G.S, rows_kv = (long long)G.B * G.Hkv * G.S;
+  const long long rows_slot = 2LL * G.n_groups * G.L;
+  if (!make_tmap(&maps[0], q, rows_q, G.d) || !make_tmap(&maps[1], k, rows_kv, G.d) ||
+      !make_tmap(&maps[2], v, rows_kv, G.d) || !make_tmap(&maps[3], kp.slot_k, rows_slot, G.d) ||
+      !make_tmap(&maps[4], kp.slot_v, rows_slot, G.d))
+    return PSR_ERR_CUDA;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
+  cudaError_t e = G.d == 128 ? launch<128>(kp, maps, n_cta, st) : launch<64>(kp, maps, n_cta, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PSR_ERR_CUDA;
+  }
+  return PSR_OK;
+}
+
+int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* k_host, const void* v_host,
+                           void* o_host, float* lse_host, void* dq, void* dk, void* dv, void* d_o, float* d_lse,
+                           void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
+  if (!sh || !q_host || !k_host || !v_host || !o_host || !lse_host) return PSR_ERR_ARG;
+  if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->d < 1) return PSR_ERR_ARG;
+  const size_t nq = (size_t)sh->B * sh->Hq * sh->S * sh->d * 2, nkv = (size_t)sh->B * sh->Hkv * sh->S * sh->d * 2;
+  const size_t nl = (size_t)sh->B * sh->Hq * sh->S * 4;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!dq || !dk || !dv || !d_o || !d_lse) return PSR_ERR_ARG;
+  if (cudaMemcpyAsync(dq, q_host, nq, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k_host, nkv, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v_host, nkv, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return PSR_ERR_CUDA;
+  int rc = psr_ring_attn_fwd(sh, dq, dk, dv, d_o, d_lse, workspace, ws_bytes, part, stream);
+  if (rc != PSR_OK) return rc;
+  if (cudaMemcpyAsync(o_host, d_o, nq, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(lse_host, d_lse, nl, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PSR_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PSR_ERR_CUDA;
+  uint32_t err = 0;
+  if (cudaMemcpy(&err, static_cast<uint8_t*>(workspace) + offsetof(Ctrl, error), 4, cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return PSR_ERR_CUDA;
+  return err ? PSR_ERR_TIMEOUT : PSR_OK;
+}
+
+int psr_get_stats(const void* workspace, psr_stats* out, void* stream) {
+  if (!workspace || !out) return PSR_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PSR_ERR_CUDA;
+  Ctrl c;
+  if (cudaMemcpy(&c, workspace, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess) return PSR_ERR_CUDA;
+  memset(out, 0, sizeof(*out));
+  out->status = c.error ? PSR_ERR_TIMEOUT : PSR_OK;
+  out->error_site = (int)c.error;
+  out->n_cta = psr_num_ctas();
+  out->n_s_final = c.target_ns ? (int)c.target_ns - 1 : -1;
+  out->n_s_min = (int)(0xFFFFu - c.ns_min_inv);
+  out->n_s_max = (int)c.ns_max;
+  out->traj_len = (int)(c.traj_len < (uint32_t)kTrajMax ? c.traj_len : kTrajMax);
+  out->staging_cycles = c.stage_cycles;
+  out->compute_cycles = c.compute_cycles;
+  out->staging_tasks = c.stage_done;
+  out->compute_items = c.compute_items;
+  out->compute_tiles = c.compute_tiles;
+  out->staging_bytes = c.stage_bytes;
+  out->role_switches = c.role_switches;
+  out->idle_polls = c.idle_polls;
+  out->n_s_initial = (int)c.ns_initial;
+  if (out->n_s_final < 0) out->n_s_final = out->n_s_initial;
+  return out->status;
+}
+
+int psr_get_trajectory(const void* workspace, uint32_t* out_pairs, int max_entries, void* stream) {
+  if (!workspace || (!out_pairs && max_entries > 0) || max_entries < 0) return -PSR_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return -PSR_ERR_CUDA;
+  Ctrl c;
+  if (cudaMemcpy(&c, workspace, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess) return -PSR_ERR_CUDA;
+  int n = (int)(c.traj_len < (uint32_t)kTrajMax ? c.traj_len : kTrajMax);
+  if (n > max_entries) n = max_entries;
+  if (n > 0 && cudaMemcpy(out_pairs, static_cast<const uint8_t*>(workspace) + 256, (size_t)n * 8,
+                          cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -PSR_ERR_CUDA;
+  return n;
+}
+
+}  // extern "C"

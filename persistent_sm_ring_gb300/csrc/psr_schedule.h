@@ -1,0 +1,170 @@
+// Work decomposition of the emulated ring, shared by host and device code.
+//
+// Ring (mKernel pages, dataforcee/chathome kernel tables, Ring Attention row;
+// pwwt.cn Table 3): shard r consumes KV chunk j = (r - t) mod P at ring step
+// t = 0..P-1; step 0 is its own chunk, read in place (pwwt.cn §2.6 schedule
+// rule 3: local inputs first).  With a causal mask chunk j is needed by shard
+// r only when j <= r, i.e. steps t = 0..r.
+//
+// Units of work:
+//  * compute item  = 256 query rows (two 128-row tiles) of one (b, hq) in
+//                    shard r, carried through all of r's ring steps with the
+//                    accumulators resident in tensor memory;
+//  * group         = the items that read the same ring slot: shard r, batch b,
+//                    KV head kvh (all Hq/Hkv query heads of it) and, when a
+//                    group would exceed the deadlock bound, a sub-group index;
+//  * staging task  = one (group, step >= 1): copy chunk (r - step) mod P of
+//                    K and V into the group's slot (step & 1), 128-row tiles;
+//                    the pages' ring moves KV in 128-row tiles (Table 3).
+// Slot (step & 1) of a group may be overwritten for step s >= 3 only when all
+// of the group's items have loaded step s - 2: that is the double buffer's
+// back-pressure.
+#pragma once
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define PSR_HD __host__ __device__ __forceinline__
+#else
+#define PSR_HD inline
+#endif
+
+namespace psr {
+
+constexpr int kTileRows = 128;  // rows per Q tile and per KV tile
+constexpr int kItemRows = 256;  // query rows per compute item (two tiles)
+
+struct Geometry {
+  int B, Hq, Hkv, S, P, d, causal;
+  int L;         // shard length S / P
+  int gqa;       // Hq / Hkv
+  int q_pairs;   // items per (b, hq, shard): L / 256
+  int kv_tiles;  // 128-row KV tiles per chunk: L / 128
+  int G;         // items sharing one (shard, b, kvh): gqa * q_pairs
+  int n_sub;     // sub-groups per (shard, b, kvh)
+  int Gs;        // items per group: G / n_sub
+  int n_groups;  // P * B * Hkv * n_sub
+  int n_items;   // n_groups * Gs
+};
+
+struct ItemCoord {
+  int g;        // group index (dispense order)
+  int b, hq, kvh, r, qp;
+  int n_steps;  // active ring steps of shard r
+};
+
+PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int d, int causal, int max_group) {
+  G.B = B; G.Hq = Hq; G.Hkv = Hkv; G.S = S; G.P = P; G.d = d; G.causal = causal ? 1 : 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || P < 1 || d < 1) return 1;
+  if (Hq % Hkv != 0 || S % P != 0) return 1;
+  G.L = S / P;
+  if (G.L % kItemRows != 0) return 2;
+  G.gqa = Hq / Hkv;
+  G.q_pairs = G.L / kItemRows;
+  G.kv_tiles = G.L / kTileRows;
+  G.G = G.gqa * G.q_pairs;
+  // split a group into power-of-two sub-groups until it fits the bound
+  G.n_sub = 1;
+  while (G.G / G.n_sub > max_group && (G.G % (G.n_sub * 2)) == 0) G.n_sub *= 2;
+  if (G.G / G.n_sub > max_group) return 2;
+  G.Gs = G.G / G.n_sub;
+  const long long ng = (long long)P * B * Hkv * G.n_sub;
+  if (ng > (1 << 24)) return 2;
+  G.n_groups = (int)ng;
+  const long long ni = ng * G.Gs;
+  if (ni > (1LL << 30)) return 2;
+  G.n_items = (int)ni;
+  return 0;
+}
+
+// Shard of the rr-th shard in dispense order: causal runs the longest shards first.
+PSR_HD int shard_of_rank(const Geometry& G, int rr) { return G.causal ? (G.P - 1 - rr) : rr; }
+
+PSR_HD int steps_of_shard(const Geometry& G, int r) { return G.causal ? (r + 1) : G.P; }
+
+PSR_HD void group_coord(const Geometry& G, int g, int& r, int& b, int& kvh, int& sub) {
+  sub = g % G.n_sub;
+  int rest = g / G.n_sub;
+  kvh = rest % G.Hkv;
+  rest /= G.Hkv;
+  b = rest % G.B;
+  r = shard_of_rank(G, rest / G.B);
+}
+
+PSR_HD int group_steps(const Geometry& G, int g) {
+  int r, b, kvh, sub;
+  group_coord(G, g, r, b, kvh, sub);
+  return steps_of_shard(G, r);
+}
+
+PSR_HD ItemCoord item_coord(const Geometry& G, int n) {
+  ItemCoord c;
+  c.g = n / G.Gs;
+  int sub;
+  group_coord(G, c.g, c.r, c.b, c.kvh, sub);
+  const int w = sub * G.Gs + (n % G.Gs);
+  c.hq = c.kvh * G.gqa + w / G.q_pairs;
+  c.qp = w % G.q_pairs;
+  c.n_steps = steps_of_shard(G, c.r);
+  return c;
+}
+
+// KV tiles an item consumes at ring step t: under the causal mask the local
+// chunk stops at the item's own diagonal (tiles 0 .. 2*qp+1).
+PSR_HD int tiles_at_step(const Geometry& G, const ItemCoord& c, int t) {
+  return (G.causal && t == 0) ? (2 * c.qp + 2) : G.kv_tiles;
+}
+
+PSR_HD long long item_tiles(const Geometry& G, const ItemCoord& c) {
+  return G.causal ? (long long)(2 * c.qp + 2) + (long long)c.r * G.kv_tiles : (long long)G.P * G.kv_tiles;
+}
+
+PSR_HD long long total_tiles(const Geometry& G) {
+  // per (b, hq): sum over shards and q-pairs
+  long long per_bh = 0;
+  if (G.causal) {
+    for (int r = 0; r < G.P; ++r)
+      per_bh += (long long)G.q_pairs * (G.q_pairs + 1) + (long long)G.q_pairs * r * G.kv_tiles;
+  } else {
+    per_bh = (long long)G.P * G.q_pairs * G.P * G.kv_tiles;
+  }
+  return per_bh * G.B * G.Hq;
+}
+
+// Staging tasks: every (group, step >= 1).  Steps 1 and 2 land in fresh slots
+// and come from a static list in group order; steps >= 3 enter a ready queue
+// when the slot they overwrite has been consumed.
+PSR_HD long long total_staging_tasks(const Geometry& G) {
+  long long n = 0;
+  for (int rr = 0; rr < G.P; ++rr) n += steps_of_shard(G, shard_of_rank(G, rr)) - 1;
+  return n * G.B * G.Hkv * G.n_sub;
+}
+PSR_HD long long dynamic_staging_tasks(const Geometry& G) {
+  long long n = 0;
+  for (int rr = 0; rr < G.P; ++rr) {
+    int s = steps_of_shard(G, shard_of_rank(G, rr));
+    n += s > 3 ? s - 3 : 0;
+  }
+  return n * G.B * G.Hkv * G.n_sub;
+}
+
+// The pages' partition rule (pwwt.cn §2.4): equalise the predicted finish
+// times R_s*C_s/n_s and R_p*C_p/(N - n_s) of the two roles, i.e.
+//   n_s* = N * (R_s*C_s) / (R_p*C_p + R_s*C_s),
+// rounded to nearest and clamped to [max(n_min,1), min(n_max, N-1)] while both
+// roles have work; 0 once staging is finished; n_max when only staging remains.
+PSR_HD int controller_rule(int n_cta, double R_s, double C_s, double R_p, double C_p, int n_min, int n_max) {
+  if (n_cta < 2) return 0;
+  if (R_s <= 0.0) return 0;
+  int lo = n_min < 1 ? 1 : n_min;
+  int hi = n_max > n_cta - 1 ? n_cta - 1 : n_max;
+  if (hi < lo) hi = lo;
+  if (R_p <= 0.0) return hi;
+  const double ws = R_s * C_s, wp = R_p * C_p;
+  double x = (ws + wp) > 0.0 ? (double)n_cta * ws / (wp + ws) : 0.0;
+  int n = (int)(x + 0.5);
+  if (n < lo) n = lo;
+  if (n > hi) n = hi;
+  return n;
+}
+
+}  // namespace psr

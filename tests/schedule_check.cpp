@@ -1,0 +1,112 @@
+// Host check of the ring schedule used by the kernel (psr_schedule.h):
+//  * every compute item's TMA coordinates (Q tiles, home K/V tiles, slot tiles)
+//    stay inside the tensor extents the launcher encodes;
+//  * every (b, hq, row) of the output is written by exactly one item;
+//  * every (query tile, key tile) pair the causal mask allows is visited once,
+//    none that it forbids entirely is visited except the per-item diagonal pair;
+//  * flag / consumed indices stay below n_groups * P and the dynamic queue
+//    receives exactly dynamic_staging_tasks() pushes;
+//  * total_tiles() and total_staging_tasks() agree with direct enumeration.
+// Usage: schedule_check B Hq Hkv S P d causal max_group   -> prints "OK ..." or "FAIL ..."
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+
+#include "../persistent_sm_ring_gb300/csrc/psr_schedule.h"
+
+using namespace psr;
+
+#define CHECK(c, ...)                 \
+  do {                                \
+    if (!(c)) {                       \
+      std::printf("FAIL ");           \
+      std::printf(__VA_ARGS__);       \
+      std::printf("\n");              \
+      return 1;                       \
+    }                                 \
+  } while (0)
+
+int main(int argc, char** argv) {
+  if (argc != 9) return 2;
+  int a[8];
+  for (int i = 0; i < 8; ++i) a[i] = std::atoi(argv[i + 1]);
+  Geometry G;
+  int rc = geometry_init(G, a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+  if (rc != 0) {
+    std::printf("REJECT %d\n", rc);
+    return 0;
+  }
+  const long long rows_q = (long long)G.B * G.Hq * G.S, rows_kv = (long long)G.B * G.Hkv * G.S;
+  const long long rows_slot = 2LL * G.n_groups * G.L;
+  std::vector<unsigned char> covered((size_t)rows_q / kTileRows, 0);
+  std::vector<int> consumers((size_t)G.n_groups * G.P, 0);
+  long long tiles = 0;
+  for (int n = 0; n < G.n_items; ++n) {
+    ItemCoord c = item_coord(G, n);
+    CHECK(c.g >= 0 && c.g < G.n_groups, "group %d", c.g);
+    CHECK(c.b >= 0 && c.b < G.B && c.hq >= 0 && c.hq < G.Hq && c.r >= 0 && c.r < G.P, "coords item %d", n);
+    CHECK(c.kvh == c.hq / G.gqa, "gqa mapping item %d", n);
+    CHECK(c.qp >= 0 && c.qp < G.q_pairs, "qp item %d", n);
+    const long long q_row = (long long)(c.b * G.Hq + c.hq) * G.S + (long long)c.r * G.L + (long long)c.qp * kItemRows;
+    for (int i = 0; i < 2; ++i) {
+      const long long r0 = q_row + i * kTileRows;
+      CHECK(r0 >= 0 && r0 + kTileRows <= rows_q, "q rows item %d", n);
+      CHECK(r0 % kTileRows == 0, "q tile alignment");
+      CHECK(covered[r0 / kTileRows] == 0, "q tile written twice (item %d)", n);
+      covered[r0 / kTileRows] = 1;
+    }
+    long long it_tiles = 0;
+    for (int t = 0; t < c.n_steps; ++t) {
+      const int j = ((c.r - t) % G.P + G.P) % G.P;
+      if (G.causal) CHECK(j <= c.r, "causal chunk above the diagonal (item %d step %d)", n, t);
+      const int n_kt = tiles_at_step(G, c, t);
+      CHECK(n_kt >= 1 && n_kt <= G.kv_tiles, "tiles at step");
+      for (int kt = 0; kt < n_kt; ++kt) {
+        if (t == 0) {
+          const long long r0 = (long long)(c.b * G.Hkv + c.kvh) * G.S + (long long)j * G.L + (long long)kt * kTileRows;
+          CHECK(r0 >= 0 && r0 + kTileRows <= rows_kv, "home kv rows item %d", n);
+          // the home rows belong to chunk j of the item's own (b, kvh)
+          CHECK(r0 / G.S == c.b * G.Hkv + c.kvh, "home kv head");
+        } else {
+          const long long r0 = (long long)((t & 1) * G.n_groups + c.g) * G.L + (long long)kt * kTileRows;
+          CHECK(r0 >= 0 && r0 + kTileRows <= rows_slot, "slot rows item %d", n);
+        }
+        if (G.causal && t == 0) {
+          // key tile kt of the local chunk vs the item's query tiles: only the
+          // last two tiles can be (partly) above the diagonal
+          const int q_first = c.qp * kItemRows, key_first = kt * kTileRows;
+          CHECK(key_first <= q_first + kTileRows, "fully masked key tile for both query tiles");
+        }
+      }
+      it_tiles += n_kt;
+      if (t > 0) consumers[(size_t)c.g * G.P + t]++;
+    }
+    CHECK(it_tiles == item_tiles(G, c), "item_tiles mismatch item %d", n);
+    tiles += it_tiles;
+  }
+  for (size_t i = 0; i < covered.size(); ++i) CHECK(covered[i] == 1, "q tile %zu never written", i);
+  CHECK(tiles == total_tiles(G), "total_tiles %lld vs %lld", total_tiles(G), tiles);
+  long long stage = 0, dyn = 0;
+  for (int g = 0; g < G.n_groups; ++g) {
+    const int ns = group_steps(G, g);
+    for (int t = 1; t < ns; ++t) {
+      CHECK(consumers[(size_t)g * G.P + t] == G.Gs, "group %d step %d consumers %d", g, t,
+            consumers[(size_t)g * G.P + t]);
+      ++stage;
+      if (t >= 3) ++dyn;
+      // staging source: chunk j of (b, kvh), L rows; destination slot (t&1) of g
+      int r, b, kvh, sub;
+      group_coord(G, g, r, b, kvh, sub);
+      const int j = ((r - t) % G.P + G.P) % G.P;
+      const long long src0 = (long long)(b * G.Hkv + kvh) * G.S + (long long)j * G.L;
+      CHECK(src0 >= 0 && src0 + G.L <= rows_kv, "staging source rows");
+      const long long dst0 = (long long)((t & 1) * G.n_groups + g) * G.L;
+      CHECK(dst0 >= 0 && dst0 + G.L <= rows_slot, "staging destination rows");
+    }
+  }
+  CHECK(stage == total_staging_tasks(G), "staging tasks %lld vs %lld", stage, total_staging_tasks(G));
+  CHECK(dyn == dynamic_staging_tasks(G), "dynamic tasks %lld vs %lld", dyn, dynamic_staging_tasks(G));
+  std::printf("OK items=%d groups=%d Gs=%d n_sub=%d tiles=%lld staging=%lld dynamic=%lld\n", G.n_items, G.n_groups,
+              G.Gs, G.n_sub, tiles, stage, dyn);
+  return 0;
+}
