@@ -1,0 +1,507 @@
+"""Benchmark: Ring Attention forward on GB300 (one JSON line on rank 0).
+
+Workload (the headline case): B=1, H=32, S=32768 as P=16 shards of 2048, d=128,
+bf16 Q,K,V ~ N(0,1) seeded (synthetic), scale 1/sqrt(128); one step = one
+non-causal pass followed by one causal pass, each a single persistent launch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --sweep [d]      # partition-stress sweep: static 2..64 staging CTAs vs adaptive
+
+value: algorithmic TFLOP/s over the timed steps (4*d flops per unmasked
+(query, key) pair), inputs resident in HBM (805 MB per pass, larger than L2).
+e2e: the same metric through psr_ring_attn_fwd_host (pinned host buffers;
+H2D of Q,K,V and D2H of O,LSE inside the timed region).
+--impl reference: the fp64 CPU oracle on a bounded row sample of the same
+workload, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring-attn fwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 peak; ms/pass"
+WORKLOADS = ("h32_s32k_nc", "h32_s32k_c")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+PROFILE = os.path.join(ROOT, "profiles", "ring_attn_kernel_h32_s32k.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "persistent_sm_ring_gb300", "csrc", f)
+                  for f in ("psr_ring_attn.cu", "psr_device.cuh", "psr_schedule.h")]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    except Exception:
+        return dict(FALLBACK_PEAKS)
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the main kernel from the committed ncu summary, if it
+    was captured on the current kernel source; else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != kernel_source_sha():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; each rank runs an independent replica)
+# ------------------------------------------------------------------------------------------------
+
+def dist_init(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded row sample
+# ------------------------------------------------------------------------------------------------
+
+def oracle_rows_flops(w, rows):
+    import numpy as np
+    i = rows % w.S
+    keys = (i + 1) if w.causal else np.full_like(i, w.S)
+    return float(4.0 * w.d * keys.sum())
+
+
+def cpu_baseline(workloads, inputs, budget_s=12.0):
+    """Time the fp64 oracle on seeded sampled rows of each workload; TFLOP/s of algorithmic work."""
+    import numpy as np
+
+    import oracle
+    cores = oracle.default_threads()
+    flops = 0.0
+    secs = 0.0
+    n_rows_total = 0
+    per = budget_s / len(workloads)
+    for w, (q, k, v) in zip(workloads, inputs):
+        rng = np.random.default_rng(w.seed + 99)
+        n = max(cores, 64)
+        while True:  # calibrate, then fill the budget share
+            rows = np.sort(rng.choice(w.B * w.Hq * w.S, size=n, replace=False)).astype(np.int64)
+            t0 = time.perf_counter()
+            oracle.for_workload(w, q, k, v, rows=rows, n_threads=cores)
+            dt = time.perf_counter() - t0
+            if dt >= per * 0.5 or n >= w.B * w.Hq * w.S // 4:
+                break
+            n = int(min(w.B * w.Hq * w.S // 4, max(2 * n, n * per * 0.7 / max(dt, 1e-3))))
+        flops += oracle_rows_flops(w, rows)
+        secs += dt
+        n_rows_total += len(rows)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_rows_total} seeded query rows of {'+'.join(w.name for w in workloads)} "
+                      f"(fp64, every allowed key), {secs:.1f} s"}
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import persistent_sm_ring_gb300 as psr
+    import ring_inputs as ri
+
+    rank, world, local = dist_init(args.gpus)
+    psr.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wls = [ri.WORKLOADS[n] for n in WORKLOADS]
+    flops_step = sum(w.flops() for w in wls)
+    peaks = load_peaks()
+
+    # inputs: generated on the host (pinned) and copied once to HBM
+    host = []
+    devt = []
+    for w in wls[:1]:  # both passes share Q,K,V (same seed and shape)
+        q_h = torch.empty((w.B, w.Hq, w.S, w.d), dtype=torch.int16).pin_memory()
+        k_h = torch.empty((w.B, w.Hkv, w.S, w.d), dtype=torch.int16).pin_memory()
+        v_h = torch.empty((w.B, w.Hkv, w.S, w.d), dtype=torch.int16).pin_memory()
+        ri.generate(w, q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr())
+        host = [q_h, k_h, v_h]
+        devt = [t.to(dev, non_blocking=False).view(torch.bfloat16) for t in host]
+    w0 = wls[0]
+    q, k, v = devt
+    o = torch.empty_like(q)
+    lse = torch.empty((w0.B, w0.Hq, w0.S), dtype=torch.float32, device=dev)
+    shapes = [psr.make_shape(w.B, w.Hq, w.Hkv, w.S, w.P, w.d, w.causal, w.scale) for w in wls]
+    ws_bytes = max(psr.workspace_bytes(s) for s in shapes)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    part = psr.make_partition(psr.ADAPTIVE)
+    stream = torch.cuda.current_stream()
+
+    def one_pass(w):
+        psr.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, scale=w.scale, partition=part, workspace=ws, out=o,
+                          lse=lse, stream=stream)
+
+    def check_status():
+        st = psr.get_stats(ws)
+        if st["status"] != 0:
+            raise RuntimeError(f"device status {st['status']} site {st['error_site']}")
+        return st
+
+    for _ in range(args.warmup):
+        for w in wls:
+            one_pass(w)
+    check_status()
+
+    # timed region: K steps, per-launch events on the launching stream
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in wls]
+          for _ in range(args.steps)]
+    stats = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        for i, w in enumerate(wls):
+            ev[s][i][0].record(stream)
+            one_pass(w)
+            ev[s][i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    st_last = check_status()
+    per_pass_ms = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)] for i in range(len(wls))]
+    ms_step = dist_max(elapsed_ms / args.steps, world)
+    total_flops = dist_sum(flops_step * args.steps, world)
+    value = total_flops / (ms_step * args.steps / 1e3) / 1e12
+
+    # dominant kernel: the persistent launch of each pass (same kernel); algorithmic flops / mean duration
+    launch_ms = [statistics.mean(x) for x in per_pass_ms]
+    kern_achieved = flops_step / (sum(launch_ms) / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = profiled_traffic()
+
+    # per-pass statistics (non-causal, causal): one more instrumented pass each
+    passes = []
+    for i, w in enumerate(wls):
+        one_pass(w)
+        st = check_status()
+        traj = psr.get_trajectory(ws, 64)
+        passes.append({"workload": w.name, "causal": w.causal, "ms": round(launch_ms[i], 4),
+                       "tflops": round(w.flops() / (launch_ms[i] / 1e3) / 1e12, 2),
+                       "pct_peak": round(100 * w.flops() / (launch_ms[i] / 1e3) / 1e12 / peak, 2),
+                       "staging_GBps": round(2 * st["staging_bytes"] / (launch_ms[i] / 1e3) / 1e9, 1),
+                       "n_s": [st["n_s_initial"], st["n_s_min"], st["n_s_max"], st["n_s_final"]],
+                       "role_switches": st["role_switches"], "traj_head": traj[:8]})
+
+    # e2e: host buffers through the C ABI (H2D + kernel + D2H, synchronised, per pass)
+    o_h = torch.empty(host[0].shape, dtype=torch.int16).pin_memory()
+    l_h = torch.empty(tuple(host[0].shape[:3]), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t) for t in devt)
+    h2d = sum(t.numel() * 2 for t in host) * len(wls)
+    d2h = (o_h.numel() * 2 + l_h.numel() * 4) * len(wls)
+    e2e_steps = max(1, min(args.steps, 3))
+    for w in wls:  # warm the host path once
+        psr.ring_attn_fwd_host(*host, o_h, l_h, dq, dk, dv, o, lse, P=w.P, causal=w.causal, scale=w.scale,
+                               partition=part, workspace=ws, stream=stream)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for w in wls:
+            psr.ring_attn_fwd_host(*host, o_h, l_h, dq, dk, dv, o, lse, P=w.P, causal=w.causal, scale=w.scale,
+                                   partition=part, workspace=ws, stream=stream)
+    e2e_s = dist_max((time.perf_counter() - t0) / e2e_steps, world)
+    e2e_value = dist_sum(flops_step, world) / e2e_s / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np  # noqa: F401
+        qn = host[0].numpy().view(np.uint16)
+        kn = host[1].numpy().view(np.uint16)
+        vn = host[2].numpy().view(np.uint16)
+        cpu = cpu_baseline(wls, [(qn, kn, vn)] * len(wls), budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "B1 H32 S32768 P16 (L=2048) d128, one non-causal + one causal pass per step",
+                       "B": 1, "H": 32, "S": 32768, "P": 16, "d": 128, "passes": list(WORKLOADS),
+                       "partition": "adaptive", "l2": "inputs larger than L2 (Q,K,V 805 MB per pass)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_bf16_peak": round(100 * value / peak, 2),
+            "roofline": {"bound": "tensor", "achieved": round(kern_achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(kern_achieved / peak, 4), "traffic": traffic,
+                         "peak_source": f"{peaks.get('source')} bf16_tflops (burst)",
+                         "frac_of_sustained": round(kern_achieved / peak_sus, 4)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * len(wls),
+            "clocks": clk,
+            "passes": passes,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ------------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import ring_inputs as ri
+    oracle.build()
+    wls = [ri.WORKLOADS[n] for n in WORKLOADS]
+    w = wls[0]
+    q, k, v = ri.generate(w)
+    cores = oracle.default_threads()
+    rows_per_step = max(cores, args.ref_rows)
+    rng = np.random.default_rng(1234)
+    times, flops = [], []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        f = 0.0
+        for wl in wls:
+            rows = np.sort(rng.choice(wl.B * wl.Hq * wl.S, size=rows_per_step, replace=False)).astype(np.int64)
+            oracle.for_workload(wl, q, k, v, rows=rows, n_threads=cores)
+            f += oracle_rows_flops(wl, rows)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            flops.append(f)
+    value = sum(flops) / sum(times) / 1e12
+    sample = f"{rows_per_step} seeded query rows per pass of {'+'.join(x.name for x in wls)} per step (fp64)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "B1 H32 S32768 P16 (L=2048) d128, one non-causal + one causal pass per step",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# partition-stress sweep (static staging-CTA counts vs the adaptive controller)
+# ------------------------------------------------------------------------------------------------
+
+def run_sweep(args):
+    import torch
+
+    import persistent_sm_ring_gb300 as psr
+    import ring_inputs as ri
+    psr.build()
+    torch.cuda.set_device(0)
+    ds = [args.sweep] if args.sweep in (64, 128) else [64, 128]
+    statics = [2, 4, 6, 8, 12, 16, 24, 32, 48, 64]
+    rows = []
+    for d in ds:
+        base = ri.WORKLOADS[f"sweep_d{d}_P2"]
+        q_h, k_h, v_h = ri.generate(base)
+        import numpy as np
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+        q, k, v = dev(q_h), dev(k_h), dev(v_h)
+        for P in (2, 4, 8, 16, 32, 64):
+            w = ri.WORKLOADS[f"sweep_d{d}_P{P}"]
+            ws = torch.empty(psr.workspace_bytes(psr.make_shape(w.B, w.Hq, w.Hkv, w.S, w.P, w.d, False)),
+                             dtype=torch.uint8, device="cuda")
+            o = torch.empty_like(q)
+            lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device="cuda")
+
+            def timed(part):
+                for _ in range(2):
+                    psr.ring_attn_fwd(q, k, v, P=P, causal=False, scale=w.scale, partition=part, workspace=ws,
+                                      out=o, lse=lse)
+                ts = []
+                for _ in range(5):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    psr.ring_attn_fwd(q, k, v, P=P, causal=False, scale=w.scale, partition=part, workspace=ws,
+                                      out=o, lse=lse)
+                    b.record()
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b))
+                st = psr.get_stats(ws)
+                assert st["status"] == 0, st
+                return statistics.median(ts), st
+
+            res = {}
+            for n in statics:
+                try:
+                    res[n], _ = timed(psr.make_partition(psr.STATIC, n_staging=n))
+                except psr.PsrError:
+                    res[n] = None
+            ad, st = timed(psr.make_partition(psr.ADAPTIVE))
+            best_n = min((n for n in statics if res[n] is not None), key=lambda n: res[n])
+            rows.append({"d": d, "P": P, "adaptive_ms": round(ad, 4), "best_static_ms": round(res[best_n], 4),
+                         "best_static_n": best_n, "ratio": round(ad / res[best_n], 4),
+                         "worst_static_ms": round(max(v for v in res.values() if v is not None), 4),
+                         "static_ms": {str(n): (round(v, 4) if v is not None else None) for n, v in res.items()},
+                         "adaptive_n_s": [st["n_s_initial"], st["n_s_min"], st["n_s_max"], st["n_s_final"]],
+                         "tflops_adaptive": round(w.flops() / (ad / 1e3) / 1e12, 1)})
+            print(json.dumps(rows[-1]), flush=True)
+    import math
+    geo = math.exp(sum(math.log(r["ratio"]) for r in rows) / len(rows))
+    print(json.dumps({"sweep_geomean_adaptive_over_best_static": round(geo, 4),
+                      "max_ratio": max(r["ratio"] for r in rows)}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", type=int, nargs="?", const=0, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=96)
+    args = ap.parse_args()
+    if args.sweep is not None:
+        run_sweep(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
