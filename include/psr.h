@@ -136,6 +136,26 @@ PSR_API int psr_get_trajectory(const void* workspace, uint32_t* out_pairs, int m
  * R_s == 0; n_max when R_p == 0 and R_s > 0.  For tests and tooling. */
 PSR_API int psr_controller_target(int n_cta, double R_s, double C_s, double R_p, double C_p, int n_min, int n_max);
 
+/* Allocation-free variant of psr_ring_attn_fwd.  No counterpart in the
+ * mKernel pages: it exists for callers that must not call cudaMalloc (a host
+ * framework whose pool owns the device memory, a plug-in that may not
+ * allocate, a latency-critical path that cannot afford cudaMalloc's implicit
+ * synchronisation).  Same arguments and layouts as psr_ring_attn_fwd, minus the
+ * workspace: the scratch is a file-scope device array of
+ * PSR_NOALLOC_SCRATCH_BYTES held by every GPU that loads the library until the
+ * process exits.  The library allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library call).
+ *   - Returns PSR_ERR_UNSUPPORTED when psr_workspace_bytes(shape) exceeds
+ *     PSR_NOALLOC_SCRATCH_BYTES (or the shape is unsupported).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - All calls on a device share the array and each call clears its control
+ *     words first; calls whose launches overlap on the GPU race on it, so order
+ *     them (one stream, or events). */
+#define PSR_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+PSR_API int psr_ring_attn_fwd_noalloc(const psr_shape* shape, const void* q, const void* k, const void* v, void* o,
+                                      float* lse, const psr_partition* part, void* stream);
+
 /* Human-readable name of a status code (static string). */
 PSR_API const char* psr_status_string(int status);
 

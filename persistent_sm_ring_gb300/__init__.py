@@ -24,7 +24,8 @@ STATIC, ADAPTIVE = 0, 1
 FAULT_NONE, FAULT_DROP_FIRST_FLAG, FAULT_SLOW_STAGING = 0, 1, 2
 
 EXPORTED = ("psr_workspace_bytes", "psr_ring_attn_fwd", "psr_ring_attn_fwd_host", "psr_get_stats",
-            "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas")
+            "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas",
+            "psr_ring_attn_fwd_noalloc")
 
 
 class Shape(ctypes.Structure):

@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libpsr.so")
-SOURCES = [os.path.join(CSRC, "psr_ring_attn.cu")]
+SOURCES = [os.path.join(CSRC, "psr_ring_attn.cu"), os.path.join(CSRC, "psr_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("psr_device.cuh", "psr_schedule.h")] + [
     os.path.join(ROOT, "include", "psr.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
