@@ -233,6 +233,8 @@ def run_ours(args):
     psr.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     wls = [ri.WORKLOADS[n] for n in WORKLOADS]
+    if args.heads:  # a smaller same-kernel case (profiling): fewer heads, same S, P, d
+        wls = [w.with_(Hq=args.heads, Hkv=args.heads) for w in wls]
     flops_step = sum(w.flops() for w in wls)
     peaks = load_peaks()
 
@@ -305,6 +307,12 @@ def run_ours(args):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     traffic = profiled_traffic()
+
+    if args.device_only:
+        if rank == 0:
+            print(json.dumps({"device_only": True, "heads": wls[0].Hq, "ms_per_step": round(ms_step, 4),
+                              "tflops": round(value, 2), "launch_ms": [round(x, 4) for x in launch_ms]}))
+        return
 
     # per-pass statistics (non-causal, causal): one more instrumented pass each
     passes = []
@@ -494,6 +502,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=96)
+    ap.add_argument("--heads", type=int, default=0, help="profiling: run the same kernel with fewer heads")
+    ap.add_argument("--device-only", action="store_true", help="profiling: timed device passes only")
     args = ap.parse_args()
     if args.sweep is not None:
         run_sweep(args)

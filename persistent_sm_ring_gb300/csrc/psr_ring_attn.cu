@@ -118,8 +118,13 @@ struct KParams {
   float c_s0, c_p0;   // prior costs (cycles per staging task / per tile) before measurements exist
 };
 
-constexpr int kWarps = 10;
-constexpr int kThreads = kWarps * 32;  // warp 0 producer, 1 MMA, 2-5 softmax tile 0, 6-9 softmax tile 1
+// Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warp 1 = MMA issuer (and TMEM owner),
+// warps 2-3 idle during compute.  Warpgroups 1 and 2: softmax of query tiles 0 and 1.
+constexpr int kWarps = 12;
+constexpr int kThreads = kWarps * 32;
+// Registers: launched at kRegsLaunch per thread; warpgroup 0 gives registers to the softmax warpgroups.
+constexpr int kRegsLaunch = 168, kRegsCtl = 72, kRegsSoftmax = 208;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
 template <int D>
 struct Cfg {
@@ -161,7 +166,7 @@ __device__ __forceinline__ void raise_error(const KParams& p, uint32_t site) {
 }
 
 // Bounded mbarrier wait: false on timeout or abort.
-__device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KParams& p, SmemCtl* sc, uint32_t site) {
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KParams& p, SmemCtl* sc, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
@@ -176,7 +181,7 @@ __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KPar
 }
 
 // Bounded wait until *flag >= want (gpu-scope acquire).
-__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t want, uint32_t& seen, const KParams& p, SmemCtl* sc) {
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t want, uint32_t& seen, const KParams& p, SmemCtl* sc) {
   seen = ld_acquire(flag);
   if (seen >= want) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -540,6 +545,57 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
   cnt.kv += (uint32_t)(2 * n);
 }
 
+// Row maximum of 128 scores with three-input max (depth 5).
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+  float v[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i) v[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+  v[42] = fmaxf(s[126], s[127]);
+  float w[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) w[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  w[14] = v[42];
+  const float x0 = fmax3(w[0], w[1], w[2]), x1 = fmax3(w[3], w[4], w[5]), x2 = fmax3(w[6], w[7], w[8]);
+  const float x3 = fmax3(w[9], w[10], w[11]), x4 = fmax3(w[12], w[13], w[14]);
+  return fmaxf(fmax3(x0, x1, x2), fmaxf(x3, x4));
+}
+
+// p = 2^(s*sl2 - m) for the 128 scores of a row, written as bf16 pairs into the
+// 64 TMEM columns at tP (16 columns at a time, so few packed values are live);
+// returns the fp32 sum of p.  When POLY, every fourth pair takes the FMA-pipe
+// polynomial instead of MUFU (off-diagonal tiles only: no -inf there).
+template <bool POLY>
+__device__ __forceinline__ float exp_row(const float (&s)[128], float sl2, float m, uint32_t tP) {
+  const uint64_t scale2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m, -m);
+  uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = blk * 16 + q;
+      const uint64_t x = fma2(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
+      float x0, x1, y0, y1;
+      f2_unpack(x, x0, x1);
+      if (POLY && (e & 3) == 3) {
+        exp2_poly_pair(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f), y0, y1);
+      } else {
+        y0 = ex2_approx(x0);
+        y1 = ex2_approx(x1);
+      }
+      acc[e & 3] = add2(acc[e & 3], f2_pack(y0, y1));
+      pk[q] = pack_bf16x2(y0, y1);
+    }
+    tmem_st16(tP + blk * 16, pk);
+  }
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  f2_unpack(acc[0], a0, a1);
+  f2_unpack(acc[1], b0, b1);
+  f2_unpack(acc[2], c0, c1);
+  f2_unpack(acc[3], d0, d1);
+  return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+}
+
 template <int D>
 __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, int i, Counters& cnt) {
   using C = Cfg<D>;
@@ -559,38 +615,39 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
   for (int t = 0; t < it.n_steps && ok; ++t) {
     const int n_kt = tiles_at_step(G, it, t);
     for (int kt = 0; kt < n_kt; ++kt, ++jglob) {
-      if (!wait_bar(&sc->s_full[i], (cnt.tiles + jglob) & 1u, p, sc, SITE_S_FULL)) { ok = false; break; }
+      // tcgen05.ld/st below are warp-collective: every lane must take the same path
+      ok = __all_sync(0xffffffffu, wait_bar(&sc->s_full[i], (cnt.tiles + jglob) & 1u, p, sc, SITE_S_FULL));
+      if (!ok) break;
       tc_fence_after();
       float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + c * 32, r);
+      {
+        uint32_t r[128];
+        tmem_ld64(tS, r);
+        tmem_ld64(tS + 64, r + 64);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+        for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(r[e]);
       }
-      // causal mask on the shard's own chunk: key position kt*128 + c > q_local
-      if (G.causal && t == 0) {
+      // causal mask on the shard's own chunk: key position kt*128 + c > q_local.  Only the
+      // tile on this query tile's diagonal (and, for query tile 0, the one after it) can hold
+      // masked keys; the test is per tile so that it is the same for every lane of the warp.
+      const bool diag = G.causal && t == 0 && kt >= 2 * it.qp + i;
+      if (diag) {
         const int lim = q_local - kt * kTileRows;
-        if (lim < 127) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > lim) s[c] = -INFINITY;
-        }
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      const float m_tile = mx * sl2;
-      // rescale only when the max grows by more than 2^8 (values below stay in range)
+      const float m_tile = row_max128(s) * sl2;
+      // raise the running max only when it grows by more than 2^8 (values below stay in range)
       const bool need = (jglob == 0) || (m_tile > m_run + 8.0f);
-      float m_new = need ? fmaxf(m_run, m_tile) : m_run;
+      const float m_new = need ? fmaxf(m_run, m_tile) : m_run;
       if (jglob > 0 && __any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-        if (!wait_bar(&sc->o_full[i], (cnt.tiles + jglob - 1) & 1u, p, sc, SITE_O_FULL)) { ok = false; break; }
+        ok = __all_sync(0xffffffffu, wait_bar(&sc->o_full[i], (cnt.tiles + jglob - 1) & 1u, p, sc, SITE_O_FULL));
+        if (!ok) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tO + c * 32, r);
@@ -598,25 +655,13 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
           tmem_st32(tO + c * 32, r);
+          tmem_st_wait();
         }
-        tmem_st_wait();
         l_run *= alpha;
       }
       m_run = m_new;
       const float m_use = m_run == -INFINITY ? 0.0f : m_run;
-      float sum = 0.0f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * e], sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * e + 1], sl2, -m_use));
-          sum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tS + h * 32, pk);
-      }
+      const float sum = diag ? exp_row<false>(s, sl2, m_use, tS) : exp_row<true>(s, sl2, m_use, tS);
       tmem_st_wait();
       l_run += sum;
       tc_fence_before();
@@ -624,9 +669,10 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
     }
   }
   const uint32_t n = jglob;
+  ok = __all_sync(0xffffffffu, ok);
   if (ok) {
     // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
-    if (!wait_bar(&sc->o_full[i], (cnt.tiles + n - 1) & 1u, p, sc, SITE_O_FULL)) ok = false;
+    ok = __all_sync(0xffffffffu, wait_bar(&sc->o_full[i], (cnt.tiles + n - 1) & 1u, p, sc, SITE_O_FULL));
   }
   if (ok) {
     tc_fence_after();
@@ -634,18 +680,18 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
     const size_t row_id = (size_t)(it.b * G.Hq + it.hq) * G.S + (size_t)it.r * G.L + q_local;
     uint16_t* orow = p.o + row_id * D;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tO + c * 32, r);
+    for (int c = 0; c < D / 64; ++c) {
+      uint32_t r[64];
+      tmem_ld64(tO + c * 64, r);
       tmem_ld_wait();
-      uint4 v4[4];
+      uint4 v4[8];
       uint32_t* w = reinterpret_cast<uint32_t*>(v4);
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
+      for (int e = 0; e < 32; ++e)
         w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-      uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+      uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dst[e] = v4[e];
+      for (int e = 0; e < 8; ++e) dst[e] = v4[e];
     }
     p.lse[row_id] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
   } else {
@@ -702,35 +748,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-
+  // Each warpgroup role runs its own loop under its own register budget; the two
+  // loops meet at the same CTA barriers at every task boundary.
   Counters cnt{0, 0, 0};
-  uint32_t stg_phase[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  bool was_staging = false;
-  long long t_task = 0;
-  uint64_t idle_since = 0;  // first idle poll of the current idle stretch (0 = not idle)
-  while (true) {
-    if (threadIdx.x == 0) {
-      decide(p, &sc, was_staging);
-      t_task = clock64();
-    }
-    __syncthreads();
-    const int cmd = sc.cmd, arg = sc.arg;
-    if (cmd == CMD_EXIT) break;
-    if (cmd == CMD_STAGE) {
-      if (threadIdx.x == 0) run_staging<D>(p, &sc, smem_base, arg, stg_phase);
-    } else if (cmd == CMD_COMPUTE) {
-      const ItemCoord it = item_coord(p.geo, arg);
-      if (warp == 0) {
-        if (lane == 0) producer<D>(p, &sc, smem_base, it, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
-      } else if (warp == 1) {
-        if (lane == 0) mma_issuer<D>(p, &sc, smem_base, it, cnt);
-      } else {
-        softmax_wg<D>(p, &sc, it, warp < 6 ? 0 : 1, cnt);
-      }
-      cnt.items++;
-      cnt.tiles += (uint32_t)item_tiles(p.geo, it);
-    } else {
+  if (warp < 4) {
+    regs_dec<kRegsCtl>();
+    uint32_t stg_phase[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    bool was_staging = false;
+    long long t_task = 0;
+    uint64_t idle_since = 0;  // first idle poll of the current idle stretch (0 = not idle)
+    while (true) {
       if (threadIdx.x == 0) {
+        decide(p, &sc, was_staging);
+        t_task = clock64();
+      }
+      __syncthreads();
+      const int cmd = sc.cmd, arg = sc.arg;
+      if (cmd == CMD_EXIT) break;
+      if (cmd == CMD_STAGE) {
+        if (threadIdx.x == 0) run_staging<D>(p, &sc, smem_base, arg, stg_phase);
+      } else if (cmd == CMD_COMPUTE) {
+        const ItemCoord it = item_coord(p.geo, arg);
+        if (warp == 0) {
+          if (lane == 0) producer<D>(p, &sc, smem_base, it, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
+        } else if (warp == 1) {
+          if (lane == 0) mma_issuer<D>(p, &sc, smem_base, it, cnt);
+        }
+        cnt.items++;
+        cnt.tiles += (uint32_t)item_tiles(p.geo, it);
+      } else if (threadIdx.x == 0) {
         atomicAdd(&p.ctrl->idle_polls, 1ull);
         // a CTA that finds no claimable work for longer than the wait bound reports it
         const uint64_t now = globaltimer_ns();
@@ -738,42 +784,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (now - idle_since > p.timeout_ns) raise_error(p, SITE_IDLE);
         nanosleep_ns(500);
       }
+      if (threadIdx.x == 0 && cmd != CMD_IDLE) idle_since = 0;
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (threadIdx.x == 0 && cmd != CMD_IDLE) {
+        const unsigned long long dt = (unsigned long long)(clock64() - t_task);
+        if (cmd == CMD_STAGE) {
+          atomicAdd(&p.ctrl->stage_cycles, dt);
+          atomicAdd(&p.ctrl->stage_done, 1ull);
+        } else {
+          const ItemCoord it = item_coord(p.geo, arg);
+          atomicAdd(&p.ctrl->compute_cycles, dt);
+          atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles(p.geo, it));
+          atomicAdd(&p.ctrl->compute_items, 1ull);
+        }
+        const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
+        if (p.mode == PSR_ADAPTIVE && (tick % (uint32_t)p.ctrl_period) == 0) controller_update(p);
+      }
     }
-    if (threadIdx.x == 0 && cmd != CMD_IDLE) idle_since = 0;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (threadIdx.x == 0 && cmd != CMD_IDLE) {
-      const unsigned long long dt = (unsigned long long)(clock64() - t_task);
-      if (cmd == CMD_STAGE) {
-        atomicAdd(&p.ctrl->stage_cycles, dt);
-        atomicAdd(&p.ctrl->stage_done, 1ull);
-      } else {
+    // drain: every tcgen05 op issued by this CTA has completed before TMEM is released
+    if (threadIdx.x == 32) {
+      mma_commit(&sc.drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&sc.drain, 0)) {
+        if (globaltimer_ns() - t0 > 100000000ull) break;
+      }
+    }
+    if (threadIdx.x == 0) {
+      bulk_wait<0>();
+      // every TMA load this CTA issued has landed (normally already true)
+      const uint64_t t0 = globaltimer_ns();
+      for (uint32_t s = 0; s < (uint32_t)C::NSTAGE && s < cnt.kv; ++s) {
+        const uint32_t fills = (cnt.kv - s + C::NSTAGE - 1) / C::NSTAGE;  // loads that used stage s
+        while (!mbar_try_wait(&sc.kv_full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else {
+    regs_inc<kRegsSoftmax>();
+    while (true) {
+      __syncthreads();
+      const int cmd = sc.cmd, arg = sc.arg;
+      if (cmd == CMD_EXIT) break;
+      if (cmd == CMD_COMPUTE) {
         const ItemCoord it = item_coord(p.geo, arg);
-        atomicAdd(&p.ctrl->compute_cycles, dt);
-        atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles(p.geo, it));
-        atomicAdd(&p.ctrl->compute_items, 1ull);
+        softmax_wg<D>(p, &sc, it, warp < 8 ? 0 : 1, cnt);
+        cnt.items++;
+        cnt.tiles += (uint32_t)item_tiles(p.geo, it);
       }
-      const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
-      if (p.mode == PSR_ADAPTIVE && (tick % (uint32_t)p.ctrl_period) == 0) controller_update(p);
-    }
-  }
-  // drain: every tcgen05 op issued by this CTA has completed before TMEM is released
-  if (threadIdx.x == 32) {
-    mma_commit(&sc.drain);
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(&sc.drain, 0)) {
-      if (globaltimer_ns() - t0 > 100000000ull) break;
-    }
-  }
-  if (threadIdx.x == 0) {
-    bulk_wait<0>();
-    // every TMA load this CTA issued has landed (normally already true)
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t s = 0; s < (uint32_t)C::NSTAGE && s < cnt.kv; ++s) {
-      const uint32_t fills = (cnt.kv - s + C::NSTAGE - 1) / C::NSTAGE;  // loads that used stage s
-      while (!mbar_try_wait(&sc.kv_full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
-      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
     }
   }
   tc_fence_before();
@@ -861,6 +923,13 @@ static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta,
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(ring_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+    if (attr_err != cudaSuccess) return;
+    // the warpgroup register split must fit inside what the launch allocates, or the
+    // increasing warpgroups would wait forever: refuse to launch otherwise
+    cudaFuncAttributes fa;
+    attr_err = cudaFuncGetAttributes(&fa, ring_attn_kernel<D>);
+    if (attr_err == cudaSuccess && fa.numRegs * kThreads < 128 * kRegsCtl + 256 * kRegsSoftmax)
+      attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
