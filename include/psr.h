@@ -87,6 +87,14 @@ typedef struct {
   unsigned long long staging_bytes;                  /* bytes written into ring slots */
   unsigned long long role_switches;
   unsigned long long idle_polls;                     /* task-boundary polls that found no work */
+  /* Per-role cycle counters, filled only by a library built with PSR_TRACE=1
+   * (zero otherwise): softmax threads waiting for S / computing (summed over
+   * warps, lane 0 each), the two MMA-issuing threads in their issue sections /
+   * the part of that spent waiting for K,V tiles, and the TMA producer waiting
+   * for free stages / for readiness flags. */
+  unsigned long long trace_softmax_wait, trace_softmax_busy;
+  unsigned long long trace_mma_issue, trace_mma_wait_kv;
+  unsigned long long trace_producer_wait_empty, trace_producer_wait_flag;
 } psr_stats;
 
 /* Bytes of device workspace psr_ring_attn_fwd needs for this shape: the

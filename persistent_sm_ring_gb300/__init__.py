@@ -13,7 +13,7 @@ import ctypes
 import os
 import threading
 
-from .build import LIB, build as _build
+from .build import LIB, LIB_TRACE, build as _build
 
 __all__ = ["build", "load", "Shape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host", "workspace_bytes",
            "get_stats", "get_trajectory", "controller_target", "num_ctas", "status_string", "PsrError",
@@ -45,7 +45,10 @@ class Stats(ctypes.Structure):
                 ("staging_cycles", ctypes.c_ulonglong), ("compute_cycles", ctypes.c_ulonglong),
                 ("staging_tasks", ctypes.c_ulonglong), ("compute_items", ctypes.c_ulonglong),
                 ("compute_tiles", ctypes.c_ulonglong), ("staging_bytes", ctypes.c_ulonglong),
-                ("role_switches", ctypes.c_ulonglong), ("idle_polls", ctypes.c_ulonglong)]
+                ("role_switches", ctypes.c_ulonglong), ("idle_polls", ctypes.c_ulonglong),
+                ("trace_softmax_wait", ctypes.c_ulonglong), ("trace_softmax_busy", ctypes.c_ulonglong),
+                ("trace_mma_issue", ctypes.c_ulonglong), ("trace_mma_wait_kv", ctypes.c_ulonglong),
+                ("trace_producer_wait_empty", ctypes.c_ulonglong), ("trace_producer_wait_flag", ctypes.c_ulonglong)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -61,20 +64,23 @@ _lib = None
 _lock = threading.Lock()
 
 
-def build(force: bool = False) -> str:
-    """Compile libpsr.so in-tree for sm_103a."""
-    return _build(force=force)
+def build(force: bool = False, trace: bool = False) -> str:
+    """Compile libpsr.so (or, with trace=True, the cycle-tracing libpsr_trace.so) in-tree for sm_103a."""
+    return _build(force=force, trace=trace)
 
 
-def load() -> ctypes.CDLL:
-    """Load libpsr.so; raises if it has not been built (no fallback path exists)."""
+def load(trace: bool = False) -> ctypes.CDLL:
+    """Load libpsr.so (or libpsr_trace.so); raises if it has not been built (no fallback path exists).
+
+    One library per process: the first call decides which."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(LIB):
-            raise RuntimeError(f"{LIB} is missing: run persistent_sm_ring_gb300.build() (nvcc, sm_103a) first")
-        lib = ctypes.CDLL(LIB)
+        path = LIB_TRACE if trace else LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: run persistent_sm_ring_gb300.build() (nvcc, sm_103a) first")
+        lib = ctypes.CDLL(path)
         vp, sz = ctypes.c_void_p, ctypes.c_size_t
         P_shape, P_part = ctypes.POINTER(Shape), ctypes.POINTER(Partition)
         lib.psr_workspace_bytes.argtypes = [P_shape]

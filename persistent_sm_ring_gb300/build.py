@@ -9,6 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libpsr.so")
+LIB_TRACE = os.path.join(HERE, "libpsr_trace.so")  # same library with per-role cycle counters
 SOURCES = [os.path.join(CSRC, "psr_ring_attn.cu"), os.path.join(CSRC, "psr_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("psr_device.cuh", "psr_schedule.h")] + [
     os.path.join(ROOT, "include", "psr.h")]
@@ -23,22 +24,23 @@ def nvcc() -> str:
     return "nvcc"
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in DEPS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the CUDA sources into persistent_sm_ring_gb300/libpsr.so."""
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Compile the CUDA sources into persistent_sm_ring_gb300/libpsr.so (libpsr_trace.so with trace=True)."""
+    lib = LIB_TRACE if trace else LIB
     with _lock:
-        if not force and not needs_build():
-            return LIB
-        tmp = LIB + f".{os.getpid()}.tmp"
+        if not force and not needs_build(lib):
+            return lib
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
                "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"),
-               *SOURCES, "-o", tmp]
+               f"-DPSR_TRACE={1 if trace else 0}", *SOURCES, "-o", tmp]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -46,5 +48,5 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
         if verbose:
             print(res.stderr)
-        os.replace(tmp, LIB)
-        return LIB
+        os.replace(tmp, lib)
+        return lib

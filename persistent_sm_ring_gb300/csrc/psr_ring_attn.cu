@@ -34,7 +34,20 @@
 #include "psr_device.cuh"
 #include "psr_schedule.h"
 
+#ifndef PSR_TRACE
+#define PSR_TRACE 0  // 1: accumulate per-role wait/compute cycles into the control block
+#endif
+
 namespace psr {
+
+constexpr bool kTrace = PSR_TRACE != 0;
+#ifndef PSR_POLY_EVERY
+#define PSR_POLY_EVERY 4
+#endif
+// One in kPolyEvery exponential pairs of an off-diagonal tile uses the FMA-pipe
+// polynomial instead of MUFU (0: none).
+constexpr int kPolyEvery = PSR_POLY_EVERY;
+__device__ __forceinline__ long long trace_clock() { return kTrace ? clock64() : 0; }
 
 // ------------------------------------------------------------------------------------------------
 // Workspace: control block + protocol arrays + ring slots (all caller-owned device memory)
@@ -60,12 +73,14 @@ struct Ctrl {
   unsigned long long stage_done, compute_items, compute_tiles;
   unsigned long long stage_bytes;
   unsigned long long role_switches, idle_polls;
-  unsigned long long pad1[6];
+  // tracing build only (cycles summed over threads that record them)
+  unsigned long long tr_softmax_wait, tr_softmax_busy, tr_mma_issue, tr_mma_wait_kv, tr_prod_wait_empty,
+      tr_prod_wait_flag;
 };
 static_assert(sizeof(Ctrl) <= 256, "control block");
 
 struct WsLayout {
-  size_t ctrl, flags, consumed, queue, traj, slot_k, slot_v, total, reset_bytes;
+  size_t ctrl, flags, consumed, claimed, queue, traj, slot_k, slot_v, total, reset_bytes;
 };
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -76,8 +91,9 @@ static WsLayout ws_layout(const Geometry& G) {
   size_t off = 0;
   w.ctrl = off; off += 256;
   w.traj = off; off = align_up(off + (size_t)kTrajMax * 8, 256);  // fixed offset: read without the shape
-  w.flags = off; off = align_up(off + n_fc * 4, 256);
+  w.flags = off; off = align_up(off + n_fc * G.n_pieces * 4, 256);  // per (group, step, piece)
   w.consumed = off; off = align_up(off + n_fc * 4, 256);
+  w.claimed = off; off = align_up(off + n_fc * 4, 256);  // pieces claimed per (group, step)
   w.queue = off; off = align_up(off + (size_t)(dynamic_staging_tasks(G) + 1) * 4, 256);
   w.reset_bytes = off;  // everything above is zeroed before each launch
   const size_t slot_elems = (size_t)2 * G.n_groups * G.L * G.d;
@@ -100,13 +116,14 @@ struct KParams {
   uint16_t* o;
   float* lse;
   Ctrl* ctrl;
-  uint32_t* flags;
-  uint32_t* consumed;
+  uint32_t* flags;     // [n_groups][P][n_pieces]: completed tiles of each staging piece
+  uint32_t* consumed;  // [n_groups][P]: items that have loaded the step's chunk
+  uint32_t* claimed;   // [n_groups][P]: staging pieces handed out
   uint32_t* queue;
   uint32_t* traj;
   unsigned long long timeout_ns;
   unsigned long long n_tiles_total;
-  unsigned long long n_stage_total;
+  unsigned long long n_stage_total;  // staging pieces in the launch
   int n_dyn;          // dynamic staging tasks
   int n_init;         // static staging list length (2 per group)
   int mode;           // PSR_STATIC / PSR_ADAPTIVE
@@ -118,8 +135,9 @@ struct KParams {
   float c_s0, c_p0;   // prior costs (cycles per staging task / per tile) before measurements exist
 };
 
-// Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warp 1 = MMA issuer (and TMEM owner),
-// warps 2-3 idle during compute.  Warpgroups 1 and 2: softmax of query tiles 0 and 1.
+// Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warps 1 and 2 = MMA issuers
+// for query tiles 0 and 1 (warp 1 also owns the TMEM allocation), warp 3 idle.
+// Warpgroups 1 and 2: softmax of query tiles 0 and 1.
 constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 // Registers: launched at kRegsLaunch per thread; warpgroup 0 gives registers to the softmax warpgroups.
@@ -239,19 +257,24 @@ __device__ void controller_update(const KParams& p) {
 // ------------------------------------------------------------------------------------------------
 // Task selection (thread 0 of the CTA)
 // ------------------------------------------------------------------------------------------------
-// Claim a staging task without ever blocking: a ready entry of the dynamic
-// queue first, else the next static (group, step 1|2) entry if its group is
-// within the lookahead window of the compute dispense frontier.
-// Returns task id g*P + step, or -1 if none is claimable now.
+// Claim a staging piece without ever blocking: from the chunk at the head of the
+// dynamic ready queue first, else from the next static (group, step 1|2) chunk if
+// its group is within the lookahead window of the compute dispense frontier.
+// Several CTAs share a chunk: each takes the next piece index; whoever takes the
+// last piece (or finds none left) moves the list head on.
+// Returns (chunk * n_pieces + piece) with chunk = g*P + step, or -1.
 __device__ int try_claim_staging(const KParams& p) {
   Ctrl* c = p.ctrl;
   const Geometry& G = p.geo;
-  for (int attempt = 0; attempt < 4; ++attempt) {
+  for (int attempt = 0; attempt < 64; ++attempt) {
     const uint32_t h = ld_relaxed(&c->q_head);
     if (h < (uint32_t)p.n_dyn) {
       const uint32_t e = ld_acquire(&p.queue[h]);
       if (e != 0) {
-        if (atom_cas_acq_rel(&c->q_head, h, h + 1) == h) return (int)(e - 1);
+        const uint32_t chunk = e - 1;
+        const uint32_t k = atomicAdd(&p.claimed[chunk], 1u);
+        if (k + 1 >= (uint32_t)G.n_pieces) atom_cas_acq_rel(&c->q_head, h, h + 1);
+        if (k < (uint32_t)G.n_pieces) return (int)(chunk * G.n_pieces + k);
         continue;
       }
     }
@@ -261,12 +284,14 @@ __device__ int try_claim_staging(const KParams& p) {
     const uint32_t disp = ld_relaxed(&c->item_next);
     const int frontier = (int)(disp / (uint32_t)G.Gs);
     if (g > frontier + p.lookahead) return -1;
-    if (atom_cas_acq_rel(&c->init_next, i, i + 1) == i) {
-      if (step < group_steps(G, g)) return g * G.P + step;
-      // shard with fewer steps: entry is a no-op, count it as done
-      attempt = -1;  // keep looking
+    if (step >= group_steps(G, g)) {  // shard with fewer steps: nothing to stage
+      atom_cas_acq_rel(&c->init_next, i, i + 1);
       continue;
     }
+    const uint32_t chunk = (uint32_t)(g * G.P + step);
+    const uint32_t k = atomicAdd(&p.claimed[chunk], 1u);
+    if (k + 1 >= (uint32_t)G.n_pieces) atom_cas_acq_rel(&c->init_next, i, i + 1);
+    if (k < (uint32_t)G.n_pieces) return (int)(chunk * G.n_pieces + k);
   }
   return -1;
 }
@@ -312,18 +337,21 @@ template <int D>
 __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, int task, uint32_t (&stg_phase)[8]) {
   using C = Cfg<D>;
   const Geometry& G = p.geo;
-  const int g = task / G.P, step = task % G.P;
+  const int chunk = task / G.n_pieces, piece = task % G.n_pieces;
+  const int g = chunk / G.P, step = chunk % G.P;
   int r, b, kvh, sub;
   group_coord(G, g, r, b, kvh, sub);
   const int j = ((r - step) % G.P + G.P) % G.P;
   const size_t tile_elems = (size_t)kTileRows * D;
-  const uint16_t* src_k = p.k + ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L) * D;
-  const uint16_t* src_v = p.v + ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L) * D;
-  const size_t slot_off = ((size_t)(step & 1) * G.n_groups + g) * (size_t)G.L * D;
+  const int kt0 = piece * G.piece_tiles;
+  const int n_kt = (G.kv_tiles - kt0) < G.piece_tiles ? (G.kv_tiles - kt0) : G.piece_tiles;
+  const size_t src_off = ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L + (size_t)kt0 * kTileRows) * D;
+  const uint16_t* src_k = p.k + src_off;
+  const uint16_t* src_v = p.v + src_off;
+  const size_t slot_off = (((size_t)(step & 1) * G.n_groups + g) * (size_t)G.L + (size_t)kt0 * kTileRows) * D;
   uint16_t* dst_k = p.slot_k + slot_off;
   uint16_t* dst_v = p.slot_v + slot_off;
-  uint32_t* flag = p.flags + (size_t)g * G.P + step;
-  const int n_kt = G.kv_tiles;
+  uint32_t* flag = p.flags + (size_t)chunk * G.n_pieces + piece;
   const bool drop = (p.fault == PSR_FAULT_DROP_FIRST_FLAG) && (atomicAdd(&p.ctrl->fault_count, 1u) == 0u);
   if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
   // staging "acquire": queue entries were published with release after the slot's
@@ -396,10 +424,12 @@ __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, uint32_t dst
   for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * 16384, tm, 64 * h, row, bar);
 }
 
+// Returns the cycles spent waiting for readiness flags (time the item was starved of
+// staged data), which the controller does not count as compute cost.
 template <int D>
-__device__ void producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it,
-                         const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                         const CUtensorMap* tm_sk, const CUtensorMap* tm_sv, Counters& cnt) {
+__device__ long long producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it,
+                              const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                              const CUtensorMap* tm_sk, const CUtensorMap* tm_sv, Counters& cnt) {
   using C = Cfg<D>;
   const Geometry& G = p.geo;
   const uint32_t sQ = smem_base, sStage = smem_base + 2 * C::QT;
@@ -434,6 +464,8 @@ __device__ void producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, cons
     return true;
   };
   bool ok = true;
+  unsigned long long tr_empty = 0;
+  long long starved = 0;
   for (int t = 0; t < it.n_steps && ok; ++t) {
     const int j = ((it.r - t) % G.P + G.P) % G.P;
     const int n_kt = tiles_at_step(G, it, t);
@@ -441,11 +473,15 @@ __device__ void producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, cons
     const CUtensorMap* mv = t == 0 ? tm_v : tm_sv;
     const int row0 = t == 0 ? (it.b * G.Hkv + it.kvh) * G.S + j * G.L
                             : ((t & 1) * G.n_groups + it.g) * G.L;
-    const uint32_t* flag = p.flags + (size_t)it.g * G.P + t;
+    const uint32_t* flags = p.flags + ((size_t)it.g * G.P + t) * G.n_pieces;
     uint32_t seen = 0;
     for (int kt = 0; kt < n_kt && ok; ++kt) {
-      if (t > 0 && seen < (uint32_t)(kt + 1)) {
-        if (!wait_flag(flag, (uint32_t)(kt + 1), seen, p, sc)) { ok = false; break; }
+      const int pc = kt / G.piece_tiles, in_pc = kt % G.piece_tiles;
+      if (in_pc == 0) seen = 0;
+      if (t > 0 && seen < (uint32_t)(in_pc + 1)) {
+        const long long f0 = clock64();
+        if (!wait_flag(flags + pc, (uint32_t)(in_pc + 1), seen, p, sc)) { ok = false; break; }
+        starved += clock64() - f0;
         fence_proxy_async_global();  // acquire (generic) before the async-proxy reads of the slot
       }
       for (int kv = 0; kv < 2; ++kv) {
@@ -457,7 +493,9 @@ __device__ void producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, cons
         }
         if (!ok) break;
         if (pend_n > 0) resolve_one(false);
+        const long long e0 = trace_clock();
         if (fill > 0 && !wait_bar(&sc->kv_empty[stage], (fill - 1) & 1u, p, sc, SITE_KV_EMPTY)) { ok = false; break; }
+        tr_empty += trace_clock() - e0;
         mbar_expect_tx(&sc->kv_full[stage], C::QT);
         load_kv_tile<D>(kv == 0 ? mk : mv, sStage + stage * C::QT, row0 + kt * kTileRows, &sc->kv_full[stage]);
         cnt.kv++;
@@ -472,77 +510,85 @@ __device__ void producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, cons
   }
   while (ok && pend_n > 0)
     if (!resolve_one(true)) ok = false;
+  if (kTrace) {
+    atomicAdd(&p.ctrl->tr_prod_wait_empty, tr_empty);
+    atomicAdd(&p.ctrl->tr_prod_wait_flag, (unsigned long long)starved);
+  }
   if (!ok) sc->abort = 1;
+  return starved;
 }
 
+// Tensor-core issue for query tile i, run by one thread of its own warp (warp 1 + i).
+// Two issuers, one per tile, so that a tile whose P is ready never waits behind
+// the other tile's burst: the tensor core's instruction queue is only a few
+// MMAs deep, so an issuing thread stays busy for about as long as its MMAs run.
+// Order per tile: S_i(0); then for each KV tile j: PV_i(j) (reads P_i(j), which
+// overlays S_i(j) in tensor memory) and S_i(j+1) right behind it.
 template <int D>
-__device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, Counters& cnt) {
+__device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, int i,
+                           Counters& cnt) {
   using C = Cfg<D>;
   const Geometry& G = p.geo;
-  const uint32_t tb = sc->tmem_base;
-  const uint32_t sQ = smem_base, sStage = smem_base + 2 * C::QT;
   constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false);
   constexpr uint32_t IPV = idesc_bf16_f32(128, D, true);
-  long long n = item_tiles(G, it);
-  const uint32_t qpar = cnt.items & 1u;
-  if (!wait_bar(&sc->q_full[0], qpar, p, sc, SITE_Q_FULL) || !wait_bar(&sc->q_full[1], qpar, p, sc, SITE_Q_FULL)) {
+  constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // 8-row (K-major) / 8-key (V, MN-major) groups 1024 B apart
+  const uint32_t sStage = smem_base + 2 * C::QT;
+  const uint32_t q_lo = sdesc_lo(smem_base + i * C::QT, 16);
+  const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
+  const uint32_t tO = sc->tmem_base + (i ? C::COL_O1 : C::COL_O0);
+  auto stage_of = [](uint32_t c) { return c % C::NSTAGE; };
+  auto par_of = [](uint32_t c) { return (c / C::NSTAGE) & 1u; };
+  auto issue_s = [&](uint32_t kstage) {
+    const uint32_t b_lo = sdesc_lo(sStage + kstage * C::QT, 16);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+      mma_ss_w(tS, q_lo + off, kHi, b_lo + off, kHi, IQK, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(&sc->s_full[i]);
+    mma_commit(&sc->kv_empty[kstage]);
+  };
+  auto issue_pv = [&](uint32_t vstage, bool first) {
+    const uint32_t b_lo = sdesc_lo(sStage + vstage * C::QT, 16384);  // V halves of 64 columns 16 KB apart
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ts_w(tO, tS + kk * 8, b_lo + kk * (2048 >> 4), kHi, IPV, (first && kk == 0) ? 0u : 1u);
+    mma_commit(&sc->o_full[i]);
+    mma_commit(&sc->kv_empty[vstage]);
+  };
+  const uint32_t n = (uint32_t)item_tiles(G, it);
+  uint32_t ck = cnt.kv;  // load index of K_0 of this item (the producer loads K_j, V_j alternately)
+  cnt.kv += 2u * n;
+  unsigned long long tr_issue = 0, tr_kv = 0;
+  if (!wait_bar(&sc->q_full[i], cnt.items & 1u, p, sc, SITE_Q_FULL) ||
+      !wait_bar(&sc->kv_full[stage_of(ck)], par_of(ck), p, sc, SITE_KV_FULL)) {
     sc->abort = 1;
     return;
   }
   tc_fence_after();
-  auto issue_s = [&](int i, uint32_t kstage) {
-    const uint32_t a0 = sQ + i * C::QT, b0 = sStage + kstage * C::QT;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-      mma_ss(tb + (i ? C::COL_S1 : C::COL_S0), sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), IQK,
-             kk > 0 ? 1u : 0u);
-    }
-    mma_commit(&sc->s_full[i]);
-  };
-  auto issue_pv = [&](int i, uint32_t vstage, bool first) {
-    const uint32_t b0 = sStage + vstage * C::QT;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      mma_ts(tb + (i ? C::COL_O1 : C::COL_O0), tb + (i ? C::COL_S1 : C::COL_S0) + kk * 8,
-             sdesc_sw128(b0 + kk * 2048, 16384, 1024), IPV, (first && kk == 0) ? 0u : 1u);
-    }
-    mma_commit(&sc->o_full[i]);
-  };
-  auto stage_of = [](uint32_t c) { return c % C::NSTAGE; };
-  auto par_of = [](uint32_t c) { return (c / C::NSTAGE) & 1u; };
-  // prologue: S0_0, S1_0
-  uint32_t ck = cnt.kv;  // load index of K_0
-  if (!wait_bar(&sc->kv_full[stage_of(ck)], par_of(ck), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
-  tc_fence_after();
-  issue_s(0, stage_of(ck));
-  issue_s(1, stage_of(ck));
-  mma_commit(&sc->kv_empty[stage_of(ck)]);
-  for (long long jt = 0; jt < n; ++jt) {
-    const uint32_t cv = ck + 1;      // V_j
-    const uint32_t cn = ck + 2;      // K_{j+1}
-    const bool more = jt + 1 < n;
+  issue_s(stage_of(ck));
+  for (uint32_t jt = 0; jt < n; ++jt, ck += 2) {
+    const uint32_t cv = ck + 1, cn = ck + 2;  // V_j, K_{j+1}
+    const long long a0 = trace_clock();
     if (!wait_bar(&sc->kv_full[stage_of(cv)], par_of(cv), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
-    // P0_j ready
-    if (!wait_bar(&sc->p_full[0], (cnt.tiles + (uint32_t)jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
+    const long long a1 = trace_clock();
+    if (!wait_bar(&sc->p_full[i], (cnt.tiles + jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
+    const long long a2 = trace_clock();
     tc_fence_after();
-    issue_pv(0, stage_of(cv), jt == 0);
-    if (more) {
+    issue_pv(stage_of(cv), jt == 0);
+    if (jt + 1 < n) {
+      const long long b0 = trace_clock();
       if (!wait_bar(&sc->kv_full[stage_of(cn)], par_of(cn), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
-      tc_fence_after();
-      issue_s(0, stage_of(cn));
+      tr_kv += trace_clock() - b0;
+      issue_s(stage_of(cn));
     }
-    if (!wait_bar(&sc->p_full[1], (cnt.tiles + (uint32_t)jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
-    tc_fence_after();
-    issue_pv(1, stage_of(cv), jt == 0);
-    mma_commit(&sc->kv_empty[stage_of(cv)]);
-    if (more) {
-      issue_s(1, stage_of(cn));
-      mma_commit(&sc->kv_empty[stage_of(cn)]);
-    }
-    ck = cn;
+    tr_kv += a1 - a0;
+    tr_issue += trace_clock() - a2;
   }
-  cnt.kv += (uint32_t)(2 * n);
+  if (kTrace) {
+    atomicAdd(&p.ctrl->tr_mma_issue, tr_issue);
+    atomicAdd(&p.ctrl->tr_mma_wait_kv, tr_kv);
+  }
 }
 
 // Row maximum of 128 scores with three-input max (depth 5).
@@ -577,7 +623,7 @@ __device__ __forceinline__ float exp_row(const float (&s)[128], float sl2, float
       const uint64_t x = fma2(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
       float x0, x1, y0, y1;
       f2_unpack(x, x0, x1);
-      if (POLY && (e & 3) == 3) {
+      if (POLY && kPolyEvery > 0 && (e % kPolyEvery) == kPolyEvery - 1) {
         exp2_poly_pair(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f), y0, y1);
       } else {
         y0 = ex2_approx(x0);
@@ -596,6 +642,7 @@ __device__ __forceinline__ float exp_row(const float (&s)[128], float sl2, float
   return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
 }
 
+// One softmax warpgroup per 128-row query tile i.
 template <int D>
 __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, int i, Counters& cnt) {
   using C = Cfg<D>;
@@ -612,12 +659,16 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
   float l_run = 0.0f;
   uint32_t jglob = 0;
   bool ok = true;
+  unsigned long long tr_wait = 0, tr_busy = 0;
   for (int t = 0; t < it.n_steps && ok; ++t) {
     const int n_kt = tiles_at_step(G, it, t);
     for (int kt = 0; kt < n_kt; ++kt, ++jglob) {
+      const long long c0 = trace_clock();
       // tcgen05.ld/st below are warp-collective: every lane must take the same path
       ok = __all_sync(0xffffffffu, wait_bar(&sc->s_full[i], (cnt.tiles + jglob) & 1u, p, sc, SITE_S_FULL));
       if (!ok) break;
+      const long long c1 = trace_clock();
+      tr_wait += c1 - c0;
       tc_fence_after();
       float s[128];
       {
@@ -665,8 +716,13 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
       tmem_st_wait();
       l_run += sum;
       tc_fence_before();
-      mbar_arrive(&sc->p_full[i]);
+      mbar_arrive(&sc->p_full[i]);  // this thread's row of P is in tensor memory
+      tr_busy += trace_clock() - c1;
     }
+  }
+  if (kTrace && lane == 0) {
+    atomicAdd(&p.ctrl->tr_softmax_wait, tr_wait);
+    atomicAdd(&p.ctrl->tr_softmax_busy, tr_busy);
   }
   const uint32_t n = jglob;
   ok = __all_sync(0xffffffffu, ok);
@@ -717,15 +773,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sc.q_full[i], 1);
       mbar_init(&sc.s_full[i], 1);
-      mbar_init(&sc.p_full[i], 128);
+      mbar_init(&sc.p_full[i], 128);  // every softmax thread of tile i arrives once per KV tile
       mbar_init(&sc.o_full[i], 1);
     }
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&sc.kv_full[s], 1);
-      mbar_init(&sc.kv_empty[s], 1);
+      mbar_init(&sc.kv_empty[s], 2);  // both softmax warpgroups commit their reads of every K/V tile
     }
     for (int s = 0; s < C::NB; ++s) mbar_init(&sc.stg[s], 1);
-    mbar_init(&sc.drain, 1);
+    mbar_init(&sc.drain, 2);  // one commit from each warpgroup's MMA-issuing thread
     sc.abort = 0;
     fence_barrier_init();
     if (blockIdx.x == 0) {
@@ -755,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kRegsCtl>();
     uint32_t stg_phase[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     bool was_staging = false;
-    long long t_task = 0;
+    long long t_task = 0, starved = 0;
     uint64_t idle_since = 0;  // first idle poll of the current idle stretch (0 = not idle)
     while (true) {
       if (threadIdx.x == 0) {
@@ -769,11 +825,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) run_staging<D>(p, &sc, smem_base, arg, stg_phase);
       } else if (cmd == CMD_COMPUTE) {
         const ItemCoord it = item_coord(p.geo, arg);
-        if (warp == 0) {
-          if (lane == 0) producer<D>(p, &sc, smem_base, it, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
-        } else if (warp == 1) {
-          if (lane == 0) mma_issuer<D>(p, &sc, smem_base, it, cnt);
-        }
+        if (warp == 0 && lane == 0)
+          starved = producer<D>(p, &sc, smem_base, it, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
+        else if ((warp == 1 || warp == 2) && lane == 0)
+          mma_issuer<D>(p, &sc, smem_base, it, warp - 1, cnt);
         cnt.items++;
         cnt.tiles += (uint32_t)item_tiles(p.geo, it);
       } else if (threadIdx.x == 0) {
@@ -789,7 +844,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       tc_fence_after();
       if (threadIdx.x == 0 && cmd != CMD_IDLE) {
-        const unsigned long long dt = (unsigned long long)(clock64() - t_task);
+        long long busy = clock64() - t_task;
+        if (cmd == CMD_COMPUTE) busy -= starved;  // compute cost excludes waiting for staged data
+        const unsigned long long dt = (unsigned long long)(busy > 0 ? busy : 0);
         if (cmd == CMD_STAGE) {
           atomicAdd(&p.ctrl->stage_cycles, dt);
           atomicAdd(&p.ctrl->stage_done, 1ull);
@@ -804,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // drain: every tcgen05 op issued by this CTA has completed before TMEM is released
-    if (threadIdx.x == 32) {
+    if ((warp == 1 || warp == 2) && lane == 0) {
       mma_commit(&sc.drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(&sc.drain, 0)) {
@@ -1021,11 +1078,12 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
   kp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
   kp.consumed = reinterpret_cast<uint32_t*>(ws + L.consumed);
+  kp.claimed = reinterpret_cast<uint32_t*>(ws + L.claimed);
   kp.queue = reinterpret_cast<uint32_t*>(ws + L.queue);
   kp.traj = reinterpret_cast<uint32_t*>(ws + L.traj);
   kp.timeout_ns = (unsigned long long)(pt.timeout_ms > 0 ? pt.timeout_ms : 2000) * 1000000ull;
   kp.n_tiles_total = (unsigned long long)total_tiles(G);
-  kp.n_stage_total = (unsigned long long)total_staging_tasks(G);
+  kp.n_stage_total = (unsigned long long)total_staging_tasks(G) * (unsigned long long)G.n_pieces;
   kp.n_dyn = (int)dynamic_staging_tasks(G);
   kp.n_init = 2 * G.n_groups;
   kp.mode = pt.mode;
@@ -1039,9 +1097,9 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.n_min = n_min;
   kp.n_max = n_max;
   const bool any_staging = kp.n_stage_total > 0;
-  // costs before any measurement: a staging task moves 2*L*d*2 bytes at ~100 GB/s per SM;
+  // costs before any measurement: a staging piece moves 2*piece_rows*d*2 bytes at ~48 GB/s per SM;
   // a compute tile pair is 4*128*128*d flops at ~60 % of an SM's dense bf16 rate (8192 flop/clk)
-  kp.c_s0 = (float)((2.0 * G.L * G.d * 2.0) / 100e9 * 1.9e9);
+  kp.c_s0 = (float)((2.0 * G.piece_tiles * kTileRows * G.d * 2.0) / 48e9 * 1.9e9);
   kp.c_p0 = (float)(4.0 * 128.0 * 128.0 * G.d / (0.6 * 8192.0));
   int n_s;
   if (pt.mode == PSR_STATIC) {
@@ -1129,6 +1187,12 @@ int psr_get_stats(const void* workspace, psr_stats* out, void* stream) {
   out->staging_bytes = c.stage_bytes;
   out->role_switches = c.role_switches;
   out->idle_polls = c.idle_polls;
+  out->trace_softmax_wait = c.tr_softmax_wait;
+  out->trace_softmax_busy = c.tr_softmax_busy;
+  out->trace_mma_issue = c.tr_mma_issue;
+  out->trace_mma_wait_kv = c.tr_mma_wait_kv;
+  out->trace_producer_wait_empty = c.tr_prod_wait_empty;
+  out->trace_producer_wait_flag = c.tr_prod_wait_flag;
   out->n_s_initial = (int)c.ns_initial;
   if (out->n_s_final < 0) out->n_s_final = out->n_s_initial;
   return out->status;

@@ -13,9 +13,12 @@
 //  * group         = the items that read the same ring slot: shard r, batch b,
 //                    KV head kvh (all Hq/Hkv query heads of it) and, when a
 //                    group would exceed the deadlock bound, a sub-group index;
-//  * staging task  = one (group, step >= 1): copy chunk (r - step) mod P of
-//                    K and V into the group's slot (step & 1), 128-row tiles;
-//                    the pages' ring moves KV in 128-row tiles (Table 3).
+//  * staging chunk = one (group, step >= 1): chunk (r - step) mod P of K and V
+//                    copied into the group's slot (step & 1) in 128-row tiles
+//                    (the pages' ring moves KV in 128-row tiles, Table 3);
+//  * staging piece = kStagePieceTiles consecutive tiles of a chunk: the unit a
+//                    staging CTA claims, so that several CTAs fill one chunk at
+//                    once; readiness is published per piece as a tile count.
 // Slot (step & 1) of a group may be overwritten for step s >= 3 only when all
 // of the group's items have loaded step s - 2: that is the double buffer's
 // back-pressure.
@@ -32,6 +35,7 @@ namespace psr {
 
 constexpr int kTileRows = 128;  // rows per Q tile and per KV tile
 constexpr int kItemRows = 256;  // query rows per compute item (two tiles)
+constexpr int kStagePieceTiles = 4;  // tiles per staging piece
 
 struct Geometry {
   int B, Hq, Hkv, S, P, d, causal;
@@ -39,6 +43,8 @@ struct Geometry {
   int gqa;       // Hq / Hkv
   int q_pairs;   // items per (b, hq, shard): L / 256
   int kv_tiles;  // 128-row KV tiles per chunk: L / 128
+  int piece_tiles;  // tiles per staging piece
+  int n_pieces;     // staging pieces per chunk
   int G;         // items sharing one (shard, b, kvh): gqa * q_pairs
   int n_sub;     // sub-groups per (shard, b, kvh)
   int Gs;        // items per group: G / n_sub
@@ -61,6 +67,8 @@ PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int 
   G.gqa = Hq / Hkv;
   G.q_pairs = G.L / kItemRows;
   G.kv_tiles = G.L / kTileRows;
+  G.piece_tiles = G.kv_tiles < kStagePieceTiles ? G.kv_tiles : kStagePieceTiles;
+  G.n_pieces = (G.kv_tiles + G.piece_tiles - 1) / G.piece_tiles;
   G.G = G.gqa * G.q_pairs;
   // split a group into power-of-two sub-groups until it fits the bound
   G.n_sub = 1;
