@@ -42,11 +42,20 @@ namespace psr {
 
 constexpr bool kTrace = PSR_TRACE != 0;
 #ifndef PSR_POLY_EVERY
-#define PSR_POLY_EVERY 4
+#define PSR_POLY_EVERY 0
 #endif
 // One in kPolyEvery exponential pairs of an off-diagonal tile uses the FMA-pipe
-// polynomial instead of MUFU (0: none).
+// polynomial instead of MUFU (0: none).  Off by default: measured on GB300, the
+// polynomial's dense FMA-pipe instruction stream starves the warp that issues
+// tcgen05.mma on the same SM sub-partition (issue rate halves under dense FMA
+// neighbours, not under MUFU-bound ones), which costs more than it saves.
 constexpr int kPolyEvery = PSR_POLY_EVERY;
+#ifndef PSR_MMA_ISSUERS
+#define PSR_MMA_ISSUERS 1
+#endif
+// Threads issuing tcgen05.mma: 1 (both query tiles, interleaved) or 2 (one per tile).
+constexpr int kMmaIssuers = PSR_MMA_ISSUERS;
+static_assert(kMmaIssuers == 1 || kMmaIssuers == 2, "one or two MMA issuers");
 __device__ __forceinline__ long long trace_clock() { return kTrace ? clock64() : 0; }
 
 // ------------------------------------------------------------------------------------------------
@@ -56,9 +65,9 @@ constexpr int kTrajMax = 4096;
 
 struct Ctrl {
   uint32_t item_next;     // compute items dispensed
-  uint32_t init_next;     // static staging list dispensed (steps 1 and 2 of every group)
-  uint32_t q_head;        // dynamic ready queue: next entry to take
-  uint32_t q_tail;        // dynamic ready queue: next entry to fill
+  uint32_t init_next;     // static staging list: next piece to hand out (steps 1 and 2 of every group)
+  uint32_t q_head;        // ready queue: next ticket
+  uint32_t q_tail;        // ready queue: next entry to fill
   uint32_t target_ns;     // controller target + 1 (0 = not yet set)
   uint32_t error;         // first error site (0 = none)
   uint32_t abort;         // set on any error: every CTA drains and exits
@@ -69,10 +78,12 @@ struct Ctrl {
   uint32_t fault_count;
   uint32_t pad0[3];
   unsigned long long t0_ns;  // launch start (first CTA)
+  unsigned long long last_eval_ns;  // last controller evaluation
   unsigned long long stage_cycles, compute_cycles;
   unsigned long long stage_done, compute_items, compute_tiles;
   unsigned long long stage_bytes;
   unsigned long long role_switches, idle_polls;
+  unsigned long long starve_cycles;  // compute cycles spent waiting for ring steps >= 3 to be staged
   // tracing build only (cycles summed over threads that record them)
   unsigned long long tr_softmax_wait, tr_softmax_busy, tr_mma_issue, tr_mma_wait_kv, tr_prod_wait_empty,
       tr_prod_wait_flag;
@@ -80,7 +91,7 @@ struct Ctrl {
 static_assert(sizeof(Ctrl) <= 256, "control block");
 
 struct WsLayout {
-  size_t ctrl, flags, consumed, claimed, queue, traj, slot_k, slot_v, total, reset_bytes;
+  size_t ctrl, flags, consumed, queue, traj, slot_k, slot_v, total, reset_bytes;
 };
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -93,8 +104,7 @@ static WsLayout ws_layout(const Geometry& G) {
   w.traj = off; off = align_up(off + (size_t)kTrajMax * 8, 256);  // fixed offset: read without the shape
   w.flags = off; off = align_up(off + n_fc * G.n_pieces * 4, 256);  // per (group, step, piece)
   w.consumed = off; off = align_up(off + n_fc * 4, 256);
-  w.claimed = off; off = align_up(off + n_fc * 4, 256);  // pieces claimed per (group, step)
-  w.queue = off; off = align_up(off + (size_t)(dynamic_staging_tasks(G) + 1) * 4, 256);
+  w.queue = off; off = align_up(off + (size_t)(dynamic_staging_tasks(G) * G.n_pieces + 1) * 4, 256);
   w.reset_bytes = off;  // everything above is zeroed before each launch
   const size_t slot_elems = (size_t)2 * G.n_groups * G.L * G.d;
   w.slot_k = off; off = align_up(off + slot_elems * 2, 256);
@@ -118,14 +128,13 @@ struct KParams {
   Ctrl* ctrl;
   uint32_t* flags;     // [n_groups][P][n_pieces]: completed tiles of each staging piece
   uint32_t* consumed;  // [n_groups][P]: items that have loaded the step's chunk
-  uint32_t* claimed;   // [n_groups][P]: staging pieces handed out
   uint32_t* queue;
   uint32_t* traj;
   unsigned long long timeout_ns;
   unsigned long long n_tiles_total;
   unsigned long long n_stage_total;  // staging pieces in the launch
-  int n_dyn;          // dynamic staging tasks
-  int n_init;         // static staging list length (2 per group)
+  int n_dyn;          // ready-queue entries: pieces of the steps >= 3
+  int n_init;         // static list entries: pieces of steps 1 and 2 of every group
   int mode;           // PSR_STATIC / PSR_ADAPTIVE
   int n_s_init;
   int n_min, n_max;   // effective clamp
@@ -135,8 +144,8 @@ struct KParams {
   float c_s0, c_p0;   // prior costs (cycles per staging task / per tile) before measurements exist
 };
 
-// Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warps 1 and 2 = MMA issuers
-// for query tiles 0 and 1 (warp 1 also owns the TMEM allocation), warp 3 idle.
+// Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warp 1 (and warp 2 when two
+// issuers are built) = MMA issuer(s) (warp 1 also owns the TMEM allocation), others idle.
 // Warpgroups 1 and 2: softmax of query tiles 0 and 1.
 constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
@@ -225,8 +234,16 @@ __device__ int current_target(const KParams& p) {
   return t ? (int)(t - 1) : p.n_s_init;
 }
 
+constexpr unsigned long long kCtrlMinIntervalNs = 20000;  // re-evaluate at most every 20 us
+
 __device__ void controller_update(const KParams& p) {
   Ctrl* c = p.ctrl;
+  {
+    const unsigned long long now = globaltimer_ns();
+    const unsigned long long last = atomicAdd(&c->last_eval_ns, 0ull);
+    if (now - last < kCtrlMinIntervalNs) return;
+    if (atomicCAS(&c->last_eval_ns, last, now) != last) return;  // another CTA evaluates now
+  }
   const unsigned long long sd = atomicAdd(&c->stage_done, 0ull);
   const unsigned long long td = atomicAdd(&c->compute_tiles, 0ull);
   const unsigned long long scy = atomicAdd(&c->stage_cycles, 0ull);
@@ -234,14 +251,24 @@ __device__ void controller_update(const KParams& p) {
   const double R_s = (double)(p.n_stage_total > sd ? p.n_stage_total - sd : 0);
   const double R_p = (double)(p.n_tiles_total > td ? p.n_tiles_total - td : 0);
   // measured cost per unit, blended with the prior until a few units are measured
-  const double C_s = (scy + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
+  // The staging cost per piece counts the staging CTAs' busy cycles plus the cycles
+  // compute items spent starved of staged data: both are what staging costs the launch.
+  const unsigned long long sv = atomicAdd(&c->starve_cycles, 0ull);
+  const double C_s = (scy + (double)sv + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
   const double C_p = (ccy + (double)p.c_p0 * 64.0) / ((double)td + 64.0);
   int n = controller_rule((int)gridDim.x, R_s, C_s, R_p, C_p, p.n_min, p.n_max);
   const int cur = current_target(p);
-  // hysteresis: move only by a margin unless the staging work is finished
+  // hysteresis (move only by a margin unless the staging work is finished) and a rate
+  // limit (each evaluation moves the target by at most max(2, cur/8) CTAs): a CTA changes
+  // role only at a task boundary, so a target that jumps around costs whole tasks
   const int margin = 1 + cur / 16;
   if (n != 0 && n > cur - margin && n < cur + margin) return;
   if (n == cur) return;
+  if (n != 0) {
+    const int step = cur / 8 > 2 ? cur / 8 : 2;
+    if (n > cur + step) n = cur + step;
+    if (n < cur - step) n = cur - step;
+  }
   st_relaxed(&c->target_ns, (uint32_t)n + 1u);
   atomicMax(&c->ns_min_inv, 0xFFFFu - (uint32_t)n);
   atomicMax(&c->ns_max, (uint32_t)n);
@@ -257,62 +284,91 @@ __device__ void controller_update(const KParams& p) {
 // ------------------------------------------------------------------------------------------------
 // Task selection (thread 0 of the CTA)
 // ------------------------------------------------------------------------------------------------
-// Claim a staging piece without ever blocking: from the chunk at the head of the
-// dynamic ready queue first, else from the next static (group, step 1|2) chunk if
-// its group is within the lookahead window of the compute dispense frontier.
-// Several CTAs share a chunk: each takes the next piece index; whoever takes the
-// last piece (or finds none left) moves the list head on.
-// Returns (chunk * n_pieces + piece) with chunk = g*P + step, or -1.
-__device__ int try_claim_staging(const KParams& p) {
+// Staging work comes from two lists, each claimed with one atomicAdd (a ticket):
+//  * the static list: pieces of steps 1 and 2 of every group, in group order (their
+//    slots are fresh); taken only while the group is within the lookahead window
+//    of the compute dispense frontier;
+//  * the ready queue: pieces of steps >= 3, pushed by the compute CTA whose load
+//    completed the consumption of the slot they overwrite.  A ticket names one
+//    queue entry; the stager that holds it serves that entry once it has been
+//    published and does static work meanwhile, so no stager ever blocks and no
+//    claim ever retries.
+// A task is (chunk * n_pieces + piece) with chunk = g*P + step.
+struct StageTicket {
+  int held = -1;     // queue entry this CTA owns, or -1
+  bool done = false; // every queue entry has been handed out
+};
+
+__device__ int claim_static_piece(const KParams& p) {
   Ctrl* c = p.ctrl;
   const Geometry& G = p.geo;
-  for (int attempt = 0; attempt < 64; ++attempt) {
-    const uint32_t h = ld_relaxed(&c->q_head);
-    if (h < (uint32_t)p.n_dyn) {
-      const uint32_t e = ld_acquire(&p.queue[h]);
-      if (e != 0) {
-        const uint32_t chunk = e - 1;
-        const uint32_t k = atomicAdd(&p.claimed[chunk], 1u);
-        if (k + 1 >= (uint32_t)G.n_pieces) atom_cas_acq_rel(&c->q_head, h, h + 1);
-        if (k < (uint32_t)G.n_pieces) return (int)(chunk * G.n_pieces + k);
-        continue;
-      }
-    }
-    const uint32_t i = ld_relaxed(&c->init_next);
+  for (int attempt = 0; attempt < 8; ++attempt) {
+    const uint32_t i0 = ld_relaxed(&c->init_next);
+    if (i0 >= (uint32_t)p.n_init) return -1;
+    const int g0 = (int)(i0 / (2u * G.n_pieces));
+    const int frontier = (int)(ld_relaxed(&c->item_next) / (uint32_t)G.Gs);
+    if (g0 > frontier + p.lookahead) return -1;
+    const uint32_t i = atomicAdd(&c->init_next, 1u);
     if (i >= (uint32_t)p.n_init) return -1;
-    const int g = (int)(i / 2), step = 1 + (int)(i % 2);
-    const uint32_t disp = ld_relaxed(&c->item_next);
-    const int frontier = (int)(disp / (uint32_t)G.Gs);
-    if (g > frontier + p.lookahead) return -1;
-    if (step >= group_steps(G, g)) {  // shard with fewer steps: nothing to stage
-      atom_cas_acq_rel(&c->init_next, i, i + 1);
-      continue;
-    }
-    const uint32_t chunk = (uint32_t)(g * G.P + step);
-    const uint32_t k = atomicAdd(&p.claimed[chunk], 1u);
-    if (k + 1 >= (uint32_t)G.n_pieces) atom_cas_acq_rel(&c->init_next, i, i + 1);
-    if (k < (uint32_t)G.n_pieces) return (int)(chunk * G.n_pieces + k);
+    const int g = (int)(i / (2u * G.n_pieces));
+    const int step = 1 + (int)((i / G.n_pieces) % 2u);
+    const int piece = (int)(i % G.n_pieces);
+    if (step < group_steps(G, g)) return (g * G.P + step) * G.n_pieces + piece;
+    // shard with fewer steps: nothing to stage for this entry; try the next one
   }
   return -1;
 }
 
-__device__ bool staging_all_claimed(const KParams& p) {
-  return ld_relaxed(&p.ctrl->init_next) >= (uint32_t)p.n_init && ld_relaxed(&p.ctrl->q_head) >= (uint32_t)p.n_dyn;
+__device__ int try_claim_staging(const KParams& p, StageTicket& tk) {
+  Ctrl* c = p.ctrl;
+  if (tk.held >= 0) {
+    const uint32_t e = ld_acquire(&p.queue[tk.held]);
+    if (e != 0) {
+      tk.held = -1;
+      return (int)(e - 1);
+    }
+  }
+  const int t = claim_static_piece(p);
+  if (t >= 0) return t;
+  if (tk.held < 0 && !tk.done) {
+    if (ld_relaxed(&c->q_head) >= (uint32_t)p.n_dyn) {
+      tk.done = true;
+    } else {
+      const uint32_t h = atomicAdd(&c->q_head, 1u);
+      if (h >= (uint32_t)p.n_dyn) {
+        tk.done = true;
+      } else {
+        tk.held = (int)h;
+        const uint32_t e = ld_acquire(&p.queue[h]);
+        if (e != 0) {
+          tk.held = -1;
+          return (int)(e - 1);
+        }
+      }
+    }
+  }
+  return -1;
 }
 
-__device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging) {
+__device__ bool staging_all_claimed(const KParams& p, const StageTicket& tk) {
+  return tk.held < 0 && ld_relaxed(&p.ctrl->init_next) >= (uint32_t)p.n_init &&
+         ld_relaxed(&p.ctrl->q_head) >= (uint32_t)p.n_dyn;
+}
+
+__device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging, StageTicket& tk) {
   Ctrl* c = p.ctrl;
   if (sc->abort || ld_relaxed(&c->abort)) { sc->cmd = CMD_EXIT; return; }
   const int n_s = current_target(p);
-  const bool staging_role = (int)blockIdx.x < n_s;
+  // a CTA that owns a queue entry stages until it has served it
+  const bool staging_role = (int)blockIdx.x < n_s || tk.held >= 0;
   if (staging_role != was_staging) {
     atomicAdd(&c->role_switches, 1ull);
     was_staging = staging_role;
   }
   if (staging_role) {
-    const int t = try_claim_staging(p);
+    const int t = try_claim_staging(p, tk);
     if (t >= 0) { sc->cmd = CMD_STAGE; sc->arg = t; return; }
-    if (staging_all_claimed(p)) {
+    if (staging_all_claimed(p, tk)) {
       if (p.mode == PSR_STATIC) { sc->cmd = CMD_EXIT; return; }
       // adaptive: nothing left to stage; fall through to compute
     } else {
@@ -324,8 +380,8 @@ __device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging) {
     if (n < (uint32_t)p.geo.n_items) { sc->cmd = CMD_COMPUTE; sc->arg = (int)n; return; }
   }
   // no compute left
-  if (p.mode == PSR_STATIC || staging_all_claimed(p)) { sc->cmd = CMD_EXIT; return; }
-  const int t = try_claim_staging(p);
+  if (p.mode == PSR_STATIC || staging_all_claimed(p, tk)) { sc->cmd = CMD_EXIT; return; }
+  const int t = try_claim_staging(p, tk);
   if (t >= 0) { sc->cmd = CMD_STAGE; sc->arg = t; return; }
   sc->cmd = CMD_IDLE;
 }
@@ -424,10 +480,15 @@ __device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, uint32_t dst
   for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * 16384, tm, 64 * h, row, bar);
 }
 
-// Returns the cycles spent waiting for readiness flags (time the item was starved of
-// staged data), which the controller does not count as compute cost.
+// Cycles an item spent waiting for readiness flags: all of them (not compute cost)
+// and those that measure staging falling behind (charged to staging): every wait
+// except during the CTA's first item, which overlaps the ring's fill at launch.
+struct Starved {
+  long long all = 0, late = 0;
+};
+
 template <int D>
-__device__ long long producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it,
+__device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it,
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               const CUtensorMap* tm_sk, const CUtensorMap* tm_sv, Counters& cnt) {
   using C = Cfg<D>;
@@ -455,9 +516,14 @@ __device__ long long producer(const KParams& p, SmemCtl* sc, uint32_t smem_base,
     fence_proxy_async_global();
     const uint32_t old = atom_add_acq_rel(p.consumed + (size_t)it.g * G.P + t, 1u);
     if (old + 1 == (uint32_t)G.Gs && t + 2 < it.n_steps) {
-      const uint32_t k = atomicAdd(&p.ctrl->q_tail, 1u);
-      if (k < (uint32_t)p.n_dyn) st_release(p.queue + k, (uint32_t)(it.g * G.P + t + 2) + 1u);
-      else raise_error(p, SITE_QUEUE);
+      const uint32_t np = (uint32_t)G.n_pieces;
+      const uint32_t k = atomicAdd(&p.ctrl->q_tail, np);
+      const uint32_t chunk = (uint32_t)(it.g * G.P + t + 2);
+      if (k + np <= (uint32_t)p.n_dyn) {
+        for (uint32_t pc = 0; pc < np; ++pc) st_release(p.queue + k + pc, chunk * np + pc + 1u);
+      } else {
+        raise_error(p, SITE_QUEUE);
+      }
     }
     for (int i = 1; i < pend_n; ++i) { pend_step[i - 1] = pend_step[i]; pend_load[i - 1] = pend_load[i]; }
     --pend_n;
@@ -465,7 +531,7 @@ __device__ long long producer(const KParams& p, SmemCtl* sc, uint32_t smem_base,
   };
   bool ok = true;
   unsigned long long tr_empty = 0;
-  long long starved = 0;
+  Starved starved;
   for (int t = 0; t < it.n_steps && ok; ++t) {
     const int j = ((it.r - t) % G.P + G.P) % G.P;
     const int n_kt = tiles_at_step(G, it, t);
@@ -480,8 +546,18 @@ __device__ long long producer(const KParams& p, SmemCtl* sc, uint32_t smem_base,
       if (in_pc == 0) seen = 0;
       if (t > 0 && seen < (uint32_t)(in_pc + 1)) {
         const long long f0 = clock64();
+        // The staging this wait depends on may itself wait for our own "consumed"
+        // notifications: send every pending one (their loads are in flight) first.
+        seen = ld_acquire(flags + pc);
+        if (seen < (uint32_t)(in_pc + 1)) {
+          while (ok && pend_n > 0)
+            if (!resolve_one(true)) ok = false;
+          if (!ok) break;
+        }
         if (!wait_flag(flags + pc, (uint32_t)(in_pc + 1), seen, p, sc)) { ok = false; break; }
-        starved += clock64() - f0;
+        const long long waited = clock64() - f0;
+        starved.all += waited;
+        if (cnt.items > 0) starved.late += waited;
         fence_proxy_async_global();  // acquire (generic) before the async-proxy reads of the slot
       }
       for (int kv = 0; kv < 2; ++kv) {
@@ -512,20 +588,21 @@ __device__ long long producer(const KParams& p, SmemCtl* sc, uint32_t smem_base,
     if (!resolve_one(true)) ok = false;
   if (kTrace) {
     atomicAdd(&p.ctrl->tr_prod_wait_empty, tr_empty);
-    atomicAdd(&p.ctrl->tr_prod_wait_flag, (unsigned long long)starved);
+    atomicAdd(&p.ctrl->tr_prod_wait_flag, (unsigned long long)starved.all);
   }
   if (!ok) sc->abort = 1;
   return starved;
 }
 
-// Tensor-core issue for query tile i, run by one thread of its own warp (warp 1 + i).
-// Two issuers, one per tile, so that a tile whose P is ready never waits behind
-// the other tile's burst: the tensor core's instruction queue is only a few
-// MMAs deep, so an issuing thread stays busy for about as long as its MMAs run.
-// Order per tile: S_i(0); then for each KV tile j: PV_i(j) (reads P_i(j), which
-// overlays S_i(j) in tensor memory) and S_i(j+1) right behind it.
-template <int D>
-__device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, int i,
+// Tensor-core issue.  The tensor core's instruction queue is only a few MMAs
+// deep, so an issuing thread stays busy for about as long as its MMAs run.
+// NT = 2: one thread issues for both query tiles, interleaved
+//   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+// NT = 1: one thread per query tile (warp 1 + i), each PV_i(j) S_i(j+1).
+// PV_i(j) reads P_i(j), which overlays S_i(j) in tensor memory, so S_i(j+1) is
+// issued right behind it (tensor-core instructions of one thread run in order).
+template <int D, int NT>
+__device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, int i0,
                            Counters& cnt) {
   using C = Cfg<D>;
   const Geometry& G = p.geo;
@@ -533,13 +610,12 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
   constexpr uint32_t IPV = idesc_bf16_f32(128, D, true);
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // 8-row (K-major) / 8-key (V, MN-major) groups 1024 B apart
   const uint32_t sStage = smem_base + 2 * C::QT;
-  const uint32_t q_lo = sdesc_lo(smem_base + i * C::QT, 16);
-  const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
-  const uint32_t tO = sc->tmem_base + (i ? C::COL_O1 : C::COL_O0);
   auto stage_of = [](uint32_t c) { return c % C::NSTAGE; };
   auto par_of = [](uint32_t c) { return (c / C::NSTAGE) & 1u; };
-  auto issue_s = [&](uint32_t kstage) {
+  auto issue_s = [&](int i, uint32_t kstage) {
+    const uint32_t q_lo = sdesc_lo(smem_base + i * C::QT, 16);
     const uint32_t b_lo = sdesc_lo(sStage + kstage * C::QT, 16);
+    const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
@@ -548,8 +624,10 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
     mma_commit(&sc->s_full[i]);
     mma_commit(&sc->kv_empty[kstage]);
   };
-  auto issue_pv = [&](uint32_t vstage, bool first) {
+  auto issue_pv = [&](int i, uint32_t vstage, bool first) {
     const uint32_t b_lo = sdesc_lo(sStage + vstage * C::QT, 16384);  // V halves of 64 columns 16 KB apart
+    const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
+    const uint32_t tO = sc->tmem_base + (i ? C::COL_O1 : C::COL_O0);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_ts_w(tO, tS + kk * 8, b_lo + kk * (2048 >> 4), kHi, IPV, (first && kk == 0) ? 0u : 1u);
@@ -560,30 +638,30 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
   uint32_t ck = cnt.kv;  // load index of K_0 of this item (the producer loads K_j, V_j alternately)
   cnt.kv += 2u * n;
   unsigned long long tr_issue = 0, tr_kv = 0;
-  if (!wait_bar(&sc->q_full[i], cnt.items & 1u, p, sc, SITE_Q_FULL) ||
-      !wait_bar(&sc->kv_full[stage_of(ck)], par_of(ck), p, sc, SITE_KV_FULL)) {
-    sc->abort = 1;
-    return;
-  }
+  for (int u = 0; u < NT; ++u)
+    if (!wait_bar(&sc->q_full[i0 + u], cnt.items & 1u, p, sc, SITE_Q_FULL)) { sc->abort = 1; return; }
+  if (!wait_bar(&sc->kv_full[stage_of(ck)], par_of(ck), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
   tc_fence_after();
-  issue_s(stage_of(ck));
+  for (int u = 0; u < NT; ++u) issue_s(i0 + u, stage_of(ck));
   for (uint32_t jt = 0; jt < n; ++jt, ck += 2) {
     const uint32_t cv = ck + 1, cn = ck + 2;  // V_j, K_{j+1}
     const long long a0 = trace_clock();
     if (!wait_bar(&sc->kv_full[stage_of(cv)], par_of(cv), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
-    const long long a1 = trace_clock();
-    if (!wait_bar(&sc->p_full[i], (cnt.tiles + jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
-    const long long a2 = trace_clock();
-    tc_fence_after();
-    issue_pv(stage_of(cv), jt == 0);
-    if (jt + 1 < n) {
-      const long long b0 = trace_clock();
-      if (!wait_bar(&sc->kv_full[stage_of(cn)], par_of(cn), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
-      tr_kv += trace_clock() - b0;
-      issue_s(stage_of(cn));
+    tr_kv += trace_clock() - a0;
+    for (int u = 0; u < NT; ++u) {
+      const int i = i0 + u;
+      if (!wait_bar(&sc->p_full[i], (cnt.tiles + jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
+      const long long a2 = trace_clock();
+      tc_fence_after();
+      issue_pv(i, stage_of(cv), jt == 0);
+      if (jt + 1 < n) {
+        const long long b0 = trace_clock();
+        if (!wait_bar(&sc->kv_full[stage_of(cn)], par_of(cn), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
+        tr_kv += trace_clock() - b0;
+        issue_s(i, stage_of(cn));
+      }
+      tr_issue += trace_clock() - a2;
     }
-    tr_kv += a1 - a0;
-    tr_issue += trace_clock() - a2;
   }
   if (kTrace) {
     atomicAdd(&p.ctrl->tr_mma_issue, tr_issue);
@@ -781,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sc.kv_empty[s], 2);  // both softmax warpgroups commit their reads of every K/V tile
     }
     for (int s = 0; s < C::NB; ++s) mbar_init(&sc.stg[s], 1);
-    mbar_init(&sc.drain, 2);  // one commit from each warpgroup's MMA-issuing thread
+    mbar_init(&sc.drain, kMmaIssuers);  // one commit from each MMA-issuing thread
     sc.abort = 0;
     fence_barrier_init();
     if (blockIdx.x == 0) {
@@ -811,11 +889,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kRegsCtl>();
     uint32_t stg_phase[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     bool was_staging = false;
-    long long t_task = 0, starved = 0;
+    StageTicket ticket;
+    long long t_task = 0;
+    Starved starved;
     uint64_t idle_since = 0;  // first idle poll of the current idle stretch (0 = not idle)
     while (true) {
       if (threadIdx.x == 0) {
-        decide(p, &sc, was_staging);
+        decide(p, &sc, was_staging, ticket);
         t_task = clock64();
       }
       __syncthreads();
@@ -827,8 +907,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ItemCoord it = item_coord(p.geo, arg);
         if (warp == 0 && lane == 0)
           starved = producer<D>(p, &sc, smem_base, it, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
-        else if ((warp == 1 || warp == 2) && lane == 0)
-          mma_issuer<D>(p, &sc, smem_base, it, warp - 1, cnt);
+        else if (kMmaIssuers == 2 && (warp == 1 || warp == 2) && lane == 0)
+          mma_issuer<D, 1>(p, &sc, smem_base, it, warp - 1, cnt);
+        else if (kMmaIssuers == 1 && warp == 1 && lane == 0)
+          mma_issuer<D, 2>(p, &sc, smem_base, it, 0, cnt);
         cnt.items++;
         cnt.tiles += (uint32_t)item_tiles(p.geo, it);
       } else if (threadIdx.x == 0) {
@@ -845,7 +927,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (threadIdx.x == 0 && cmd != CMD_IDLE) {
         long long busy = clock64() - t_task;
-        if (cmd == CMD_COMPUTE) busy -= starved;  // compute cost excludes waiting for staged data
+        if (cmd == CMD_COMPUTE) {
+          busy -= starved.all;  // compute cost excludes waiting for staged data ...
+          atomicAdd(&p.ctrl->starve_cycles, (unsigned long long)(starved.late > 0 ? starved.late : 0));  // ... charged to staging
+        }
         const unsigned long long dt = (unsigned long long)(busy > 0 ? busy : 0);
         if (cmd == CMD_STAGE) {
           atomicAdd(&p.ctrl->stage_cycles, dt);
@@ -861,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // drain: every tcgen05 op issued by this CTA has completed before TMEM is released
-    if ((warp == 1 || warp == 2) && lane == 0) {
+    if ((warp == 1 || (kMmaIssuers == 2 && warp == 2)) && lane == 0) {
       mma_commit(&sc.drain);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(&sc.drain, 0)) {
@@ -1078,19 +1163,20 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
   kp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
   kp.consumed = reinterpret_cast<uint32_t*>(ws + L.consumed);
-  kp.claimed = reinterpret_cast<uint32_t*>(ws + L.claimed);
   kp.queue = reinterpret_cast<uint32_t*>(ws + L.queue);
   kp.traj = reinterpret_cast<uint32_t*>(ws + L.traj);
   kp.timeout_ns = (unsigned long long)(pt.timeout_ms > 0 ? pt.timeout_ms : 2000) * 1000000ull;
   kp.n_tiles_total = (unsigned long long)total_tiles(G);
   kp.n_stage_total = (unsigned long long)total_staging_tasks(G) * (unsigned long long)G.n_pieces;
-  kp.n_dyn = (int)dynamic_staging_tasks(G);
-  kp.n_init = 2 * G.n_groups;
+  kp.n_dyn = (int)(dynamic_staging_tasks(G) * G.n_pieces);
+  kp.n_init = 2 * G.n_groups * G.n_pieces;
   kp.mode = pt.mode;
   kp.fault = pt.fault;
   // clamps: at least one stager while staging remains; enough compute CTAs to hold a group
   const int hard_max = n_cta - G.Gs - 1 < 1 ? 1 : n_cta - G.Gs - 1;
-  int n_max = pt.n_max > 0 ? pt.n_max : hard_max;
+  // default upper clamp: at most half of the CTAs stage (a compute item's ring steps are
+  // sequential, so compute throughput needs items in flight as well as staged data)
+  int n_max = pt.n_max > 0 ? pt.n_max : (n_cta / 2 < hard_max ? n_cta / 2 : hard_max);
   if (n_max > hard_max) n_max = hard_max;
   int n_min = pt.n_min > 0 ? pt.n_min : 1;
   if (n_min > n_max) n_min = n_max;

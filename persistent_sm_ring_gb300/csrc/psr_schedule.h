@@ -16,9 +16,10 @@
 //  * staging chunk = one (group, step >= 1): chunk (r - step) mod P of K and V
 //                    copied into the group's slot (step & 1) in 128-row tiles
 //                    (the pages' ring moves KV in 128-row tiles, Table 3);
-//  * staging piece = kStagePieceTiles consecutive tiles of a chunk: the unit a
-//                    staging CTA claims, so that several CTAs fill one chunk at
-//                    once; readiness is published per piece as a tile count.
+//  * staging piece = a quarter of a chunk (1..kStagePieceMaxTiles tiles): the
+//                    unit a staging CTA claims, so that several CTAs fill one
+//                    chunk at once; readiness is published per piece as a tile
+//                    count.
 // Slot (step & 1) of a group may be overwritten for step s >= 3 only when all
 // of the group's items have loaded step s - 2: that is the double buffer's
 // back-pressure.
@@ -35,7 +36,7 @@ namespace psr {
 
 constexpr int kTileRows = 128;  // rows per Q tile and per KV tile
 constexpr int kItemRows = 256;  // query rows per compute item (two tiles)
-constexpr int kStagePieceTiles = 4;  // tiles per staging piece
+constexpr int kStagePieceMaxTiles = 8;  // staging piece: a quarter of a chunk, 1..8 tiles
 
 struct Geometry {
   int B, Hq, Hkv, S, P, d, causal;
@@ -67,7 +68,7 @@ PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int 
   G.gqa = Hq / Hkv;
   G.q_pairs = G.L / kItemRows;
   G.kv_tiles = G.L / kTileRows;
-  G.piece_tiles = G.kv_tiles < kStagePieceTiles ? G.kv_tiles : kStagePieceTiles;
+  G.piece_tiles = G.kv_tiles / 4 < 1 ? 1 : (G.kv_tiles / 4 > kStagePieceMaxTiles ? kStagePieceMaxTiles : G.kv_tiles / 4);
   G.n_pieces = (G.kv_tiles + G.piece_tiles - 1) / G.piece_tiles;
   G.G = G.gqa * G.q_pairs;
   // split a group into power-of-two sub-groups until it fits the bound
