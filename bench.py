@@ -471,19 +471,29 @@ def run_sweep(args):
                 assert st["status"] == 0, st
                 return statistics.median(ts), st
 
-            res = {}
+            res, cost = {}, {}
             for n in statics:
                 try:
-                    res[n], _ = timed(psr.make_partition(psr.STATIC, n_staging=n))
+                    res[n], sst = timed(psr.make_partition(psr.STATIC, n_staging=n))
+                    # measured unit costs (CTA-cycles per staging piece / per compute tile) at this split
+                    cost[n] = (sst["staging_cycles"] / max(1, sst["staging_tasks"]),
+                               sst["compute_cycles"] / max(1, sst["compute_tiles"]), sst["staging_tasks"],
+                               sst["compute_tiles"])
                 except psr.PsrError:
                     res[n] = None
             ad, st = timed(psr.make_partition(psr.ADAPTIVE))
             best_n = min((n for n in statics if res[n] is not None), key=lambda n: res[n])
+            # the partition rule evaluated with the unit costs measured at the best static split
+            c_s, c_p, r_s, r_p = cost[best_n]
+            rule_n = psr.controller_target(psr.num_ctas(), r_s, c_s, r_p, c_p)
             rows.append({"d": d, "P": P, "adaptive_ms": round(ad, 4), "best_static_ms": round(res[best_n], 4),
                          "best_static_n": best_n, "ratio": round(ad / res[best_n], 4),
                          "worst_static_ms": round(max(v for v in res.values() if v is not None), 4),
                          "static_ms": {str(n): (round(v, 4) if v is not None else None) for n, v in res.items()},
                          "adaptive_n_s": [st["n_s_initial"], st["n_s_min"], st["n_s_max"], st["n_s_final"]],
+                         "rule_n_at_best_costs": rule_n, "C_s": round(c_s, 1), "C_p": round(c_p, 1),
+                         "adaptive_C_s": round(st["staging_cycles"] / max(1, st["staging_tasks"]), 1),
+                         "adaptive_C_p": round(st["compute_cycles"] / max(1, st["compute_tiles"]), 1),
                          "tflops_adaptive": round(w.flops() / (ad / 1e3) / 1e12, 1)})
             print(json.dumps(rows[-1]), flush=True)
     import math

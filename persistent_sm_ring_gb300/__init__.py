@@ -13,7 +13,7 @@ import ctypes
 import os
 import threading
 
-from .build import LIB, LIB_TRACE, build as _build
+from .build import LIB, LIB_PAIRS, LIB_TRACE, build as _build
 
 __all__ = ["build", "load", "Shape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host", "workspace_bytes",
            "get_stats", "get_trajectory", "controller_target", "num_ctas", "status_string", "PsrError",
@@ -64,20 +64,22 @@ _lib = None
 _lock = threading.Lock()
 
 
-def build(force: bool = False, trace: bool = False) -> str:
-    """Compile libpsr.so (or, with trace=True, the cycle-tracing libpsr_trace.so) in-tree for sm_103a."""
-    return _build(force=force, trace=trace)
+def build(force: bool = False, trace: bool = False, variant: str = "") -> str:
+    """Compile libpsr.so in-tree for sm_103a, or a variant: "trace" (trace=True; cycle-tracing
+    libpsr_trace.so) or "pairs" (libpsr_pairs.so, CTA-pair compute units for d = 128)."""
+    return _build(force=force, trace=trace, variant=variant)
 
 
-def load(trace: bool = False) -> ctypes.CDLL:
-    """Load libpsr.so (or libpsr_trace.so); raises if it has not been built (no fallback path exists).
+def load(trace: bool = False, variant: str = "") -> ctypes.CDLL:
+    """Load libpsr.so (or the variant built by build(variant=...)); raises if it has not been built
+    (no fallback path exists).
 
     One library per process: the first call decides which."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = LIB_TRACE if trace else LIB
+        path = LIB_TRACE if (trace or variant == "trace") else (LIB_PAIRS if variant == "pairs" else LIB)
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is missing: run persistent_sm_ring_gb300.build() (nvcc, sm_103a) first")
         lib = ctypes.CDLL(path)

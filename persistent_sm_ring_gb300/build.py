@@ -10,6 +10,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libpsr.so")
 LIB_TRACE = os.path.join(HERE, "libpsr_trace.so")  # same library with per-role cycle counters
+LIB_PAIRS = os.path.join(HERE, "libpsr_pairs.so")  # same library with CTA-pair compute units for d = 128
+# variant -> (extra nvcc defines, output)
+VARIANTS = {"": ([], LIB), "trace": (["-DPSR_TRACE=1"], LIB_TRACE), "pairs": (["-DPSR_PAIRS=1"], LIB_PAIRS)}
 SOURCES = [os.path.join(CSRC, "psr_ring_attn.cu"), os.path.join(CSRC, "psr_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("psr_device.cuh", "psr_schedule.h")] + [
     os.path.join(ROOT, "include", "psr.h")]
@@ -31,16 +34,20 @@ def needs_build(lib: str = LIB) -> bool:
     return any(os.path.getmtime(f) > t for f in DEPS)
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
-    """Compile the CUDA sources into persistent_sm_ring_gb300/libpsr.so (libpsr_trace.so with trace=True)."""
-    lib = LIB_TRACE if trace else LIB
+def build(force: bool = False, verbose: bool = False, trace: bool = False, variant: str = "") -> str:
+    """Compile the CUDA sources into persistent_sm_ring_gb300/libpsr.so, or a variant of it:
+    "trace" (libpsr_trace.so, per-role cycle counters; also trace=True) or "pairs"
+    (libpsr_pairs.so, CTA-pair compute units for d = 128)."""
+    if trace:
+        variant = "trace"
+    defines, lib = VARIANTS[variant]
     with _lock:
         if not force and not needs_build(lib):
             return lib
         tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
                "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"),
-               f"-DPSR_TRACE={1 if trace else 0}", *SOURCES, "-o", tmp]
+               *defines, *SOURCES, "-o", tmp]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         res = subprocess.run(cmd, capture_output=True, text=True)

@@ -13,12 +13,15 @@
 //    (t & 1) of shard r with TMA bulk loads/stores through shared memory and
 //    publish, per chunk, the count of completed 128-row tiles with a
 //    gpu-scope release after the bulk stores have completed;
-//  * compute CTAs process 256-query-row items across all ring steps of their
+//  * compute units (one CTA, or a CTA pair when d = 128 and the shard length is a
+//    multiple of 512) process query-row items across all ring steps of their
 //    shard: step 0 reads the shard's own chunk in place, later steps read
 //    the slot after acquiring its flag; QK^T and PV run on tcgen05 with the
-//    accumulators in tensor memory, the online softmax runs in two
-//    128-thread warpgroups, and the exact merge across chunks is the running
-//    max / sum of the online softmax itself;
+//    accumulators in tensor memory (a pair runs M = 256 MMAs with each CTA
+//    holding half of every K/V tile, which halves the K/V bytes each SM must
+//    receive), the online softmax runs in two 128-thread warpgroups per CTA,
+//    and the exact merge across chunks is the running max / sum of the online
+//    softmax itself;
 //  * the controller re-evaluates n_s* = N*(R_s*C_s)/(R_p*C_p + R_s*C_s) at task
 //    boundaries from cycle-counter costs and remaining-work counters.
 #include <cuda.h>
@@ -50,12 +53,13 @@ constexpr bool kTrace = PSR_TRACE != 0;
 // tcgen05.mma on the same SM sub-partition (issue rate halves under dense FMA
 // neighbours, not under MUFU-bound ones), which costs more than it saves.
 constexpr int kPolyEvery = PSR_POLY_EVERY;
-#ifndef PSR_MMA_ISSUERS
-#define PSR_MMA_ISSUERS 1
+#ifndef PSR_P_PARTS
+#define PSR_P_PARTS 2
 #endif
-// Threads issuing tcgen05.mma: 1 (both query tiles, interleaved) or 2 (one per tile).
-constexpr int kMmaIssuers = PSR_MMA_ISSUERS;
-static_assert(kMmaIssuers == 1 || kMmaIssuers == 2, "one or two MMA issuers");
+// P of a query tile is published in this many parts (key ranges of 128 / kPParts), so
+// that the PV MMAs of the first keys run while the softmax computes the rest.
+constexpr int kPParts = PSR_P_PARTS;
+static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P parts: 1, 2 or 4");
 __device__ __forceinline__ long long trace_clock() { return kTrace ? clock64() : 0; }
 
 // ------------------------------------------------------------------------------------------------
@@ -144,24 +148,31 @@ struct KParams {
   float c_s0, c_p0;   // prior costs (cycles per staging task / per tile) before measurements exist
 };
 
-// Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warp 1 (and warp 2 when two
-// issuers are built) = MMA issuer(s) (warp 1 also owns the TMEM allocation), others idle.
-// Warpgroups 1 and 2: softmax of query tiles 0 and 1.
+// Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warp 1 = MMA issuer (in a
+// pair, the even CTA's only) and owner of the TMEM allocation, others idle.
+// Warpgroups 1 and 2: softmax of the CTA's query tiles 0 and 1.
 constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 // Registers: launched at kRegsLaunch per thread; warpgroup 0 gives registers to the softmax warpgroups.
 constexpr int kRegsLaunch = 168, kRegsCtl = 72, kRegsSoftmax = 208;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
-template <int D>
+// CG = CTAs per compute unit.  In a pair (CG = 2) each CTA holds half of every K tile
+// (64 of its 128 rows) and half of every V tile (64 of its d = 128 columns): the B
+// operands of the M = 256 MMAs are split along N between the two shared memories.
+template <int D, int CG>
 struct Cfg {
+  static_assert(CG == 1 || (CG == 2 && D == 128), "CTA pairs are built for d = 128");
   static constexpr int QT = kTileRows * D * 2;  // bytes of one 128-row bf16 tile
-  static constexpr int NSTAGE = D == 128 ? 5 : 12;
-  static constexpr int NB = D == 128 ? 3 : 7;  // staging buffers of one K tile + one V tile
-  static constexpr int SMEM = 1024 + 2 * QT + NSTAGE * QT;
+  static constexpr int KVB = QT / CG;           // bytes of this CTA's share of one K or V tile
+  static constexpr int NSTAGE = CG == 2 ? 10 : (D == 128 ? 5 : 12);
+  static constexpr int NB = D == 128 ? 6 : 14;  // staging buffers of one K or V tile each
+  static constexpr int SMEM = 1024 + 2 * QT + NSTAGE * KVB;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
-  static_assert(NB * 2 * QT <= 2 * QT + NSTAGE * QT, "staging buffers must fit in the compute region");
+  static constexpr uint32_t KBLK = (kTileRows / CG) * 128;  // bytes of one 64-column block of the K share
+  static_assert(NB * QT <= 2 * QT + NSTAGE * KVB, "staging buffers must fit in the compute region");
+  static_assert(NB <= 16, "staging barriers");
   static_assert(SMEM <= 232448 - 512, "shared memory");
 };
 
@@ -178,13 +189,15 @@ struct SmemCtl {
   uint64_t kv_full[16];
   uint64_t kv_empty[16];
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_full[2][4];  // [query tile][part]: that part of P is in tensor memory (in every CTA)
   uint64_t o_full[2];
-  uint64_t stg[8];
+  uint64_t stg[16];
   uint64_t drain;
   uint32_t tmem_base;
   int cmd, arg;
   volatile uint32_t abort;
+  uint32_t peer_held;  // pair: the odd CTA holds a ready-queue ticket (written by that CTA)
+  uint32_t p_sink[4];  // pair: landing words of the odd CTA's P-ready signals (never read)
 };
 
 __device__ __forceinline__ void raise_error(const KParams& p, uint32_t site) {
@@ -192,13 +205,16 @@ __device__ __forceinline__ void raise_error(const KParams& p, uint32_t site) {
   st_release(&p.ctrl->abort, 1u);
 }
 
-// Bounded mbarrier wait: false on timeout or abort.
+// Bounded mbarrier wait: false on timeout or abort.  CL: the acquire also covers
+// arrivals released by the other CTA of a pair.
+template <bool CL = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KParams& p, SmemCtl* sc, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return CL ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((++it & 15u) == 0) {
       if (sc->abort) return false;
       if (ld_relaxed(&p.ctrl->abort)) { sc->abort = 1; return false; }
@@ -235,6 +251,11 @@ __device__ int current_target(const KParams& p) {
 }
 
 constexpr unsigned long long kCtrlMinIntervalNs = 20000;  // re-evaluate at most every 20 us
+constexpr double kStageHeadroom = 2.0;  // initial split: staging capacity over the average rate
+// The initial split stands until this fraction of the compute tiles is done: it covers the
+// ring's fill, when every active group needs its first staged steps at once and measured
+// costs are still dominated by start-up.
+constexpr double kCtrlHold = 0.1;
 
 __device__ void controller_update(const KParams& p) {
   Ctrl* c = p.ctrl;
@@ -250,7 +271,8 @@ __device__ void controller_update(const KParams& p) {
   const unsigned long long ccy = atomicAdd(&c->compute_cycles, 0ull);
   const double R_s = (double)(p.n_stage_total > sd ? p.n_stage_total - sd : 0);
   const double R_p = (double)(p.n_tiles_total > td ? p.n_tiles_total - td : 0);
-  // measured cost per unit, blended with the prior until a few units are measured
+  if ((double)td < kCtrlHold * (double)p.n_tiles_total) return;
+  // measured cost per unit, blended with the prior until a few units are measured.
   // The staging cost per piece counts the staging CTAs' busy cycles plus the cycles
   // compute items spent starved of staged data: both are what staging costs the launch.
   const unsigned long long sv = atomicAdd(&c->starve_cycles, 0ull);
@@ -282,7 +304,8 @@ __device__ void controller_update(const KParams& p) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Task selection (thread 0 of the CTA)
+// Task selection: thread 0 of a compute unit (the CTA, or the even CTA of a pair) picks the
+// unit's role; a staging unit's CTAs then claim pieces each on its own.
 // ------------------------------------------------------------------------------------------------
 // Staging work comes from two lists, each claimed with one atomicAdd (a ticket):
 //  * the static list: pieces of steps 1 and 2 of every group, in group order (their
@@ -350,48 +373,69 @@ __device__ int try_claim_staging(const KParams& p, StageTicket& tk) {
   return -1;
 }
 
-__device__ bool staging_all_claimed(const KParams& p, const StageTicket& tk) {
-  return tk.held < 0 && ld_relaxed(&p.ctrl->init_next) >= (uint32_t)p.n_init &&
-         ld_relaxed(&p.ctrl->q_head) >= (uint32_t)p.n_dyn;
+// every static-list entry and every ready-queue ticket has been handed out
+__device__ bool staging_all_claimed(const KParams& p) {
+  return ld_relaxed(&p.ctrl->init_next) >= (uint32_t)p.n_init && ld_relaxed(&p.ctrl->q_head) >= (uint32_t)p.n_dyn;
 }
 
-__device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging, StageTicket& tk) {
+// Role of the compute unit for its next task: CMD_STAGE (each CTA of the unit then claims a
+// piece, or idles when none is claimable), CMD_COMPUTE with item `arg`, or CMD_EXIT.
+// Unit u stages while u * CG < n_s (the controller's target counts CTAs).
+template <int CG>
+__device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging, const StageTicket& tk) {
   Ctrl* c = p.ctrl;
   if (sc->abort || ld_relaxed(&c->abort)) { sc->cmd = CMD_EXIT; return; }
   const int n_s = current_target(p);
-  // a CTA that owns a queue entry stages until it has served it
-  const bool staging_role = (int)blockIdx.x < n_s || tk.held >= 0;
+  const int unit = (int)blockIdx.x / CG;
+  // a unit whose CTA owns a queue entry stages until that entry is served
+  const bool held = tk.held >= 0 || (CG == 2 && sc->peer_held != 0);
+  const bool staging_role = unit * CG < n_s || held;
   if (staging_role != was_staging) {
     atomicAdd(&c->role_switches, 1ull);
     was_staging = staging_role;
   }
+  const bool all_claimed = !held && staging_all_claimed(p);
   if (staging_role) {
-    const int t = try_claim_staging(p, tk);
-    if (t >= 0) { sc->cmd = CMD_STAGE; sc->arg = t; return; }
-    if (staging_all_claimed(p, tk)) {
-      if (p.mode == PSR_STATIC) { sc->cmd = CMD_EXIT; return; }
-      // adaptive: nothing left to stage; fall through to compute
-    } else {
-      sc->cmd = CMD_IDLE; return;
-    }
+    if (!all_claimed) { sc->cmd = CMD_STAGE; return; }
+    if (p.mode == PSR_STATIC) { sc->cmd = CMD_EXIT; return; }
+    // adaptive: nothing left to stage; fall through to compute
   }
   if (ld_relaxed(&c->item_next) < (uint32_t)p.geo.n_items) {
     const uint32_t n = atomicAdd(&c->item_next, 1u);
     if (n < (uint32_t)p.geo.n_items) { sc->cmd = CMD_COMPUTE; sc->arg = (int)n; return; }
   }
   // no compute left
-  if (p.mode == PSR_STATIC || staging_all_claimed(p, tk)) { sc->cmd = CMD_EXIT; return; }
-  const int t = try_claim_staging(p, tk);
-  if (t >= 0) { sc->cmd = CMD_STAGE; sc->arg = t; return; }
-  sc->cmd = CMD_IDLE;
+  if (p.mode == PSR_STATIC || all_claimed) { sc->cmd = CMD_EXIT; return; }
+  sc->cmd = CMD_STAGE;
 }
 
 // ------------------------------------------------------------------------------------------------
 // Staging task (thread 0): chunk (r - step) mod P of K and V -> slot (step & 1) of group g
 // ------------------------------------------------------------------------------------------------
-template <int D>
-__device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, int task, uint32_t (&stg_phase)[8]) {
-  using C = Cfg<D>;
+// A piece is copied as 2*n_kt units (K_kt and V_kt alternately), each a 128-row tile, through
+// NB shared-memory buffers: a load waits only for the buffer's previous store to have read
+// shared memory.  The piece's readiness flag (its tile count) is published
+// once all of its stores have completed; when the same CTA goes on to stage another piece, that
+// publication is deferred until the next piece's first loads are in flight, so that the store
+// completion of one piece overlaps the loads of the next.
+struct StagePending {
+  uint32_t* flag = nullptr;
+  uint32_t value = 0;
+};
+
+// Publish a deferred flag (thread 0 of a staging CTA; its bulk stores are the only ones pending).
+__device__ __forceinline__ void publish_pending(StagePending& pend) {
+  if (pend.flag == nullptr) return;
+  bulk_wait<0>();              // every store of the piece has completed
+  fence_proxy_async_global();  // async-proxy writes before the generic release
+  st_release(pend.flag, pend.value);
+  pend.flag = nullptr;
+}
+
+template <int D, int CG>
+__device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, int task, uint32_t (&stg_phase)[16],
+                            StagePending& pend) {
+  using C = Cfg<D, CG>;
   const Geometry& G = p.geo;
   const int chunk = task / G.n_pieces, piece = task % G.n_pieces;
   const int g = chunk / G.P, step = chunk % G.P;
@@ -402,11 +446,7 @@ __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, i
   const int kt0 = piece * G.piece_tiles;
   const int n_kt = (G.kv_tiles - kt0) < G.piece_tiles ? (G.kv_tiles - kt0) : G.piece_tiles;
   const size_t src_off = ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L + (size_t)kt0 * kTileRows) * D;
-  const uint16_t* src_k = p.k + src_off;
-  const uint16_t* src_v = p.v + src_off;
   const size_t slot_off = (((size_t)(step & 1) * G.n_groups + g) * (size_t)G.L + (size_t)kt0 * kTileRows) * D;
-  uint16_t* dst_k = p.slot_k + slot_off;
-  uint16_t* dst_v = p.slot_v + slot_off;
   uint32_t* flag = p.flags + (size_t)chunk * G.n_pieces + piece;
   const bool drop = (p.fault == PSR_FAULT_DROP_FIRST_FLAG) && (atomicAdd(&p.ctrl->fault_count, 1u) == 0u);
   if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
@@ -415,21 +455,22 @@ __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, i
   fence_proxy_async_global();
 
   constexpr int NB = C::NB;
-  constexpr uint32_t BUF = 2 * C::QT;
-  auto issue_load = [&](int kt) {
-    const int bi = kt % NB;
-    uint64_t* bar = &sc->stg[bi];
-    mbar_expect_tx(bar, BUF);
-    bulk_load(smem_base + bi * BUF, src_k + (size_t)kt * tile_elems, C::QT, bar);
-    bulk_load(smem_base + bi * BUF + C::QT, src_v + (size_t)kt * tile_elems, C::QT, bar);
+  const int n_u = 2 * n_kt;  // unit u: tile u / 2 of K (u even) or V (u odd)
+  auto src_of = [&](int u) { return ((u & 1) ? p.v : p.k) + src_off + (size_t)(u >> 1) * tile_elems; };
+  auto dst_of = [&](int u) { return ((u & 1) ? p.slot_v : p.slot_k) + slot_off + (size_t)(u >> 1) * tile_elems; };
+  auto issue_load = [&](int u) {
+    const int bi = u % NB;
+    mbar_expect_tx(&sc->stg[bi], C::QT);
+    bulk_load(smem_base + bi * C::QT, src_of(u), C::QT, &sc->stg[bi]);
   };
-  const int pre = n_kt < NB - 1 ? n_kt : NB - 1;
-  for (int kt = 0; kt < pre; ++kt) issue_load(kt);
+  const int pre = n_u < NB - 1 ? n_u : NB - 1;
+  for (int u = 0; u < pre; ++u) issue_load(u);
   int issued = pre;
+  publish_pending(pend);  // the previous piece's stores complete while these loads are in flight
   bool ok = true;
-  for (int kt = 0; kt < n_kt; ++kt) {
-    const int bi = kt % NB;
-    if (kt >= issued) break;  // aborted: no more loads were issued
+  for (int u = 0; u < n_u; ++u) {
+    const int bi = u % NB;
+    if (u >= issued) break;  // aborted: no more loads were issued
     if (ok && !wait_bar(&sc->stg[bi], stg_phase[bi] & 1u, p, sc, SITE_STAGE_LOAD)) ok = false;
     if (!ok) {
       // drain this load (bounded) so that no bulk copy targets shared memory after we leave
@@ -439,26 +480,21 @@ __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, i
     }
     stg_phase[bi]++;
     if (ok) {
-      bulk_store(dst_k + (size_t)kt * tile_elems, smem_base + bi * BUF, C::QT);
-      bulk_store(dst_v + (size_t)kt * tile_elems, smem_base + bi * BUF + C::QT, C::QT);
+      bulk_store(dst_of(u), smem_base + bi * C::QT, C::QT);
+      bulk_commit();
     }
-    bulk_commit();
-    const int nk = kt + NB - 1;
-    if (nk < n_kt && ok) {
-      bulk_wait_read<1>();  // the store that used buffer nk % NB (tile kt-1) has read shared memory
-      issue_load(nk);
-      issued = nk + 1;
-    }
-    if (kt >= 2 && ok && !drop) {
-      bulk_wait<2>();  // stores of tiles <= kt-2 are complete
-      fence_proxy_async_global();
-      st_release(flag, (uint32_t)(kt - 1));
+    const int nu = u + NB - 1;
+    if (nu < n_u && ok) {
+      bulk_wait_read<1>();  // the store that used buffer nu % NB (unit u - 1) has read shared memory
+      issue_load(nu);
+      issued = nu + 1;
     }
   }
-  bulk_wait<0>();
   if (ok && !drop) {
-    fence_proxy_async_global();
-    st_release(flag, (uint32_t)n_kt);
+    pend.flag = flag;
+    pend.value = (uint32_t)n_kt;
+  } else {
+    bulk_wait<0>();
   }
   atomicAdd(&p.ctrl->stage_bytes, (unsigned long long)n_kt * 2ull * C::QT);
 }
@@ -474,10 +510,45 @@ struct Counters {
   uint32_t tiles;  // KV tiles processed before the current item (S, P and O barrier phases)
 };
 
-template <int D>
-__device__ __forceinline__ void load_kv_tile(const CUtensorMap* tm, uint32_t dst, int row, uint64_t* bar) {
+// Tiled TMA load into this CTA's shared memory.  In a pair the completion is counted
+// on the even CTA's mbarrier (bar_cl, a shared::cluster address), which therefore
+// counts the bytes of both CTAs.
+template <int CG>
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
+                                         uint32_t bar_cl) {
+  if constexpr (CG == 1)
+    tma_load_2d(dst, tm, x, y, bar);
+  else
+    tma_load_2d_pair(dst, tm, x, y, bar_cl);
+}
+// 128 rows x D columns as D/64 boxes of 64 columns, 16 KB apart (a Q tile, or a whole K/V tile)
+template <int D, int CG>
+__device__ __forceinline__ void load_rows128(const CUtensorMap* tm, uint32_t dst, int row, uint64_t* bar,
+                                             uint32_t bar_cl) {
 #pragma unroll
-  for (int h = 0; h < D / 64; ++h) tma_load_2d(dst + h * 16384, tm, 64 * h, row, bar);
+  for (int h = 0; h < D / 64; ++h) tma_load<CG>(dst + h * 16384, tm, 64 * h, row, bar, bar_cl);
+}
+// This CTA's share of K tile rows [row, row+128): all of it, or in a pair rows
+// row + 64*rank .. +64 (the K tensor maps then have 64-row boxes), 8 KB per 64 columns.
+template <int D, int CG>
+__device__ __forceinline__ void load_k_share(const CUtensorMap* tm, uint32_t dst, int row, uint32_t rank,
+                                             uint64_t* bar, uint32_t bar_cl) {
+  if constexpr (CG == 1) {
+    load_rows128<D, 1>(tm, dst, row, bar, bar_cl);
+  } else {
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) tma_load<2>(dst + h * 8192, tm, 64 * h, row + 64 * (int)rank, bar, bar_cl);
+  }
+}
+// This CTA's share of V tile rows [row, row+128): all of it, or in a pair the 64 columns
+// 64*rank .. +64 (one box, 16 KB).
+template <int D, int CG>
+__device__ __forceinline__ void load_v_share(const CUtensorMap* tm, uint32_t dst, int row, uint32_t rank,
+                                             uint64_t* bar, uint32_t bar_cl) {
+  if constexpr (CG == 1)
+    load_rows128<D, 1>(tm, dst, row, bar, bar_cl);
+  else
+    tma_load<2>(dst, tm, 64 * (int)rank, row, bar, bar_cl);
 }
 
 // Cycles an item spent waiting for readiness flags: all of them (not compute cost)
@@ -487,18 +558,22 @@ struct Starved {
   long long all = 0, late = 0;
 };
 
-template <int D>
-__device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it,
+// In a pair both CTAs run a producer for their own shares; only the even CTA's
+// barriers count the bytes (for both) and only it sends "consumed" notifications.
+template <int D, int CG>
+__device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, uint32_t rank,
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               const CUtensorMap* tm_sk, const CUtensorMap* tm_sv, Counters& cnt) {
-  using C = Cfg<D>;
+  using C = Cfg<D, CG>;
   const Geometry& G = p.geo;
+  const bool leader = rank == 0;
   const uint32_t sQ = smem_base, sStage = smem_base + 2 * C::QT;
+  auto bar_cl = [](uint64_t* b) -> uint32_t { return CG == 2 ? mapa_shared(smem_u32(b), 0) : 0u; };
   // Q tiles (the barrier phase of q_full is the item count)
-  const int q_row = (it.b * G.Hq + it.hq) * G.S + it.r * G.L + it.qp * kItemRows;
+  const int q_row = (it.b * G.Hq + it.hq) * G.S + it.r * G.L + it.qp * G.item_rows + (int)rank * kCtaRows;
   for (int i = 0; i < 2; ++i) {
-    mbar_expect_tx(&sc->q_full[i], C::QT);
-    load_kv_tile<D>(tm_q, sQ + i * C::QT, q_row + i * kTileRows, &sc->q_full[i]);
+    if (leader) mbar_expect_tx(&sc->q_full[i], CG * C::QT);
+    load_rows128<D, CG>(tm_q, sQ + i * C::QT, q_row + i * kTileRows, &sc->q_full[i], bar_cl(&sc->q_full[i]));
   }
   // pending "slot consumed" notifications: (step, load index of the step's last tile)
   int pend_step[4] = {0, 0, 0, 0};
@@ -572,12 +647,16 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
         const long long e0 = trace_clock();
         if (fill > 0 && !wait_bar(&sc->kv_empty[stage], (fill - 1) & 1u, p, sc, SITE_KV_EMPTY)) { ok = false; break; }
         tr_empty += trace_clock() - e0;
-        mbar_expect_tx(&sc->kv_full[stage], C::QT);
-        load_kv_tile<D>(kv == 0 ? mk : mv, sStage + stage * C::QT, row0 + kt * kTileRows, &sc->kv_full[stage]);
+        if (leader) mbar_expect_tx(&sc->kv_full[stage], CG * C::KVB);
+        const uint32_t dst = sStage + stage * C::KVB;
+        if (kv == 0)
+          load_k_share<D, CG>(mk, dst, row0 + kt * kTileRows, rank, &sc->kv_full[stage], bar_cl(&sc->kv_full[stage]));
+        else
+          load_v_share<D, CG>(mv, dst, row0 + kt * kTileRows, rank, &sc->kv_full[stage], bar_cl(&sc->kv_full[stage]));
         cnt.kv++;
       }
     }
-    if (ok && t > 0) {
+    if (ok && t > 0 && leader) {
       if (pend_n == 4 && !resolve_one(true)) ok = false;
       pend_step[pend_n] = t;
       pend_load[pend_n] = cnt.kv - 1;
@@ -594,66 +673,71 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
   return starved;
 }
 
-// Tensor-core issue.  The tensor core's instruction queue is only a few MMAs
-// deep, so an issuing thread stays busy for about as long as its MMAs run.
-// NT = 2: one thread issues for both query tiles, interleaved
+// Tensor-core issue (one thread; in a pair, the even CTA's, for both CTAs).  The tensor
+// core's instruction queue is only a few MMAs deep, so the issuing thread stays busy
+// for about as long as its MMAs run.  It issues for both query tiles, interleaved:
 //   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
-// NT = 1: one thread per query tile (warp 1 + i), each PV_i(j) S_i(j+1).
-// PV_i(j) reads P_i(j), which overlays S_i(j) in tensor memory, so S_i(j+1) is
-// issued right behind it (tensor-core instructions of one thread run in order).
-template <int D, int NT>
-__device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, int i0,
-                           Counters& cnt) {
-  using C = Cfg<D>;
+// PV_i(j) reads P_i(j), which overlays S_i(j) in tensor memory, so S_i(j+1) is issued
+// right behind it (tensor-core instructions of one thread run in order).
+template <int D, int CG>
+__device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, Counters& cnt) {
+  using C = Cfg<D, CG>;
   const Geometry& G = p.geo;
-  constexpr uint32_t IQK = idesc_bf16_f32(128, 128, false);
-  constexpr uint32_t IPV = idesc_bf16_f32(128, D, true);
+  constexpr uint32_t M = kTileRows * CG;  // query rows per MMA: the pair's two tiles i stacked
+  constexpr uint32_t IQK = idesc_bf16_f32(M, 128, false);
+  constexpr uint32_t IPV = idesc_bf16_f32(M, D, true);
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // 8-row (K-major) / 8-key (V, MN-major) groups 1024 B apart
   const uint32_t sStage = smem_base + 2 * C::QT;
   auto stage_of = [](uint32_t c) { return c % C::NSTAGE; };
   auto par_of = [](uint32_t c) { return (c / C::NSTAGE) & 1u; };
   auto issue_s = [&](int i, uint32_t kstage) {
     const uint32_t q_lo = sdesc_lo(smem_base + i * C::QT, 16);
-    const uint32_t b_lo = sdesc_lo(sStage + kstage * C::QT, 16);
+    const uint32_t b_lo = sdesc_lo(sStage + kstage * C::KVB, 16);
     const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-      mma_ss_w(tS, q_lo + off, kHi, b_lo + off, kHi, IQK, kk > 0 ? 1u : 0u);
+      const uint32_t a_off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+      const uint32_t b_off = ((kk / 4) * C::KBLK + (kk % 4) * 32) >> 4;
+      mma_ss_cg<CG>(tS, q_lo + a_off, kHi, b_lo + b_off, kHi, IQK, kk > 0 ? 1u : 0u);
     }
-    mma_commit(&sc->s_full[i]);
-    mma_commit(&sc->kv_empty[kstage]);
+    mma_commit_cg<CG>(&sc->s_full[i]);
+    mma_commit_cg<CG>(&sc->kv_empty[kstage]);
   };
-  auto issue_pv = [&](int i, uint32_t vstage, bool first) {
-    const uint32_t b_lo = sdesc_lo(sStage + vstage * C::QT, 16384);  // V halves of 64 columns 16 KB apart
+  // PV_i(j) part by part: the K = 16 steps over the keys of each published part of P
+  auto issue_pv = [&](int i, uint32_t vstage, bool first, uint32_t parity) -> bool {
+    // V share MN-major: 64-column halves 16 KB apart (a pair's CTA holds one half)
+    const uint32_t b_lo = sdesc_lo(sStage + vstage * C::KVB, 16384);
     const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = sc->tmem_base + (i ? C::COL_O1 : C::COL_O0);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-      mma_ts_w(tO, tS + kk * 8, b_lo + kk * (2048 >> 4), kHi, IPV, (first && kk == 0) ? 0u : 1u);
-    mma_commit(&sc->o_full[i]);
-    mma_commit(&sc->kv_empty[vstage]);
+    for (int part = 0; part < kPParts; ++part) {
+      if (!wait_bar<CG == 2>(&sc->p_full[i][part], parity, p, sc, SITE_P_FULL)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = part * (8 / kPParts); kk < (part + 1) * (8 / kPParts); ++kk)
+        mma_ts_cg<CG>(tO, tS + kk * 8, b_lo + kk * (2048 >> 4), kHi, IPV, (first && kk == 0) ? 0u : 1u);
+    }
+    mma_commit_cg<CG>(&sc->o_full[i]);
+    mma_commit_cg<CG>(&sc->kv_empty[vstage]);
+    return true;
   };
   const uint32_t n = (uint32_t)item_tiles(G, it);
   uint32_t ck = cnt.kv;  // load index of K_0 of this item (the producer loads K_j, V_j alternately)
   cnt.kv += 2u * n;
   unsigned long long tr_issue = 0, tr_kv = 0;
-  for (int u = 0; u < NT; ++u)
-    if (!wait_bar(&sc->q_full[i0 + u], cnt.items & 1u, p, sc, SITE_Q_FULL)) { sc->abort = 1; return; }
+  for (int i = 0; i < 2; ++i)
+    if (!wait_bar(&sc->q_full[i], cnt.items & 1u, p, sc, SITE_Q_FULL)) { sc->abort = 1; return; }
   if (!wait_bar(&sc->kv_full[stage_of(ck)], par_of(ck), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
   tc_fence_after();
-  for (int u = 0; u < NT; ++u) issue_s(i0 + u, stage_of(ck));
+  for (int i = 0; i < 2; ++i) issue_s(i, stage_of(ck));
   for (uint32_t jt = 0; jt < n; ++jt, ck += 2) {
     const uint32_t cv = ck + 1, cn = ck + 2;  // V_j, K_{j+1}
     const long long a0 = trace_clock();
     if (!wait_bar(&sc->kv_full[stage_of(cv)], par_of(cv), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
     tr_kv += trace_clock() - a0;
-    for (int u = 0; u < NT; ++u) {
-      const int i = i0 + u;
-      if (!wait_bar(&sc->p_full[i], (cnt.tiles + jt) & 1u, p, sc, SITE_P_FULL)) { sc->abort = 1; return; }
+    for (int i = 0; i < 2; ++i) {
       const long long a2 = trace_clock();
-      tc_fence_after();
-      issue_pv(i, stage_of(cv), jt == 0);
+      if (!issue_pv(i, stage_of(cv), jt == 0, (cnt.tiles + jt) & 1u)) { sc->abort = 1; return; }
       if (jt + 1 < n) {
         const long long b0 = trace_clock();
         if (!wait_bar(&sc->kv_full[stage_of(cn)], par_of(cn), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
@@ -684,16 +768,15 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
   return fmaxf(fmax3(x0, x1, x2), fmaxf(x3, x4));
 }
 
-// p = 2^(s*sl2 - m) for the 128 scores of a row, written as bf16 pairs into the
-// 64 TMEM columns at tP (16 columns at a time, so few packed values are live);
-// returns the fp32 sum of p.  When POLY, every fourth pair takes the FMA-pipe
-// polynomial instead of MUFU (off-diagonal tiles only: no -inf there).
-template <bool POLY>
-__device__ __forceinline__ float exp_row(const float (&s)[128], float sl2, float m, uint32_t tP) {
+// p = 2^(s*sl2 - m) for scores [32*B0, 32*B1) of a row, written as bf16 pairs into TMEM
+// columns [16*B0, 16*B1) at tP (16 columns at a time, so few packed values are live);
+// the fp32 sums of p accumulate in acc.  When POLY, one in kPolyEvery pairs takes the
+// FMA-pipe polynomial instead of MUFU (off-diagonal tiles only: no -inf there).
+template <bool POLY, int B0, int B1>
+__device__ __forceinline__ void exp_blocks(const float (&s)[128], float sl2, float m, uint32_t tP, uint64_t (&acc)[4]) {
   const uint64_t scale2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m, -m);
-  uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {
+  for (int blk = B0; blk < B1; ++blk) {
     uint32_t pk[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
@@ -701,7 +784,8 @@ __device__ __forceinline__ float exp_row(const float (&s)[128], float sl2, float
       const uint64_t x = fma2(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
       float x0, x1, y0, y1;
       f2_unpack(x, x0, x1);
-      if (POLY && kPolyEvery > 0 && (e % kPolyEvery) == kPolyEvery - 1) {
+      constexpr int kEvery = kPolyEvery > 0 ? kPolyEvery : 1;
+      if (POLY && kPolyEvery > 0 && (e % kEvery) == kEvery - 1) {
         exp2_poly_pair(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f), y0, y1);
       } else {
         y0 = ex2_approx(x0);
@@ -712,6 +796,8 @@ __device__ __forceinline__ float exp_row(const float (&s)[128], float sl2, float
     }
     tmem_st16(tP + blk * 16, pk);
   }
+}
+__device__ __forceinline__ float acc_sum(const uint64_t (&acc)[4]) {
   float a0, a1, b0, b1, c0, c1, d0, d1;
   f2_unpack(acc[0], a0, a1);
   f2_unpack(acc[1], b0, b1);
@@ -720,15 +806,34 @@ __device__ __forceinline__ float exp_row(const float (&s)[128], float sl2, float
   return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
 }
 
-// One softmax warpgroup per 128-row query tile i.
-template <int D>
-__device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, int i, Counters& cnt) {
-  using C = Cfg<D>;
+// One softmax warpgroup per 128-row query tile i of the CTA (in a pair, CTA `rank`
+// holds query tiles 2*rank and 2*rank + 1 of the item).
+template <int D, int CG>
+__device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, int i, uint32_t rank, Counters& cnt) {
+  using C = Cfg<D, CG>;
   const Geometry& G = p.geo;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quarter = warp % 4;
-  const int row = quarter * 32 + lane;                         // TMEM lane = tile row
-  const int q_local = it.qp * kItemRows + i * kTileRows + row;  // position within the shard
+  const int row = quarter * 32 + lane;  // TMEM lane = tile row
+  const int tile = it.qp * G.item_qt + 2 * (int)rank + i;  // query tile within the shard
+  const int q_local = tile * kTileRows + row;               // position within the shard
+  // P ready, per part: one arrival per warp; in a pair the odd CTA's warps signal the even
+  // CTA's barrier with a 4-byte st.async each (16 bytes that its warp 0 expects)
+  const uint32_t p_full_cl = CG == 2 ? mapa_shared(smem_u32(&sc->p_full[i][0]), 0) : 0u;
+  const uint32_t p_sink_cl = CG == 2 ? mapa_shared(smem_u32(&sc->p_sink[quarter]), 0) : 0u;
+  auto publish = [&](int part) {
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (CG == 1 || rank == 0) {
+        if (CG == 2 && quarter == 0) mbar_expect_tx(&sc->p_full[i][part], 16);
+        else mbar_arrive(&sc->p_full[i][part]);
+      } else {
+        st_async_signal(p_sink_cl, 1u, p_full_cl + 8u * (uint32_t)part);
+      }
+    }
+  };
   const uint32_t lane_base = sc->tmem_base + ((uint32_t)(quarter * 32) << 16);
   const uint32_t tS = lane_base + (i ? C::COL_S1 : C::COL_S0);
   const uint32_t tO = lane_base + (i ? C::COL_O1 : C::COL_O0);
@@ -757,10 +862,10 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
 #pragma unroll
         for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(r[e]);
       }
-      // causal mask on the shard's own chunk: key position kt*128 + c > q_local.  Only the
-      // tile on this query tile's diagonal (and, for query tile 0, the one after it) can hold
+      // causal mask on the shard's own chunk: key position kt*128 + c > q_local.  Only key
+      // tiles from this query tile's diagonal on (up to the item's last diagonal) can hold
       // masked keys; the test is per tile so that it is the same for every lane of the warp.
-      const bool diag = G.causal && t == 0 && kt >= 2 * it.qp + i;
+      const bool diag = G.causal && t == 0 && kt >= tile;
       if (diag) {
         const int lim = q_local - kt * kTileRows;
 #pragma unroll
@@ -790,11 +895,28 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
       }
       m_run = m_new;
       const float m_use = m_run == -INFINITY ? 0.0f : m_run;
-      const float sum = diag ? exp_row<false>(s, sl2, m_use, tS) : exp_row<true>(s, sl2, m_use, tS);
-      tmem_st_wait();
-      l_run += sum;
-      tc_fence_before();
-      mbar_arrive(&sc->p_full[i]);  // this thread's row of P is in tensor memory
+      uint64_t acc[4] = {0, 0, 0, 0};
+      constexpr int BP = 4 / kPParts;  // 32-key blocks per part
+      if (diag) {
+        exp_blocks<false, 0, BP>(s, sl2, m_use, tS, acc);
+      } else {
+        exp_blocks<true, 0, BP>(s, sl2, m_use, tS, acc);
+      }
+      publish(0);
+      if constexpr (kPParts >= 2) {
+        if (diag) exp_blocks<false, BP, 2 * BP>(s, sl2, m_use, tS, acc);
+        else exp_blocks<true, BP, 2 * BP>(s, sl2, m_use, tS, acc);
+        publish(1);
+      }
+      if constexpr (kPParts == 4) {
+        if (diag) exp_blocks<false, 2, 3>(s, sl2, m_use, tS, acc);
+        else exp_blocks<true, 2, 3>(s, sl2, m_use, tS, acc);
+        publish(2);
+        if (diag) exp_blocks<false, 3, 4>(s, sl2, m_use, tS, acc);
+        else exp_blocks<true, 3, 4>(s, sl2, m_use, tS, acc);
+        publish(3);
+      }
+      l_run += acc_sum(acc);
       tr_busy += trace_clock() - c1;
     }
   }
@@ -836,31 +958,55 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
 // ------------------------------------------------------------------------------------------------
 // The persistent kernel
 // ------------------------------------------------------------------------------------------------
-template <int D>
+// Task boundary: every thread of the compute unit (the CTA, or both CTAs of a pair).
+template <int CG>
+__device__ __forceinline__ void unit_sync() {
+  if constexpr (CG == 1)
+    __syncthreads();
+  else
+    cluster_sync();
+}
+// The unit's command, written by thread 0 of the unit's first CTA before unit_sync().
+template <int CG>
+__device__ __forceinline__ void read_cmd(SmemCtl& sc, uint32_t rank, int& cmd, int& arg) {
+  if (CG == 1 || rank == 0) {
+    cmd = sc.cmd;
+    arg = sc.arg;
+  } else {
+    cmd = (int)ld_shared_cluster(mapa_shared(smem_u32(&sc.cmd), 0));
+    arg = (int)ld_shared_cluster(mapa_shared(smem_u32(&sc.arg), 0));
+  }
+}
+
+template <int D, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_sk, const __grid_constant__ CUtensorMap tm_sv) {
-  using C = Cfg<D>;
+  using C = Cfg<D, CG>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ SmemCtl sc;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sc.q_full[i], 1);
       mbar_init(&sc.s_full[i], 1);
-      mbar_init(&sc.p_full[i], 128);  // every softmax thread of tile i arrives once per KV tile
+      // one arrival per softmax warp of tile i per part (in a pair, the even CTA's four
+      // warps, the first with the 16 bytes the odd CTA's warps send)
+      for (int part = 0; part < 4; ++part) mbar_init(&sc.p_full[i][part], 4);
       mbar_init(&sc.o_full[i], 1);
     }
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&sc.kv_full[s], 1);
-      mbar_init(&sc.kv_empty[s], 2);  // both softmax warpgroups commit their reads of every K/V tile
+      mbar_init(&sc.kv_empty[s], 2);  // both query tiles' MMAs commit their reads of every K/V tile
     }
     for (int s = 0; s < C::NB; ++s) mbar_init(&sc.stg[s], 1);
-    mbar_init(&sc.drain, kMmaIssuers);  // one commit from each MMA-issuing thread
+    mbar_init(&sc.drain, 1);
     sc.abort = 0;
+    sc.peer_held = 0;
     fence_barrier_init();
     if (blockIdx.x == 0) {
       unsigned long long z = 0;
@@ -876,18 +1022,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_sv);
   }
   if (warp == 1) {
-    tmem_alloc(&sc.tmem_base, C::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_cg<CG>(&sc.tmem_base, C::TMEM_COLS);
+    tmem_relinquish_cg<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the other CTA's barriers exist before any remote arrival
   tc_fence_after();
   // Each warpgroup role runs its own loop under its own register budget; the two
-  // loops meet at the same CTA barriers at every task boundary.
+  // loops meet at the same unit barriers at every task boundary.
   Counters cnt{0, 0, 0};
   if (warp < 4) {
     regs_dec<kRegsCtl>();
-    uint32_t stg_phase[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t stg_phase[16] = {};
+    StagePending pend;  // thread 0: flag of the last staged piece, not yet published
     bool was_staging = false;
     StageTicket ticket;
     long long t_task = 0;
@@ -895,95 +1043,117 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t idle_since = 0;  // first idle poll of the current idle stretch (0 = not idle)
     while (true) {
       if (threadIdx.x == 0) {
-        decide(p, &sc, was_staging, ticket);
+        if (rank == 0) decide<CG>(p, &sc, was_staging, ticket);
         t_task = clock64();
       }
-      __syncthreads();
-      const int cmd = sc.cmd, arg = sc.arg;
+      unit_sync<CG>();
+      int cmd, arg;
+      read_cmd<CG>(sc, rank, cmd, arg);
       if (cmd == CMD_EXIT) break;
+      int done_kind = cmd;  // thread 0: CMD_STAGE (a piece was staged), CMD_COMPUTE or CMD_IDLE
+      // a deferred publication waits only while this CTA goes straight on to another piece
+      if (threadIdx.x == 0 && cmd != CMD_STAGE) publish_pending(pend);
       if (cmd == CMD_STAGE) {
-        if (threadIdx.x == 0) run_staging<D>(p, &sc, smem_base, arg, stg_phase);
+        if (threadIdx.x == 0) {
+          const int task = try_claim_staging(p, ticket);
+          if (task >= 0) {
+            run_staging<D, CG>(p, &sc, smem_base, task, stg_phase, pend);
+            idle_since = 0;
+          } else {
+            publish_pending(pend);
+            done_kind = CMD_IDLE;
+            atomicAdd(&p.ctrl->idle_polls, 1ull);
+            // a CTA that finds no claimable work for longer than the wait bound reports it
+            const uint64_t now = globaltimer_ns();
+            if (idle_since == 0) idle_since = now;
+            else if (now - idle_since > p.timeout_ns) raise_error(p, SITE_IDLE);
+            nanosleep_ns(500);
+          }
+          // the pair's role decision needs to know whether this CTA still holds a ticket
+          if constexpr (CG == 2)
+            if (rank == 1) st_shared_cluster(mapa_shared(smem_u32(&sc.peer_held), 0), ticket.held >= 0 ? 1u : 0u);
+        }
       } else if (cmd == CMD_COMPUTE) {
         const ItemCoord it = item_coord(p.geo, arg);
         if (warp == 0 && lane == 0)
-          starved = producer<D>(p, &sc, smem_base, it, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
-        else if (kMmaIssuers == 2 && (warp == 1 || warp == 2) && lane == 0)
-          mma_issuer<D, 1>(p, &sc, smem_base, it, warp - 1, cnt);
-        else if (kMmaIssuers == 1 && warp == 1 && lane == 0)
-          mma_issuer<D, 2>(p, &sc, smem_base, it, 0, cnt);
+          starved = producer<D, CG>(p, &sc, smem_base, it, rank, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
+        else if (warp == 1 && lane == 0 && rank == 0)
+          mma_issuer<D, CG>(p, &sc, smem_base, it, cnt);
         cnt.items++;
         cnt.tiles += (uint32_t)item_tiles(p.geo, it);
-      } else if (threadIdx.x == 0) {
-        atomicAdd(&p.ctrl->idle_polls, 1ull);
-        // a CTA that finds no claimable work for longer than the wait bound reports it
-        const uint64_t now = globaltimer_ns();
-        if (idle_since == 0) idle_since = now;
-        else if (now - idle_since > p.timeout_ns) raise_error(p, SITE_IDLE);
-        nanosleep_ns(500);
+        if (threadIdx.x == 0) idle_since = 0;
       }
-      if (threadIdx.x == 0 && cmd != CMD_IDLE) idle_since = 0;
       tc_fence_before();
-      __syncthreads();
+      unit_sync<CG>();
       tc_fence_after();
-      if (threadIdx.x == 0 && cmd != CMD_IDLE) {
+      if (threadIdx.x == 0 && done_kind != CMD_IDLE) {
         long long busy = clock64() - t_task;
-        if (cmd == CMD_COMPUTE) {
+        if (done_kind == CMD_COMPUTE) {
           busy -= starved.all;  // compute cost excludes waiting for staged data ...
           atomicAdd(&p.ctrl->starve_cycles, (unsigned long long)(starved.late > 0 ? starved.late : 0));  // ... charged to staging
         }
         const unsigned long long dt = (unsigned long long)(busy > 0 ? busy : 0);
-        if (cmd == CMD_STAGE) {
+        if (done_kind == CMD_STAGE) {
           atomicAdd(&p.ctrl->stage_cycles, dt);
           atomicAdd(&p.ctrl->stage_done, 1ull);
         } else {
-          const ItemCoord it = item_coord(p.geo, arg);
+          // cycles from every CTA of the unit (the cost of a tile in CTA-cycles); tiles and items once
           atomicAdd(&p.ctrl->compute_cycles, dt);
-          atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles(p.geo, it));
-          atomicAdd(&p.ctrl->compute_items, 1ull);
+          if (rank == 0) {
+            const ItemCoord it = item_coord(p.geo, arg);
+            atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles(p.geo, it));
+            atomicAdd(&p.ctrl->compute_items, 1ull);
+          }
         }
         const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
         if (p.mode == PSR_ADAPTIVE && (tick % (uint32_t)p.ctrl_period) == 0) controller_update(p);
       }
     }
     // drain: every tcgen05 op issued by this CTA has completed before TMEM is released
-    if ((warp == 1 || (kMmaIssuers == 2 && warp == 2)) && lane == 0) {
-      mma_commit(&sc.drain);
+    if (warp == 1 && lane == 0 && rank == 0) {
+      mma_commit_cg<CG>(&sc.drain, 1);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(&sc.drain, 0)) {
         if (globaltimer_ns() - t0 > 100000000ull) break;
       }
     }
     if (threadIdx.x == 0) {
+      publish_pending(pend);
       bulk_wait<0>();
-      // every TMA load this CTA issued has landed (normally already true)
-      const uint64_t t0 = globaltimer_ns();
-      for (uint32_t s = 0; s < (uint32_t)C::NSTAGE && s < cnt.kv; ++s) {
-        const uint32_t fills = (cnt.kv - s + C::NSTAGE - 1) / C::NSTAGE;  // loads that used stage s
-        while (!mbar_try_wait(&sc.kv_full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      // every TMA load of a compute item has landed (normally already true); a pair's
+      // loads are all counted on the even CTA's barriers
+      if (rank == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t s = 0; s < (uint32_t)C::NSTAGE && s < cnt.kv; ++s) {
+          const uint32_t fills = (cnt.kv - s + C::NSTAGE - 1) / C::NSTAGE;  // loads that used stage s
+          while (!mbar_try_wait(&sc.kv_full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+          }
         }
       }
     }
   } else {
     regs_inc<kRegsSoftmax>();
     while (true) {
-      __syncthreads();
-      const int cmd = sc.cmd, arg = sc.arg;
+      unit_sync<CG>();
+      int cmd, arg;
+      read_cmd<CG>(sc, rank, cmd, arg);
       if (cmd == CMD_EXIT) break;
       if (cmd == CMD_COMPUTE) {
         const ItemCoord it = item_coord(p.geo, arg);
-        softmax_wg<D>(p, &sc, it, warp < 8 ? 0 : 1, cnt);
+        softmax_wg<D, CG>(p, &sc, it, warp < 8 ? 0 : 1, rank, cnt);
         cnt.items++;
         cnt.tiles += (uint32_t)item_tiles(p.geo, it);
       }
       tc_fence_before();
-      __syncthreads();
+      unit_sync<CG>();
       tc_fence_after();
     }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while the other may still signal it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(sc.tmem_base, C::TMEM_COLS);
+  if (warp == 1) tmem_dealloc_cg<CG>(sc.tmem_base, C::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1023,24 +1193,39 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows][d] bf16, box = 64 columns x 128 rows, 128-byte swizzle
-static bool make_tmap(CUtensorMap* m, const void* base, long long rows, int d) {
+// [rows][d] bf16, box = 64 columns x box_rows rows, 128-byte swizzle
+static bool make_tmap(CUtensorMap* m, const void* base, long long rows, int d, int box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int max_group_items(int n_cta) {
-  // the compute CTAs must be able to hold a whole group at once; leave room for
-  // at least a quarter of the CTAs to stage
-  int m = n_cta - n_cta / 4 - 1;
+static int max_group_items(int n_units) {
+  // the compute units must be able to hold a whole group at once; leave room for
+  // at least a quarter of the units to stage
+  int m = n_units - n_units / 4 - 1;
   return m < 1 ? 1 : m;
+}
+
+#ifndef PSR_PAIRS
+#define PSR_PAIRS 0
+#endif
+// CTAs per compute unit for a shape.  Built with PSR_PAIRS=1: CTA pairs for d = 128 when a
+// shard holds whole 512-row items (a pair halves the K/V bytes each SM receives per flop).
+// Off by default: measured on GB300 the pair kernel computes ~4 % slower per SM (the softmax
+// of both CTAs gates every PV), and two staging CTAs of one pair copy at ~30 GB/s each
+// against ~50 GB/s for single CTAs, so the single-CTA kernel is faster at every split.
+static int units_cg(const psr_shape* sh, int n_cta) {
+  return (PSR_PAIRS && sh->d == 128 && sh->P > 0 && sh->S % sh->P == 0 && (sh->S / sh->P) % (2 * kCtaRows) == 0 &&
+          n_cta >= 4)
+             ? 2
+             : 1;
 }
 
 static int shape_geometry(const psr_shape* sh, Geometry& G, int n_cta) {
@@ -1052,24 +1237,27 @@ static int shape_geometry(const psr_shape* sh, Geometry& G, int n_cta) {
   if (!(sh->scale == sh->scale)) return PSR_ERR_ARG;  // NaN
   const long long rows_q = (long long)sh->B * sh->Hq * sh->S;
   if (rows_q >= (1LL << 31) || rows_q * sh->d >= (1LL << 40)) return PSR_ERR_UNSUPPORTED;
-  const int rc = geometry_init(G, sh->B, sh->Hq, sh->Hkv, sh->S, sh->P, sh->d, sh->causal, max_group_items(n_cta));
+  const int cg = units_cg(sh, n_cta);
+  const int rc =
+      geometry_init(G, sh->B, sh->Hq, sh->Hkv, sh->S, sh->P, sh->d, sh->causal, max_group_items(n_cta / cg), cg);
   if (rc == 1) return PSR_ERR_ARG;
   if (rc != 0) return PSR_ERR_UNSUPPORTED;
   if (2LL * G.n_groups * G.L >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;  // slot rows index with int32
   return PSR_OK;
 }
 
-template <int D>
+template <int D, int CG>
 static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(ring_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+  auto kern = ring_attn_kernel<D, CG>;
+  std::call_once(once, [kern] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, CG>::SMEM);
     if (attr_err != cudaSuccess) return;
     // the warpgroup register split must fit inside what the launch allocates, or the
     // increasing warpgroups would wait forever: refuse to launch otherwise
     cudaFuncAttributes fa;
-    attr_err = cudaFuncGetAttributes(&fa, ring_attn_kernel<D>);
+    attr_err = cudaFuncGetAttributes(&fa, kern);
     if (attr_err == cudaSuccess && fa.numRegs * kThreads < 128 * kRegsCtl + 256 * kRegsSoftmax)
       attr_err = cudaErrorInvalidConfiguration;
   });
@@ -1077,14 +1265,39 @@ static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_cta);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<D, CG>::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: they wait on each other
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: they wait on each other
+  attr[na].val.cooperative = 1;
+  ++na;
+  if (CG == 2) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    // every pair must be resident at once
+    int max_clusters = 0;
+    cfg.attrs = attr + 1;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters * 2 < n_cta) return cudaErrorCooperativeLaunchTooLarge;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ring_attn_kernel<D>, kp, maps[0], maps[1], maps[2], maps[3], maps[4]);
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp, maps[0], maps[1], maps[2], maps[3], maps[4]);
+  if (e != cudaSuccess && CG == 2) {
+    // cooperative launch of clusters unavailable: the occupancy check above still
+    // guarantees that all pairs fit on the device at once
+    cudaGetLastError();
+    cfg.attrs = attr + 1;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, kp, maps[0], maps[1], maps[2], maps[3], maps[4]);
+  }
+  return e;
 }
 
 }  // namespace psr
@@ -1135,10 +1348,12 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   DeviceInfo di;
   if (!device_info(di)) return PSR_ERR_CUDA;
   if (di.cc_major != 10 || di.cc_minor != 3) return PSR_ERR_UNSUPPORTED;
-  const int n_cta = di.n_sm;
   Geometry G;
-  int rc = shape_geometry(sh, G, n_cta);
+  int rc = shape_geometry(sh, G, di.n_sm);
   if (rc != PSR_OK) return rc;
+  const int cg = G.cg;
+  const int n_cta = di.n_sm / cg * cg;  // whole pairs
+  const int n_units = n_cta / cg;
   const WsLayout L = ws_layout(G);
   if (ws_bytes < L.total) return PSR_ERR_ARG;
 
@@ -1172,8 +1387,9 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.n_init = 2 * G.n_groups * G.n_pieces;
   kp.mode = pt.mode;
   kp.fault = pt.fault;
-  // clamps: at least one stager while staging remains; enough compute CTAs to hold a group
-  const int hard_max = n_cta - G.Gs - 1 < 1 ? 1 : n_cta - G.Gs - 1;
+  // clamps (in CTAs; a unit stages while unit * cg < n_s): at least one stager while
+  // staging remains; enough compute units to hold a group
+  const int hard_max = n_cta - cg * (G.Gs + 1) < 1 ? 1 : n_cta - cg * (G.Gs + 1);
   // default upper clamp: at most half of the CTAs stage (a compute item's ring steps are
   // sequential, so compute throughput needs items in flight as well as staged data)
   int n_max = pt.n_max > 0 ? pt.n_max : (n_cta / 2 < hard_max ? n_cta / 2 : hard_max);
@@ -1183,20 +1399,33 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.n_min = n_min;
   kp.n_max = n_max;
   const bool any_staging = kp.n_stage_total > 0;
-  // costs before any measurement: a staging piece moves 2*piece_rows*d*2 bytes at ~48 GB/s per SM;
-  // a compute tile pair is 4*128*128*d flops at ~60 % of an SM's dense bf16 rate (8192 flop/clk)
-  kp.c_s0 = (float)((2.0 * G.piece_tiles * kTileRows * G.d * 2.0) / 48e9 * 1.9e9);
-  kp.c_p0 = (float)(4.0 * 128.0 * 128.0 * G.d / (0.6 * 8192.0));
+  // costs before any measurement (CTA-cycles), from GB300 measurements: a staging piece moves
+  // 2*piece_rows*d*2 bytes at ~50 GB/s per SM (32 KB tile copies; ~33 GB/s for d = 64's 16 KB
+  // ones) and takes no less than ~6500 cycles (its loads, stores and their completion do not
+  // overlap with another piece's); a compute tile (a CTA's two query tiles against one KV tile:
+  // QK^T and PV, 2 * 2*128*128*d flops) at ~60 % of an SM's dense bf16 rate (8192 flop/clk),
+  // but no less than the ~2800 cycles two 128x128 softmax tiles take whatever d is
+  const double piece_bytes = 2.0 * G.piece_tiles * kTileRows * G.d * 2.0;
+  const double copy_cycles = piece_bytes / (G.d >= 128 ? 50e9 : 33e9) * 1.95e9;
+  kp.c_s0 = (float)(copy_cycles > 6500.0 ? copy_cycles : 6500.0);
+  const double mma_cycles = 2.0 * 2.0 * 2.0 * 128.0 * 128.0 * G.d / (0.6 * 8192.0);
+  kp.c_p0 = (float)(cg * (mma_cycles > 2800.0 ? mma_cycles : 2800.0));
   int n_s;
   if (pt.mode == PSR_STATIC) {
     n_s = pt.n_staging;
     if (!any_staging) n_s = 0;
     else if (n_s < 1 || n_s > n_cta - 1) return PSR_ERR_ARG;
-    if (any_staging && n_cta - n_s < G.Gs) return PSR_ERR_ARG;  // a group could never be fully resident
+    // a group could never be fully resident
+    if (any_staging && n_units - (n_s + cg - 1) / cg < G.Gs) return PSR_ERR_ARG;
   } else {
+    // initial split: the rule on the prior costs with twice the staging cost.  The double
+    // buffer lets a group's staging run at most about one ring step ahead of its compute,
+    // and at launch every active group needs steps 1 and 2 at once, so the stagers need
+    // capacity above the average rate (measured best static splits for P = 4..16 sit near
+    // twice the balanced split); the measured costs and starvation then move the target
     n_s = pt.n_staging > 0 ? pt.n_staging
-                           : controller_rule(n_cta, (double)kp.n_stage_total, kp.c_s0, (double)kp.n_tiles_total,
-                                             kp.c_p0, n_min, n_max);
+                           : controller_rule(n_cta, (double)kp.n_stage_total, kStageHeadroom * kp.c_s0,
+                                             (double)kp.n_tiles_total, kp.c_p0, n_min, n_max);
     if (!any_staging) n_s = 0;
     else {
       if (n_s < n_min) n_s = n_min;
@@ -1204,20 +1433,23 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
     }
   }
   kp.n_s_init = n_s;
-  kp.lookahead = n_cta / G.Gs + 2;
+  kp.lookahead = n_units / G.Gs + 2;
   kp.ctrl_period = n_cta / 8 > 1 ? n_cta / 8 : 1;
 
   CUtensorMap maps[5];
   const long long rows_q = (long long)G.B * G.Hq * G.S, rows_kv = (long long)G.B * G.Hkv * G.S;
   const long long rows_slot = 2LL * G.n_groups * G.L;
-  if (!make_tmap(&maps[0], q, rows_q, G.d) || !make_tmap(&maps[1], k, rows_kv, G.d) ||
-      !make_tmap(&maps[2], v, rows_kv, G.d) || !make_tmap(&maps[3], kp.slot_k, rows_slot, G.d) ||
+  // K maps: a pair's CTA loads 64 of every 128 K rows
+  const int k_box = kTileRows / cg;
+  if (!make_tmap(&maps[0], q, rows_q, G.d) || !make_tmap(&maps[1], k, rows_kv, G.d, k_box) ||
+      !make_tmap(&maps[2], v, rows_kv, G.d) || !make_tmap(&maps[3], kp.slot_k, rows_slot, G.d, k_box) ||
       !make_tmap(&maps[4], kp.slot_v, rows_slot, G.d))
     return PSR_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
-  cudaError_t e = G.d == 128 ? launch<128>(kp, maps, n_cta, st) : launch<64>(kp, maps, n_cta, st);
+  cudaError_t e = cg == 2 ? launch<128, 2>(kp, maps, n_cta, st)
+                          : (G.d == 128 ? launch<128, 1>(kp, maps, n_cta, st) : launch<64, 1>(kp, maps, n_cta, st));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PSR_ERR_CUDA;

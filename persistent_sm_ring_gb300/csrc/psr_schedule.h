@@ -7,9 +7,11 @@
 // r only when j <= r, i.e. steps t = 0..r.
 //
 // Units of work:
-//  * compute item  = 256 query rows (two 128-row tiles) of one (b, hq) in
-//                    shard r, carried through all of r's ring steps with the
-//                    accumulators resident in tensor memory;
+//  * compute item  = the query rows one compute unit carries through all of
+//                    shard r's ring steps with the accumulators resident in
+//                    tensor memory, for one (b, hq): 256 rows (two 128-row
+//                    tiles) for a single CTA, 512 rows (two tiles in each CTA)
+//                    for a CTA pair that shares every K/V tile;
 //  * group         = the items that read the same ring slot: shard r, batch b,
 //                    KV head kvh (all Hq/Hkv query heads of it) and, when a
 //                    group would exceed the deadlock bound, a sub-group index;
@@ -35,18 +37,21 @@
 namespace psr {
 
 constexpr int kTileRows = 128;  // rows per Q tile and per KV tile
-constexpr int kItemRows = 256;  // query rows per compute item (two tiles)
+constexpr int kCtaRows = 256;   // query rows one CTA holds during an item (two tiles)
 constexpr int kStagePieceMaxTiles = 8;  // staging piece: a quarter of a chunk, 1..8 tiles
 
 struct Geometry {
   int B, Hq, Hkv, S, P, d, causal;
   int L;         // shard length S / P
   int gqa;       // Hq / Hkv
-  int q_pairs;   // items per (b, hq, shard): L / 256
+  int cg;        // CTAs per compute unit: 1, or 2 (a CTA pair)
+  int item_rows; // query rows per item: 256 * cg
+  int item_qt;   // 128-row query tiles per item: item_rows / 128
+  int q_blocks;  // items per (b, hq, shard): L / item_rows
   int kv_tiles;  // 128-row KV tiles per chunk: L / 128
   int piece_tiles;  // tiles per staging piece
   int n_pieces;     // staging pieces per chunk
-  int G;         // items sharing one (shard, b, kvh): gqa * q_pairs
+  int G;         // items sharing one (shard, b, kvh): gqa * q_blocks
   int n_sub;     // sub-groups per (shard, b, kvh)
   int Gs;        // items per group: G / n_sub
   int n_groups;  // P * B * Hkv * n_sub
@@ -59,18 +64,25 @@ struct ItemCoord {
   int n_steps;  // active ring steps of shard r
 };
 
-PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int d, int causal, int max_group) {
+// max_group: most items one group may hold (all of them must be able to run at once);
+// cg: CTAs per compute unit (1 or 2).
+PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int d, int causal, int max_group,
+                         int cg = 1) {
   G.B = B; G.Hq = Hq; G.Hkv = Hkv; G.S = S; G.P = P; G.d = d; G.causal = causal ? 1 : 0;
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || P < 1 || d < 1) return 1;
   if (Hq % Hkv != 0 || S % P != 0) return 1;
+  if (cg != 1 && cg != 2) return 1;
+  G.cg = cg;
+  G.item_rows = kCtaRows * cg;
+  G.item_qt = G.item_rows / kTileRows;
   G.L = S / P;
-  if (G.L % kItemRows != 0) return 2;
+  if (G.L % G.item_rows != 0) return 2;
   G.gqa = Hq / Hkv;
-  G.q_pairs = G.L / kItemRows;
+  G.q_blocks = G.L / G.item_rows;
   G.kv_tiles = G.L / kTileRows;
   G.piece_tiles = G.kv_tiles / 4 < 1 ? 1 : (G.kv_tiles / 4 > kStagePieceMaxTiles ? kStagePieceMaxTiles : G.kv_tiles / 4);
   G.n_pieces = (G.kv_tiles + G.piece_tiles - 1) / G.piece_tiles;
-  G.G = G.gqa * G.q_pairs;
+  G.G = G.gqa * G.q_blocks;
   // split a group into power-of-two sub-groups until it fits the bound
   G.n_sub = 1;
   while (G.G / G.n_sub > max_group && (G.G % (G.n_sub * 2)) == 0) G.n_sub *= 2;
@@ -111,30 +123,30 @@ PSR_HD ItemCoord item_coord(const Geometry& G, int n) {
   int sub;
   group_coord(G, c.g, c.r, c.b, c.kvh, sub);
   const int w = sub * G.Gs + (n % G.Gs);
-  c.hq = c.kvh * G.gqa + w / G.q_pairs;
-  c.qp = w % G.q_pairs;
+  c.hq = c.kvh * G.gqa + w / G.q_blocks;
+  c.qp = w % G.q_blocks;
   c.n_steps = steps_of_shard(G, c.r);
   return c;
 }
 
 // KV tiles an item consumes at ring step t: under the causal mask the local
-// chunk stops at the item's own diagonal (tiles 0 .. 2*qp+1).
+// chunk stops at the diagonal of the item's last row (tiles 0 .. (qp+1)*item_qt - 1).
 PSR_HD int tiles_at_step(const Geometry& G, const ItemCoord& c, int t) {
-  return (G.causal && t == 0) ? (2 * c.qp + 2) : G.kv_tiles;
+  return (G.causal && t == 0) ? (c.qp + 1) * G.item_qt : G.kv_tiles;
 }
 
 PSR_HD long long item_tiles(const Geometry& G, const ItemCoord& c) {
-  return G.causal ? (long long)(2 * c.qp + 2) + (long long)c.r * G.kv_tiles : (long long)G.P * G.kv_tiles;
+  return G.causal ? (long long)(c.qp + 1) * G.item_qt + (long long)c.r * G.kv_tiles : (long long)G.P * G.kv_tiles;
 }
 
 PSR_HD long long total_tiles(const Geometry& G) {
-  // per (b, hq): sum over shards and q-pairs
+  // per (b, hq): sum over shards and items
   long long per_bh = 0;
   if (G.causal) {
-    for (int r = 0; r < G.P; ++r)
-      per_bh += (long long)G.q_pairs * (G.q_pairs + 1) + (long long)G.q_pairs * r * G.kv_tiles;
+    const long long nb = G.q_blocks;
+    for (int r = 0; r < G.P; ++r) per_bh += (long long)G.item_qt * nb * (nb + 1) / 2 + nb * r * G.kv_tiles;
   } else {
-    per_bh = (long long)G.P * G.q_pairs * G.P * G.kv_tiles;
+    per_bh = (long long)G.P * G.q_blocks * G.P * G.kv_tiles;
   }
   return per_bh * G.B * G.Hq;
 }

@@ -7,7 +7,8 @@
 //  * flag / consumed indices stay below n_groups * P and the dynamic queue
 //    receives exactly dynamic_staging_tasks() pushes;
 //  * total_tiles() and total_staging_tasks() agree with direct enumeration.
-// Usage: schedule_check B Hq Hkv S P d causal max_group   -> prints "OK ..." or "FAIL ..."
+// Usage: schedule_check B Hq Hkv S P d causal max_group [cg]   -> prints "OK ..." or "FAIL ..."
+// (cg: CTAs per compute unit, 1 or 2; default 1)
 #include <cstdio>
 #include <cstdlib>
 #include <vector>
@@ -27,11 +28,11 @@ using namespace psr;
   } while (0)
 
 int main(int argc, char** argv) {
-  if (argc != 9) return 2;
-  int a[8];
-  for (int i = 0; i < 8; ++i) a[i] = std::atoi(argv[i + 1]);
+  if (argc != 9 && argc != 10) return 2;
+  int a[9] = {0, 0, 0, 0, 0, 0, 0, 0, 1};
+  for (int i = 0; i < argc - 1; ++i) a[i] = std::atoi(argv[i + 1]);
   Geometry G;
-  int rc = geometry_init(G, a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+  int rc = geometry_init(G, a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[8]);
   if (rc != 0) {
     std::printf("REJECT %d\n", rc);
     return 0;
@@ -46,9 +47,9 @@ int main(int argc, char** argv) {
     CHECK(c.g >= 0 && c.g < G.n_groups, "group %d", c.g);
     CHECK(c.b >= 0 && c.b < G.B && c.hq >= 0 && c.hq < G.Hq && c.r >= 0 && c.r < G.P, "coords item %d", n);
     CHECK(c.kvh == c.hq / G.gqa, "gqa mapping item %d", n);
-    CHECK(c.qp >= 0 && c.qp < G.q_pairs, "qp item %d", n);
-    const long long q_row = (long long)(c.b * G.Hq + c.hq) * G.S + (long long)c.r * G.L + (long long)c.qp * kItemRows;
-    for (int i = 0; i < 2; ++i) {
+    CHECK(c.qp >= 0 && c.qp < G.q_blocks, "qp item %d", n);
+    const long long q_row = (long long)(c.b * G.Hq + c.hq) * G.S + (long long)c.r * G.L + (long long)c.qp * G.item_rows;
+    for (int i = 0; i < G.item_qt; ++i) {
       const long long r0 = q_row + i * kTileRows;
       CHECK(r0 >= 0 && r0 + kTileRows <= rows_q, "q rows item %d", n);
       CHECK(r0 % kTileRows == 0, "q tile alignment");
@@ -72,10 +73,10 @@ int main(int argc, char** argv) {
           CHECK(r0 >= 0 && r0 + kTileRows <= rows_slot, "slot rows item %d", n);
         }
         if (G.causal && t == 0) {
-          // key tile kt of the local chunk vs the item's query tiles: only the
-          // last two tiles can be (partly) above the diagonal
-          const int q_first = c.qp * kItemRows, key_first = kt * kTileRows;
-          CHECK(key_first <= q_first + kTileRows, "fully masked key tile for both query tiles");
+          // key tile kt of the local chunk vs the item's query tiles: no key tile lies
+          // entirely above the diagonal of the item's last query tile
+          const int q_first = c.qp * G.item_rows, key_first = kt * kTileRows;
+          CHECK(key_first <= q_first + G.item_rows - kTileRows, "key tile masked for every query tile of the item");
         }
       }
       it_tiles += n_kt;

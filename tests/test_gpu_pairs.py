@@ -1,0 +1,84 @@
+"""The CTA-pair compute path (cta_group::2 MMAs with M = 256 across two CTAs, each CTA
+holding half of every K/V tile) against the fp64 oracle.
+
+Pairs are built only into the "pairs" variant of the library (libpsr_pairs.so); the
+default library uses single-CTA compute units.  Each case runs in a fresh process
+(one library per process) through the same C ABI, and checks that pair items ran
+(512 query rows per item) as well as parity with the tolerances of the other GPU tests.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = r"""
+import json, sys
+import numpy as np
+sys.path.insert(0, ROOT)
+import torch
+import oracle
+import ring_inputs as ri
+import persistent_sm_ring_gb300 as psr
+psr.build(variant="pairs")
+psr.load(variant="pairs")
+cases = [
+    ri.WORKLOADS["small"].with_(name="pair_nc", S=2048, P=2, d=128, seed=17),
+    ri.WORKLOADS["small"].with_(name="pair_gqa_c", B=2, Hq=4, Hkv=2, S=3072, P=3, d=128, causal=True, seed=18,
+                                qmul=2.0, kmul=2.0),
+    ri.WORKLOADS["small"].with_(name="pair_p1_c", S=1024, P=1, d=128, causal=True, seed=19),
+    ri.WORKLOADS["small"].with_(name="pair_p4_c", Hq=3, Hkv=3, S=6144, P=4, d=128, causal=True, seed=20),
+]
+out = []
+for w in cases:
+    q, k, v = ri.generate(w)
+    o_ref, lse_ref = oracle.for_workload(w, q, k, v)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    for part in (psr.make_partition(psr.ADAPTIVE), psr.make_partition(psr.STATIC, n_staging=3)):
+        o, lse, ws = psr.ring_attn_fwd(dev(q), dev(k), dev(v), P=w.P, causal=w.causal, scale=w.scale, partition=part)
+        st = psr.get_stats(ws)
+        o = o.view(-1, w.d).float().cpu().numpy().astype(np.float64)
+        lse = lse.view(-1).cpu().numpy().astype(np.float64)
+        out.append({"name": w.name, "mode": part.mode, "status": st["status"],
+                    "items_ok": st["compute_items"] == w.B * w.Hq * w.S // 512,
+                    "max_abs": float(np.abs(o - o_ref).max()),
+                    "rel": float(np.linalg.norm(o - o_ref) / np.linalg.norm(o_ref)),
+                    "lse": float(np.abs(lse - lse_ref).max()), "finite": bool(np.all(np.isfinite(o)))})
+# a dropped readiness flag: every pair must leave the kernel together and the context survive
+w = cases[3].with_(name="pair_fault", causal=False, seed=51)
+q, k, v = ri.generate(w)
+part = psr.make_partition(psr.ADAPTIVE, fault=psr.FAULT_DROP_FIRST_FLAG, timeout_ms=200)
+o, lse, ws = psr.ring_attn_fwd(dev(q), dev(k), dev(v), P=w.P, causal=False, scale=w.scale, partition=part)
+st = psr.get_stats(ws)
+out.append({"name": "fault", "status": st["status"], "site": st["error_site"]})
+o_ref, lse_ref = oracle.for_workload(w, q, k, v)
+o, lse, ws = psr.ring_attn_fwd(dev(q), dev(k), dev(v), P=w.P, causal=False, scale=w.scale)
+o = o.view(-1, w.d).float().cpu().numpy().astype(np.float64)
+out.append({"name": "after_fault", "status": psr.get_stats(ws)["status"], "max_abs": float(np.abs(o - o_ref).max())})
+print("RESULT " + json.dumps(out))
+"""
+
+
+def test_pair_kernel_parity_and_fault_exit():
+    pytest.importorskip("torch")
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    res = subprocess.run([sys.executable, "-c", SCRIPT.replace("ROOT", repr(ROOT), 1)], capture_output=True, text=True,
+                         timeout=900, cwd=ROOT)
+    lines = [l for l in res.stdout.splitlines() if l.startswith("RESULT ")]
+    assert res.returncode == 0 and lines, res.stdout[-2000:] + res.stderr[-3000:]
+    out = json.loads(lines[0][len("RESULT "):])
+    for r in out:
+        if r["name"] == "fault":
+            assert r["status"] != 0 and r["site"] in (1, 11), r
+        elif r["name"] == "after_fault":
+            assert r["status"] == 0 and r["max_abs"] <= 2e-2, r
+        else:
+            assert r["status"] == 0 and r["items_ok"] and r["finite"], r
+            assert r["max_abs"] <= 2e-2 and r["rel"] <= 5e-3 and r["lse"] <= 1e-3, r

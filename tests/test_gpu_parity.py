@@ -60,6 +60,12 @@ def check(o, lse, o_ref, lse_ref, what=""):
 _cache = {}
 
 
+def item_rows_allowed(w):
+    # single CTAs take 256-row items; a library built with CTA pairs takes 512-row items
+    # for d = 128 when a shard holds whole 512-row items
+    return (256, 512) if (w.d == 128 and (w.S // w.P) % 512 == 0) else (256,)
+
+
 def inputs(w):
     key = w
     if key not in _cache:
@@ -82,6 +88,12 @@ SMALL = [
     ri.WORKLOADS["small"].with_(name="p8_c_d128", S=2048, P=8, d=128, causal=True, seed=14),
     ri.WORKLOADS["small"].with_(name="b3_p5", B=3, Hq=4, Hkv=4, S=1280, P=5, seed=15),
     ri.WORKLOADS["long_s128k_c"].with_(name="outlier_small", S=4096, P=4, Hq=2, Hkv=2, seed=16),
+    # d = 128 with shards of whole 512-row items (CTA-pair items in a library built with pairs)
+    ri.WORKLOADS["small"].with_(name="l1024_nc", S=2048, P=2, d=128, seed=17),
+    ri.WORKLOADS["small"].with_(name="l1024_gqa_c", B=2, Hq=4, Hkv=2, S=3072, P=3, d=128, causal=True, seed=18,
+                                qmul=2.0, kmul=2.0),
+    ri.WORKLOADS["small"].with_(name="l1024_p1_c", S=1024, P=1, d=128, causal=True, seed=19),
+    ri.WORKLOADS["small"].with_(name="l1536_p4_c", Hq=3, Hkv=3, S=6144, P=4, d=128, causal=True, seed=20),
 ]
 
 
@@ -92,12 +104,15 @@ def test_small_all_rows(psr, w):
     o, lse, st = gpu_run(psr, w, q, k, v)
     check(o, lse, o_ref, lse_ref, w.name)
     assert st["staging_bytes"] == w.staging_bytes()
-    assert st["compute_items"] == w.B * w.Hq * w.S // 256
+    assert any(st["compute_items"] == w.B * w.Hq * w.S // r for r in item_rows_allowed(w))
 
 
 @pytest.mark.parametrize("n_s", [1, 3, 16])
-def test_small_static_partitions(psr, n_s):
-    w = ri.WORKLOADS["small"].with_(name="small_static", S=2048, P=8, causal=True, seed=21)
+@pytest.mark.parametrize("d", [64, 128])
+def test_small_static_partitions(psr, n_s, d):
+    # d = 128 with 512-row shards runs CTA pairs (a pair stages while 2 * pair < n_s)
+    w = ri.WORKLOADS["small"].with_(name=f"small_static_d{d}", S=4096 if d == 128 else 2048, P=8 if d == 64 else 4,
+                                    d=d, causal=True, seed=21)
     q, k, v = inputs(w)
     o_ref, lse_ref = oracle.for_workload(w, q, k, v)
     o, lse, st = gpu_run(psr, w, q, k, v, partition=psr.make_partition(psr.STATIC, n_staging=n_s))
@@ -196,9 +211,12 @@ def test_host_buffer_entry_point(psr):
     check(o, lh.numpy().astype(np.float64).reshape(-1), o_ref, lse_ref, "host entry")
 
 
-def test_dropped_flag_times_out_and_context_survives(psr):
+@pytest.mark.parametrize("d", [64, 128])
+def test_dropped_flag_times_out_and_context_survives(psr, d):
+    # d = 128 with 1024-row shards runs CTA pairs: both CTAs of every pair must leave together
     torch = _torch()
-    w = ri.WORKLOADS["small"].with_(name="fault", S=2048, P=8, seed=51)
+    w = ri.WORKLOADS["small"].with_(name=f"fault_d{d}", S=2048 if d == 64 else 4096, P=8 if d == 64 else 4, d=d,
+                                    seed=51)
     q, k, v = inputs(w)
     qd, kd, vd = to_dev(torch, q), to_dev(torch, k), to_dev(torch, v)
     part = psr.make_partition(psr.ADAPTIVE, fault=psr.FAULT_DROP_FIRST_FLAG, timeout_ms=200)

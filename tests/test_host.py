@@ -121,6 +121,22 @@ def test_schedule_bounds_and_coverage(schedule_check, shape):
     assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
 
 
+# CTA-pair items (512 query rows): shards whose length is a multiple of 512
+PAIR_SHAPES = [s for s in SHAPES if (s[3] // s[4]) % 512 == 0] + [(1, 2, 2, 2048, 2, 128, 1), (2, 8, 2, 3072, 3, 128, 1)]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_schedule_pair_items(schedule_check, shape):
+    out = subprocess.run([schedule_check, *map(str, shape), "56", "2"], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
+
+
+def test_schedule_pair_rejects_short_shards(schedule_check):
+    out = subprocess.run([schedule_check, "1", "16", "16", "16384", "64", "128", "0", "56", "2"], capture_output=True,
+                         text=True).stdout
+    assert out.startswith("REJECT")  # L = 256 cannot hold a 512-row pair item
+
+
 def test_schedule_splits_large_groups(schedule_check):
     # GQA with 4 query heads per KV head and L = 4096: 64 items read one slot; a bound of 20 splits it in 4
     out = subprocess.run([schedule_check, "2", "32", "8", "65536", "16", "128", "1", "20"], capture_output=True,
