@@ -54,10 +54,12 @@ constexpr bool kTrace = PSR_TRACE != 0;
 // neighbours, not under MUFU-bound ones), which costs more than it saves.
 constexpr int kPolyEvery = PSR_POLY_EVERY;
 #ifndef PSR_P_PARTS
-#define PSR_P_PARTS 2
+#define PSR_P_PARTS 1
 #endif
 // P of a query tile is published in this many parts (key ranges of 128 / kPParts), so
-// that the PV MMAs of the first keys run while the softmax computes the rest.
+// that the PV MMAs of the first keys can run while the softmax computes the rest.  One part
+// by default: measured on GB300 (single CTAs), the per-part store waits and arrivals cost
+// more than the overlap gains (1249 / 1185 / 1077 TFLOP/s for 1 / 2 / 4 parts).
 constexpr int kPParts = PSR_P_PARTS;
 static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P parts: 1, 2 or 4");
 __device__ __forceinline__ long long trace_clock() { return kTrace ? clock64() : 0; }
