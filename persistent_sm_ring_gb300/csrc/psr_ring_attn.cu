@@ -10,7 +10,7 @@
 //
 // On one GPU the P ring ranks are P shards held in HBM:
 //  * staging CTAs copy chunk (r - t) mod P of K and V into the ring slot
-//    (t & 1) of shard r with TMA bulk loads/stores through shared memory and
+//    (t mod 3) of shard r with TMA bulk loads/stores through shared memory and
 //    publish, per chunk, the count of completed 128-row tiles with a
 //    gpu-scope release after the bulk stores have completed;
 //  * compute units (one CTA, or a CTA pair when d = 128 and the shard length is a
@@ -71,7 +71,7 @@ constexpr int kTrajMax = 4096;
 
 struct Ctrl {
   uint32_t item_next;     // compute items dispensed
-  uint32_t init_next;     // static staging list: next piece to hand out (steps 1 and 2 of every group)
+  uint32_t init_next;     // static staging list: next piece to hand out (steps 1..kRingSlots of every group)
   uint32_t q_head;        // ready queue: next ticket
   uint32_t q_tail;        // ready queue: next entry to fill
   uint32_t target_ns;     // controller target + 1 (0 = not yet set)
@@ -89,7 +89,7 @@ struct Ctrl {
   unsigned long long stage_done, compute_items, compute_tiles;
   unsigned long long stage_bytes;
   unsigned long long role_switches, idle_polls;
-  unsigned long long starve_cycles;  // compute cycles spent waiting for ring steps >= 3 to be staged
+  unsigned long long starve_cycles;  // compute cycles spent waiting for staged ring steps (after a CTA's first item)
   // tracing build only (cycles summed over threads that record them)
   unsigned long long tr_softmax_wait, tr_softmax_busy, tr_mma_issue, tr_mma_wait_kv, tr_prod_wait_empty,
       tr_prod_wait_flag;
@@ -112,7 +112,7 @@ static WsLayout ws_layout(const Geometry& G) {
   w.consumed = off; off = align_up(off + n_fc * 4, 256);
   w.queue = off; off = align_up(off + (size_t)(dynamic_staging_tasks(G) * G.n_pieces + 1) * 4, 256);
   w.reset_bytes = off;  // everything above is zeroed before each launch
-  const size_t slot_elems = (size_t)2 * G.n_groups * G.L * G.d;
+  const size_t slot_elems = (size_t)kRingSlots * G.n_groups * G.L * G.d;
   w.slot_k = off; off = align_up(off + slot_elems * 2, 256);
   w.slot_v = off; off = align_up(off + slot_elems * 2, 256);
   w.total = off;
@@ -139,8 +139,8 @@ struct KParams {
   unsigned long long timeout_ns;
   unsigned long long n_tiles_total;
   unsigned long long n_stage_total;  // staging pieces in the launch
-  int n_dyn;          // ready-queue entries: pieces of the steps >= 3
-  int n_init;         // static list entries: pieces of steps 1 and 2 of every group
+  int n_dyn;          // ready-queue entries: pieces of the steps > kRingSlots
+  int n_init;         // static list entries: pieces of steps 1..kRingSlots of every group
   int mode;           // PSR_STATIC / PSR_ADAPTIVE
   int n_s_init;
   int n_min, n_max;   // effective clamp
@@ -253,7 +253,14 @@ __device__ int current_target(const KParams& p) {
 }
 
 constexpr unsigned long long kCtrlMinIntervalNs = 20000;  // re-evaluate at most every 20 us
-constexpr double kStageHeadroom = 2.0;  // initial split: staging capacity over the average rate
+#ifndef PSR_STAGE_HEADROOM
+#define PSR_STAGE_HEADROOM 200
+#endif
+#ifndef PSR_STARVE_WEIGHT
+#define PSR_STARVE_WEIGHT 100
+#endif
+constexpr double kStageHeadroom = PSR_STAGE_HEADROOM / 100.0;  // initial split: staging capacity over the average rate
+constexpr double kStarveWeight = PSR_STARVE_WEIGHT / 100.0;    // share of starved compute cycles charged to staging
 // The initial split stands until this fraction of the compute tiles is done: it covers the
 // ring's fill, when every active group needs its first staged steps at once and measured
 // costs are still dominated by start-up.
@@ -278,7 +285,7 @@ __device__ void controller_update(const KParams& p) {
   // The staging cost per piece counts the staging CTAs' busy cycles plus the cycles
   // compute items spent starved of staged data: both are what staging costs the launch.
   const unsigned long long sv = atomicAdd(&c->starve_cycles, 0ull);
-  const double C_s = (scy + (double)sv + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
+  const double C_s = (scy + kStarveWeight * (double)sv + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
   const double C_p = (ccy + (double)p.c_p0 * 64.0) / ((double)td + 64.0);
   int n = controller_rule((int)gridDim.x, R_s, C_s, R_p, C_p, p.n_min, p.n_max);
   const int cur = current_target(p);
@@ -310,10 +317,10 @@ __device__ void controller_update(const KParams& p) {
 // unit's role; a staging unit's CTAs then claim pieces each on its own.
 // ------------------------------------------------------------------------------------------------
 // Staging work comes from two lists, each claimed with one atomicAdd (a ticket):
-//  * the static list: pieces of steps 1 and 2 of every group, in group order (their
+//  * the static list: pieces of steps 1..kRingSlots of every group, in group order (their
 //    slots are fresh); taken only while the group is within the lookahead window
 //    of the compute dispense frontier;
-//  * the ready queue: pieces of steps >= 3, pushed by the compute CTA whose load
+//  * the ready queue: pieces of later steps, pushed by the compute CTA whose load
 //    completed the consumption of the slot they overwrite.  A ticket names one
 //    queue entry; the stager that holds it serves that entry once it has been
 //    published and does static work meanwhile, so no stager ever blocks and no
@@ -330,13 +337,13 @@ __device__ int claim_static_piece(const KParams& p) {
   for (int attempt = 0; attempt < 8; ++attempt) {
     const uint32_t i0 = ld_relaxed(&c->init_next);
     if (i0 >= (uint32_t)p.n_init) return -1;
-    const int g0 = (int)(i0 / (2u * G.n_pieces));
+    const int g0 = (int)(i0 / ((uint32_t)kRingSlots * G.n_pieces));
     const int frontier = (int)(ld_relaxed(&c->item_next) / (uint32_t)G.Gs);
     if (g0 > frontier + p.lookahead) return -1;
     const uint32_t i = atomicAdd(&c->init_next, 1u);
     if (i >= (uint32_t)p.n_init) return -1;
-    const int g = (int)(i / (2u * G.n_pieces));
-    const int step = 1 + (int)((i / G.n_pieces) % 2u);
+    const int g = (int)(i / ((uint32_t)kRingSlots * G.n_pieces));
+    const int step = 1 + (int)((i / G.n_pieces) % (uint32_t)kRingSlots);
     const int piece = (int)(i % G.n_pieces);
     if (step < group_steps(G, g)) return (g * G.P + step) * G.n_pieces + piece;
     // shard with fewer steps: nothing to stage for this entry; try the next one
@@ -412,7 +419,7 @@ __device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging, const S
 }
 
 // ------------------------------------------------------------------------------------------------
-// Staging task (thread 0): chunk (r - step) mod P of K and V -> slot (step & 1) of group g
+// Staging task (thread 0): chunk (r - step) mod P of K and V -> slot slot_of(step) of group g
 // ------------------------------------------------------------------------------------------------
 // A piece is copied as 2*n_kt units (K_kt and V_kt alternately), each a 128-row tile, through
 // NB shared-memory buffers: a load waits only for the buffer's previous store to have read
@@ -448,7 +455,7 @@ __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, i
   const int kt0 = piece * G.piece_tiles;
   const int n_kt = (G.kv_tiles - kt0) < G.piece_tiles ? (G.kv_tiles - kt0) : G.piece_tiles;
   const size_t src_off = ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L + (size_t)kt0 * kTileRows) * D;
-  const size_t slot_off = (((size_t)(step & 1) * G.n_groups + g) * (size_t)G.L + (size_t)kt0 * kTileRows) * D;
+  const size_t slot_off = (((size_t)slot_of(step) * G.n_groups + g) * (size_t)G.L + (size_t)kt0 * kTileRows) * D;
   uint32_t* flag = p.flags + (size_t)chunk * G.n_pieces + piece;
   const bool drop = (p.fault == PSR_FAULT_DROP_FIRST_FLAG) && (atomicAdd(&p.ctrl->fault_count, 1u) == 0u);
   if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
@@ -592,10 +599,10 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
     const int t = pend_step[0];
     fence_proxy_async_global();
     const uint32_t old = atom_add_acq_rel(p.consumed + (size_t)it.g * G.P + t, 1u);
-    if (old + 1 == (uint32_t)G.Gs && t + 2 < it.n_steps) {
+    if (old + 1 == (uint32_t)G.Gs && t + kRingSlots < it.n_steps) {
       const uint32_t np = (uint32_t)G.n_pieces;
       const uint32_t k = atomicAdd(&p.ctrl->q_tail, np);
-      const uint32_t chunk = (uint32_t)(it.g * G.P + t + 2);
+      const uint32_t chunk = (uint32_t)(it.g * G.P + t + kRingSlots);
       if (k + np <= (uint32_t)p.n_dyn) {
         for (uint32_t pc = 0; pc < np; ++pc) st_release(p.queue + k + pc, chunk * np + pc + 1u);
       } else {
@@ -615,7 +622,7 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
     const CUtensorMap* mk = t == 0 ? tm_k : tm_sk;
     const CUtensorMap* mv = t == 0 ? tm_v : tm_sv;
     const int row0 = t == 0 ? (it.b * G.Hkv + it.kvh) * G.S + j * G.L
-                            : ((t & 1) * G.n_groups + it.g) * G.L;
+                            : (slot_of(t) * G.n_groups + it.g) * G.L;
     const uint32_t* flags = p.flags + ((size_t)it.g * G.P + t) * G.n_pieces;
     uint32_t seen = 0;
     for (int kt = 0; kt < n_kt && ok; ++kt) {
@@ -1244,7 +1251,7 @@ static int shape_geometry(const psr_shape* sh, Geometry& G, int n_cta) {
       geometry_init(G, sh->B, sh->Hq, sh->Hkv, sh->S, sh->P, sh->d, sh->causal, max_group_items(n_cta / cg), cg);
   if (rc == 1) return PSR_ERR_ARG;
   if (rc != 0) return PSR_ERR_UNSUPPORTED;
-  if (2LL * G.n_groups * G.L >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;  // slot rows index with int32
+  if ((long long)kRingSlots * G.n_groups * G.L >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;  // slot rows index with int32
   return PSR_OK;
 }
 
@@ -1386,7 +1393,7 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.n_tiles_total = (unsigned long long)total_tiles(G);
   kp.n_stage_total = (unsigned long long)total_staging_tasks(G) * (unsigned long long)G.n_pieces;
   kp.n_dyn = (int)(dynamic_staging_tasks(G) * G.n_pieces);
-  kp.n_init = 2 * G.n_groups * G.n_pieces;
+  kp.n_init = kRingSlots * G.n_groups * G.n_pieces;
   kp.mode = pt.mode;
   kp.fault = pt.fault;
   // clamps (in CTAs; a unit stages while unit * cg < n_s): at least one stager while
@@ -1420,11 +1427,12 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
     // a group could never be fully resident
     if (any_staging && n_units - (n_s + cg - 1) / cg < G.Gs) return PSR_ERR_ARG;
   } else {
-    // initial split: the rule on the prior costs with twice the staging cost.  The double
-    // buffer lets a group's staging run at most about one ring step ahead of its compute,
-    // and at launch every active group needs steps 1 and 2 at once, so the stagers need
-    // capacity above the average rate (measured best static splits for P = 4..16 sit near
-    // twice the balanced split); the measured costs and starvation then move the target
+    // initial split: the rule on the prior costs with twice the staging cost.  At launch every
+    // active group needs its first staged steps at once, and later a group's staging can run
+    // only a step or two ahead of its compute, so the stagers need capacity above the average
+    // rate (measured best static splits for P = 4..16 sit near twice the balanced split); the
+    // measured costs and starvation then move the target.  (Measured alternatives: 1.5x
+    // headroom, or half the starvation charged, were 1-5 % further from the best static split.)
     n_s = pt.n_staging > 0 ? pt.n_staging
                            : controller_rule(n_cta, (double)kp.n_stage_total, kStageHeadroom * kp.c_s0,
                                              (double)kp.n_tiles_total, kp.c_p0, n_min, n_max);
@@ -1440,7 +1448,7 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
 
   CUtensorMap maps[5];
   const long long rows_q = (long long)G.B * G.Hq * G.S, rows_kv = (long long)G.B * G.Hkv * G.S;
-  const long long rows_slot = 2LL * G.n_groups * G.L;
+  const long long rows_slot = (long long)kRingSlots * G.n_groups * G.L;
   // K maps: a pair's CTA loads 64 of every 128 K rows
   const int k_box = kTileRows / cg;
   if (!make_tmap(&maps[0], q, rows_q, G.d) || !make_tmap(&maps[1], k, rows_kv, G.d, k_box) ||

@@ -16,15 +16,15 @@
 //                    KV head kvh (all Hq/Hkv query heads of it) and, when a
 //                    group would exceed the deadlock bound, a sub-group index;
 //  * staging chunk = one (group, step >= 1): chunk (r - step) mod P of K and V
-//                    copied into the group's slot (step & 1) in 128-row tiles
+//                    copied into the group's slot (step mod kRingSlots) in 128-row tiles
 //                    (the pages' ring moves KV in 128-row tiles, Table 3);
 //  * staging piece = a quarter of a chunk (1..kStagePieceMaxTiles tiles): the
 //                    unit a staging CTA claims, so that several CTAs fill one
 //                    chunk at once; readiness is published per piece as a tile
 //                    count.
-// Slot (step & 1) of a group may be overwritten for step s >= 3 only when all
-// of the group's items have loaded step s - 2: that is the double buffer's
-// back-pressure.
+// Slot (s mod kRingSlots) of a group may be overwritten for step s > kRingSlots only
+// when all of the group's items have loaded step s - kRingSlots: that is the ring
+// buffer's back-pressure.
 #pragma once
 #include <cstdint>
 
@@ -39,6 +39,15 @@ namespace psr {
 constexpr int kTileRows = 128;  // rows per Q tile and per KV tile
 constexpr int kCtaRows = 256;   // query rows one CTA holds during an item (two tiles)
 constexpr int kStagePieceMaxTiles = 8;  // staging piece: a quarter of a chunk, 1..8 tiles
+#ifndef PSR_RING_SLOTS
+#define PSR_RING_SLOTS 3
+#endif
+// Ring slots per group.  Three rather than two: under the causal mask a group's items spend
+// (qp+1)*2 tiles on the local step 0, so they reach the staged steps up to a whole step apart,
+// and with two slots the items ahead wait for the one behind to release step s - 2.
+constexpr int kRingSlots = PSR_RING_SLOTS;
+static_assert(kRingSlots >= 2, "at least a double buffer");
+PSR_HD int slot_of(int step) { return step % kRingSlots; }
 
 struct Geometry {
   int B, Hq, Hkv, S, P, d, causal;
@@ -151,8 +160,8 @@ PSR_HD long long total_tiles(const Geometry& G) {
   return per_bh * G.B * G.Hq;
 }
 
-// Staging tasks: every (group, step >= 1).  Steps 1 and 2 land in fresh slots
-// and come from a static list in group order; steps >= 3 enter a ready queue
+// Staging tasks: every (group, step >= 1).  Steps 1..kRingSlots land in fresh slots
+// and come from a static list in group order; later steps enter a ready queue
 // when the slot they overwrite has been consumed.
 PSR_HD long long total_staging_tasks(const Geometry& G) {
   long long n = 0;
@@ -163,7 +172,7 @@ PSR_HD long long dynamic_staging_tasks(const Geometry& G) {
   long long n = 0;
   for (int rr = 0; rr < G.P; ++rr) {
     int s = steps_of_shard(G, shard_of_rank(G, rr));
-    n += s > 3 ? s - 3 : 0;
+    n += s > kRingSlots + 1 ? s - (kRingSlots + 1) : 0;
   }
   return n * G.B * G.Hkv * G.n_sub;
 }

@@ -38,7 +38,7 @@ int main(int argc, char** argv) {
     return 0;
   }
   const long long rows_q = (long long)G.B * G.Hq * G.S, rows_kv = (long long)G.B * G.Hkv * G.S;
-  const long long rows_slot = 2LL * G.n_groups * G.L;
+  const long long rows_slot = (long long)kRingSlots * G.n_groups * G.L;
   std::vector<unsigned char> covered((size_t)rows_q / kTileRows, 0);
   std::vector<int> consumers((size_t)G.n_groups * G.P, 0);
   long long tiles = 0;
@@ -69,7 +69,7 @@ int main(int argc, char** argv) {
           // the home rows belong to chunk j of the item's own (b, kvh)
           CHECK(r0 / G.S == c.b * G.Hkv + c.kvh, "home kv head");
         } else {
-          const long long r0 = (long long)((t & 1) * G.n_groups + c.g) * G.L + (long long)kt * kTileRows;
+          const long long r0 = (long long)(slot_of(t) * G.n_groups + c.g) * G.L + (long long)kt * kTileRows;
           CHECK(r0 >= 0 && r0 + kTileRows <= rows_slot, "slot rows item %d", n);
         }
         if (G.causal && t == 0) {
@@ -94,14 +94,14 @@ int main(int argc, char** argv) {
       CHECK(consumers[(size_t)g * G.P + t] == G.Gs, "group %d step %d consumers %d", g, t,
             consumers[(size_t)g * G.P + t]);
       ++stage;
-      if (t >= 3) ++dyn;
-      // staging source: chunk j of (b, kvh), L rows; destination slot (t&1) of g
+      if (t > kRingSlots) ++dyn;
+      // staging source: chunk j of (b, kvh), L rows; destination slot slot_of(t) of g
       int r, b, kvh, sub;
       group_coord(G, g, r, b, kvh, sub);
       const int j = ((r - t) % G.P + G.P) % G.P;
       const long long src0 = (long long)(b * G.Hkv + kvh) * G.S + (long long)j * G.L;
       CHECK(src0 >= 0 && src0 + G.L <= rows_kv, "staging source rows");
-      const long long dst0 = (long long)((t & 1) * G.n_groups + g) * G.L;
+      const long long dst0 = (long long)(slot_of(t) * G.n_groups + g) * G.L;
       CHECK(dst0 >= 0 && dst0 + G.L <= rows_slot, "staging destination rows");
     }
   }
