@@ -18,10 +18,11 @@
 //  * staging chunk = one (group, step >= 1): chunk (r - step) mod P of K and V
 //                    copied into the group's slot (step mod kRingSlots) in 128-row tiles
 //                    (the pages' ring moves KV in 128-row tiles, Table 3);
-//  * staging piece = a quarter of a chunk (1..kStagePieceMaxTiles tiles): the
-//                    unit a staging CTA claims, so that several CTAs fill one
-//                    chunk at once; readiness is published per piece as a tile
-//                    count.
+//  * staging piece = a quarter of a chunk, but at least 512 KiB of K+V and at most
+//                    kStagePieceMaxTiles tiles: the unit a staging CTA claims, so
+//                    that several CTAs fill one chunk at once while each copy stays
+//                    long enough to hide its fixed cost; readiness is published per
+//                    piece as a tile count.
 // Slot (s mod kRingSlots) of a group may be overwritten for step s > kRingSlots only
 // when all of the group's items have loaded step s - kRingSlots: that is the ring
 // buffer's back-pressure.
@@ -38,7 +39,18 @@ namespace psr {
 
 constexpr int kTileRows = 128;  // rows per Q tile and per KV tile
 constexpr int kCtaRows = 256;   // query rows one CTA holds during an item (two tiles)
-constexpr int kStagePieceMaxTiles = 8;  // staging piece: a quarter of a chunk, 1..8 tiles
+#ifndef PSR_PIECE_DIV
+#define PSR_PIECE_DIV 4
+#endif
+constexpr int kStagePieceDiv = PSR_PIECE_DIV;  // staging piece: 1/kStagePieceDiv of a chunk ...
+constexpr int kStagePieceMaxTiles = 8;         // ... of 1..8 tiles ...
+#ifndef PSR_PIECE_MIN_KB
+#define PSR_PIECE_MIN_KB 512
+#endif
+// ... and at least this many KiB of K+V.  Measured on GB300: a piece's copy costs ~6500 cycles
+// even when it is a single 64 KiB tile, so 1-2 tile pieces halved the staging CTAs' rate;
+// 512 KiB pieces cut the partition sweep's total time by 27 % (P = 64: 8.97 -> 5.43 ms).
+constexpr int kStagePieceMinKB = PSR_PIECE_MIN_KB;
 #ifndef PSR_RING_SLOTS
 #define PSR_RING_SLOTS 3
 #endif
@@ -89,7 +101,16 @@ PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int 
   G.gqa = Hq / Hkv;
   G.q_blocks = G.L / G.item_rows;
   G.kv_tiles = G.L / kTileRows;
-  G.piece_tiles = G.kv_tiles / 4 < 1 ? 1 : (G.kv_tiles / 4 > kStagePieceMaxTiles ? kStagePieceMaxTiles : G.kv_tiles / 4);
+  {
+    // 1/kStagePieceDiv of a chunk, but at least kStagePieceMinKB of K+V (a piece's copy has a
+    // fixed cost of a few microseconds), at most kStagePieceMaxTiles tiles and one chunk
+    const int min_tiles = (kStagePieceMinKB * 1024 + 2 * kTileRows * d * 2 - 1) / (2 * kTileRows * d * 2);
+    int pt = G.kv_tiles / kStagePieceDiv;
+    if (pt < min_tiles) pt = min_tiles;
+    if (pt > kStagePieceMaxTiles) pt = kStagePieceMaxTiles;
+    if (pt > G.kv_tiles) pt = G.kv_tiles;
+    G.piece_tiles = pt < 1 ? 1 : pt;
+  }
   G.n_pieces = (G.kv_tiles + G.piece_tiles - 1) / G.piece_tiles;
   G.G = G.gqa * G.q_blocks;
   // split a group into power-of-two sub-groups until it fits the bound
