@@ -254,13 +254,22 @@ __device__ int current_target(const KParams& p) {
 
 constexpr unsigned long long kCtrlMinIntervalNs = 20000;  // re-evaluate at most every 20 us
 #ifndef PSR_STAGE_HEADROOM
-#define PSR_STAGE_HEADROOM 200
+#define PSR_STAGE_HEADROOM 150
 #endif
 #ifndef PSR_STARVE_WEIGHT
-#define PSR_STARVE_WEIGHT 100
+#define PSR_STARVE_WEIGHT 50
 #endif
-constexpr double kStageHeadroom = PSR_STAGE_HEADROOM / 100.0;  // initial split: staging capacity over the average rate
-constexpr double kStarveWeight = PSR_STARVE_WEIGHT / 100.0;    // share of starved compute cycles charged to staging
+// Staging capacity kept above the rule's balanced split (initial split and updates), and the
+// share of compute cycles starved of staged data that is charged to staging.  Chosen on
+// GB300 over the partition sweep and the headline (medians of 3 runs; alternatives: 2x
+// initial only with full starvation charge, sweep geomean 1.025 / worst 1.14; 1.5x without
+// starvation charge, 1.015 / 1.11; this setting 1.011 / 1.12, headline 1.016 / 1.012).
+constexpr double kStageHeadroom = PSR_STAGE_HEADROOM / 100.0;
+constexpr double kStarveWeight = PSR_STARVE_WEIGHT / 100.0;
+#ifndef PSR_UPDATE_HEADROOM
+#define PSR_UPDATE_HEADROOM 150
+#endif
+constexpr double kUpdateHeadroom = PSR_UPDATE_HEADROOM / 100.0;  // staging headroom in the updates
 // The initial split stands until this fraction of the compute tiles is done: it covers the
 // ring's fill, when every active group needs its first staged steps at once and measured
 // costs are still dominated by start-up.
@@ -287,7 +296,7 @@ __device__ void controller_update(const KParams& p) {
   const unsigned long long sv = atomicAdd(&c->starve_cycles, 0ull);
   const double C_s = (scy + kStarveWeight * (double)sv + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
   const double C_p = (ccy + (double)p.c_p0 * 64.0) / ((double)td + 64.0);
-  int n = controller_rule((int)gridDim.x, R_s, C_s, R_p, C_p, p.n_min, p.n_max);
+  int n = controller_rule((int)gridDim.x, R_s, kUpdateHeadroom * C_s, R_p, C_p, p.n_min, p.n_max);
   const int cur = current_target(p);
   // hysteresis (move only by a margin unless the staging work is finished) and a rate
   // limit (each evaluation moves the target by at most max(2, cur/8) CTAs): a CTA changes
@@ -1427,12 +1436,11 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
     // a group could never be fully resident
     if (any_staging && n_units - (n_s + cg - 1) / cg < G.Gs) return PSR_ERR_ARG;
   } else {
-    // initial split: the rule on the prior costs with twice the staging cost.  At launch every
+    // initial split: the rule on the prior costs with the staging cost raised by the headroom.  At launch every
     // active group needs its first staged steps at once, and later a group's staging can run
     // only a step or two ahead of its compute, so the stagers need capacity above the average
-    // rate (measured best static splits for P = 4..16 sit near twice the balanced split); the
-    // measured costs and starvation then move the target.  (Measured alternatives: 1.5x
-    // headroom, or half the starvation charged, were 1-5 % further from the best static split.)
+    // rate (measured best static splits for P = 4..16 sit 1.2-3x above the balanced split); the
+    // measured costs and starvation then move the target.
     n_s = pt.n_staging > 0 ? pt.n_staging
                            : controller_rule(n_cta, (double)kp.n_stage_total, kStageHeadroom * kp.c_s0,
                                              (double)kp.n_tiles_total, kp.c_p0, n_min, n_max);
