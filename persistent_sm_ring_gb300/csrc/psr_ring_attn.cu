@@ -270,6 +270,7 @@ constexpr double kStarveWeight = PSR_STARVE_WEIGHT / 100.0;
 #define PSR_UPDATE_HEADROOM 150
 #endif
 constexpr double kUpdateHeadroom = PSR_UPDATE_HEADROOM / 100.0;  // staging headroom in the updates
+
 // The initial split stands until this fraction of the compute tiles is done: it covers the
 // ring's fill, when every active group needs its first staged steps at once and measured
 // costs are still dominated by start-up.
