@@ -99,8 +99,8 @@ typedef struct {
 
 /* Bytes of device workspace psr_ring_attn_fwd needs for this shape: the
  * control block, readiness flags, consumption counters, the staging ready
- * queue, the trajectory log and the two ring slots for K and V
- * (2 x [n_groups][L][d] bf16 each).  Returns 0 for an invalid shape. */
+ * queue, the trajectory log and the three ring slots for K and V
+ * (3 x [n_groups][L][d] bf16 each).  Returns 0 for an invalid shape. */
 PSR_API size_t psr_workspace_bytes(const psr_shape* shape);
 
 /* Ring Attention forward.
@@ -120,10 +120,17 @@ PSR_API size_t psr_workspace_bytes(const psr_shape* shape);
 PSR_API int psr_ring_attn_fwd(const psr_shape* shape, const void* q, const void* k, const void* v, void* o, float* lse,
                       void* workspace, size_t workspace_bytes, const psr_partition* part, void* stream);
 
-/* Same operation with HOST buffers: copies q, k, v (host, ideally pinned) to
- * the caller's device buffers dq, dk, dv on `stream`, runs psr_ring_attn_fwd,
- * copies O and LSE back to o_host / lse_host, and synchronises the stream.
- * Returns the launch status, or PSR_ERR_TIMEOUT if the device reported one. */
+/* Same operation with HOST buffers: copies q, k, v (host; pinned for overlap)
+ * to the caller's device buffers dq, dk, dv (same layouts and sizes as the
+ * device entry's q, k, v, o, lse), runs the attention, copies O and LSE back
+ * to o_host / lse_host, and returns when they are there.  Shapes of 64 MB of
+ * Q or more run in up to 4 slices of whole batches (B > 1) or of whole
+ * KV-head groups with their query heads (B = 1): the copies in of slice c+1
+ * and out of slice c-1 overlap the kernel of slice c (two internal streams,
+ * created once per device; one launch per slice on `stream`).  The workspace
+ * is sized for the whole shape.  psr_get_stats afterwards describes the last
+ * slice's launch.  Returns the first failing status, or PSR_ERR_TIMEOUT if a
+ * slice's launch reported a device timeout. */
 PSR_API int psr_ring_attn_fwd_host(const psr_shape* shape, const void* q_host, const void* k_host, const void* v_host,
                            void* o_host, float* lse_host, void* dq, void* dk, void* dv, void* d_o, float* d_lse,
                            void* workspace, size_t workspace_bytes, const psr_partition* part, void* stream);

@@ -200,7 +200,8 @@ def ring_attn_fwd(q, k, v, *, P, causal, scale=None, partition=None, workspace=N
 
 def ring_attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, dq, dk, dv, d_o, d_lse, *, P, causal, scale=None,
                        partition=None, workspace=None, stream=None):
-    """Host-buffer variant: copies in, runs, copies out and synchronises (one C call)."""
+    """Host-buffer variant: copies in, runs, copies out and synchronises (one C call; large shapes
+    run in slices whose copies overlap the kernels)."""
     import torch
     lib = load()
     B, Hq, S, d = q_host.shape

@@ -1319,6 +1319,41 @@ static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta,
   return e;
 }
 
+// Streams and events of the host-buffer entry point, one set per device and process (created on
+// first use, never freed); calls on one device serialise on a mutex.  err_host is pinned host
+// memory that receives each slice's error word.
+constexpr int kHostSlices = 4;
+struct HostPipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[kHostSlices] = {}, ev_out[kHostSlices] = {};
+  uint32_t* err_host = nullptr;
+  std::mutex mu;
+};
+
+static HostPipe* host_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static HostPipe pipes[64];
+  static std::mutex init_mu;
+  std::lock_guard<std::mutex> lk(init_mu);
+  HostPipe& hp = pipes[dev];
+  if (hp.err_host) return &hp;
+  bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.ev_start, cudaEventDisableTiming) == cudaSuccess;
+  for (int c = 0; ok && c < kHostSlices; ++c)
+    ok = cudaEventCreateWithFlags(&hp.ev_in[c], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.ev_out[c], cudaEventDisableTiming) == cudaSuccess;
+  void* pinned = nullptr;
+  ok = ok && cudaHostAlloc(&pinned, kHostSlices * sizeof(uint32_t), cudaHostAllocDefault) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  hp.err_host = static_cast<uint32_t*>(pinned);
+  return &hp;
+}
+
 }  // namespace psr
 
 using namespace psr;
@@ -1481,25 +1516,71 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
                            void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
   if (!sh || !q_host || !k_host || !v_host || !o_host || !lse_host) return PSR_ERR_ARG;
   if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->d < 1) return PSR_ERR_ARG;
-  const size_t nq = (size_t)sh->B * sh->Hq * sh->S * sh->d * 2, nkv = (size_t)sh->B * sh->Hkv * sh->S * sh->d * 2;
-  const size_t nl = (size_t)sh->B * sh->Hq * sh->S * 4;
+  if (!dq || !dk || !dv || !d_o || !d_lse || !workspace) return PSR_ERR_ARG;
+  if (sh->Hq % sh->Hkv != 0) return PSR_ERR_UNSUPPORTED;
+  // The whole shape must be launchable (validates the shape and the workspace size once).
+  {
+    Geometry G;
+    DeviceInfo di;
+    if (!device_info(di)) return PSR_ERR_CUDA;
+    const int rc = shape_geometry(sh, G, di.n_sm);
+    if (rc != PSR_OK) return rc;
+    if (ws_bytes < ws_layout(G).total) return PSR_ERR_ARG;
+  }
+  // Slices: contiguous batches, or (one batch) contiguous KV-head groups with their query heads.
+  // Slice c+1 is copied in while slice c computes and slice c-1 is copied out.
+  const size_t row_b = (size_t)sh->S * sh->d * 2;  // bytes of one head's Q/K/V/O rows
+  const size_t q_bytes = (size_t)sh->B * sh->Hq * row_b;
+  const int units = sh->B > 1 ? sh->B : sh->Hkv;
+  int n_sl = 1;
+  if (q_bytes >= ((size_t)64 << 20))
+    for (int c = kHostSlices; c >= 2; --c)
+      if (units % c == 0) { n_sl = c; break; }
+  psr_shape ss = *sh;
+  if (sh->B > 1) ss.B = sh->B / n_sl;
+  else { ss.Hkv = sh->Hkv / n_sl; ss.Hq = sh->Hq / n_sl; }
+  const size_t q_sl = (size_t)ss.B * ss.Hq * row_b, kv_sl = (size_t)ss.B * ss.Hkv * row_b;
+  const size_t l_sl = (size_t)ss.B * ss.Hq * sh->S * 4;
+
+  HostPipe* hp = host_pipe();
+  if (!hp) return PSR_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(hp->mu);  // the pipeline's streams, events and error words are per device
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!dq || !dk || !dv || !d_o || !d_lse) return PSR_ERR_ARG;
-  if (cudaMemcpyAsync(dq, q_host, nq, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dk, k_host, nkv, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dv, v_host, nkv, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  // the copies must not overtake work already queued on the caller's stream
+  if (cudaEventRecord(hp->ev_start, st) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0) != cudaSuccess)
     return PSR_ERR_CUDA;
-  int rc = psr_ring_attn_fwd(sh, dq, dk, dv, d_o, d_lse, workspace, ws_bytes, part, stream);
-  if (rc != PSR_OK) return rc;
-  if (cudaMemcpyAsync(o_host, d_o, nq, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaMemcpyAsync(lse_host, d_lse, nl, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return PSR_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return PSR_ERR_CUDA;
-  uint32_t err = 0;
-  if (cudaMemcpy(&err, static_cast<uint8_t*>(workspace) + offsetof(Ctrl, error), 4, cudaMemcpyDeviceToHost) !=
-      cudaSuccess)
-    return PSR_ERR_CUDA;
-  return err ? PSR_ERR_TIMEOUT : PSR_OK;
+  auto cp_in = [&](void* dst, const void* src, size_t off, size_t n) {
+    return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + off, static_cast<const uint8_t*>(src) + off, n,
+                           cudaMemcpyHostToDevice, hp->h2d);
+  };
+  for (int c = 0; c < n_sl; ++c) {
+    if (cp_in(dq, q_host, c * q_sl, q_sl) != cudaSuccess || cp_in(dk, k_host, c * kv_sl, kv_sl) != cudaSuccess ||
+        cp_in(dv, v_host, c * kv_sl, kv_sl) != cudaSuccess || cudaEventRecord(hp->ev_in[c], hp->h2d) != cudaSuccess)
+      return PSR_ERR_CUDA;
+  }
+  for (int c = 0; c < n_sl; ++c) {
+    if (cudaStreamWaitEvent(st, hp->ev_in[c], 0) != cudaSuccess) return PSR_ERR_CUDA;
+    const int rc = psr_ring_attn_fwd(&ss, static_cast<const uint8_t*>(dq) + c * q_sl,
+                                     static_cast<const uint8_t*>(dk) + c * kv_sl,
+                                     static_cast<const uint8_t*>(dv) + c * kv_sl, static_cast<uint8_t*>(d_o) + c * q_sl,
+                                     reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(d_lse) + c * l_sl), workspace,
+                                     ws_bytes, part, st);
+    if (rc != PSR_OK) return rc;
+    // this slice's error word, before the next launch resets the control block
+    if (cudaMemcpyAsync(hp->err_host + c, static_cast<uint8_t*>(workspace) + offsetof(Ctrl, error), 4,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaEventRecord(hp->ev_out[c], st) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->ev_out[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + c * q_sl, static_cast<const uint8_t*>(d_o) + c * q_sl, q_sl,
+                        cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess ||
+        cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + c * l_sl,
+                        reinterpret_cast<const uint8_t*>(d_lse) + c * l_sl, l_sl, cudaMemcpyDeviceToHost,
+                        hp->d2h) != cudaSuccess)
+      return PSR_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(hp->d2h) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) return PSR_ERR_CUDA;
+  for (int c = 0; c < n_sl; ++c)
+    if (hp->err_host[c] != 0) return PSR_ERR_TIMEOUT;
+  return PSR_OK;
 }
 
 int psr_get_stats(const void* workspace, psr_stats* out, void* stream) {
