@@ -269,3 +269,84 @@ def sample_rows(w: Workload, n_random: int = 4096) -> np.ndarray:
         ids.add(splitmix64(seed, n) % total)
         n += 1
     return np.array(sorted(ids), dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------------------------
+# AllGather + GEMM (tensor-parallel linear layer) workloads
+# ----------------------------------------------------------------------------------------------
+# The mKernel pages' AllGather+GEMM kernel (dataforcee / chathome "five fused kernels" table,
+# AllGather+GEMM row; pwwt.cn analysis §2.6): every rank holds a row shard of A, gathers the
+# other ranks' shards, and its local GEMM consumes A tiles as they arrive.  Emulated on one
+# GPU: P ranks, rank r owns rows [r*M/P, (r+1)*M/P) of A and the weight slice W_r
+# ([Ns][K], K-major), and produces C_r = gather(A) @ W_r^T ([M][Ns]).
+
+@dataclasses.dataclass(frozen=True)
+class AgGemmWorkload:
+    name: str
+    M: int      # rows of the gathered A (tokens)
+    K: int      # contraction (hidden size)
+    Ns: int     # output columns per rank (N / P)
+    P: int      # ranks
+    seed: int
+    amul: float = 1.0
+    wmul: float = 1.0 / 64.0   # power of two: exact in bf16; keeps |C| near 1 for K ~ 4096
+
+    @property
+    def Ms(self) -> int:
+        return self.M // self.P
+
+    @property
+    def n_a(self) -> int:
+        return self.M * self.K
+
+    @property
+    def n_w(self) -> int:
+        return self.P * self.Ns * self.K
+
+    def flops(self) -> float:
+        """2*M*K*Ns per rank, times P."""
+        return 2.0 * self.M * self.K * self.Ns * self.P
+
+    def gather_bytes(self) -> int:
+        """A bytes copied by the emulated all-gather: every rank receives the P-1 other shards."""
+        return self.P * (self.P - 1) * self.Ms * self.K * 2
+
+    def with_(self, **kw) -> "AgGemmWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+AG_WORKLOADS = {
+    # small: every output element is checked against the oracle
+    "ag_small": AgGemmWorkload("ag_small", 1024, 512, 256, 4, seed=700),
+    # a tensor-parallel MLP up-projection: 8192 tokens, hidden 8192, N = 28672 over 8 ranks
+    "ag_m8k_k8k_n28k_p8": AgGemmWorkload("ag_m8k_k8k_n28k_p8", 8192, 8192, 3584, 8, seed=701),
+}
+
+
+def generate_ag_gemm(w: AgGemmWorkload, a_addr: int | None = None, w_addr: int | None = None):
+    """A ([M][K]) then W ([P][Ns][K]) as uint16 bf16 bit patterns, from the same stream as the
+    attention inputs (A first).  With addresses, values are written there and None returned."""
+    out = []
+    first = 0
+    for count, mult, addr, shape in ((w.n_a, w.amul, a_addr, (w.M, w.K)), (w.n_w, w.wmul, w_addr, (w.P, w.Ns, w.K))):
+        if addr is None:
+            out.append(normal_bf16(w.seed, first, count, mult).reshape(shape))
+        else:
+            normal_bf16_into(addr, w.seed, first, count, mult)
+            out.append(None)
+        first += count
+    return tuple(out)
+
+
+def ag_sample_rows(w: AgGemmWorkload, n_random: int = 1024) -> np.ndarray:
+    """Fixed sample of row indices of the gathered A (the same rows for every rank): each
+    shard's first, second and last rows, then seeded uniform rows up to `n_random`."""
+    ids = set()
+    for j in range(w.P):
+        ids.update((j * w.Ms, j * w.Ms + 1, (j + 1) * w.Ms - 1))
+    seed = (w.seed * 7919 + 23) & (2**64 - 1)
+    n = 0
+    while len(ids) < n_random:
+        ids.add(splitmix64(seed, n) % w.M)
+        n += 1
+    return np.array(sorted(ids), dtype=np.int64)
