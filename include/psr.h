@@ -178,6 +178,45 @@ PSR_API const char* psr_status_string(int status);
  * or a negative status. */
 PSR_API int psr_num_ctas(void);
 
+/* ---- AllGather + GEMM ------------------------------------------------------------------------ */
+/* The pages' second fused pattern (dataforcee / chathome "five fused kernels"
+ * table, AllGather+GEMM row; pwwt.cn analysis §2.6: 128-row chunks, local
+ * inputs first): every rank holds a row shard of A; while the ranks gather
+ * the peers' shards, the local GEMM consumes A tiles as they arrive.  On one
+ * GPU the P ranks are emulated in HBM: rank r owns rows [r*M/P, (r+1)*M/P) of
+ * A and the weight slice W_r, and produces
+ *     C_r = gather(A) @ W_r^T      (fp32 accumulation, bf16 result, RNE),
+ * the gathered A being the shards concatenated in rank order.  Staging CTAs
+ * copy peer shards into each rank's gather buffer in the workspace (pieces of
+ * >= 512 KiB, each published with a readiness flag); compute CTAs each produce
+ * one 256 x 256 tile of one rank on tcgen05, reading the rank's own shard in
+ * place and a peer's rows after acquiring their flags; the same controller as
+ * the Ring Attention splits the CTAs between the two roles. */
+typedef struct {
+  int M;   /* rows of the gathered A; M/P must be a multiple of 256 */
+  int K;   /* contraction; a multiple of 128 */
+  int Ns;  /* output columns per rank; a multiple of 256 */
+  int P;   /* ranks */
+} psr_ag_shape;
+
+/* Bytes of device workspace psr_ag_gemm needs: the control block and
+ * trajectory log (the same layout as psr_ring_attn_fwd's, so psr_get_stats and
+ * psr_get_trajectory read it), the readiness flags [P][P][pieces] and the P
+ * gather buffers ([P][M][K] bf16).  Returns 0 for an invalid shape. */
+PSR_API size_t psr_ag_gemm_workspace_bytes(const psr_ag_shape* shape);
+
+/* AllGather + GEMM.
+ *   a: device, bf16, [M][K] contiguous (rank j's shard = rows j*M/P ..)   (read)
+ *   w: device, bf16, [P][Ns][K] contiguous (rank r's weight, K-major)     (read)
+ *   c: device, bf16, [P][M][Ns] contiguous (rank r's output)              (written)
+ *   workspace: device, >= psr_ag_gemm_workspace_bytes(shape), 256-byte aligned, caller-owned.
+ *   part: partition policy (NULL = adaptive); stream: a cudaStream_t (NULL = default).
+ * Asynchronous (one flag reset and one persistent launch on `stream`); a
+ * device timeout is reported by psr_get_stats.  PSR_ERR_UNSUPPORTED for shapes
+ * outside the constraints above or a device other than sm_103. */
+PSR_API int psr_ag_gemm(const psr_ag_shape* shape, const void* a, const void* w, void* c, void* workspace,
+                        size_t workspace_bytes, const psr_partition* part, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

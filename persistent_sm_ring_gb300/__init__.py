@@ -15,7 +15,8 @@ import threading
 
 from .build import LIB, LIB_PAIRS, LIB_TRACE, build as _build
 
-__all__ = ["build", "load", "Shape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host", "workspace_bytes",
+__all__ = ["build", "load", "Shape", "AgShape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host",
+           "workspace_bytes", "ag_gemm", "ag_gemm_workspace_bytes",
            "get_stats", "get_trajectory", "controller_target", "num_ctas", "status_string", "PsrError",
            "STATIC", "ADAPTIVE", "FAULT_NONE", "FAULT_DROP_FIRST_FLAG", "FAULT_SLOW_STAGING"]
 
@@ -25,12 +26,16 @@ FAULT_NONE, FAULT_DROP_FIRST_FLAG, FAULT_SLOW_STAGING = 0, 1, 2
 
 EXPORTED = ("psr_workspace_bytes", "psr_ring_attn_fwd", "psr_ring_attn_fwd_host", "psr_get_stats",
             "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas",
-            "psr_ring_attn_fwd_noalloc")
+            "psr_ring_attn_fwd_noalloc", "psr_ag_gemm_workspace_bytes", "psr_ag_gemm")
 
 
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("S", ctypes.c_int),
                 ("P", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+class AgShape(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int), ("K", ctypes.c_int), ("Ns", ctypes.c_int), ("P", ctypes.c_int)]
 
 
 class Partition(ctypes.Structure):
@@ -100,6 +105,11 @@ def load(trace: bool = False, variant: str = "") -> ctypes.CDLL:
         lib.psr_controller_target.restype = ctypes.c_int
         lib.psr_status_string.argtypes = [ctypes.c_int]
         lib.psr_status_string.restype = ctypes.c_char_p
+        P_ag = ctypes.POINTER(AgShape)
+        lib.psr_ag_gemm_workspace_bytes.argtypes = [P_ag]
+        lib.psr_ag_gemm_workspace_bytes.restype = sz
+        lib.psr_ag_gemm.argtypes = [P_ag, vp, vp, vp, vp, sz, P_part, vp]
+        lib.psr_ag_gemm.restype = ctypes.c_int
         lib.psr_num_ctas.argtypes = []
         lib.psr_num_ctas.restype = ctypes.c_int
         _lib = lib
@@ -218,6 +228,37 @@ def ring_attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, dq, dk, dv, d_o
     if rc != OK:
         raise PsrError(rc, "psr_ring_attn_fwd_host")
     return workspace
+
+
+def ag_gemm_workspace_bytes(M, K, Ns, P) -> int:
+    n = load().psr_ag_gemm_workspace_bytes(ctypes.byref(AgShape(int(M), int(K), int(Ns), int(P))))
+    if n == 0:
+        raise PsrError(ERR_UNSUPPORTED, "psr_ag_gemm_workspace_bytes")
+    return int(n)
+
+
+def ag_gemm(a, w, *, P, partition=None, workspace=None, out=None, stream=None):
+    """AllGather + GEMM through the C ABI: a [M][K] bf16 (rank j's shard = rows j*M/P..),
+    w [P][Ns][K] bf16 -> c [P][M][Ns] bf16, C_r = gather(A) @ W_r^T.  Returns (c, workspace)."""
+    import torch
+    lib = load()
+    M, K = a.shape
+    Ns = w.shape[1]
+    shape = AgShape(int(M), int(K), int(Ns), int(P))
+    need = ag_gemm_workspace_bytes(M, K, Ns, P)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    if out is None:
+        out = torch.empty((P, M, Ns), dtype=torch.bfloat16, device=a.device)
+    for t in (a, w, out):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("ag_gemm: a, w and out must be contiguous bf16 CUDA tensors")
+    part = partition if partition is not None else make_partition()
+    rc = lib.psr_ag_gemm(ctypes.byref(shape), a.data_ptr(), w.data_ptr(), out.data_ptr(), workspace.data_ptr(),
+                         workspace.numel(), ctypes.byref(part), _stream_handle(stream))
+    if rc != OK:
+        raise PsrError(rc, "psr_ag_gemm")
+    return out, workspace
 
 
 def get_stats(workspace, stream=None) -> dict:

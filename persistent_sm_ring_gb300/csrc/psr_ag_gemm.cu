@@ -1,0 +1,589 @@
+// AllGather + GEMM as one persistent kernel on sm_103a.
+//
+// The mKernel pages' AllGather+GEMM kernel (dataforcee / chathome "five fused kernels"
+// table, AllGather+GEMM row; pwwt.cn analysis §2.6, 128-row chunks, local inputs first):
+// every rank holds a row shard of A; while the ranks gather the peers' shards, the local
+// GEMM consumes A tiles as soon as they arrive.  On one GPU the P ranks are emulated in
+// HBM: rank r owns rows [r*Ms, (r+1)*Ms) of A (Ms = M/P) and the weight slice W_r
+// ([Ns][K], K-major), and produces C_r = gather(A) @ W_r^T.
+//
+//  * staging CTAs copy a peer shard's rows, in pieces of >= 512 KiB, into rank r's gather
+//    buffer (the same row positions) with TMA bulk copies through shared memory, and publish
+//    a per-piece readiness flag with a gpu-scope release once the stores are complete;
+//  * compute CTAs each produce one 256 x 256 output tile of one rank per task: two 128-row
+//    A tiles against one 256-row W tile per 64-wide K step, on tcgen05 (M = 128, N = 256)
+//    with both accumulators in tensor memory; the rank's own shard is read in place, a
+//    peer's only after acquiring the piece flags that cover the tile's rows;
+//  * tasks run in availability order: every rank's local tiles first, then the tiles of
+//    shard r+1, r+2, ... (the order in which staging delivers them);
+//  * the shared controller re-splits CTAs between the roles with the pages' rule.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/psr.h"
+#include "psr_control.cuh"
+#include "psr_device.cuh"
+#include "psr_schedule.h"
+
+namespace psr {
+namespace ag {
+
+constexpr int kBM = 256;          // output rows per task (two 128-row A tiles)
+constexpr int kBN = 256;          // output columns per task (one W tile)
+constexpr int kBK = 64;           // K per stage (one 128-byte swizzle atom of bf16)
+constexpr int kNStage = 3;        // stages of A0 | A1 | W
+constexpr int kATile = 128 * kBK * 2;   // 16 KiB
+constexpr int kWTile = kBN * kBK * 2;   // 32 KiB
+constexpr int kStageBytes = 2 * kATile + kWTile;
+constexpr int kSmem = 1024 + kNStage * kStageBytes;
+constexpr int kCopyUnit = 32768;  // staging copy unit
+constexpr int kNCopyBuf = kNStage * kStageBytes / kCopyUnit;
+constexpr int kWarps = 12, kThreads = kWarps * 32;
+constexpr int kPieceMinBytes = 512 * 1024;
+static_assert(kSmem <= 232448 - 512, "shared memory");
+static_assert(kNCopyBuf <= 16, "staging barriers");
+
+enum : uint32_t { SITE_FLAG = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_ACC = 4, SITE_STAGE_LOAD = 8, SITE_IDLE = 11 };
+enum : int { CMD_EXIT = 0, CMD_COMPUTE = 1, CMD_STAGE = 2, CMD_IDLE = 3 };
+
+struct Geo {
+  int M, K, Ns, P, Ms;
+  int n_mb;          // 256-row blocks per shard
+  int n_nb;          // 256-column blocks per rank
+  int piece_rows;    // rows per staging piece (a multiple of 128 dividing Ms)
+  int n_pieces;      // pieces per shard
+  long long n_items;   // compute tasks: P ranks x P shards x n_mb x n_nb
+  long long n_stage;   // staging pieces: P ranks x (P-1) peers x n_pieces
+};
+
+struct Params {
+  Geo g;
+  const uint16_t* a;
+  uint16_t* gbuf;      // [P][M][K]: rank r's gathered copy of A (peer rows only are written)
+  uint16_t* c;         // [P][M][Ns]
+  uint32_t* flags;     // [P][P][n_pieces]
+  Ctrl* ctrl;
+  uint32_t* traj;
+  unsigned long long timeout_ns;
+  unsigned long long n_tiles_total, n_stage_total;
+  int mode, n_s_init, n_min, n_max, fault;
+  float c_s0, c_p0;
+};
+
+struct Smem {
+  uint64_t full[kNStage], empty[kNStage];
+  uint64_t acc_full;
+  uint64_t stg[16];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int cmd, arg;
+  volatile uint32_t abort;
+};
+
+// task index -> (rank, shard, m-block, n-block); stage order jj: shard = (rank + jj) mod P
+struct Item {
+  int r, j, mb, nb;
+};
+__device__ __host__ inline Item item_of(const Geo& g, long long idx) {
+  Item it;
+  it.nb = (int)(idx % g.n_nb);
+  idx /= g.n_nb;
+  it.mb = (int)(idx % g.n_mb);
+  idx /= g.n_mb;
+  it.r = (int)(idx % g.P);
+  const int jj = (int)(idx / g.P);
+  it.j = (it.r + jj) % g.P;
+  return it;
+}
+// staging task index -> (rank, shard, piece), peers in the same order as the compute tasks
+__device__ inline void stage_of(const Geo& g, long long idx, int& r, int& j, int& piece) {
+  piece = (int)(idx % g.n_pieces);
+  idx /= g.n_pieces;
+  r = (int)(idx % g.P);
+  const int jj = 1 + (int)(idx / g.P);
+  j = (r + jj) % g.P;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Task selection (thread 0)
+// ------------------------------------------------------------------------------------------------
+__device__ void decide(const Params& p, Smem* sc, bool& was_staging) {
+  Ctrl* c = p.ctrl;
+  if (sc->abort || ld_relaxed(&c->abort)) { sc->cmd = CMD_EXIT; return; }
+  const int n_s = current_target(p);
+  const bool staging_role = (int)blockIdx.x < n_s;
+  if (staging_role != was_staging) {
+    atomicAdd(&c->role_switches, 1ull);
+    was_staging = staging_role;
+  }
+  const bool all_claimed = ld_relaxed(&c->init_next) >= (uint32_t)p.g.n_stage;
+  if (staging_role && !all_claimed) {
+    const uint32_t t = atomicAdd(&c->init_next, 1u);
+    if (t < (uint32_t)p.g.n_stage) { sc->cmd = CMD_STAGE; sc->arg = (int)t; return; }
+  }
+  if (staging_role && p.mode == PSR_STATIC) { sc->cmd = CMD_EXIT; return; }
+  if (ld_relaxed(&c->item_next) < (uint32_t)p.g.n_items) {
+    const uint32_t n = atomicAdd(&c->item_next, 1u);
+    if (n < (uint32_t)p.g.n_items) { sc->cmd = CMD_COMPUTE; sc->arg = (int)n; return; }
+  }
+  // no compute left: help with staging while any piece is unclaimed
+  if (p.mode == PSR_ADAPTIVE && ld_relaxed(&c->init_next) < (uint32_t)p.g.n_stage) {
+    const uint32_t t = atomicAdd(&c->init_next, 1u);
+    if (t < (uint32_t)p.g.n_stage) { sc->cmd = CMD_STAGE; sc->arg = (int)t; return; }
+  }
+  sc->cmd = CMD_EXIT;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Staging task (thread 0): a piece of shard j's rows -> rank r's gather buffer, same rows
+// ------------------------------------------------------------------------------------------------
+__device__ void run_staging(const Params& p, Smem* sc, uint32_t smem_base, int task, uint32_t (&phase)[16]) {
+  const Geo& g = p.g;
+  int r, j, piece;
+  stage_of(g, task, r, j, piece);
+  const size_t row0 = (size_t)j * g.Ms + (size_t)piece * g.piece_rows;
+  const size_t bytes = (size_t)g.piece_rows * g.K * 2;
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(p.a + row0 * g.K);
+  uint8_t* dst = reinterpret_cast<uint8_t*>(p.gbuf + ((size_t)r * g.M + row0) * g.K);
+  uint32_t* flag = p.flags + ((size_t)r * g.P + j) * g.n_pieces + piece;
+  const bool drop = (p.fault == PSR_FAULT_DROP_FIRST_FLAG) && (atomicAdd(&p.ctrl->fault_count, 1u) == 0u);
+  if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
+  const int n_u = (int)((bytes + kCopyUnit - 1) / kCopyUnit);
+  auto unit_bytes = [&](int u) {
+    const size_t rem = bytes - (size_t)u * kCopyUnit;
+    return (uint32_t)(rem < (size_t)kCopyUnit ? rem : (size_t)kCopyUnit);
+  };
+  auto issue_load = [&](int u) {
+    const int b = u % kNCopyBuf;
+    mbar_expect_tx(&sc->stg[b], unit_bytes(u));
+    bulk_load(smem_base + b * kCopyUnit, src + (size_t)u * kCopyUnit, unit_bytes(u), &sc->stg[b]);
+  };
+  const int pre = n_u < kNCopyBuf - 1 ? n_u : kNCopyBuf - 1;
+  for (int u = 0; u < pre; ++u) issue_load(u);
+  int issued = pre;
+  bool ok = true;
+  for (int u = 0; u < n_u; ++u) {
+    const int b = u % kNCopyBuf;
+    if (u >= issued) break;
+    if (ok && !wait_bar(&sc->stg[b], phase[b] & 1u, p, sc, SITE_STAGE_LOAD)) ok = false;
+    if (!ok) {
+      const uint64_t t0 = globaltimer_ns();  // drain this load (bounded)
+      while (!mbar_try_wait(&sc->stg[b], phase[b] & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+    phase[b]++;
+    if (ok) {
+      bulk_store(dst + (size_t)u * kCopyUnit, smem_base + b * kCopyUnit, unit_bytes(u));
+      bulk_commit();
+    }
+    const int nu = u + kNCopyBuf - 1;
+    if (nu < n_u && ok) {
+      bulk_wait_read<1>();  // the store that used buffer nu % kNCopyBuf has read shared memory
+      issue_load(nu);
+      issued = nu + 1;
+    }
+  }
+  bulk_wait<0>();  // every store of the piece has completed
+  if (ok && !drop) {
+    fence_proxy_async_global();
+    st_release(flag, 1u);
+  }
+  atomicAdd(&p.ctrl->stage_bytes, (unsigned long long)bytes);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Compute task: producer (TMA), MMA issuer (tcgen05), epilogue warpgroups
+// ------------------------------------------------------------------------------------------------
+struct Counters {
+  uint32_t fills;  // stage fills issued (producer) / consumed (issuer)
+  uint32_t items;  // compute tasks done (accumulator phase)
+};
+
+// Returns the cycles spent waiting for readiness flags.
+__device__ long long producer(const Params& p, Smem* sc, uint32_t smem_base, const Item& it, const CUtensorMap* tm_a,
+                              const CUtensorMap* tm_g, const CUtensorMap* tm_w, Counters& cnt, bool& ok) {
+  const Geo& g = p.g;
+  long long waited = 0;
+  const CUtensorMap* ma = tm_a;
+  int arow = it.j * g.Ms + it.mb * kBM;  // rows of A (local) ...
+  if (it.j != it.r) {
+    // ... or of rank r's gather buffer, once the pieces covering the tile's rows are there
+    ma = tm_g;
+    const int p0 = (it.mb * kBM) / g.piece_rows, p1 = (it.mb * kBM + kBM - 1) / g.piece_rows;
+    const uint32_t* f = p.flags + ((size_t)it.r * g.P + it.j) * g.n_pieces;
+    for (int pc = p0; pc <= p1 && ok; ++pc) {
+      uint32_t seen = ld_acquire(f + pc);
+      if (seen < 1u) {
+        const long long f0 = clock64();
+        if (!wait_flag(f + pc, 1u, seen, p, sc, SITE_FLAG)) ok = false;
+        waited += clock64() - f0;
+      }
+    }
+    fence_proxy_async_global();  // acquire (generic) before the async-proxy reads of the buffer
+    arow = it.r * g.M + it.j * g.Ms + it.mb * kBM;
+  }
+  const int wrow = it.r * g.Ns + it.nb * kBN;
+  const int n_k = g.K / kBK;
+  for (int ks = 0; ks < n_k && ok; ++ks) {
+    const uint32_t c = cnt.fills++;
+    const uint32_t s = c % kNStage, fill = c / kNStage;
+    if (fill > 0 && !wait_bar(&sc->empty[s], (fill - 1) & 1u, p, sc, SITE_KV_EMPTY)) { ok = false; break; }
+    const uint32_t base = smem_base + s * kStageBytes;
+    mbar_expect_tx(&sc->full[s], kStageBytes);
+    tma_load_2d(base, ma, ks * kBK, arow, &sc->full[s]);
+    tma_load_2d(base + kATile, ma, ks * kBK, arow + 128, &sc->full[s]);
+    tma_load_2d(base + 2 * kATile, tm_w, ks * kBK, wrow, &sc->full[s]);
+  }
+  if (!ok) sc->abort = 1;
+  return waited;
+}
+
+__device__ void mma_issuer(const Params& p, Smem* sc, uint32_t smem_base, Counters& cnt) {
+  const Geo& g = p.g;
+  constexpr uint32_t ID = idesc_bf16_f32(128, kBN, false);
+  constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+  const int n_k = g.K / kBK;
+  for (int ks = 0; ks < n_k; ++ks) {
+    const uint32_t c = cnt.fills++;
+    const uint32_t s = c % kNStage, fill = c / kNStage;
+    if (!wait_bar(&sc->full[s], fill & 1u, p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
+    tc_fence_after();
+    const uint32_t base = smem_base + s * kStageBytes;
+    const uint32_t w_lo = sdesc_lo(base + 2 * kATile, 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t a_lo = sdesc_lo(base + i * kATile, 16);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        mma_ss_w(sc->tmem_base + i * kBN, a_lo + kk * 2, kHi, w_lo + kk * 2, kHi, ID, (ks > 0 || kk > 0) ? 1u : 0u);
+    }
+    mma_commit(&sc->empty[s]);
+  }
+  mma_commit(&sc->acc_full);
+}
+
+// One warpgroup per 128-row half of the tile: accumulator -> bf16 -> C_r.
+__device__ void epilogue(const Params& p, Smem* sc, const Item& it, int i, const Counters& cnt, bool& ok) {
+  const Geo& g = p.g;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quarter = warp % 4;
+  const int row = quarter * 32 + lane;
+  ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full, cnt.items & 1u, p, sc, SITE_ACC));
+  if (!ok) { sc->abort = 1; return; }
+  tc_fence_after();
+  const uint32_t tacc = sc->tmem_base + ((uint32_t)(quarter * 32) << 16) + i * kBN;
+  const size_t grow = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + i * 128 + row;
+  uint16_t* crow = p.c + ((size_t)it.r * g.M + grow) * g.Ns + (size_t)it.nb * kBN;
+#pragma unroll 1
+  for (int cb = 0; cb < kBN / 64; ++cb) {
+    uint32_t v[64];
+    tmem_ld64(tacc + cb * 64, v);
+    tmem_ld_wait();
+    uint4 o[8];
+    uint32_t* w = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+    uint4* dst = reinterpret_cast<uint4*>(crow + cb * 64);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[e] = o[e];
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ag_gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_a,
+                   const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_w) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Smem sc;
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNStage; ++s) {
+      mbar_init(&sc.full[s], 1);
+      mbar_init(&sc.empty[s], 1);
+    }
+    mbar_init(&sc.acc_full, 1);
+    for (int b = 0; b < 16; ++b) mbar_init(&sc.stg[b], 1);
+    mbar_init(&sc.drain, 1);
+    sc.abort = 0;
+    fence_barrier_init();
+    if (blockIdx.x == 0) {
+      unsigned long long z = 0;
+      atomicCAS(&p.ctrl->t0_ns, z, (unsigned long long)globaltimer_ns());
+      p.ctrl->ns_initial = (uint32_t)p.n_s_init;
+      atomicMax(&p.ctrl->ns_max, (uint32_t)p.n_s_init);
+      atomicMax(&p.ctrl->ns_min_inv, 0xFFFFu - (uint32_t)p.n_s_init);
+    }
+    prefetch_tmap(&tm_a);
+    prefetch_tmap(&tm_g);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sc.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  Counters cnt{0, 0};
+  uint32_t stg_phase[16] = {};
+  bool was_staging = false;
+  long long t_task = 0, starved = 0;
+  while (true) {
+    if (threadIdx.x == 0) {
+      decide(p, &sc, was_staging);
+      t_task = clock64();
+    }
+    __syncthreads();
+    const int cmd = sc.cmd, arg = sc.arg;
+    if (cmd == CMD_EXIT) break;
+    if (cmd == CMD_STAGE) {
+      if (threadIdx.x == 0) run_staging(p, &sc, smem_base, arg, stg_phase);
+    } else if (cmd == CMD_COMPUTE) {
+      const Item it = item_of(p.g, arg);
+      bool ok = true;
+      if (warp == 0 && lane == 0) {
+        Counters c2 = cnt;
+        starved = producer(p, &sc, smem_base, it, &tm_a, &tm_g, &tm_w, c2, ok);
+      } else if (warp == 1 && lane == 0) {
+        Counters c2 = cnt;
+        mma_issuer(p, &sc, smem_base, c2);
+      } else if (warp >= 4) {
+        epilogue(p, &sc, it, warp < 8 ? 0 : 1, cnt, ok);
+      }
+      cnt.fills += (uint32_t)(p.g.K / kBK);
+      cnt.items++;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0 && cmd != CMD_IDLE) {
+      long long busy = clock64() - t_task;
+      if (cmd == CMD_COMPUTE) {
+        busy -= starved;
+        atomicAdd(&p.ctrl->starve_cycles, (unsigned long long)(starved > 0 ? starved : 0));
+        starved = 0;
+      }
+      const unsigned long long dt = (unsigned long long)(busy > 0 ? busy : 0);
+      if (cmd == CMD_STAGE) {
+        atomicAdd(&p.ctrl->stage_cycles, dt);
+        atomicAdd(&p.ctrl->stage_done, 1ull);
+      } else {
+        atomicAdd(&p.ctrl->compute_cycles, dt);
+        atomicAdd(&p.ctrl->compute_tiles, 1ull);
+        atomicAdd(&p.ctrl->compute_items, 1ull);
+      }
+      const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
+      if (p.mode == PSR_ADAPTIVE && (tick % 16u) == 0) controller_update(p);
+    }
+  }
+  // drain: every tcgen05 op has completed and every TMA load has landed before TMEM is released
+  if (warp == 1 && lane == 0) {
+    mma_commit(&sc.drain);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&sc.drain, 0)) {
+      if (globaltimer_ns() - t0 > 100000000ull) break;
+    }
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait<0>();
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t s = 0; s < (uint32_t)kNStage && s < cnt.fills; ++s) {
+      const uint32_t fills = (cnt.fills - s + kNStage - 1) / kNStage;
+      while (!mbar_try_wait(&sc.full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(sc.tmem_base, 512);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------------
+struct Layout {
+  size_t ctrl, traj, flags, gbuf, total, reset_bytes;
+};
+
+static int geometry(const psr_ag_shape* sh, Geo& g) {
+  if (!sh) return PSR_ERR_ARG;
+  if (sh->M < 1 || sh->K < 1 || sh->Ns < 1 || sh->P < 1) return PSR_ERR_ARG;
+  if (sh->M % sh->P != 0) return PSR_ERR_UNSUPPORTED;
+  g.M = sh->M; g.K = sh->K; g.Ns = sh->Ns; g.P = sh->P;
+  g.Ms = sh->M / sh->P;
+  if (g.Ms % kBM != 0 || g.Ns % kBN != 0 || g.K % 128 != 0) return PSR_ERR_UNSUPPORTED;
+  if ((long long)g.P * g.M >= (1LL << 31) || (long long)g.P * g.Ns >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
+  g.n_mb = g.Ms / kBM;
+  g.n_nb = g.Ns / kBN;
+  // piece: >= 512 KiB of rows, a multiple of 128 rows dividing the shard
+  const long long row_bytes = (long long)g.K * 2;
+  int pr = 128;
+  while ((long long)pr * row_bytes < kPieceMinBytes && pr < g.Ms) pr *= 2;
+  while (g.Ms % pr != 0) pr /= 2;
+  if (pr < 128) pr = 128;
+  g.piece_rows = pr;
+  g.n_pieces = g.Ms / pr;
+  g.n_items = (long long)g.P * g.P * g.n_mb * g.n_nb;
+  g.n_stage = (long long)g.P * (g.P - 1) * g.n_pieces;
+  if (g.n_items >= (1LL << 31) || g.n_stage >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
+  return PSR_OK;
+}
+
+static size_t au(size_t x) { return (x + 255) / 256 * 256; }
+
+static Layout layout(const Geo& g) {
+  Layout l;
+  size_t off = 0;
+  l.ctrl = off; off += 256;
+  l.traj = off; off = au(off + (size_t)kTrajMax * 8);  // the same offsets as the attention workspace
+  l.flags = off; off = au(off + (size_t)g.P * g.P * g.n_pieces * 4);
+  l.reset_bytes = off;
+  l.gbuf = off; off = au(off + (size_t)g.P * g.M * g.K * 2);
+  l.total = off;
+  return l;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [rows][K] bf16, box = 64 columns x box_rows rows, 128-byte swizzle
+static bool tmap(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace ag
+}  // namespace psr
+
+using namespace psr;
+using namespace psr::ag;
+
+extern "C" {
+
+size_t psr_ag_gemm_workspace_bytes(const psr_ag_shape* sh) {
+  Geo g;
+  if (geometry(sh, g) != PSR_OK) return 0;
+  return layout(g).total;
+}
+
+int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, void* workspace, size_t ws_bytes,
+                const psr_partition* part, void* stream) {
+  if (!sh || !a || !w || !c || !workspace) return PSR_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PSR_ERR_ARG;
+  for (const void* ptr : {a, w, (const void*)c})
+    if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return PSR_ERR_ARG;
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PSR_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return PSR_ERR_UNSUPPORTED;
+  const int n_cta = prop.multiProcessorCount;
+  Geo g;
+  int rc = geometry(sh, g);
+  if (rc != PSR_OK) return rc;
+  const Layout L = layout(g);
+  if (ws_bytes < L.total) return PSR_ERR_ARG;
+  psr_partition pt;
+  if (part) pt = *part;
+  else { pt.mode = PSR_ADAPTIVE; pt.n_staging = 0; pt.n_min = 0; pt.n_max = 0; pt.fault = 0; pt.timeout_ms = 0; }
+  if (pt.mode != PSR_STATIC && pt.mode != PSR_ADAPTIVE) return PSR_ERR_ARG;
+  if (pt.fault < 0 || pt.fault > PSR_FAULT_SLOW_STAGING) return PSR_ERR_ARG;
+
+  Params kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.g = g;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  kp.a = static_cast<const uint16_t*>(a);
+  kp.gbuf = reinterpret_cast<uint16_t*>(ws + L.gbuf);
+  kp.c = static_cast<uint16_t*>(c);
+  kp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+  kp.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  kp.traj = reinterpret_cast<uint32_t*>(ws + L.traj);
+  kp.timeout_ns = (unsigned long long)(pt.timeout_ms > 0 ? pt.timeout_ms : 2000) * 1000000ull;
+  kp.n_tiles_total = (unsigned long long)g.n_items;
+  kp.n_stage_total = (unsigned long long)g.n_stage;
+  kp.mode = pt.mode;
+  kp.fault = pt.fault;
+  // priors (CTA-cycles): a piece at ~50 GB/s per staging SM (no less than ~6500 cycles); a task
+  // (2*256*256*K flops) at ~60 % of an SM's dense bf16 rate
+  const double piece_cycles = (double)g.piece_rows * g.K * 2 / 50e9 * 1.95e9;
+  kp.c_s0 = (float)(piece_cycles > 6500.0 ? piece_cycles : 6500.0);
+  kp.c_p0 = (float)(2.0 * kBM * kBN * (double)g.K / (0.6 * 8192.0));
+  const int hard_max = n_cta - 1;
+  int n_max = pt.n_max > 0 ? pt.n_max : n_cta / 2;
+  if (n_max > hard_max) n_max = hard_max;
+  int n_min = pt.n_min > 0 ? pt.n_min : 1;
+  if (n_min > n_max) n_min = n_max;
+  kp.n_min = n_min;
+  kp.n_max = n_max;
+  const bool any_staging = g.n_stage > 0;
+  int n_s;
+  if (pt.mode == PSR_STATIC) {
+    n_s = any_staging ? pt.n_staging : 0;
+    if (any_staging && (n_s < 1 || n_s > n_cta - 1)) return PSR_ERR_ARG;
+  } else {
+    n_s = pt.n_staging > 0 ? pt.n_staging
+                           : controller_rule(n_cta, (double)g.n_stage, kStageHeadroom * kp.c_s0, (double)g.n_items,
+                                             kp.c_p0, n_min, n_max);
+    if (!any_staging) n_s = 0;
+    else {
+      if (n_s < n_min) n_s = n_min;
+      if (n_s > n_max) n_s = n_max;
+    }
+  }
+  kp.n_s_init = n_s;
+
+  CUtensorMap ma, mg, mw;
+  if (!tmap(&ma, a, g.M, g.K, 128) || !tmap(&mg, kp.gbuf, (long long)g.P * g.M, g.K, 128) ||
+      !tmap(&mw, w, (long long)g.P * g.Ns, g.K, kBN))
+    return PSR_ERR_CUDA;
+
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(ag_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (attr_err != cudaSuccess) return PSR_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_cta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: compute waits on staging
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, ag_gemm_kernel, kp, ma, mg, mw) != cudaSuccess) {
+    cudaGetLastError();
+    return PSR_ERR_CUDA;
+  }
+  return PSR_OK;
+}
+
+}  // extern "C"
