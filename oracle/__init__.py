@@ -18,6 +18,11 @@ Parity status of each function (pins in tests/test_oracle_pins.py):
                     key permutation and key duplication invariants.
   attn_fwd_chunked  pinned: equals attn_fwd for every P dividing S and for
                     random chunk orders (the merge identity).
+  causal=2          (load-balanced shards: shard r holds half-chunks r and
+                    2P-1-r) pinned: Decimal brute force over positions built
+                    from the half-chunk list, equality with the contiguous
+                    causal result on the same sequence re-ordered, P = 1
+                    reduces bit for bit to causal=1, chunked merge identity.
 """
 from __future__ import annotations
 
@@ -80,7 +85,10 @@ def _prep(q, k, v, B, Hq, Hkv, S, P, d, causal, scale, rows):
         raise ValueError("oracle: tensor sizes do not match the shape")
     if scale is None:
         scale = 1.0 / np.sqrt(d)
-    sh = OracleShape(B, Hq, Hkv, S, P, d, int(bool(causal)), float(scale))
+    causal = int(causal)  # 0, 1, or 2 = causal over load-balanced shards
+    if causal not in (0, 1, 2):
+        raise ValueError("oracle: causal must be 0, 1 or 2")
+    sh = OracleShape(B, Hq, Hkv, S, P, d, causal, float(scale))
     if rows is None:
         n = B * Hq * S
         rows_arr = None

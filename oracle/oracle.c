@@ -16,6 +16,7 @@
  * optional causal mask over global positions, plus the per-row log-sum-exp:
  *
  *   A_i   = [0, S)            (non-causal)   or   [0, i]   (causal)
+ *         or {j : pos(j) <= pos(i)}   (causal over load-balanced shards, causal == 2)
  *   s_ij  = scale * sum_c Q[b,hq,i,c] * K[b,kv,j,c]      for j in A_i
  *   m_i   = max_j s_ij
  *   l_i   = sum_j exp(s_ij - m_i)
@@ -23,6 +24,12 @@
  *   LSE_i = m_i + ln l_i                                  (natural log)
  *
  * with kv = floor(hq / (Hq / Hkv)) (consecutive query heads share a KV head).
+ *
+ * Load-balanced shards (causal == 2; not on the pages, the usual balancing of
+ * causal ring attention): the S axis is stored shard by shard, L = S/P rows
+ * each, and shard r holds the half-chunks r and 2P-1-r of the sequence (L/2
+ * positions each), in that order.  pos(i) is the global position of stored
+ * row i; the mask compares positions, and outputs stay in stored order.
  * Inputs are bf16 bit patterns widened exactly to fp64; every step is fp64.
  *
  * Two modes:
@@ -85,23 +92,40 @@ static inline int64_t allowed_end(const oracle_shape *sh, int64_t i) {
   return sh->causal ? i + 1 : sh->S;
 }
 
-/* Direct definition for one row, keys [k0, k1) only.  Writes the normalised
- * output and returns the log-sum-exp of that key range (-inf if empty). */
+/* Global position of stored row i: i itself, or under load-balanced shards the
+ * position inside half-chunk r (rows 0 .. L/2-1 of shard r) or 2P-1-r (the rest). */
+static inline int64_t position(const oracle_shape *sh, int64_t i) {
+  if (sh->causal != 2) return i;
+  const int64_t L = sh->S / sh->P, h = L / 2;
+  const int64_t r = i / L, loc = i % L;
+  return loc < h ? r * h + loc : (2 * (int64_t)sh->P - 1 - r) * h + (loc - h);
+}
+
+/* Direct definition for one row, keys [k0, k1) only (under load-balanced shards,
+ * only those at positions <= qpos).  Writes the normalised output and returns the
+ * log-sum-exp of those keys (-inf if there are none). */
 static double attend_range(const oracle_shape *sh, const uint16_t *qrow, const uint16_t *kbase,
-                           const uint16_t *vbase, int64_t k0, int64_t k1, double *s_buf, double *out) {
+                           const uint16_t *vbase, int64_t k0, int64_t k1, int64_t qpos, double *s_buf,
+                           double *out) {
   const int d = sh->d;
   for (int c = 0; c < d; ++c) out[c] = 0.0;
   if (k1 <= k0) return -INFINITY;
   /* pass 1: scores and their maximum */
   double m = -INFINITY;
   for (int64_t j = k0; j < k1; ++j) {
+    if (sh->causal == 2 && position(sh, j) > qpos) { /* masked key */
+      s_buf[j - k0] = -INFINITY;
+      continue;
+    }
     double s = sh->scale * dot_bf16(qrow, kbase + j * d, d);
     s_buf[j - k0] = s;
     if (s > m) m = s;
   }
+  if (m == -INFINITY) return -INFINITY; /* every key masked */
   /* pass 2: exponentials, their sum and the weighted sum of V rows */
   double l = 0.0;
   for (int64_t j = k0; j < k1; ++j) {
+    if (s_buf[j - k0] == -INFINITY) continue;
     double p = exp(s_buf[j - k0] - m);
     l += p;
     const uint16_t *vr = vbase + j * d;
@@ -136,9 +160,10 @@ static void *worker(void *arg) {
     const uint16_t *kb = jb->k + (b * sh->Hkv + kv) * S * d;
     const uint16_t *vb = jb->v + (b * sh->Hkv + kv) * S * d;
     double *orow = jb->o + n * d;
-    const int64_t kend = allowed_end(sh, i);
+    const int64_t kend = sh->causal == 2 ? S : allowed_end(sh, i);
+    const int64_t qpos = position(sh, i);
     if (!jb->chunked) {
-      jb->lse[n] = attend_range(sh, qrow, kb, vb, 0, kend, s_buf, orow);
+      jb->lse[n] = attend_range(sh, qrow, kb, vb, 0, kend, qpos, s_buf, orow);
       continue;
     }
     /* ring order: shard r = i / L consumes chunk (r - t) mod P at step t */
@@ -149,7 +174,8 @@ static void *worker(void *arg) {
       int64_t k0 = j * L, k1 = (j + 1) * L;
       if (k1 > kend) k1 = kend; /* causal: keys beyond i are masked */
       if (k1 <= k0) continue;   /* fully masked chunk: skipped */
-      part_lse[np] = attend_range(sh, qrow, kb, vb, k0, k1, s_buf, part_o + (size_t)np * d);
+      part_lse[np] = attend_range(sh, qrow, kb, vb, k0, k1, qpos, s_buf, part_o + (size_t)np * d);
+      if (part_lse[np] == -INFINITY) continue; /* every key of the chunk masked: skipped */
       ++np;
     }
     if (np == 0) {
@@ -179,6 +205,8 @@ static int check_shape(const oracle_shape *sh) {
   if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->P < 1 || sh->d < 1) return 1;
   if (sh->Hq % sh->Hkv) return 1;
   if (sh->S % sh->P) return 1;
+  if (sh->causal < 0 || sh->causal > 2) return 1;
+  if (sh->causal == 2 && (sh->S / sh->P) % 2) return 1; /* shards split in two halves */
   return 0;
 }
 

@@ -13,6 +13,8 @@
 extern "C" {
 #endif
 
+/* causal: 0 none; 1 mask over contiguous shards (stored row i = position i);
+ * 2 mask over load-balanced shards (shard r holds half-chunks r and 2P-1-r). */
 typedef struct {
   int B, Hq, Hkv, S, P, d, causal;
   double scale;

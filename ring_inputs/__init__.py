@@ -139,7 +139,7 @@ class Workload:
     S: int
     P: int
     d: int
-    causal: bool
+    causal: int      # 0, 1, or 2 = causal over load-balanced shards
     seed: int
     qmul: float = 1.0
     kmul: float = 1.0
@@ -170,11 +170,15 @@ class Workload:
 
     def staging_transfers(self) -> int:
         """(shard, chunk) transfers the ring performs: the local chunk is never moved."""
-        return self.P * (self.P - 1) // 2 if self.causal else self.P * (self.P - 1)
+        return self.P * (self.P - 1) // 2 if self.causal == 1 else self.P * (self.P - 1)
 
     def staging_bytes(self) -> int:
-        """Bytes written into ring slots (K and V); the same amount is read from home."""
-        return self.staging_transfers() * 2 * self.L * self.d * 2 * self.B * self.Hkv
+        """Bytes written into ring slots (K and V); the same amount is read from home.  Over
+        load-balanced shards half of the transfers (chunks below the shard) move half a chunk."""
+        rows = self.staging_transfers() * self.L
+        if self.causal == 2:
+            rows -= self.P * (self.P - 1) // 2 * (self.L // 2)
+        return rows * 2 * self.d * 2 * self.B * self.Hkv
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -190,6 +194,8 @@ WORKLOADS = {
     # B1 H32 S32768 P16 d128, non-causal and causal: the headline throughput case
     "h32_s32k_nc": Workload("h32_s32k_nc", 1, 32, 32, 32768, 16, 128, False, seed=2),
     "h32_s32k_c": Workload("h32_s32k_c", 1, 32, 32, 32768, 16, 128, True, seed=2),
+    # the same causal pass over load-balanced shards (shard r holds half-chunks r and 2P-1-r)
+    "h32_s32k_cb": Workload("h32_s32k_cb", 1, 32, 32, 32768, 16, 128, 2, seed=2),
     # GQA, causal, B2 Hq32 Hkv8 S65536 P16 d128, Q and K x2
     "gqa_s64k_c": Workload("gqa_s64k_c", 2, 32, 8, 65536, 16, 128, True, seed=3, qmul=2.0, kmul=2.0),
     # long sequence, causal, B1 H8 S131072 P32 d128, 1 % of K rows x8

@@ -48,8 +48,17 @@ def run(q, k, v, causal, P=1, scale=None, rows=None, chunked=False, perm=None):
 # Exact brute force (Python Decimal, 40 digits)
 # ------------------------------------------------------------------------------------------------
 
-def decimal_attention(q, k, v, causal, scale):
-    """Softmax attention evaluated in 40-digit decimal arithmetic, one row at a time."""
+def balanced_positions(S, P):
+    """Global position of each stored row under load-balanced shards, built from the
+    list of half-chunks each shard holds: shard r holds half-chunks r and 2P-1-r."""
+    h = S // P // 2
+    chunks = [c for r in range(P) for c in (r, 2 * P - 1 - r)]
+    return np.concatenate([np.arange(c * h, (c + 1) * h) for c in chunks])
+
+
+def decimal_attention(q, k, v, causal, scale, positions=None):
+    """Softmax attention evaluated in 40-digit decimal arithmetic, one row at a time.
+    With `positions`, key j is visible to row i when positions[j] <= positions[i]."""
     ctx = decimal.Context(prec=40)
     B, Hq, S, d = q.shape
     Hkv = k.shape[1]
@@ -60,7 +69,10 @@ def decimal_attention(q, k, v, causal, scale):
     lse = np.zeros((B, Hq, S))
     for b, h, i in itertools.product(range(B), range(Hq), range(S)):
         kv = h // g
-        keys = range(i + 1) if causal else range(S)
+        if positions is not None:
+            keys = [j for j in range(S) if positions[j] <= positions[i]]
+        else:
+            keys = range(i + 1) if causal else range(S)
         s = []
         for j in keys:
             acc = D(0)
@@ -235,6 +247,67 @@ def test_chunked_merge_equals_direct_for_every_P(causal):
         assert np.max(np.abs(lse - lsec)) <= 1e-12
 
 
+# ------------------------------------------------------------------------------------------------
+# Load-balanced causal shards (causal=2)
+# ------------------------------------------------------------------------------------------------
+
+def test_balanced_positions_are_a_permutation():
+    for S, P in ((8, 2), (12, 3), (64, 4), (4096, 16)):
+        pos = balanced_positions(S, P)
+        assert np.array_equal(np.sort(pos), np.arange(S))
+        # every shard holds the same number of (query, key) pairs under the mask
+        L = S // P
+        work = [int(np.sum(pos[r * L:(r + 1) * L] + 1)) for r in range(P)]
+        assert len(set(work)) == 1, work
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,P,d", [(1, 1, 1, 8, 2, 4), (1, 2, 1, 12, 3, 4), (2, 2, 2, 16, 4, 3)])
+def test_balanced_decimal_brute_force(B, Hq, Hkv, S, P, d):
+    rng = np.random.default_rng(300 + S + P)
+    q, k, v = make(rng, B, Hq, Hkv, S, d, scale=1.5)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run(q, k, v, 2, P=P, scale=scale)
+    o_ref, lse_ref = decimal_attention(q, k, v, True, scale, positions=balanced_positions(S, P))
+    assert np.max(np.abs(o - o_ref)) <= 1e-13
+    assert np.max(np.abs(lse - lse_ref)) <= 1e-13
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+def test_balanced_equals_contiguous_on_the_reordered_sequence(P):
+    # attention under a positional mask depends on positions only: storing the natural
+    # sequence in balanced shard order must give the contiguous causal rows, re-ordered
+    rng = np.random.default_rng(20 + P)
+    B, Hq, Hkv, S, d = 1, 4, 2, 64, 8
+    q, k, v = make(rng, B, Hq, Hkv, S, d, scale=1.5)
+    o_nat, lse_nat = run(q, k, v, True)
+    pos = balanced_positions(S, P)  # stored row i holds natural row pos[i]
+    o_bal, lse_bal = run(q[:, :, pos], k[:, :, pos], v[:, :, pos], 2, P=P)
+    o_nat = o_nat.reshape(B, Hq, S, d)[:, :, pos].reshape(-1, d)
+    lse_nat = lse_nat.reshape(B, Hq, S)[:, :, pos].reshape(-1)
+    if P == 1:  # identity layout: the same arithmetic in the same order
+        assert np.array_equal(o_bal, o_nat) and np.array_equal(lse_bal, lse_nat)
+    assert np.max(np.abs(o_bal - o_nat)) <= 1e-12
+    assert np.max(np.abs(lse_bal - lse_nat)) <= 1e-12
+
+
+def test_balanced_chunked_merge_equals_direct():
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, S, d = 1, 2, 1, 128, 16
+    q, k, v = make(rng, B, Hq, Hkv, S, d, scale=1.5)
+    for P in (1, 2, 4, 8, 16, 32, 64):
+        o, lse = run(q, k, v, 2, P=P)
+        oc, lsec = run(q, k, v, 2, P=P, chunked=True)
+        assert np.max(np.abs(o - oc)) <= 1e-12, P
+        assert np.max(np.abs(lse - lsec)) <= 1e-12, P
+
+
+def test_balanced_rejects_odd_shards():
+    rng = np.random.default_rng(22)
+    q, k, v = make(rng, 1, 1, 1, 12, 4)
+    with pytest.raises(ValueError):
+        run(q, k, v, 2, P=4)  # L = 3 cannot be split in two halves
+
+
 def test_row_subset_matches_full():
     w = ri.WORKLOADS["small"]
     q, k, v = ri.generate(w)
@@ -273,6 +346,9 @@ MUTANTS = {
     "unnormalised": ("for (int c = 0; c < d; ++c) out[c] /= l;", "(void)0;"),
     "transposed_kv": ("const uint16_t *vr = vbase + j * d;", "const uint16_t *vr = kbase + j * d;"),
     "merge_sign": ("const double w = exp(part_lse[t] - lse);", "const double w = exp(lse - part_lse[t]);"),
+    "balanced_half_order": ("(2 * (int64_t)sh->P - 1 - r) * h", "(sh->P + r) * h"),
+    "balanced_mask_strict": ("position(sh, j) > qpos", "position(sh, j) >= qpos"),
+    "balanced_first_half": ("return loc < h ? r * h + loc", "return loc < h ? r * L + loc"),
 }
 
 
@@ -322,6 +398,13 @@ def _pins_pass(so):
         o, lse = call(q, k, v, causal)
         oc, lsec = call(q, k, v, causal, P=4, chunked=True)
         if np.max(np.abs(o - oc)) > 1e-12 or np.max(np.abs(lse - lsec)) > 1e-12:
+            return False
+    # load-balanced shards: brute force over the half-chunk positions
+    for S, P in ((8, 2), (12, 3)):
+        q, k, v = make(rng, 1, 2, 1, S, 4, scale=1.5)
+        o, lse = call(q, k, v, 2, P=P)
+        o_ref, lse_ref = decimal_attention(q, k, v, True, 1.0 / np.sqrt(4), positions=balanced_positions(S, P))
+        if np.max(np.abs(o - o_ref)) > 1e-13 or np.max(np.abs(lse - lse_ref)) > 1e-13:
             return False
     return True
 
