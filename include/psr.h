@@ -55,6 +55,16 @@ extern "C" {
 #define PSR_FAULT_DROP_FIRST_FLAG 1 /* the first staged chunk never publishes its readiness flag */
 #define PSR_FAULT_SLOW_STAGING 2    /* every staging task sleeps ~20 us before copying */
 
+/* Causal layouts (psr_shape.causal).  With PSR_CAUSAL_BALANCED, shard r (rows r*L .. r*L+L-1
+ * of the S axis, L = S/P) holds two halves of the sequence: its rows i < L/2 are global
+ * position r*L/2 + i and its rows i >= L/2 are global position (2P-1-r)*L/2 + (i - L/2).  Every
+ * shard then does the same causal work at every ring step (with contiguous shards shard r does
+ * r+1 of the P steps).  The caller stores Q, K, V (and receives O, LSE) in that shard order;
+ * the mask is over the global positions.  This layout is not on the mKernel pages: it is the
+ * usual load balancing of causal ring attention.  Requires L a multiple of 512. */
+#define PSR_CAUSAL 1
+#define PSR_CAUSAL_BALANCED 2
+
 typedef struct {
   int B;        /* batch */
   int Hq;       /* query heads */
@@ -62,7 +72,9 @@ typedef struct {
   int S;        /* global sequence length */
   int P;        /* ring size (number of shards); S % P == 0 */
   int d;        /* head dim: 64 or 128 */
-  int causal;   /* 0 or 1: mask k_pos > q_pos over global positions */
+  int causal;   /* 0: none; PSR_CAUSAL (1): mask k_pos > q_pos over global positions, shard r
+                   holding positions r*L .. r*L+L-1; PSR_CAUSAL_BALANCED (2): the same mask over
+                   load-balanced shards (see below) */
   float scale;  /* <= 0 selects 1/sqrt(d) */
 } psr_shape;
 
@@ -115,8 +127,8 @@ PSR_API size_t psr_workspace_bytes(const psr_shape* shape);
  * Asynchronous: enqueues a flag reset and one persistent launch on `stream`
  * and returns.  The library allocates no device memory.  A device-side
  * timeout is reported by psr_get_stats, not here.
- * Supported: d in {64, 128}; S % P == 0; L = S/P a multiple of 256;
- * Hq % Hkv == 0; sm_103 device.  Otherwise PSR_ERR_UNSUPPORTED. */
+ * Supported: d in {64, 128}; S % P == 0; L = S/P a multiple of 256 (of 512 with
+ * PSR_CAUSAL_BALANCED); Hq % Hkv == 0; sm_103 device.  Otherwise PSR_ERR_UNSUPPORTED. */
 PSR_API int psr_ring_attn_fwd(const psr_shape* shape, const void* q, const void* k, const void* v, void* o, float* lse,
                       void* workspace, size_t workspace_bytes, const psr_partition* part, void* stream);
 

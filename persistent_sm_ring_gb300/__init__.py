@@ -18,11 +18,13 @@ from .build import LIB, LIB_PAIRS, LIB_TRACE, build as _build
 __all__ = ["build", "load", "Shape", "AgShape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host",
            "workspace_bytes", "ag_gemm", "ag_gemm_workspace_bytes",
            "get_stats", "get_trajectory", "controller_target", "num_ctas", "status_string", "PsrError",
-           "STATIC", "ADAPTIVE", "FAULT_NONE", "FAULT_DROP_FIRST_FLAG", "FAULT_SLOW_STAGING"]
+           "STATIC", "ADAPTIVE", "FAULT_NONE", "FAULT_DROP_FIRST_FLAG", "FAULT_SLOW_STAGING", "CAUSAL",
+           "CAUSAL_BALANCED"]
 
 OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 STATIC, ADAPTIVE = 0, 1
 FAULT_NONE, FAULT_DROP_FIRST_FLAG, FAULT_SLOW_STAGING = 0, 1, 2
+CAUSAL, CAUSAL_BALANCED = 1, 2
 
 EXPORTED = ("psr_workspace_bytes", "psr_ring_attn_fwd", "psr_ring_attn_fwd_host", "psr_get_stats",
             "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas",
@@ -121,7 +123,8 @@ def status_string(status: int) -> str:
 
 
 def make_shape(B, Hq, Hkv, S, P, d, causal, scale=None) -> Shape:
-    return Shape(int(B), int(Hq), int(Hkv), int(S), int(P), int(d), int(bool(causal)),
+    """causal: False/0, True/1 (CAUSAL), or 2 (CAUSAL_BALANCED: load-balanced shards)."""
+    return Shape(int(B), int(Hq), int(Hkv), int(S), int(P), int(d), int(causal),
                  float(scale) if scale is not None else 0.0)
 
 

@@ -83,7 +83,7 @@ static WsLayout ws_layout(const Geometry& G) {
   w.traj = off; off = align_up(off + (size_t)kTrajMax * 8, 256);  // fixed offset: read without the shape
   w.flags = off; off = align_up(off + n_fc * G.n_pieces * 4, 256);  // per (group, step, piece)
   w.consumed = off; off = align_up(off + n_fc * 4, 256);
-  w.queue = off; off = align_up(off + (size_t)(dynamic_staging_tasks(G) * G.n_pieces + 1) * 4, 256);
+  w.queue = off; off = align_up(off + (size_t)(dynamic_staging_pieces(G) + 1) * 4, 256);
   w.reset_bytes = off;  // everything above is zeroed before each launch
   const size_t slot_elems = (size_t)kRingSlots * G.n_groups * G.L * G.d;
   w.slot_k = off; off = align_up(off + slot_elems * 2, 256);
@@ -195,6 +195,7 @@ struct StageTicket {
   bool done = false; // every queue entry has been handed out
 };
 
+template <int BAL>
 __device__ int claim_static_piece(const KParams& p) {
   Ctrl* c = p.ctrl;
   const Geometry& G = p.geo;
@@ -209,12 +210,17 @@ __device__ int claim_static_piece(const KParams& p) {
     const int g = (int)(i / ((uint32_t)kRingSlots * G.n_pieces));
     const int step = 1 + (int)((i / G.n_pieces) % (uint32_t)kRingSlots);
     const int piece = (int)(i % G.n_pieces);
-    if (step < group_steps(G, g)) return (g * G.P + step) * G.n_pieces + piece;
-    // shard with fewer steps: nothing to stage for this entry; try the next one
+    int r, b, kvh, sub;
+    group_coord<BAL>(G, g, r, b, kvh, sub);
+    if (step < steps_of_shard<BAL>(G, r) && piece < stage_pieces<BAL>(G, r, step))
+      return (g * G.P + step) * G.n_pieces + piece;
+    // a shard with fewer steps, or a piece beyond the tiles the step needs: nothing to stage
+    // for this entry; try the next one
   }
   return -1;
 }
 
+template <int BAL>
 __device__ int try_claim_staging(const KParams& p, StageTicket& tk) {
   Ctrl* c = p.ctrl;
   if (tk.held >= 0) {
@@ -224,7 +230,7 @@ __device__ int try_claim_staging(const KParams& p, StageTicket& tk) {
       return (int)(e - 1);
     }
   }
-  const int t = claim_static_piece(p);
+  const int t = claim_static_piece<BAL>(p);
   if (t >= 0) return t;
   if (tk.held < 0 && !tk.done) {
     if (ld_relaxed(&c->q_head) >= (uint32_t)p.n_dyn) {
@@ -305,7 +311,7 @@ __device__ __forceinline__ void publish_pending(StagePending& pend) {
   pend.flag = nullptr;
 }
 
-template <int D, int CG>
+template <int D, int CG, int BAL>
 __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, int task, uint32_t (&stg_phase)[16],
                             StagePending& pend) {
   using C = Cfg<D, CG>;
@@ -313,11 +319,12 @@ __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, i
   const int chunk = task / G.n_pieces, piece = task % G.n_pieces;
   const int g = chunk / G.P, step = chunk % G.P;
   int r, b, kvh, sub;
-  group_coord(G, g, r, b, kvh, sub);
+  group_coord<BAL>(G, g, r, b, kvh, sub);
   const int j = ((r - step) % G.P + G.P) % G.P;
   const size_t tile_elems = (size_t)kTileRows * D;
   const int kt0 = piece * G.piece_tiles;
-  const int n_kt = (G.kv_tiles - kt0) < G.piece_tiles ? (G.kv_tiles - kt0) : G.piece_tiles;
+  const int need = stage_tiles<BAL>(G, r, step);  // tiles of the chunk any item of the group reads
+  const int n_kt = (need - kt0) < G.piece_tiles ? (need - kt0) : G.piece_tiles;
   const size_t src_off = ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L + (size_t)kt0 * kTileRows) * D;
   const size_t slot_off = (((size_t)slot_of(step) * G.n_groups + g) * (size_t)G.L + (size_t)kt0 * kTileRows) * D;
   uint32_t* flag = p.flags + (size_t)chunk * G.n_pieces + piece;
@@ -433,7 +440,7 @@ struct Starved {
 
 // In a pair both CTAs run a producer for their own shares; only the even CTA's
 // barriers count the bytes (for both) and only it sends "consumed" notifications.
-template <int D, int CG>
+template <int D, int CG, int BAL>
 __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, uint32_t rank,
                               const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               const CUtensorMap* tm_sk, const CUtensorMap* tm_sv, Counters& cnt) {
@@ -464,11 +471,11 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
     fence_proxy_async_global();
     const uint32_t old = atom_add_acq_rel(p.consumed + (size_t)it.g * G.P + t, 1u);
     if (old + 1 == (uint32_t)G.Gs && t + kRingSlots < it.n_steps) {
-      const uint32_t np = (uint32_t)G.n_pieces;
+      const uint32_t np = (uint32_t)stage_pieces<BAL>(G, it.r, t + kRingSlots);
       const uint32_t k = atomicAdd(&p.ctrl->q_tail, np);
       const uint32_t chunk = (uint32_t)(it.g * G.P + t + kRingSlots);
       if (k + np <= (uint32_t)p.n_dyn) {
-        for (uint32_t pc = 0; pc < np; ++pc) st_release(p.queue + k + pc, chunk * np + pc + 1u);
+        for (uint32_t pc = 0; pc < np; ++pc) st_release(p.queue + k + pc, chunk * (uint32_t)G.n_pieces + pc + 1u);
       } else {
         raise_error(p, SITE_QUEUE);
       }
@@ -482,7 +489,7 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
   Starved starved;
   for (int t = 0; t < it.n_steps && ok; ++t) {
     const int j = ((it.r - t) % G.P + G.P) % G.P;
-    const int n_kt = tiles_at_step(G, it, t);
+    const int n_kt = tiles_at_step<BAL>(G, it, t);
     const CUtensorMap* mk = t == 0 ? tm_k : tm_sk;
     const CUtensorMap* mv = t == 0 ? tm_v : tm_sv;
     const int row0 = t == 0 ? (it.b * G.Hkv + it.kvh) * G.S + j * G.L
@@ -552,7 +559,7 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
 //   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
 // PV_i(j) reads P_i(j), which overlays S_i(j) in tensor memory, so S_i(j+1) is issued
 // right behind it (tensor-core instructions of one thread run in order).
-template <int D, int CG>
+template <int D, int CG, int BAL>
 __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, const ItemCoord& it, Counters& cnt) {
   using C = Cfg<D, CG>;
   const Geometry& G = p.geo;
@@ -594,7 +601,7 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
     mma_commit_cg<CG>(&sc->kv_empty[vstage]);
     return true;
   };
-  const uint32_t n = (uint32_t)item_tiles(G, it);
+  const uint32_t n = (uint32_t)item_tiles<BAL>(G, it);
   uint32_t ck = cnt.kv;  // load index of K_0 of this item (the producer loads K_j, V_j alternately)
   cnt.kv += 2u * n;
   unsigned long long tr_issue = 0, tr_kv = 0;
@@ -681,7 +688,7 @@ __device__ __forceinline__ float acc_sum(const uint64_t (&acc)[4]) {
 
 // One softmax warpgroup per 128-row query tile i of the CTA (in a pair, CTA `rank`
 // holds query tiles 2*rank and 2*rank + 1 of the item).
-template <int D, int CG>
+template <int D, int CG, int BAL>
 __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, int i, uint32_t rank, Counters& cnt) {
   using C = Cfg<D, CG>;
   const Geometry& G = p.geo;
@@ -717,7 +724,7 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
   bool ok = true;
   unsigned long long tr_wait = 0, tr_busy = 0;
   for (int t = 0; t < it.n_steps && ok; ++t) {
-    const int n_kt = tiles_at_step(G, it, t);
+    const int n_kt = tiles_at_step<BAL>(G, it, t);
     for (int kt = 0; kt < n_kt; ++kt, ++jglob) {
       const long long c0 = trace_clock();
       // tcgen05.ld/st below are warp-collective: every lane must take the same path
@@ -851,7 +858,7 @@ __device__ __forceinline__ void read_cmd(SmemCtl& sc, uint32_t rank, int& cmd, i
   }
 }
 
-template <int D, int CG>
+template <int D, int CG, int BAL>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -928,9 +935,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == 0 && cmd != CMD_STAGE) publish_pending(pend);
       if (cmd == CMD_STAGE) {
         if (threadIdx.x == 0) {
-          const int task = try_claim_staging(p, ticket);
+          const int task = try_claim_staging<BAL>(p, ticket);
           if (task >= 0) {
-            run_staging<D, CG>(p, &sc, smem_base, task, stg_phase, pend);
+            run_staging<D, CG, BAL>(p, &sc, smem_base, task, stg_phase, pend);
             idle_since = 0;
           } else {
             publish_pending(pend);
@@ -947,13 +954,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rank == 1) st_shared_cluster(mapa_shared(smem_u32(&sc.peer_held), 0), ticket.held >= 0 ? 1u : 0u);
         }
       } else if (cmd == CMD_COMPUTE) {
-        const ItemCoord it = item_coord(p.geo, arg);
+        const ItemCoord it = item_coord<BAL>(p.geo, arg);
         if (warp == 0 && lane == 0)
-          starved = producer<D, CG>(p, &sc, smem_base, it, rank, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
+          starved = producer<D, CG, BAL>(p, &sc, smem_base, it, rank, &tm_q, &tm_k, &tm_v, &tm_sk, &tm_sv, cnt);
         else if (warp == 1 && lane == 0 && rank == 0)
-          mma_issuer<D, CG>(p, &sc, smem_base, it, cnt);
+          mma_issuer<D, CG, BAL>(p, &sc, smem_base, it, cnt);
         cnt.items++;
-        cnt.tiles += (uint32_t)item_tiles(p.geo, it);
+        cnt.tiles += (uint32_t)item_tiles<BAL>(p.geo, it);
         if (threadIdx.x == 0) idle_since = 0;
       }
       tc_fence_before();
@@ -973,8 +980,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // cycles from every CTA of the unit (the cost of a tile in CTA-cycles); tiles and items once
           atomicAdd(&p.ctrl->compute_cycles, dt);
           if (rank == 0) {
-            const ItemCoord it = item_coord(p.geo, arg);
-            atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles(p.geo, it));
+            const ItemCoord it = item_coord<BAL>(p.geo, arg);
+            atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles<BAL>(p.geo, it));
             atomicAdd(&p.ctrl->compute_items, 1ull);
           }
         }
@@ -1012,10 +1019,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       read_cmd<CG>(sc, rank, cmd, arg);
       if (cmd == CMD_EXIT) break;
       if (cmd == CMD_COMPUTE) {
-        const ItemCoord it = item_coord(p.geo, arg);
-        softmax_wg<D, CG>(p, &sc, it, warp < 8 ? 0 : 1, rank, cnt);
+        const ItemCoord it = item_coord<BAL>(p.geo, arg);
+        softmax_wg<D, CG, BAL>(p, &sc, it, warp < 8 ? 0 : 1, rank, cnt);
         cnt.items++;
-        cnt.tiles += (uint32_t)item_tiles(p.geo, it);
+        cnt.tiles += (uint32_t)item_tiles<BAL>(p.geo, it);
       }
       tc_fence_before();
       unit_sync<CG>();
@@ -1095,8 +1102,9 @@ static int max_group_items(int n_units) {
 // of both CTAs gates every PV), and two staging CTAs of one pair copy at ~30 GB/s each
 // against ~50 GB/s for single CTAs, so the single-CTA kernel is faster at every split.
 static int units_cg(const psr_shape* sh, int n_cta) {
-  return (PSR_PAIRS && sh->d == 128 && sh->P > 0 && sh->S % sh->P == 0 && (sh->S / sh->P) % (2 * kCtaRows) == 0 &&
-          n_cta >= 4)
+  // a pair item holds 2 * kCtaRows query rows; balanced shards need whole items in each half
+  const int rows = (sh->causal == 2 ? 2 : 1) * 2 * kCtaRows;
+  return (PSR_PAIRS && sh->d == 128 && sh->P > 0 && sh->S % sh->P == 0 && (sh->S / sh->P) % rows == 0 && n_cta >= 4)
              ? 2
              : 1;
 }
@@ -1106,7 +1114,7 @@ static int shape_geometry(const psr_shape* sh, Geometry& G, int n_cta) {
   if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->P < 1) return PSR_ERR_ARG;
   if (sh->Hq % sh->Hkv != 0 || sh->S % sh->P != 0) return PSR_ERR_UNSUPPORTED;
   if (sh->d != 64 && sh->d != 128) return PSR_ERR_UNSUPPORTED;
-  if (sh->causal != 0 && sh->causal != 1) return PSR_ERR_ARG;
+  if (sh->causal < 0 || sh->causal > PSR_CAUSAL_BALANCED) return PSR_ERR_ARG;
   if (!(sh->scale == sh->scale)) return PSR_ERR_ARG;  // NaN
   const long long rows_q = (long long)sh->B * sh->Hq * sh->S;
   if (rows_q >= (1LL << 31) || rows_q * sh->d >= (1LL << 40)) return PSR_ERR_UNSUPPORTED;
@@ -1119,11 +1127,11 @@ static int shape_geometry(const psr_shape* sh, Geometry& G, int n_cta) {
   return PSR_OK;
 }
 
-template <int D, int CG>
+template <int D, int CG, int BAL>
 static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  auto kern = ring_attn_kernel<D, CG>;
+  auto kern = ring_attn_kernel<D, CG, BAL>;
   std::call_once(once, [kern] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, CG>::SMEM);
     if (attr_err != cudaSuccess) return;
@@ -1290,8 +1298,8 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.traj = reinterpret_cast<uint32_t*>(ws + L.traj);
   kp.timeout_ns = (unsigned long long)(pt.timeout_ms > 0 ? pt.timeout_ms : 2000) * 1000000ull;
   kp.n_tiles_total = (unsigned long long)total_tiles(G);
-  kp.n_stage_total = (unsigned long long)total_staging_tasks(G) * (unsigned long long)G.n_pieces;
-  kp.n_dyn = (int)(dynamic_staging_tasks(G) * G.n_pieces);
+  kp.n_stage_total = (unsigned long long)total_staging_pieces(G);
+  kp.n_dyn = (int)dynamic_staging_pieces(G);
   kp.n_init = kRingSlots * G.n_groups * G.n_pieces;
   kp.mode = pt.mode;
   kp.fault = pt.fault;
@@ -1356,8 +1364,18 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
-  cudaError_t e = cg == 2 ? launch<128, 2>(kp, maps, n_cta, st)
-                          : (G.d == 128 ? launch<128, 1>(kp, maps, n_cta, st) : launch<64, 1>(kp, maps, n_cta, st));
+  // one kernel per (d, compute unit, shard layout); CTA-pair kernels only in a library built with pairs
+  const bool bal = G.balanced != 0;
+  cudaError_t e;
+#if PSR_PAIRS
+  if (cg == 2)
+    e = bal ? launch<128, 2, 1>(kp, maps, n_cta, st) : launch<128, 2, 0>(kp, maps, n_cta, st);
+  else
+#endif
+  if (G.d == 128)
+    e = bal ? launch<128, 1, 1>(kp, maps, n_cta, st) : launch<128, 1, 0>(kp, maps, n_cta, st);
+  else
+    e = bal ? launch<64, 1, 1>(kp, maps, n_cta, st) : launch<64, 1, 0>(kp, maps, n_cta, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PSR_ERR_CUDA;

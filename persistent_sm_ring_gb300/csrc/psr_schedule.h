@@ -6,6 +6,16 @@
 // rule 3: local inputs first).  With a causal mask chunk j is needed by shard
 // r only when j <= r, i.e. steps t = 0..r.
 //
+// Load-balanced causal shards (causal == 2).  Shard r holds two halves of the
+// sequence: local rows [0, L/2) are global positions r*L/2 + i and local rows
+// [L/2, L) are (2P-1-r)*L/2 + (i - L/2).  Then every shard does the same causal
+// work at every step: at t = 0 the local chunk is masked as in the contiguous
+// case (positions rise with the local index inside a shard); at 1 <= t <= r
+// (chunk j < r) every query row sees exactly the first half of the chunk; at
+// t > r (chunk j > r) the first-half query rows see none of it and the
+// second-half rows see all of it.  No tile other than a step-0 diagonal tile is
+// ever partly masked.
+//
 // Units of work:
 //  * compute item  = the query rows one compute unit carries through all of
 //                    shard r's ring steps with the accumulators resident in
@@ -63,6 +73,7 @@ PSR_HD int slot_of(int step) { return step % kRingSlots; }
 
 struct Geometry {
   int B, Hq, Hkv, S, P, d, causal;
+  int balanced;  // causal over load-balanced shards (causal == 2 at the API)
   int L;         // shard length S / P
   int gqa;       // Hq / Hkv
   int cg;        // CTAs per compute unit: 1, or 2 (a CTA pair)
@@ -72,6 +83,7 @@ struct Geometry {
   int kv_tiles;  // 128-row KV tiles per chunk: L / 128
   int piece_tiles;  // tiles per staging piece
   int n_pieces;     // staging pieces per chunk
+  int half_pieces;  // staging pieces of the first half of a chunk
   int G;         // items sharing one (shard, b, kvh): gqa * q_blocks
   int n_sub;     // sub-groups per (shard, b, kvh)
   int Gs;        // items per group: G / n_sub
@@ -90,6 +102,8 @@ struct ItemCoord {
 PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int d, int causal, int max_group,
                          int cg = 1) {
   G.B = B; G.Hq = Hq; G.Hkv = Hkv; G.S = S; G.P = P; G.d = d; G.causal = causal ? 1 : 0;
+  G.balanced = causal == 2 ? 1 : 0;
+  if (causal < 0 || causal > 2) return 1;
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || P < 1 || d < 1) return 1;
   if (Hq % Hkv != 0 || S % P != 0) return 1;
   if (cg != 1 && cg != 2) return 1;
@@ -98,6 +112,7 @@ PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int 
   G.item_qt = G.item_rows / kTileRows;
   G.L = S / P;
   if (G.L % G.item_rows != 0) return 2;
+  if (G.balanced && G.L % (2 * G.item_rows) != 0) return 2;  // each half holds whole items
   G.gqa = Hq / Hkv;
   G.q_blocks = G.L / G.item_rows;
   G.kv_tiles = G.L / kTileRows;
@@ -112,6 +127,7 @@ PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int 
     G.piece_tiles = pt < 1 ? 1 : pt;
   }
   G.n_pieces = (G.kv_tiles + G.piece_tiles - 1) / G.piece_tiles;
+  G.half_pieces = (G.kv_tiles / 2 + G.piece_tiles - 1) / G.piece_tiles;
   G.G = G.gqa * G.q_blocks;
   // split a group into power-of-two sub-groups until it fits the bound
   G.n_sub = 1;
@@ -127,58 +143,105 @@ PSR_HD int geometry_init(Geometry& G, int B, int Hq, int Hkv, int S, int P, int 
   return 0;
 }
 
-// Shard of the rr-th shard in dispense order: causal runs the longest shards first.
-PSR_HD int shard_of_rank(const Geometry& G, int rr) { return G.causal ? (G.P - 1 - rr) : rr; }
+// The shard layout of the functions below: kBal = -1 reads G.balanced; 0 or 1 fixes it at
+// compile time (the device code instantiates one kernel per layout, so that the contiguous
+// kernel carries none of the balanced layout's branches).
+template <int kBal = -1>
+PSR_HD bool is_balanced(const Geometry& G) { return kBal < 0 ? G.balanced != 0 : kBal != 0; }
 
-PSR_HD int steps_of_shard(const Geometry& G, int r) { return G.causal ? (r + 1) : G.P; }
+// Contiguous causal shards: shard r needs steps 0..r only, and runs longest first.
+template <int kBal = -1>
+PSR_HD bool skewed(const Geometry& G) { return G.causal && !is_balanced<kBal>(G); }
 
+// Shard of the rr-th shard in dispense order: contiguous causal runs the longest shards first.
+template <int kBal = -1>
+PSR_HD int shard_of_rank(const Geometry& G, int rr) { return skewed<kBal>(G) ? (G.P - 1 - rr) : rr; }
+
+template <int kBal = -1>
+PSR_HD int steps_of_shard(const Geometry& G, int r) { return skewed<kBal>(G) ? (r + 1) : G.P; }
+
+template <int kBal = -1>
 PSR_HD void group_coord(const Geometry& G, int g, int& r, int& b, int& kvh, int& sub) {
   sub = g % G.n_sub;
   int rest = g / G.n_sub;
   kvh = rest % G.Hkv;
   rest /= G.Hkv;
   b = rest % G.B;
-  r = shard_of_rank(G, rest / G.B);
+  r = shard_of_rank<kBal>(G, rest / G.B);
 }
 
+template <int kBal = -1>
 PSR_HD int group_steps(const Geometry& G, int g) {
   int r, b, kvh, sub;
-  group_coord(G, g, r, b, kvh, sub);
-  return steps_of_shard(G, r);
+  group_coord<kBal>(G, g, r, b, kvh, sub);
+  return steps_of_shard<kBal>(G, r);
 }
 
+template <int kBal = -1>
 PSR_HD ItemCoord item_coord(const Geometry& G, int n) {
   ItemCoord c;
   c.g = n / G.Gs;
   int sub;
-  group_coord(G, c.g, c.r, c.b, c.kvh, sub);
+  group_coord<kBal>(G, c.g, c.r, c.b, c.kvh, sub);
   const int w = sub * G.Gs + (n % G.Gs);
   c.hq = c.kvh * G.gqa + w / G.q_blocks;
   c.qp = w % G.q_blocks;
-  c.n_steps = steps_of_shard(G, c.r);
+  c.n_steps = steps_of_shard<kBal>(G, c.r);
   return c;
 }
 
-// KV tiles an item consumes at ring step t: under the causal mask the local
-// chunk stops at the diagonal of the item's last row (tiles 0 .. (qp+1)*item_qt - 1).
+// KV tiles an item consumes at ring step t, always a prefix 0 .. n-1 of the chunk's tiles:
+// under the causal mask the local chunk stops at the diagonal of the item's last row
+// ((qp+1)*item_qt tiles); over balanced shards a later step gives the first half of the
+// chunk (chunk below the shard), or all / none of it (chunk above: second / first half items).
+PSR_HD bool second_half(const Geometry& G, const ItemCoord& c) { return 2 * c.qp >= G.q_blocks; }
+
+template <int kBal = -1>
 PSR_HD int tiles_at_step(const Geometry& G, const ItemCoord& c, int t) {
-  return (G.causal && t == 0) ? (c.qp + 1) * G.item_qt : G.kv_tiles;
+  if (!G.causal) return G.kv_tiles;
+  if (t == 0) return (c.qp + 1) * G.item_qt;
+  if (!is_balanced<kBal>(G)) return G.kv_tiles;
+  if (t <= c.r) return G.kv_tiles / 2;
+  return second_half(G, c) ? G.kv_tiles : 0;
 }
 
+template <int kBal = -1>
 PSR_HD long long item_tiles(const Geometry& G, const ItemCoord& c) {
-  return G.causal ? (long long)(c.qp + 1) * G.item_qt + (long long)c.r * G.kv_tiles : (long long)G.P * G.kv_tiles;
+  if (!G.causal) return (long long)G.P * G.kv_tiles;
+  const long long diag = (long long)(c.qp + 1) * G.item_qt;
+  if (!is_balanced<kBal>(G)) return diag + (long long)c.r * G.kv_tiles;
+  return diag + (long long)c.r * (G.kv_tiles / 2) + (second_half(G, c) ? (long long)(G.P - 1 - c.r) * G.kv_tiles : 0);
 }
 
 PSR_HD long long total_tiles(const Geometry& G) {
   // per (b, hq): sum over shards and items
   long long per_bh = 0;
-  if (G.causal) {
-    const long long nb = G.q_blocks;
-    for (int r = 0; r < G.P; ++r) per_bh += (long long)G.item_qt * nb * (nb + 1) / 2 + nb * r * G.kv_tiles;
+  const long long nb = G.q_blocks;
+  if (!G.causal) {
+    per_bh = (long long)G.P * nb * G.P * G.kv_tiles;
   } else {
-    per_bh = (long long)G.P * G.q_blocks * G.P * G.kv_tiles;
+    for (int r = 0; r < G.P; ++r) {
+      per_bh += (long long)G.item_qt * nb * (nb + 1) / 2;
+      if (G.balanced)
+        per_bh += nb * r * (G.kv_tiles / 2) + (nb / 2) * (G.P - 1 - r) * G.kv_tiles;
+      else
+        per_bh += nb * r * G.kv_tiles;
+    }
   }
   return per_bh * G.B * G.Hq;
+}
+
+// Tiles of the chunk that staging copies for shard r's step t >= 1: the most any of the
+// group's items consumes (over balanced shards, only the first half of a chunk below r).
+template <int kBal = -1>
+PSR_HD int stage_tiles(const Geometry& G, int r, int t) {
+  return (is_balanced<kBal>(G) && t <= r) ? G.kv_tiles / 2 : G.kv_tiles;
+}
+// (no division: the producer inlines this into its slot-release path, and an integer division
+// there slowed the compute CTAs by ~15 % on GB300)
+template <int kBal = -1>
+PSR_HD int stage_pieces(const Geometry& G, int r, int t) {
+  return (is_balanced<kBal>(G) && t <= r) ? G.half_pieces : G.n_pieces;
 }
 
 // Staging tasks: every (group, step >= 1).  Steps 1..kRingSlots land in fresh slots
@@ -195,6 +258,19 @@ PSR_HD long long dynamic_staging_tasks(const Geometry& G) {
     int s = steps_of_shard(G, shard_of_rank(G, rr));
     n += s > kRingSlots + 1 ? s - (kRingSlots + 1) : 0;
   }
+  return n * G.B * G.Hkv * G.n_sub;
+}
+// The same two counts in staging pieces (the units the lists hand out).
+PSR_HD long long total_staging_pieces(const Geometry& G) {
+  long long n = 0;
+  for (int r = 0; r < G.P; ++r)
+    for (int t = 1; t < steps_of_shard(G, r); ++t) n += stage_pieces(G, r, t);
+  return n * G.B * G.Hkv * G.n_sub;
+}
+PSR_HD long long dynamic_staging_pieces(const Geometry& G) {
+  long long n = 0;
+  for (int r = 0; r < G.P; ++r)
+    for (int t = kRingSlots + 1; t < steps_of_shard(G, r); ++t) n += stage_pieces(G, r, t);
   return n * G.B * G.Hkv * G.n_sub;
 }
 

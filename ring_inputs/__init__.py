@@ -256,13 +256,17 @@ def generate(w: Workload, q_addr: int | None = None, k_addr: int | None = None, 
 def sample_rows(w: Workload, n_random: int = 4096) -> np.ndarray:
     """Fixed row sample: flat row ids ((b*Hq + hq)*S + i), sorted and unique.
 
-    For every (b, hq): rows 0, 1, 127, 128, each shard's first and last row and
-    S-1; then uniformly drawn rows (seeded) until at least `n_random` rows in total.
+    For every (b, hq): rows 0, 1, 127, 128, each shard's first and last row (and, over
+    load-balanced shards, the two rows at its half boundary) and S-1; then uniformly
+    drawn rows (seeded) until at least `n_random` rows in total.
     """
     base = {0, 1, 127, 128, w.S - 1}
     for r in range(w.P):
         base.add(r * w.L)
         base.add((r + 1) * w.L - 1)
+        if w.causal == 2:  # load-balanced shards: the rows on either side of the half boundary
+            base.add(r * w.L + w.L // 2 - 1)
+            base.add(r * w.L + w.L // 2)
     base = sorted(i for i in base if 0 <= i < w.S)
     ids = []
     for bh in range(w.B * w.Hq):

@@ -2,20 +2,33 @@
 //  * every compute item's TMA coordinates (Q tiles, home K/V tiles, slot tiles)
 //    stay inside the tensor extents the launcher encodes;
 //  * every (b, hq, row) of the output is written by exactly one item;
-//  * every (query tile, key tile) pair the causal mask allows is visited once,
-//    none that it forbids entirely is visited except the per-item diagonal pair;
+//  * under a causal mask (contiguous or load-balanced shards), derived from the global
+//    positions of the rows: the KV tiles an item reads at a step are exactly those in
+//    which some key is visible to some row of the item; at a step t > 0 every tile read
+//    is visible in full to every row of the item (the kernel masks step 0 only), and at
+//    step 0 positions rise with the local index (the kernel masks by local index);
+//  * staging copies, per (group, step), exactly the tiles the group's items read;
 //  * flag / consumed indices stay below n_groups * P and the dynamic queue
 //    receives exactly dynamic_staging_tasks() pushes;
-//  * total_tiles() and total_staging_tasks() agree with direct enumeration.
+//  * total_tiles(), total_staging_tasks() and the piece counts agree with direct enumeration.
 // Usage: schedule_check B Hq Hkv S P d causal max_group [cg]   -> prints "OK ..." or "FAIL ..."
-// (cg: CTAs per compute unit, 1 or 2; default 1)
+// (causal: 0, 1, or 2 = load-balanced shards; cg: CTAs per compute unit, 1 or 2; default 1)
 #include <cstdio>
+#include <algorithm>
 #include <cstdlib>
 #include <vector>
 
 #include "../persistent_sm_ring_gb300/csrc/psr_schedule.h"
 
 using namespace psr;
+
+// Global position of local row i of shard r: contiguous shards, or load-balanced shards
+// (local rows [0, L/2) are half-chunk r, rows [L/2, L) half-chunk 2P-1-r).
+static long long pos_of(const Geometry& G, int r, long long i) {
+  if (!G.balanced) return (long long)r * G.L + i;
+  const long long h = G.L / 2;
+  return i < h ? (long long)r * h + i : (long long)(2 * G.P - 1 - r) * h + (i - h);
+}
 
 #define CHECK(c, ...)                 \
   do {                                \
@@ -41,6 +54,15 @@ int main(int argc, char** argv) {
   const long long rows_slot = (long long)kRingSlots * G.n_groups * G.L;
   std::vector<unsigned char> covered((size_t)rows_q / kTileRows, 0);
   std::vector<int> consumers((size_t)G.n_groups * G.P, 0);
+  std::vector<int> max_read((size_t)G.n_groups * G.P, 0);  // most tiles any item of g reads at t
+  if (G.causal) {
+    // every 128-row tile covers 128 consecutive positions, and inside a shard positions rise
+    for (int r = 0; r < G.P; ++r)
+      for (long long i = 0; i + 1 < G.L; ++i) {
+        CHECK(pos_of(G, r, i + 1) > pos_of(G, r, i), "positions fall inside shard %d", r);
+        if ((i + 1) % kTileRows != 0) CHECK(pos_of(G, r, i + 1) == pos_of(G, r, i) + 1, "tile not contiguous");
+      }
+  }
   long long tiles = 0;
   for (int n = 0; n < G.n_items; ++n) {
     ItemCoord c = item_coord(G, n);
@@ -59,9 +81,28 @@ int main(int argc, char** argv) {
     long long it_tiles = 0;
     for (int t = 0; t < c.n_steps; ++t) {
       const int j = ((c.r - t) % G.P + G.P) % G.P;
-      if (G.causal) CHECK(j <= c.r, "causal chunk above the diagonal (item %d step %d)", n, t);
+      if (G.causal && !G.balanced) CHECK(j <= c.r, "causal chunk above the diagonal (item %d step %d)", n, t);
       const int n_kt = tiles_at_step(G, c, t);
-      CHECK(n_kt >= 1 && n_kt <= G.kv_tiles, "tiles at step");
+      CHECK(n_kt >= (t == 0 ? 1 : 0) && n_kt <= G.kv_tiles, "tiles at step");
+      if (G.causal) {
+        // the tiles with a key visible to some row of the item are exactly 0 .. n_kt-1
+        const long long q_lo = pos_of(G, c.r, (long long)c.qp * G.item_rows);
+        long long q_hi = q_lo;
+        for (int i = 0; i < G.item_qt; ++i)
+          q_hi = std::max(q_hi, pos_of(G, c.r, (long long)c.qp * G.item_rows + i * kTileRows + kTileRows - 1));
+        long long q_min = q_lo;
+        for (int i = 0; i < G.item_qt; ++i)
+          q_min = std::min(q_min, pos_of(G, c.r, (long long)c.qp * G.item_rows + i * kTileRows));
+        for (int kt = 0; kt < G.kv_tiles; ++kt) {
+          const long long k_lo = pos_of(G, j, (long long)kt * kTileRows);
+          const long long k_hi = k_lo + kTileRows - 1;
+          const bool any_visible = k_lo <= q_hi;
+          CHECK(any_visible == (kt < n_kt), "item %d step %d tile %d: visible %d but read %d", n, t, kt,
+                (int)any_visible, (int)(kt < n_kt));
+          if (t > 0 && kt < n_kt) CHECK(k_hi <= q_min, "item %d step %d tile %d partly masked off step 0", n, t, kt);
+        }
+      }
+      max_read[(size_t)c.g * G.P + t] = std::max(max_read[(size_t)c.g * G.P + t], n_kt);
       for (int kt = 0; kt < n_kt; ++kt) {
         if (t == 0) {
           const long long r0 = (long long)(c.b * G.Hkv + c.kvh) * G.S + (long long)j * G.L + (long long)kt * kTileRows;
@@ -87,7 +128,7 @@ int main(int argc, char** argv) {
   }
   for (size_t i = 0; i < covered.size(); ++i) CHECK(covered[i] == 1, "q tile %zu never written", i);
   CHECK(tiles == total_tiles(G), "total_tiles %lld vs %lld", total_tiles(G), tiles);
-  long long stage = 0, dyn = 0;
+  long long stage = 0, dyn = 0, pieces = 0, dyn_pieces = 0;
   for (int g = 0; g < G.n_groups; ++g) {
     const int ns = group_steps(G, g);
     for (int t = 1; t < ns; ++t) {
@@ -95,6 +136,14 @@ int main(int argc, char** argv) {
             consumers[(size_t)g * G.P + t]);
       ++stage;
       if (t > kRingSlots) ++dyn;
+      int r_, b_, kvh_, sub_;
+      group_coord(G, g, r_, b_, kvh_, sub_);
+      CHECK(stage_tiles(G, r_, t) == max_read[(size_t)g * G.P + t], "group %d step %d stages %d tiles, items read %d",
+            g, t, stage_tiles(G, r_, t), max_read[(size_t)g * G.P + t]);
+      const int np = stage_pieces(G, r_, t);
+      CHECK(np >= 1 && np <= G.n_pieces && (np - 1) * G.piece_tiles < stage_tiles(G, r_, t), "pieces of a step");
+      pieces += np;
+      if (t > kRingSlots) dyn_pieces += np;
       // staging source: chunk j of (b, kvh), L rows; destination slot slot_of(t) of g
       int r, b, kvh, sub;
       group_coord(G, g, r, b, kvh, sub);
@@ -107,6 +156,9 @@ int main(int argc, char** argv) {
   }
   CHECK(stage == total_staging_tasks(G), "staging tasks %lld vs %lld", stage, total_staging_tasks(G));
   CHECK(dyn == dynamic_staging_tasks(G), "dynamic tasks %lld vs %lld", dyn, dynamic_staging_tasks(G));
+  CHECK(pieces == total_staging_pieces(G), "staging pieces %lld vs %lld", pieces, total_staging_pieces(G));
+  CHECK(dyn_pieces == dynamic_staging_pieces(G), "dynamic pieces %lld vs %lld", dyn_pieces,
+        dynamic_staging_pieces(G));
   std::printf("OK items=%d groups=%d Gs=%d n_sub=%d tiles=%lld staging=%lld dynamic=%lld\n", G.n_items, G.n_groups,
               G.Gs, G.n_sub, tiles, stage, dyn);
   return 0;

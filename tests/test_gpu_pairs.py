@@ -33,6 +33,7 @@ cases = [
                                 qmul=2.0, kmul=2.0),
     ri.WORKLOADS["small"].with_(name="pair_p1_c", S=1024, P=1, d=128, causal=True, seed=19),
     ri.WORKLOADS["small"].with_(name="pair_p4_c", Hq=3, Hkv=3, S=6144, P=4, d=128, causal=True, seed=20),
+    ri.WORKLOADS["small"].with_(name="pair_p4_cb", Hq=2, Hkv=2, S=4096, P=4, d=128, causal=2, seed=22),
 ]
 out = []
 for w in cases:

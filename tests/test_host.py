@@ -112,6 +112,13 @@ SHAPES = [
     (3, 6, 2, 768, 3, 64, 1),
     (2, 4, 1, 2560, 5, 128, 0),
     (1, 1, 1, 256, 1, 64, 1),
+    # causal over load-balanced shards
+    (1, 2, 2, 2048, 4, 64, 2),
+    (1, 32, 32, 32768, 16, 128, 2),
+    (2, 32, 8, 65536, 16, 128, 2),
+    (1, 8, 8, 131072, 32, 128, 2),
+    (3, 6, 2, 1536, 3, 64, 2),
+    (1, 1, 1, 512, 1, 64, 2),
 ] + [(1, 16, 16, 16384, P, d, 0) for d in (64, 128) for P in (2, 4, 8, 16, 32, 64)]
 
 
@@ -122,7 +129,8 @@ def test_schedule_bounds_and_coverage(schedule_check, shape):
 
 
 # CTA-pair items (512 query rows): shards whose length is a multiple of 512
-PAIR_SHAPES = [s for s in SHAPES if (s[3] // s[4]) % 512 == 0] + [(1, 2, 2, 2048, 2, 128, 1), (2, 8, 2, 3072, 3, 128, 1)]
+PAIR_SHAPES = [s for s in SHAPES if (s[3] // s[4]) % (1024 if s[6] == 2 else 512) == 0] + [
+    (1, 2, 2, 2048, 2, 128, 1), (2, 8, 2, 3072, 3, 128, 1), (1, 2, 2, 2048, 2, 128, 2)]
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES)
@@ -142,6 +150,22 @@ def test_schedule_splits_large_groups(schedule_check):
     out = subprocess.run([schedule_check, "2", "32", "8", "65536", "16", "128", "1", "20"], capture_output=True,
                          text=True).stdout
     assert out.startswith("OK") and "Gs=16 n_sub=4" in out
+
+
+def test_schedule_balanced_rejects_half_items(schedule_check):
+    # L = 256: each half of a balanced shard would hold half an item
+    out = subprocess.run([schedule_check, "1", "2", "2", "1024", "4", "64", "2", "100"], capture_output=True,
+                         text=True).stdout
+    assert out.startswith("REJECT")
+
+
+def test_library_balanced_rejects_half_items(psr):
+    # L = 256: a half of a balanced shard cannot hold a whole 256-row item
+    with pytest.raises(psr.PsrError):
+        psr.workspace_bytes(psr.make_shape(1, 2, 2, 1024, 4, 64, psr.CAUSAL_BALANCED))
+    assert psr.workspace_bytes(psr.make_shape(1, 2, 2, 2048, 4, 64, psr.CAUSAL_BALANCED)) > 0
+    with pytest.raises(psr.PsrError):
+        psr.workspace_bytes(psr.make_shape(1, 2, 2, 2048, 4, 64, 3))
 
 
 def test_schedule_rejects_unsupported(schedule_check):
