@@ -3,6 +3,7 @@ validation, schedule geometry and the partition controller rule."""
 import ctypes
 import os
 import re
+import shutil
 import subprocess
 import tempfile
 
@@ -150,6 +151,35 @@ def test_schedule_splits_large_groups(schedule_check):
     out = subprocess.run([schedule_check, "2", "32", "8", "65536", "16", "128", "1", "20"], capture_output=True,
                          text=True).stdout
     assert out.startswith("OK") and "Gs=16 n_sub=4" in out
+
+
+SCHEDULE_MUTANTS = {
+    # a chunk below the shard read in full, or its first half missed by the items
+    "below_full": ("if (t <= c.r) return G.kv_tiles / 2;", "if (t < c.r) return G.kv_tiles / 2;"),
+    # a chunk above the shard read only half by the second-half items
+    "above_half": ("return second_half(G, c) ? G.kv_tiles : 0;", "return second_half(G, c) ? G.kv_tiles / 2 : 0;"),
+    # staging copies half a chunk where the items read all of it
+    "stage_half": ("return (is_balanced<kBal>(G) && t <= r) ? G.kv_tiles / 2 : G.kv_tiles;",
+                   "return (is_balanced<kBal>(G) && t < r) ? G.kv_tiles / 2 : G.kv_tiles;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCHEDULE_MUTANTS))
+def test_schedule_check_catches_planted_mistakes(name):
+    old, new = SCHEDULE_MUTANTS[name]
+    d = tempfile.mkdtemp(prefix="psr_sched_mut_")
+    src = open(os.path.join(ROOT, "persistent_sm_ring_gb300", "csrc", "psr_schedule.h")).read()
+    assert old in src
+    os.makedirs(os.path.join(d, "persistent_sm_ring_gb300", "csrc"))
+    os.makedirs(os.path.join(d, "tests"))
+    with open(os.path.join(d, "persistent_sm_ring_gb300", "csrc", "psr_schedule.h"), "w") as f:
+        f.write(src.replace(old, new, 1))
+    shutil.copy(os.path.join(ROOT, "tests", "schedule_check.cpp"), os.path.join(d, "tests"))
+    exe = os.path.join(d, "sc")
+    subprocess.check_call(["g++", "-O2", "-std=c++17", os.path.join(d, "tests", "schedule_check.cpp"), "-o", exe])
+    out = subprocess.run([exe, "1", "2", "2", "2048", "4", "64", "2", "113"], capture_output=True, text=True).stdout
+    shutil.rmtree(d, ignore_errors=True)
+    assert out.startswith("FAIL"), out
 
 
 def test_schedule_balanced_rejects_half_items(schedule_check):
