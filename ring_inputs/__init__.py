@@ -360,3 +360,82 @@ def ag_sample_rows(w: AgGemmWorkload, n_random: int = 1024) -> np.ndarray:
         ids.add(splitmix64(seed, n) % w.M)
         n += 1
     return np.array(sorted(ids), dtype=np.int64)
+
+
+# ----------------------------------------------------------------------------------------------
+# GEMM + ReduceScatter (tensor-parallel row-parallel linear layer) workloads
+# ----------------------------------------------------------------------------------------------
+# P ranks; rank r holds its K-shard A_r ([M][Ks]) of the activations and W_r ([N][Ks], K-major)
+# of the weights; the output rows [q*M/P, (q+1)*M/P) of sum_r A_r @ W_r^T belong to rank q.
+
+@dataclasses.dataclass(frozen=True)
+class GemmRsWorkload:
+    name: str
+    M: int      # output rows (tokens)
+    N: int      # output columns (hidden size)
+    Ks: int     # contraction per rank (K / P)
+    P: int      # ranks
+    seed: int
+    amul: float = 1.0
+    wmul: float = 1.0 / 64.0   # power of two: exact in bf16; keeps |out| near 1 for K ~ 4096
+
+    @property
+    def Mq(self) -> int:
+        return self.M // self.P
+
+    @property
+    def n_a(self) -> int:
+        return self.P * self.M * self.Ks
+
+    @property
+    def n_w(self) -> int:
+        return self.P * self.N * self.Ks
+
+    def flops(self) -> float:
+        """2*M*N*Ks per rank, times P."""
+        return 2.0 * self.M * self.N * self.Ks * self.P
+
+    def reduce_bytes(self) -> int:
+        """fp32 partial bytes the emulated reduce-scatter reads: every rank's [M][N] partial."""
+        return self.P * self.M * self.N * 4
+
+    def with_(self, **kw) -> "GemmRsWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+RS_WORKLOADS = {
+    # small: every output element is checked against the oracle
+    "rs_small": GemmRsWorkload("rs_small", 1024, 512, 256, 4, seed=800),
+    # a tensor-parallel MLP down-projection: 8192 tokens, hidden 8192, K = 28672 over 8 ranks
+    "rs_m8k_n8k_k28k_p8": GemmRsWorkload("rs_m8k_n8k_k28k_p8", 8192, 8192, 3584, 8, seed=801),
+}
+
+
+def generate_gemm_rs(w: GemmRsWorkload, a_addr: int | None = None, w_addr: int | None = None):
+    """A ([P][M][Ks]) then W ([P][N][Ks]) as uint16 bf16 bit patterns, from the same stream as
+    the other inputs (A first).  With addresses, values are written there and None returned."""
+    out = []
+    first = 0
+    for count, mult, addr, shape in ((w.n_a, w.amul, a_addr, (w.P, w.M, w.Ks)),
+                                     (w.n_w, w.wmul, w_addr, (w.P, w.N, w.Ks))):
+        if addr is None:
+            out.append(normal_bf16(w.seed, first, count, mult).reshape(shape))
+        else:
+            normal_bf16_into(addr, w.seed, first, count, mult)
+            out.append(None)
+        first += count
+    return tuple(out)
+
+
+def rs_sample_rows(w: GemmRsWorkload, n_random: int = 1024) -> np.ndarray:
+    """Fixed sample of output rows: each owner's first, second and last rows, then seeded
+    uniform rows up to `n_random`."""
+    ids = set()
+    for q in range(w.P):
+        ids.update((q * w.Mq, q * w.Mq + 1, (q + 1) * w.Mq - 1))
+    seed = (w.seed * 7919 + 29) & (2**64 - 1)
+    n = 0
+    while len(ids) < n_random:
+        ids.add(splitmix64(seed, n) % w.M)
+        n += 1
+    return np.array(sorted(ids), dtype=np.int64)
