@@ -7,6 +7,7 @@ non-causal pass followed by one causal pass, each a single persistent launch.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --sweep [d]      # partition-stress sweep: static 2..64 staging CTAs vs adaptive
   python bench.py --ag-gemm        # AllGather+GEMM, M8192 K8192 N28672 over 8 ranks
+  python bench.py --gemm-rs        # GEMM+ReduceScatter, M8192 N8192 K28672 over 8 ranks
 
 value: algorithmic TFLOP/s over the timed steps (4*d flops per unmasked
 (query, key) pair), inputs resident in HBM (805 MB per pass, larger than L2).
@@ -647,6 +648,129 @@ def run_ag(args):
     }), flush=True)
 
 
+# ------------------------------------------------------------------------------------------------
+# GEMM + ReduceScatter (compute feeds the reduce-scatter; a separate line, not the headline)
+# ------------------------------------------------------------------------------------------------
+
+RS_METRIC = "gemm+reducescatter TFLOP/s (bf16, 1 GB300, P ranks emulated as shards)"
+
+
+def rs_cpu_baseline(w, a, ww, budget_s):
+    """The fp64 oracle on seeded sampled output rows (every rank's partial of each row)."""
+    import numpy as np
+
+    from oracle import gemm_rs as og
+    rng = np.random.default_rng(w.seed + 99)
+    n = 16
+    while True:
+        rows = np.sort(rng.choice(w.M, size=n, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        og.for_workload(w, a, ww, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s * 0.5 or n >= w.M // 4:
+            break
+        n = int(min(w.M // 4, max(2 * n, n * budget_s * 0.7 / max(dt, 1e-3))))
+    flops = 2.0 * len(rows) * w.N * w.Ks * w.P
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(rows)} seeded output rows, all {w.P} ranks' partials (fp64 numpy), {dt:.1f} s"}
+
+
+def run_rs(args):
+    import numpy as np
+    import torch
+
+    import persistent_sm_ring_gb300 as psr
+    import ring_inputs as ri
+    psr.build()
+    torch.cuda.set_device(0)
+    w = ri.RS_WORKLOADS["rs_m8k_n8k_k28k_p8"]
+    a_h, w_h = ri.generate_gemm_rs(w)
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+    a_p, w_p = pin(a_h), pin(w_h)
+    a = a_p.cuda().view(torch.bfloat16)
+    ww = w_p.cuda().view(torch.bfloat16)
+    out, ws = psr.gemm_rs(a, ww)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    def timed(fn, reps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+    def ours(part):
+        return lambda: psr.gemm_rs(a, ww, partition=part, workspace=ws, out=out, stream=stream)
+
+    adaptive = psr.make_partition(psr.ADAPTIVE)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    ts = timed(ours(adaptive), args.steps)
+    clk = clocks.stop()
+    st = psr.get_stats(ws)
+    if st["status"] != 0:
+        raise RuntimeError(f"device status {st['status']} site {st['error_site']}")
+    ms = statistics.mean(ts)
+    value = w.flops() / (ms / 1e3) / 1e12
+
+    statics = {}
+    for n in (4, 8, 12, 16, 24):
+        t = statistics.median(timed(ours(psr.make_partition(psr.STATIC, n_staging=n)), 5))
+        statics[str(n)] = round(w.flops() / (t / 1e3) / 1e12, 1)
+    # context: cuBLAS on the same P partial products, then the reduction by torch (no overlap)
+    wt = ww.transpose(1, 2)
+    t_lib = statistics.median(timed(lambda: torch.bmm(a, wt).float().sum(0), 5))
+
+    # e2e: pinned host A, W in; the reduced output out; through the public binding
+    o_h = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
+    e2e_steps = 3
+
+    def e2e_step():
+        a.view(torch.int16).copy_(a_p, non_blocking=True)
+        ww.view(torch.int16).copy_(w_p, non_blocking=True)
+        psr.gemm_rs(a, ww, partition=adaptive, workspace=ws, out=out, stream=stream)
+        o_h.copy_(out.view(torch.int16), non_blocking=True)
+        torch.cuda.synchronize()
+
+    e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    cpu = None if args.no_cpu_baseline else rs_cpu_baseline(w, a_h, w_h, args.cpu_budget)
+    print(json.dumps({
+        "metric": RS_METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"GEMM+ReduceScatter M{w.M} N{w.N} K{w.Ks * w.P} over P{w.P} "
+                               f"(out = sum_r A_r @ W_r^T, row block q to rank q)",
+                   "M": w.M, "N": w.N, "Ks": w.Ks, "P": w.P, "partition": "adaptive",
+                   "l2": f"inputs larger than L2 (A {w.n_a * 2 / 1e6:.0f} MB, W {w.n_w * 2 / 1e6:.0f} MB)"},
+        "roofline": {"bound": "tensor", "achieved": round(value, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(value / peak, 4), "traffic": None,
+                     "peak_source": f"{peaks.get('source')} bf16_tflops (burst)"},
+        "static_tflops": statics, "best_static_tflops": max(statics.values()),
+        "adaptive_over_best_static_time": round(max(statics.values()) / value, 4),
+        "n_s": [st["n_s_initial"], st["n_s_min"], st["n_s_max"], st["n_s_final"]],
+        "reduce_GBps": round(st["staging_bytes"] / (ms / 1e3) / 1e9, 1),
+        "cublas_bmm_then_sum_tflops": round(w.flops() / (t_lib / 1e3) / 1e12, 1),
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(w.flops() / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": (w.n_a + w.n_w) * 2, "d2h_bytes_per_step": o_h.numel() * 2},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -655,6 +779,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", type=int, nargs="?", const=0, default=None)
     ap.add_argument("--ag-gemm", action="store_true", help="the AllGather+GEMM path instead of attention")
+    ap.add_argument("--gemm-rs", action="store_true", help="the GEMM+ReduceScatter path instead of attention")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=96)
@@ -665,6 +790,8 @@ def main():
         run_sweep(args)
     elif args.ag_gemm:
         run_ag(args)
+    elif args.gemm_rs:
+        run_rs(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -229,6 +229,49 @@ PSR_API size_t psr_ag_gemm_workspace_bytes(const psr_ag_shape* shape);
 PSR_API int psr_ag_gemm(const psr_ag_shape* shape, const void* a, const void* w, void* c, void* workspace,
                         size_t workspace_bytes, const psr_partition* part, void* stream);
 
+/* ---- GEMM + ReduceScatter ---------------------------------------------------------------------
+ * The mKernel pages' GEMM+ReduceScatter kernel (dataforcee and chathome "five
+ * fused kernels" tables, GEMM + ReduceScatter row; pwwt.cn analysis §2.6
+ * Table 3: tensor parallel, compute feeds communication): rank r holds its
+ * K-shard A_r of the activations and W_r of the weights and computes the
+ * partial product A_r @ W_r^T; the ranks reduce-scatter the partials, so rank q
+ * receives rows [q*M/P, (q+1)*M/P) of
+ *     out = sum_r A_r @ W_r^T      (fp32 partials summed in rank order, bf16 result, RNE),
+ * each output tile being reduced and forwarded as soon as its partials exist.
+ * On one GPU the P ranks are emulated in HBM: compute CTAs each produce one
+ * 256 x 256 fp32 partial tile of one rank on tcgen05 into the workspace, and
+ * the completion of an output tile's P partials enqueues it; reduce CTAs (the
+ * communication role) stream the P partials through shared memory with TMA
+ * bulk copies and write the owner's rows.  The same controller splits the CTAs
+ * between the roles; as compute feeds the reductions, the adaptive launch
+ * starts with no reduce CTA (part->n_staging > 0 overrides). */
+typedef struct {
+  int M;   /* output rows (tokens); M/P must be a multiple of 256 */
+  int N;   /* output columns; a multiple of 256 */
+  int Ks;  /* contraction per rank (K/P); a multiple of 64 */
+  int P;   /* ranks, 1..64 */
+} psr_rs_shape;
+
+/* Bytes of device workspace psr_gemm_rs needs: the control block and
+ * trajectory log (the same layout as the other entries, so psr_get_stats and
+ * psr_get_trajectory read it), per-tile arrival counters and the ready queue,
+ * and the fp32 partial tiles ([P][M][N] fp32).  Returns 0 for an invalid shape. */
+PSR_API size_t psr_gemm_rs_workspace_bytes(const psr_rs_shape* shape);
+
+/* GEMM + ReduceScatter.
+ *   a:   device, bf16, [P][M][Ks] contiguous (rank r's activations, K-major)  (read)
+ *   w:   device, bf16, [P][N][Ks] contiguous (rank r's weights, K-major)      (read)
+ *   out: device, bf16, [M][N] contiguous (rows q*M/P .. belong to rank q)     (written)
+ *   workspace: device, >= psr_gemm_rs_workspace_bytes(shape), 256-byte aligned, caller-owned.
+ *   part: partition policy (NULL = adaptive; static needs n_staging >= 1 reduce CTAs).
+ *   stream: a cudaStream_t (NULL = default).
+ * Asynchronous (one counter reset and one persistent launch on `stream`); a
+ * device timeout is reported by psr_get_stats (staging_tasks counts the tile
+ * reductions, staging_bytes the partial bytes they read).  PSR_ERR_UNSUPPORTED
+ * for shapes outside the constraints above or a device other than sm_103. */
+PSR_API int psr_gemm_rs(const psr_rs_shape* shape, const void* a, const void* w, void* out, void* workspace,
+                        size_t workspace_bytes, const psr_partition* part, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

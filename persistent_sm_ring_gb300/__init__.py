@@ -15,8 +15,8 @@ import threading
 
 from .build import LIB, LIB_PAIRS, LIB_TRACE, build as _build
 
-__all__ = ["build", "load", "Shape", "AgShape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host",
-           "workspace_bytes", "ag_gemm", "ag_gemm_workspace_bytes",
+__all__ = ["build", "load", "Shape", "AgShape", "RsShape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host",
+           "workspace_bytes", "ag_gemm", "ag_gemm_workspace_bytes", "gemm_rs", "gemm_rs_workspace_bytes",
            "get_stats", "get_trajectory", "controller_target", "num_ctas", "status_string", "PsrError",
            "STATIC", "ADAPTIVE", "FAULT_NONE", "FAULT_DROP_FIRST_FLAG", "FAULT_SLOW_STAGING", "CAUSAL",
            "CAUSAL_BALANCED"]
@@ -28,7 +28,8 @@ CAUSAL, CAUSAL_BALANCED = 1, 2
 
 EXPORTED = ("psr_workspace_bytes", "psr_ring_attn_fwd", "psr_ring_attn_fwd_host", "psr_get_stats",
             "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas",
-            "psr_ring_attn_fwd_noalloc", "psr_ag_gemm_workspace_bytes", "psr_ag_gemm")
+            "psr_ring_attn_fwd_noalloc", "psr_ag_gemm_workspace_bytes", "psr_ag_gemm", "psr_gemm_rs_workspace_bytes",
+            "psr_gemm_rs")
 
 
 class Shape(ctypes.Structure):
@@ -38,6 +39,10 @@ class Shape(ctypes.Structure):
 
 class AgShape(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int), ("K", ctypes.c_int), ("Ns", ctypes.c_int), ("P", ctypes.c_int)]
+
+
+class RsShape(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int), ("N", ctypes.c_int), ("Ks", ctypes.c_int), ("P", ctypes.c_int)]
 
 
 class Partition(ctypes.Structure):
@@ -112,6 +117,11 @@ def load(trace: bool = False, variant: str = "") -> ctypes.CDLL:
         lib.psr_ag_gemm_workspace_bytes.restype = sz
         lib.psr_ag_gemm.argtypes = [P_ag, vp, vp, vp, vp, sz, P_part, vp]
         lib.psr_ag_gemm.restype = ctypes.c_int
+        P_rs = ctypes.POINTER(RsShape)
+        lib.psr_gemm_rs_workspace_bytes.argtypes = [P_rs]
+        lib.psr_gemm_rs_workspace_bytes.restype = sz
+        lib.psr_gemm_rs.argtypes = [P_rs, vp, vp, vp, vp, sz, P_part, vp]
+        lib.psr_gemm_rs.restype = ctypes.c_int
         lib.psr_num_ctas.argtypes = []
         lib.psr_num_ctas.restype = ctypes.c_int
         _lib = lib
@@ -261,6 +271,40 @@ def ag_gemm(a, w, *, P, partition=None, workspace=None, out=None, stream=None):
                          workspace.numel(), ctypes.byref(part), _stream_handle(stream))
     if rc != OK:
         raise PsrError(rc, "psr_ag_gemm")
+    return out, workspace
+
+
+def gemm_rs_workspace_bytes(M, N, Ks, P) -> int:
+    n = load().psr_gemm_rs_workspace_bytes(ctypes.byref(RsShape(int(M), int(N), int(Ks), int(P))))
+    if n == 0:
+        raise PsrError(ERR_UNSUPPORTED, "psr_gemm_rs_workspace_bytes")
+    return int(n)
+
+
+def gemm_rs(a, w, *, partition=None, workspace=None, out=None, stream=None):
+    """GEMM + ReduceScatter through the C ABI: a [P][M][Ks] bf16 (rank r's activations),
+    w [P][N][Ks] bf16 (rank r's weights) -> out [M][N] bf16 = sum_r a[r] @ w[r]^T, rows
+    q*M/P .. belonging to rank q.  Returns (out, workspace)."""
+    import torch
+    lib = load()
+    P, M, Ks = a.shape
+    N = w.shape[1]
+    shape = RsShape(int(M), int(N), int(Ks), int(P))
+    need = gemm_rs_workspace_bytes(M, N, Ks, P)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    for t in (a, w, out):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("gemm_rs: a, w and out must be contiguous bf16 CUDA tensors")
+    if tuple(w.shape) != (P, N, Ks) or tuple(out.shape) != (M, N):
+        raise ValueError("gemm_rs: shapes a [P][M][Ks], w [P][N][Ks], out [M][N]")
+    part = partition if partition is not None else make_partition()
+    rc = lib.psr_gemm_rs(ctypes.byref(shape), a.data_ptr(), w.data_ptr(), out.data_ptr(), workspace.data_ptr(),
+                         workspace.numel(), ctypes.byref(part), _stream_handle(stream))
+    if rc != OK:
+        raise PsrError(rc, "psr_gemm_rs")
     return out, workspace
 
 

@@ -28,24 +28,16 @@
 #include "../../include/psr.h"
 #include "psr_control.cuh"
 #include "psr_device.cuh"
+#include "psr_gemm_tile.cuh"
 #include "psr_schedule.h"
 
 namespace psr {
 namespace ag {
 
-constexpr int kBM = 256;          // output rows per task (two 128-row A tiles)
-constexpr int kBN = 256;          // output columns per task (one W tile)
-constexpr int kBK = 64;           // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int kNStage = 3;        // stages of A0 | A1 | W
-constexpr int kATile = 128 * kBK * 2;   // 16 KiB
-constexpr int kWTile = kBN * kBK * 2;   // 32 KiB
-constexpr int kStageBytes = 2 * kATile + kWTile;
-constexpr int kSmem = 1024 + kNStage * kStageBytes;
+using namespace gemm;  // the 256 x 256 tile: stages, MMA issue, accumulator read-back
 constexpr int kCopyUnit = 32768;  // staging copy unit
-constexpr int kNCopyBuf = kNStage * kStageBytes / kCopyUnit;
-constexpr int kWarps = 12, kThreads = kWarps * 32;
+constexpr int kNCopyBuf = kStageArea / kCopyUnit;
 constexpr int kPieceMinBytes = 512 * 1024;
-static_assert(kSmem <= 232448 - 512, "shared memory");
 static_assert(kNCopyBuf <= 16, "staging barriers");
 
 enum : uint32_t { SITE_FLAG = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_ACC = 4, SITE_STAGE_LOAD = 8, SITE_IDLE = 11 };
@@ -75,15 +67,6 @@ struct Params {
   float c_s0, c_p0;
 };
 
-struct Smem {
-  uint64_t full[kNStage], empty[kNStage];
-  uint64_t acc_full;
-  uint64_t stg[16];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int cmd, arg;
-  volatile uint32_t abort;
-};
 
 // task index -> (rank, shard, m-block, n-block); stage order jj: shard = (rank + jj) mod P
 struct Item {
@@ -199,11 +182,6 @@ __device__ void run_staging(const Params& p, Smem* sc, uint32_t smem_base, int t
 // ------------------------------------------------------------------------------------------------
 // Compute task: producer (TMA), MMA issuer (tcgen05), epilogue warpgroups
 // ------------------------------------------------------------------------------------------------
-struct Counters {
-  uint32_t fills;  // stage fills issued (producer) / consumed (issuer)
-  uint32_t items;  // compute tasks done (accumulator phase)
-};
-
 // Returns the cycles spent waiting for readiness flags.
 __device__ long long producer(const Params& p, Smem* sc, uint32_t smem_base, const Item& it, const CUtensorMap* tm_a,
                               const CUtensorMap* tm_g, const CUtensorMap* tm_w, Counters& cnt, bool& ok) {
@@ -228,62 +206,17 @@ __device__ long long producer(const Params& p, Smem* sc, uint32_t smem_base, con
     arow = it.r * g.M + it.j * g.Ms + it.mb * kBM;
   }
   const int wrow = it.r * g.Ns + it.nb * kBN;
-  const int n_k = g.K / kBK;
-  for (int ks = 0; ks < n_k && ok; ++ks) {
-    const uint32_t c = cnt.fills++;
-    const uint32_t s = c % kNStage, fill = c / kNStage;
-    if (fill > 0 && !wait_bar(&sc->empty[s], (fill - 1) & 1u, p, sc, SITE_KV_EMPTY)) { ok = false; break; }
-    const uint32_t base = smem_base + s * kStageBytes;
-    mbar_expect_tx(&sc->full[s], kStageBytes);
-    tma_load_2d(base, ma, ks * kBK, arow, &sc->full[s]);
-    tma_load_2d(base + kATile, ma, ks * kBK, arow + 128, &sc->full[s]);
-    tma_load_2d(base + 2 * kATile, tm_w, ks * kBK, wrow, &sc->full[s]);
-  }
+  if (ok && !load_tile(p, sc, smem_base, ma, arow, tm_w, wrow, g.K / kBK, cnt, SITE_KV_EMPTY)) ok = false;
   if (!ok) sc->abort = 1;
   return waited;
-}
-
-__device__ void mma_issuer(const Params& p, Smem* sc, uint32_t smem_base, Counters& cnt) {
-  const Geo& g = p.g;
-  constexpr uint32_t ID = idesc_bf16_f32(128, kBN, false);
-  constexpr uint32_t kHi = sdesc_hi_sw128(1024);
-  const int n_k = g.K / kBK;
-  for (int ks = 0; ks < n_k; ++ks) {
-    const uint32_t c = cnt.fills++;
-    const uint32_t s = c % kNStage, fill = c / kNStage;
-    if (!wait_bar(&sc->full[s], fill & 1u, p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
-    tc_fence_after();
-    const uint32_t base = smem_base + s * kStageBytes;
-    const uint32_t w_lo = sdesc_lo(base + 2 * kATile, 16);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t a_lo = sdesc_lo(base + i * kATile, 16);
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        mma_ss_w(sc->tmem_base + i * kBN, a_lo + kk * 2, kHi, w_lo + kk * 2, kHi, ID, (ks > 0 || kk > 0) ? 1u : 0u);
-    }
-    mma_commit(&sc->empty[s]);
-  }
-  mma_commit(&sc->acc_full);
 }
 
 // One warpgroup per 128-row half of the tile: accumulator -> bf16 -> C_r.
 __device__ void epilogue(const Params& p, Smem* sc, const Item& it, int i, const Counters& cnt, bool& ok) {
   const Geo& g = p.g;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int quarter = warp % 4;
-  const int row = quarter * 32 + lane;
-  ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full, cnt.items & 1u, p, sc, SITE_ACC));
-  if (!ok) { sc->abort = 1; return; }
-  tc_fence_after();
-  const uint32_t tacc = sc->tmem_base + ((uint32_t)(quarter * 32) << 16) + i * kBN;
-  const size_t grow = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + i * 128 + row;
-  uint16_t* crow = p.c + ((size_t)it.r * g.M + grow) * g.Ns + (size_t)it.nb * kBN;
-#pragma unroll 1
-  for (int cb = 0; cb < kBN / 64; ++cb) {
-    uint32_t v[64];
-    tmem_ld64(tacc + cb * 64, v);
-    tmem_ld_wait();
+  const size_t grow0 = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + i * 128;
+  ok = read_tile(p, sc, i, cnt, SITE_ACC, [&](int row, int cb, const uint32_t(&v)[64]) {
+    uint16_t* crow = p.c + ((size_t)it.r * g.M + grow0 + row) * g.Ns + (size_t)it.nb * kBN;
     uint4 o[8];
     uint32_t* w = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
@@ -291,7 +224,7 @@ __device__ void epilogue(const Params& p, Smem* sc, const Item& it, int i, const
     uint4* dst = reinterpret_cast<uint4*>(crow + cb * 64);
 #pragma unroll
     for (int e = 0; e < 8; ++e) dst[e] = o[e];
-  }
+  });
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -352,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         starved = producer(p, &sc, smem_base, it, &tm_a, &tm_g, &tm_w, c2, ok);
       } else if (warp == 1 && lane == 0) {
         Counters c2 = cnt;
-        mma_issuer(p, &sc, smem_base, c2);
+        mma_tile(p, &sc, smem_base, p.g.K / kBK, c2, SITE_KV_FULL);
       } else if (warp >= 4) {
         epilogue(p, &sc, it, warp < 8 ? 0 : 1, cnt, ok);
       }
@@ -382,27 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.mode == PSR_ADAPTIVE && (tick % 16u) == 0) controller_update(p);
     }
   }
-  // drain: every tcgen05 op has completed and every TMA load has landed before TMEM is released
-  if (warp == 1 && lane == 0) {
-    mma_commit(&sc.drain);
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(&sc.drain, 0)) {
-      if (globaltimer_ns() - t0 > 100000000ull) break;
-    }
-  }
-  if (threadIdx.x == 0) {
-    bulk_wait<0>();
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t s = 0; s < (uint32_t)kNStage && s < cnt.fills; ++s) {
-      const uint32_t fills = (cnt.fills - s + kNStage - 1) / kNStage;
-      while (!mbar_try_wait(&sc.full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(sc.tmem_base, 512);
+  drain_and_release(&sc, cnt);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -448,32 +361,6 @@ static Layout layout(const Geo& g) {
   l.gbuf = off; off = au(off + (size_t)g.P * g.M * g.K * 2);
   l.total = off;
   return l;
-}
-
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// [rows][K] bf16, box = 64 columns x box_rows rows, 128-byte swizzle
-static bool tmap(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace ag
@@ -557,8 +444,8 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   kp.n_s_init = n_s;
 
   CUtensorMap ma, mg, mw;
-  if (!tmap(&ma, a, g.M, g.K, 128) || !tmap(&mg, kp.gbuf, (long long)g.P * g.M, g.K, 128) ||
-      !tmap(&mw, w, (long long)g.P * g.Ns, g.K, kBN))
+  if (!tmap_kmajor(&ma, a, g.M, g.K, 128) || !tmap_kmajor(&mg, kp.gbuf, (long long)g.P * g.M, g.K, 128) ||
+      !tmap_kmajor(&mw, w, (long long)g.P * g.Ns, g.K, kBN))
     return PSR_ERR_CUDA;
 
   static std::once_flag once;
