@@ -37,7 +37,7 @@ WORKLOADS = ("h32_s32k_nc", "h32_s32k_c")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 PROFILE = os.path.join(ROOT, "profiles", "ring_attn_kernel_h32_s32k.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "persistent_sm_ring_gb300", "csrc", f)
-                  for f in ("psr_ring_attn.cu", "psr_device.cuh", "psr_schedule.h")]
+                  for f in ("psr_ring_attn.cu", "psr_device.cuh", "psr_schedule.h", "psr_control.cuh")]
 
 
 def log(*a):
