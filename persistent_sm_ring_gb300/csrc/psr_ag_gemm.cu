@@ -14,8 +14,9 @@
 //    A tiles against one 256-row W tile per 64-wide K step, on tcgen05 (M = 128, N = 256)
 //    with both accumulators in tensor memory; the rank's own shard is read in place, a
 //    peer's only after acquiring the piece flags that cover the tile's rows;
-//  * tasks run in availability order: every rank's local tiles first, then the tiles of
-//    shard r+1, r+2, ... (the order in which staging delivers them);
+//  * each rank's tasks run in availability order: its local tiles first, then the tiles of
+//    shard r+1, r+2, ... (the order in which staging delivers them); ranks run one after
+//    another, so that a rank's weight slice is read from HBM once;
 //  * the shared controller re-splits CTAs between the roles with the pages' rule.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -68,27 +69,30 @@ struct Params {
 };
 
 
-// task index -> (rank, shard, m-block, n-block); stage order jj: shard = (rank + jj) mod P
+// task index -> (rank, shard, m-block, n-block): rank by rank (rank r's weight slice stays in L2
+// across its shards), shards in availability order jj = 0, 1, .. (shard = (rank + jj) mod P,
+// the local one first), then W tile by W tile with the m-blocks that share it
 struct Item {
   int r, j, mb, nb;
 };
 __device__ __host__ inline Item item_of(const Geo& g, long long idx) {
   Item it;
-  it.nb = (int)(idx % g.n_nb);
-  idx /= g.n_nb;
   it.mb = (int)(idx % g.n_mb);
   idx /= g.n_mb;
-  it.r = (int)(idx % g.P);
-  const int jj = (int)(idx / g.P);
+  it.nb = (int)(idx % g.n_nb);
+  idx /= g.n_nb;
+  const int jj = (int)(idx % g.P);
+  it.r = (int)(idx / g.P);
   it.j = (it.r + jj) % g.P;
   return it;
 }
-// staging task index -> (rank, shard, piece), peers in the same order as the compute tasks
+// staging task index -> (rank, shard, piece), in the compute tasks' order (rank by rank, peers
+// r+1, r+2, ..)
 __device__ inline void stage_of(const Geo& g, long long idx, int& r, int& j, int& piece) {
   piece = (int)(idx % g.n_pieces);
   idx /= g.n_pieces;
-  r = (int)(idx % g.P);
-  const int jj = 1 + (int)(idx / g.P);
+  const int jj = 1 + (int)(idx % (g.P - 1));
+  r = (int)(idx / (g.P - 1));
   j = (r + jj) % g.P;
 }
 

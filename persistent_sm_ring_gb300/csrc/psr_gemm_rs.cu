@@ -16,7 +16,7 @@
 //  * reduce CTAs (the communication role) take enqueued tiles, stream the P partials through
 //    shared memory with TMA bulk copies, sum them in rank order (fixed, so the result does not
 //    depend on timing) and write the owner's bf16 rows;
-//  * compute tasks run window by window (wm x wn output tiles, every rank's partials of the
+//  * compute tasks run window by window (up to 8 x 8 output tiles, every rank's partials of the
 //    window before the next window), so reductions start one window after the launch and a
 //    window's partials are still in L2 when they are reduced;
 //  * the shared controller splits CTAs between the roles with the pages' rule.  Compute feeds
@@ -361,7 +361,7 @@ static int geometry(const psr_rs_shape* sh, Geo& g) {
   g.n_mb = g.M / kBM;
   g.n_nb = g.N / kBN;
   g.wm = largest_divisor_upto(g.n_mb, 8);
-  g.wn = largest_divisor_upto(g.n_nb, 4);
+  g.wn = largest_divisor_upto(g.n_nb, 8);
   const long long n_out = (long long)g.n_mb * g.n_nb;
   if (n_out >= (1LL << 30) || n_out * g.P >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   g.n_out = (int)n_out;
