@@ -190,6 +190,43 @@ PSR_API const char* psr_status_string(int status);
  * or a negative status. */
 PSR_API int psr_num_ctas(void);
 
+/* ---- Ring Attention backward ------------------------------------------------------------------
+ * The gradient of psr_ring_attn_fwd (the mKernel pages describe only the
+ * forward; the backward follows the same ring and reuses the forward's LSE).
+ * With P_ij = exp(scale q_i.k_j - LSE_i) over the allowed keys, D_i = dO_i.O_i,
+ * dP_ij = dO_i.v_j and dS_ij = P_ij (dP_ij - D_i):
+ *     dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
+ * (dK, dV summed over the query heads that share the KV head).  In the ring
+ * each KV chunk travels with its dK/dV partial sums while the queries stay;
+ * on one GPU each persistent CTA holds one 128-row K/V tile and its dK/dV
+ * accumulators in tensor memory while it visits the query shards in ring
+ * order, and dQ is accumulated in fp32 (vector atomic adds) and rounded at the
+ * end.  All matrix products run on tcgen05 with bf16 operands (P and dS
+ * rounded to bf16) and fp32 accumulation. */
+
+/* Bytes of device workspace psr_ring_attn_bwd needs: the control block (the
+ * shared prefix, read by psr_get_stats), D ([B][Hq][S] fp32) and the dQ
+ * accumulator ([B][Hq][S][d] fp32).  Returns 0 for an invalid or unsupported
+ * shape. */
+PSR_API size_t psr_ring_attn_bwd_workspace_bytes(const psr_shape* shape);
+
+/* Ring Attention backward.
+ *   q, o, dout: device, bf16, [B][Hq][S][d]          (read; o = the forward output)
+ *   k, v:       device, bf16, [B][Hkv][S][d]         (read)
+ *   lse:        device, fp32, [B][Hq][S]             (read; the forward's natural-log LSE)
+ *   dq:         device, bf16, [B][Hq][S][d]          (written)
+ *   dk, dv:     device, bf16, [B][Hkv][S][d]         (written)
+ *   workspace:  device, >= psr_ring_attn_bwd_workspace_bytes(shape), 256-byte aligned.
+ *   timeout_ms: bound on every device wait (<= 0: 2000 ms); stream: a cudaStream_t.
+ * All pointers 16-byte aligned.  Asynchronous: enqueues a workspace reset, the
+ * D kernel, one persistent launch and the dQ rounding on `stream`; a device
+ * timeout is reported by psr_get_stats.  Supported: d in {64, 128}; causal 0 or
+ * 1 (PSR_CAUSAL_BALANCED: PSR_ERR_UNSUPPORTED); L = S/P a multiple of 128;
+ * Hq % Hkv == 0; sm_103 device. */
+PSR_API int psr_ring_attn_bwd(const psr_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, int timeout_ms, void* stream);
+
 /* ---- AllGather + GEMM ------------------------------------------------------------------------ */
 /* The pages' second fused pattern (dataforcee / chathome "five fused kernels"
  * table, AllGather+GEMM row; pwwt.cn analysis §2.6: 128-row chunks, local

@@ -17,6 +17,7 @@ from .build import LIB, LIB_PAIRS, LIB_TRACE, build as _build
 
 __all__ = ["build", "load", "Shape", "AgShape", "RsShape", "Partition", "Stats", "ring_attn_fwd", "ring_attn_fwd_host",
            "workspace_bytes", "ag_gemm", "ag_gemm_workspace_bytes", "gemm_rs", "gemm_rs_workspace_bytes",
+           "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
            "get_stats", "get_trajectory", "controller_target", "num_ctas", "status_string", "PsrError",
            "STATIC", "ADAPTIVE", "FAULT_NONE", "FAULT_DROP_FIRST_FLAG", "FAULT_SLOW_STAGING", "CAUSAL",
            "CAUSAL_BALANCED"]
@@ -29,7 +30,7 @@ CAUSAL, CAUSAL_BALANCED = 1, 2
 EXPORTED = ("psr_workspace_bytes", "psr_ring_attn_fwd", "psr_ring_attn_fwd_host", "psr_get_stats",
             "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas",
             "psr_ring_attn_fwd_noalloc", "psr_ag_gemm_workspace_bytes", "psr_ag_gemm", "psr_gemm_rs_workspace_bytes",
-            "psr_gemm_rs")
+            "psr_gemm_rs", "psr_ring_attn_bwd_workspace_bytes", "psr_ring_attn_bwd")
 
 
 class Shape(ctypes.Structure):
@@ -117,6 +118,11 @@ def load(trace: bool = False, variant: str = "") -> ctypes.CDLL:
         lib.psr_ag_gemm_workspace_bytes.restype = sz
         lib.psr_ag_gemm.argtypes = [P_ag, vp, vp, vp, vp, sz, P_part, vp]
         lib.psr_ag_gemm.restype = ctypes.c_int
+        lib.psr_ring_attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Shape)]
+        lib.psr_ring_attn_bwd_workspace_bytes.restype = sz
+        lib.psr_ring_attn_bwd.argtypes = [ctypes.POINTER(Shape), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                          ctypes.c_int, vp]
+        lib.psr_ring_attn_bwd.restype = ctypes.c_int
         P_rs = ctypes.POINTER(RsShape)
         lib.psr_gemm_rs_workspace_bytes.argtypes = [P_rs]
         lib.psr_gemm_rs_workspace_bytes.restype = sz
@@ -272,6 +278,41 @@ def ag_gemm(a, w, *, P, partition=None, workspace=None, out=None, stream=None):
     if rc != OK:
         raise PsrError(rc, "psr_ag_gemm")
     return out, workspace
+
+
+def ring_attn_bwd_workspace_bytes(shape: Shape) -> int:
+    n = load().psr_ring_attn_bwd_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise PsrError(ERR_UNSUPPORTED, "psr_ring_attn_bwd_workspace_bytes")
+    return int(n)
+
+
+def ring_attn_bwd(q, k, v, o, lse, dout, *, P, causal, scale=None, workspace=None, dq=None, dk=None, dv=None,
+                  timeout_ms=0, stream=None):
+    """Ring Attention backward through the C ABI: q, o, dout [B][Hq][S][d], k, v [B][Hkv][S][d]
+    (bf16), lse [B][Hq][S] fp32 (the forward's) -> (dq, dk, dv, workspace)."""
+    import torch
+    lib = load()
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    shape = make_shape(B, Hq, Hkv, S, P, d, causal, scale)
+    need = ring_attn_bwd_workspace_bytes(shape)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t in (q, k, v, o, dout, dq, dk, dv):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("ring_attn_bwd: q, k, v, o, dout, dq, dk, dv must be contiguous bf16 CUDA tensors")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("ring_attn_bwd: lse must be a contiguous fp32 CUDA tensor")
+    rc = lib.psr_ring_attn_bwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               workspace.data_ptr(), workspace.numel(), int(timeout_ms), _stream_handle(stream))
+    if rc != OK:
+        raise PsrError(rc, "psr_ring_attn_bwd")
+    return dq, dk, dv, workspace
 
 
 def gemm_rs_workspace_bytes(M, N, Ks, P) -> int:

@@ -13,7 +13,8 @@ LIB_TRACE = os.path.join(HERE, "libpsr_trace.so")  # same library with per-role 
 LIB_PAIRS = os.path.join(HERE, "libpsr_pairs.so")  # same library with CTA-pair compute units for d = 128
 # variant -> (extra nvcc defines, output)
 VARIANTS = {"": ([], LIB), "trace": (["-DPSR_TRACE=1"], LIB_TRACE), "pairs": (["-DPSR_PAIRS=1"], LIB_PAIRS)}
-SOURCES = [os.path.join(CSRC, f) for f in ("psr_ring_attn.cu", "psr_ag_gemm.cu", "psr_gemm_rs.cu", "psr_noalloc.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("psr_ring_attn.cu", "psr_ring_attn_bwd.cu", "psr_ag_gemm.cu", "psr_gemm_rs.cu",
+                                            "psr_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f)
                   for f in ("psr_device.cuh", "psr_schedule.h", "psr_control.cuh", "psr_gemm_tile.cuh")] + [
     os.path.join(ROOT, "include", "psr.h")]

@@ -439,3 +439,9 @@ def rs_sample_rows(w: GemmRsWorkload, n_random: int = 1024) -> np.ndarray:
         ids.add(splitmix64(seed, n) % w.M)
         n += 1
     return np.array(sorted(ids), dtype=np.int64)
+
+
+def generate_dout(w: Workload) -> np.ndarray:
+    """The upstream gradient dO ([B][Hq][S][d] bf16 bits) of an attention workload: the next
+    elements of the workload's seeded stream, after Q, K and V."""
+    return normal_bf16(w.seed, w.n_q + 2 * w.n_kv, w.n_q).reshape(w.B, w.Hq, w.S, w.d)
