@@ -8,6 +8,7 @@ non-causal pass followed by one causal pass, each a single persistent launch.
   python bench.py --sweep [d]      # partition-stress sweep: static 2..64 staging CTAs vs adaptive
   python bench.py --ag-gemm        # AllGather+GEMM, M8192 K8192 N28672 over 8 ranks
   python bench.py --gemm-rs        # GEMM+ReduceScatter, M8192 N8192 K28672 over 8 ranks
+  python bench.py --bwd            # Ring Attention backward, B1 H32 S32768 P16 d128
 
 value: algorithmic TFLOP/s over the timed steps (4*d flops per unmasked
 (query, key) pair), inputs resident in HBM (805 MB per pass, larger than L2).
@@ -771,6 +772,108 @@ def run_rs(args):
     }), flush=True)
 
 
+# ------------------------------------------------------------------------------------------------
+# Ring Attention backward (a separate line, not the headline)
+# ------------------------------------------------------------------------------------------------
+
+BWD_METRIC = "ring-attn bwd TFLOP/s (bf16, 1 GB300; 10*d flops per unmasked (query, key) pair)"
+
+
+def bwd_flops(w):
+    pairs = w.S * (w.S + 1) // 2 if w.causal else w.S * w.S
+    return 10.0 * w.d * pairs * w.B * w.Hq
+
+
+def bwd_cpu_baseline(w, q, k, v, do, budget_s):
+    """The fp64 oracle's dQ rows (each with its own forward row) on a seeded sample of query rows."""
+    import numpy as np
+
+    from oracle import attn_bwd as ob
+    rng = np.random.default_rng(w.seed + 99)
+    n = 8
+    while True:
+        rows = np.sort(rng.choice(w.B * w.Hq * w.S, size=n, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        ob.attn_bwd_dq_rows(q, k, v, do, causal=bool(w.causal), scale=w.scale, bh_rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s * 0.5 or n >= 4096:
+            break
+        n = int(min(4096, max(2 * n, n * budget_s * 0.7 / max(dt, 1e-3))))
+    keys = (rows % w.S) + 1 if w.causal else np.full(len(rows), w.S)
+    flops = float(10.0 * w.d * keys.sum())
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(rows)} seeded query rows of {w.name}: dQ rows with their own forward rows "
+                      f"(fp64 numpy, every allowed key), {dt:.1f} s"}
+
+
+def run_bwd(args):
+    import numpy as np
+    import torch
+
+    import persistent_sm_ring_gb300 as psr
+    import ring_inputs as ri
+    psr.build()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    base = ri.WORKLOADS["h32_s32k_c"]
+    q_h, k_h, v_h = ri.generate(base)
+    do_h = ri.generate_dout(base)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
+    q, k, v, do = dev(q_h), dev(k_h), dev(v_h), dev(do_h)
+    stream = torch.cuda.current_stream()
+    passes = []
+    clk = None
+    for name in ("h32_s32k_c", "h32_s32k_nc"):
+        w = ri.WORKLOADS[name]
+        o, lse, _ = psr.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, scale=w.scale)
+        dq, dk, dv, ws = psr.ring_attn_bwd(q, k, v, o, lse, do, P=w.P, causal=w.causal, scale=w.scale)
+
+        def step():
+            psr.ring_attn_bwd(q, k, v, o, lse, do, P=w.P, causal=w.causal, scale=w.scale, workspace=ws, dq=dq,
+                              dk=dk, dv=dv, stream=stream)
+        for _ in range(max(3, args.warmup)):
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        c = clocks.stop()
+        clk = clk or c
+        st = psr.get_stats(ws)
+        if st["status"] != 0:
+            raise RuntimeError(f"device status {st['status']} site {st['error_site']}")
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+        passes.append({"workload": name, "causal": bool(w.causal), "ms": round(ms, 4),
+                       "tflops": round(bwd_flops(w) / (ms / 1e3) / 1e12, 2),
+                       "pct_peak": round(100 * bwd_flops(w) / (ms / 1e3) / 1e12 / peak, 2), "clocks": c})
+    w = ri.WORKLOADS["h32_s32k_c"]
+    ms = passes[0]["ms"]
+    value = bwd_flops(w) / (ms / 1e3) / 1e12
+    cpu = None if args.no_cpu_baseline else bwd_cpu_baseline(w, q_h, k_h, v_h, do_h, args.cpu_budget)
+    print(json.dumps({
+        "metric": BWD_METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "Ring Attention backward B1 H32 S32768 P16 (L=2048) d128, causal "
+                               "(dQ, dK, dV from Q, K, V, O, LSE, dO)",
+                   "l2": "inputs larger than L2 (Q, K, V, O, dO 1.34 GB)"},
+        "roofline": {"bound": "tensor", "achieved": round(value, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(value / peak, 4), "traffic": None,
+                     "peak_source": f"{peaks.get('source')} bf16_tflops (burst)"},
+        "cpu_baseline": cpu,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "passes": passes,
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -780,6 +883,7 @@ def main():
     ap.add_argument("--sweep", type=int, nargs="?", const=0, default=None)
     ap.add_argument("--ag-gemm", action="store_true", help="the AllGather+GEMM path instead of attention")
     ap.add_argument("--gemm-rs", action="store_true", help="the GEMM+ReduceScatter path instead of attention")
+    ap.add_argument("--bwd", action="store_true", help="the Ring Attention backward instead of the forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=96)
@@ -792,6 +896,8 @@ def main():
         run_ag(args)
     elif args.gemm_rs:
         run_rs(args)
+    elif args.bwd:
+        run_bwd(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -135,5 +135,30 @@ def attn_bwd_rows(q_bits, k_bits, v_bits, do_bits, *, causal, scale, bh_rows, kv
     return dq, dk, dv
 
 
+def attn_bwd_dq_rows(q_bits, k_bits, v_bits, do_bits, *, causal, scale, bh_rows):
+    """dQ rows only, each from its own row of the forward (its LSE and D need no other
+    query row).  bh_rows: flat query-row ids ((b*Hq + hq)*S + i).  Returns [len][d]."""
+    B, Hq, S, d = q_bits.shape
+    g = Hq // k_bits.shape[1]
+    out = np.zeros((len(bh_rows), d))
+    for n, r in enumerate(bh_rows):
+        bh, i = int(r) // S, int(r) % S
+        b, h = bh // Hq, bh % Hq
+        n_keys = i + 1 if causal else S
+        kk = bf16_to_f64(k_bits[b, h // g, :n_keys])
+        vv = bf16_to_f64(v_bits[b, h // g, :n_keys])
+        qi = bf16_to_f64(q_bits[b, h, i])
+        doi = bf16_to_f64(do_bits[b, h, i])
+        s = scale * (kk @ qi)
+        m = s.max()
+        e = np.exp(s - m)
+        l = e.sum()
+        p = e / l
+        D = doi @ (p @ vv)
+        ds = p * (vv @ doi - D)
+        out[n] = scale * (ds @ kk)
+    return out
+
+
 def for_workload(w, q, k, v, do):
     return attn_bwd(q, k, v, do, causal=bool(w.causal), scale=w.scale)

@@ -162,3 +162,15 @@ def test_sampled_rows_match_full():
         assert np.allclose(sq, dq.reshape(-1, d)[qr], rtol=1e-12, atol=1e-13)
         assert np.allclose(sk, dk.reshape(-1, d)[kr], rtol=1e-12, atol=1e-13)
         assert np.allclose(sv, dv.reshape(-1, d)[kr], rtol=1e-12, atol=1e-13)
+
+
+def test_dq_rows_match_full():
+    rng = np.random.default_rng(16)
+    for causal in (False, True):
+        B, Hq, Hkv, S, d = 1, 4, 2, 32, 8
+        q, k, v, do = _bits(rng, (B, Hq, S, d)), _bits(rng, (B, Hkv, S, d)), _bits(rng, (B, Hkv, S, d)), \
+            _bits(rng, (B, Hq, S, d))
+        dq, _, _ = ob.attn_bwd(q, k, v, do, causal=causal, scale=0.4)
+        rows = np.array([0, 3, S - 1, S + 1, 2 * S + 30, B * Hq * S - 1])
+        got = ob.attn_bwd_dq_rows(q, k, v, do, causal=causal, scale=0.4, bh_rows=rows)
+        assert np.allclose(got, dq.reshape(-1, d)[rows], rtol=1e-12, atol=1e-13)
