@@ -7,21 +7,23 @@
 //     dV_j += P_ij dO_i,   dK_j += scale dS_ij q_i,   dQ_i += scale dS_ij k_j.
 // In the ring, each KV chunk travels around the ranks together with its dK / dV partial sums
 // while every rank keeps its queries; the partials are back at the owner after P steps.  On one
-// GPU an item holds one 128-row K/V tile and its dK / dV accumulators on chip for the whole
-// ring, visiting the query shards in ring order (its own shard first, then r+1, r+2, ...), so
-// nothing needs to be copied; dQ is accumulated in fp32 with vector atomic adds.
+// GPU two persistent kernels follow the two data flows:
 //
-// Per (query tile, K/V tile) pair, with the key rows on the tensor-memory lanes:
-//     S^T  = K Q^T          (tcgen05, SS)                      -> TMEM cols [0, 128)
-//     dP^T = V dO^T         (tcgen05, SS)                      -> TMEM cols [128, 256)
-//     P^T, dS^T             (one warpgroup, in place, bf16)    -> over S^T / over dP^T, and dS
-//                                                                 into shared memory (MN-major)
-//     dV  += P^T dO         (tcgen05, TS)                      -> TMEM cols [256, 256+d)
-//     dK  += dS^T Q         (tcgen05, TS)                      -> TMEM cols [256+d, 256+2d)
-//     dQ_t  = dS K          (tcgen05, SS)                      -> TMEM cols [128, 128+d)
-//     dQ_acc += dQ_t        (one warpgroup: tcgen05.ld, red.global.add.v4.f32)
-// One thread issues every MMA in that order; tensor-core instructions of one thread run in
-// order, so an MMA that overwrites columns another MMA reads is simply issued after it.
+//  * dK, dV (K/V-stationary): an item holds one 128-row K/V tile and its dK / dV accumulators
+//    in tensor memory for the whole ring, visiting the query shards in ring order (its own
+//    shard first, then r+1, r+2, ...); per query tile, with the key rows on the lanes:
+//        S^T = K Q^T, dP^T = V dO^T (SS)  ->  P^T, dS^T in place (bf16)  ->
+//        dV += P^T dO, dK += dS^T Q (TS)
+//  * dQ (Q-stationary, the forward's ring order): an item holds one 128-row query tile and its
+//    dQ accumulator; per K/V tile, with the query rows on the lanes:
+//        S = Q K^T, dP = dO V^T (SS)  ->  dS in place (bf16)  ->  dQ += dS K (TS)
+//
+// dQ could also be accumulated by the first kernel with atomic adds, saving the second
+// kernel's S and dP products; on GB300 those fp32 atomics (64 KiB per tile pair) ran at
+// ~1.6 TB/s and bounded the whole pass, 2x slower than recomputing.  In each kernel one thread
+// issues every MMA; tensor-core instructions of one thread run in order, so an MMA that
+// overwrites columns another MMA reads is simply issued after it.  Two warpgroups share the
+// elementwise work, each on half of the columns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -42,49 +44,87 @@ constexpr int kRows = 128;                 // rows of a query tile and of a K/V 
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
-struct BCfg {
-  static constexpr int TILE = kRows * D * 2;  // one tile of Q, dO, K or V (bf16), D/64 boxes of 16 KiB
-  static constexpr int DS_BYTES = kRows * kRows * 2;
-  static constexpr int OFF_K = 0, OFF_V = TILE;
-  static constexpr int OFF_Q = 2 * TILE;      // + qb * 2 * TILE (two buffers of Q | dO)
-  static constexpr int OFF_DS = 6 * TILE;
-  static constexpr int SMEM = 1024 + 6 * TILE + DS_BYTES;
-  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
-  static_assert(SMEM <= 232448 - 1024, "shared memory");
-};
-
 enum : uint32_t { SITE_KV = 21, SITE_Q_FULL = 22, SITE_Q_EMPTY = 23, SITE_S = 24, SITE_DP = 25, SITE_P = 26,
-                  SITE_DS = 27, SITE_DQ_FULL = 28, SITE_DQ_EMPTY = 29, SITE_DS_FREE = 30, SITE_ACC = 31 };
+                  SITE_DS = 27, SITE_WG = 28, SITE_ACC = 29, SITE_KV_EMPTY = 30 };
 
 struct BParams {
   int B, Hq, Hkv, S, P, L, gqa, causal;
   int tiles_per_shard;  // L / 128
-  int n_items;          // B * Hkv * (S / 128)
+  int n_items_kv;       // B * Hkv * (S / 128)
+  int n_items_q;        // B * Hq * (S / 128)
   float sl2;            // scale * log2(e)
   float scale;
   const float* lse;     // [B][Hq][S] natural-log LSE of the forward
   const float* delta;   // [B][Hq][S] D = rowsum(dO * O)
-  float* dq_acc;        // [B][Hq][S][d] fp32 (zeroed before the launch)
+  uint16_t* dq;         // [B][Hq][S][d] bf16
   uint16_t* dk;         // [B][Hkv][S][d] bf16
   uint16_t* dv;
   Ctrl* ctrl;
   unsigned long long timeout_ns;
 };
 
-struct BSmem {
-  uint64_t kv_full, q_full[2], q_empty[2], s_full, dp_full, p_ready, ds_ready, dq_full, dq_empty, ds_free, acc_full;
-  uint64_t drain;
+__host__ __device__ constexpr uint32_t idesc_ab(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+  return idesc_bf16_f32(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
+}
+
+// Shared-memory descriptors of a [128 rows][D cols] tile stored as D/64 boxes of 16 KiB
+// (128-byte swizzle): K-major use (rows = M or N, K = columns) for the 16-column step kk, and
+// MN-major use (rows = K, columns = M or N) for the 16-row step kk.
+__device__ __forceinline__ uint32_t kmaj_lo(uint32_t tile, int kk) {
+  return sdesc_lo(tile + (kk / 4) * 16384 + (kk % 4) * 32, 16);
+}
+__device__ __forceinline__ uint32_t mnmaj_lo(uint32_t tile, int kk) { return sdesc_lo(tile + kk * 2048, 16384); }
+
+__device__ __forceinline__ void unpack_bf16x2(uint32_t v, float& lo, float& hi) {
+  lo = __uint_as_float(v << 16);
+  hi = __uint_as_float(v & 0xFFFF0000u);
+}
+
+// The two elementwise warpgroups (warps 4..11) meet here before either overwrites fp32 columns
+// that the other still reads: an mbarrier with bounded waits (a plain bar.sync would wait
+// forever if the other warpgroup had left on a timeout).
+template <class KP, class SC>
+__device__ __forceinline__ bool wg_meet(uint64_t* bar, uint32_t& phase, const KP& p, SC* sc) {
+  __syncwarp();
+  if ((threadIdx.x % 32) == 0) mbar_arrive(bar);
+  const bool ok = __all_sync(0xffffffffu, wait_bar(bar, phase & 1u, p, sc, SITE_WG));
+  ++phase;
+  return ok;
+}
+
+// Store 64 bf16 values (32 pairs) of this thread's row to global memory.
+__device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t* w) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+}
+
+// ================================================================================================
+// dK, dV: K/V-stationary
+// ================================================================================================
+template <int D>
+struct KvCfg {
+  static constexpr int TILE = kRows * D * 2;
+  static constexpr int OFF_K = 0, OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;      // + qb * TILE
+  static constexpr int OFF_DO = 4 * TILE;     // + qb * TILE
+  static constexpr int OFF_LD = 6 * TILE;     // + qb * 1024: LSE[128] then D[128] (fp32)
+  static constexpr int SMEM = 1024 + OFF_LD + 2 * 1024;
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
+  static_assert(SMEM <= 232448 - 1024, "shared memory");
+};
+
+struct KvSmem {
+  uint64_t kv_full, q_full[2], q_empty[2], s_full, dp_full, p_ready, ds_ready, wg_sync, acc_full, drain;
   uint32_t tmem_base;
   int arg;
   volatile uint32_t abort;
 };
 
-struct Item {
+struct KvItem {
   int b, kvh, gk;  // batch, KV head, K/V tile (global 128-row index)
 };
-__device__ inline Item item_of(const BParams& p, int n) {
-  Item it;
+__device__ inline KvItem kv_item_of(const BParams& p, int n) {
+  KvItem it;
   it.gk = n / (p.B * p.Hkv);  // the earliest K/V tiles have the most causal work: dispensed first
   const int rest = n % (p.B * p.Hkv);
   it.b = rest / p.Hkv;
@@ -95,7 +135,7 @@ __device__ inline Item item_of(const BParams& p, int n) {
 // The item's (query head, query tile) pairs in ring order: shard j of the K/V tile first, then
 // j+1, j+2, ... (mod P); under the causal mask only query tiles at or after the K/V tile.
 template <class F>
-__device__ __forceinline__ void for_each_pair(const BParams& p, const Item& it, F&& f) {
+__device__ __forceinline__ void for_each_q(const BParams& p, const KvItem& it, F&& f) {
   const int j = it.gk / p.tiles_per_shard;
   for (int t = 0; t < p.P; ++t) {
     const int r = (j + t) % p.P;
@@ -111,34 +151,10 @@ __device__ __forceinline__ void for_each_pair(const BParams& p, const Item& it, 
   }
 }
 
-__host__ __device__ constexpr uint32_t idesc_ab(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
-  return idesc_bf16_f32(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
-}
-
-// Shared-memory descriptors of a [128 rows][D cols] tile stored as D/64 boxes of 16 KiB
-// (128-byte swizzle): K-major use (rows = M or N, K = columns) for the 16-column step kk, and
-// MN-major use (rows = K, columns = M or N) for the 16-row step kk.
-__device__ __forceinline__ uint32_t kmaj_lo(uint32_t tile, int kk) {
-  return sdesc_lo(tile + (kk / 4) * 16384 + (kk % 4) * 32, 16);
-}
-__device__ __forceinline__ uint32_t mnmaj_lo(uint32_t tile, int kk) { return sdesc_lo(tile + kk * 2048, 16384); }
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ void unpack_bf16x2(uint32_t v, float& lo, float& hi) {
-  lo = __uint_as_float(v << 16);
-  hi = __uint_as_float(v & 0xFFFF0000u);
-}
-
-// ------------------------------------------------------------------------------------------------
-// Roles
-// ------------------------------------------------------------------------------------------------
 template <int D>
-__device__ void producer(const BParams& p, BSmem* sc, uint32_t sbase, const Item& it, const CUtensorMap* tq,
-                         const CUtensorMap* tdo, const CUtensorMap* tk, const CUtensorMap* tv, uint32_t& qcnt) {
-  using C = BCfg<D>;
+__device__ void kv_producer(const BParams& p, KvSmem* sc, uint32_t sbase, const KvItem& it, const CUtensorMap* tq,
+                            const CUtensorMap* tdo, const CUtensorMap* tk, const CUtensorMap* tv, uint32_t& qcnt) {
+  using C = KvCfg<D>;
   const int kv_row = (it.b * p.Hkv + it.kvh) * p.S + it.gk * kRows;
   mbar_expect_tx(&sc->kv_full, 2 * C::TILE);
 #pragma unroll
@@ -146,160 +162,145 @@ __device__ void producer(const BParams& p, BSmem* sc, uint32_t sbase, const Item
     tma_load_2d(sbase + C::OFF_K + h * 16384, tk, 64 * h, kv_row, &sc->kv_full);
     tma_load_2d(sbase + C::OFF_V + h * 16384, tv, 64 * h, kv_row, &sc->kv_full);
   }
-  for_each_pair(p, it, [&](int hq, int gq, bool) -> bool {
+  for_each_q(p, it, [&](int hq, int gq, bool) -> bool {
     const uint32_t qb = qcnt % 2, fill = qcnt / 2;
     if (fill > 0 && !wait_bar(&sc->q_empty[qb], (fill - 1) & 1u, p, sc, SITE_Q_EMPTY)) return false;
     const int q_row = (it.b * p.Hq + hq) * p.S + gq * kRows;
-    const uint32_t qs = sbase + C::OFF_Q + qb * 2 * C::TILE;
-    mbar_expect_tx(&sc->q_full[qb], 2 * C::TILE);
+    const uint32_t ld = sbase + C::OFF_LD + qb * 1024;
+    mbar_expect_tx(&sc->q_full[qb], 2 * C::TILE + 1024);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {
-      tma_load_2d(qs + h * 16384, tq, 64 * h, q_row, &sc->q_full[qb]);
-      tma_load_2d(qs + C::TILE + h * 16384, tdo, 64 * h, q_row, &sc->q_full[qb]);
+      tma_load_2d(sbase + C::OFF_Q + qb * C::TILE + h * 16384, tq, 64 * h, q_row, &sc->q_full[qb]);
+      tma_load_2d(sbase + C::OFF_DO + qb * C::TILE + h * 16384, tdo, 64 * h, q_row, &sc->q_full[qb]);
     }
+    bulk_load(ld, p.lse + q_row, 512, &sc->q_full[qb]);
+    bulk_load(ld + 512, p.delta + q_row, 512, &sc->q_full[qb]);
     ++qcnt;
     return true;
   });
 }
 
+// Order per query tile j: dP^T(j), dV(j), S^T(j+1), dK(j); S^T(j+1) is issued as soon as dV(j)
+// has been issued (it reads P^T(j) from the columns S^T(j+1) overwrites), so that the tensor
+// core computes it while the warpgroups form dS^T(j).
 template <int D>
-__device__ void mma_issuer(const BParams& p, BSmem* sc, uint32_t sbase, const Item& it, uint32_t items,
-                           uint32_t& qcnt, uint32_t& jg) {
-  using C = BCfg<D>;
-  constexpr uint32_t I_SS = idesc_ab(128, 128, false, false);  // S^T, dP^T
-  constexpr uint32_t I_TS = idesc_ab(128, D, false, true);     // dV, dK: A in TMEM, B MN-major
-  constexpr uint32_t I_DQ = idesc_ab(128, D, true, true);      // dQ: A = dS MN-major, B = K MN-major
+__device__ void kv_mma(const BParams& p, KvSmem* sc, uint32_t sbase, const KvItem& it, uint32_t items, uint32_t& qcnt,
+                       uint32_t& jg) {
+  using C = KvCfg<D>;
+  constexpr uint32_t I_SS = idesc_ab(128, 128, false, false);
+  constexpr uint32_t I_TS = idesc_ab(128, D, false, true);
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);
   const uint32_t tm = sc->tmem_base;
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  int n_pairs = 0;
+  for_each_q(p, it, [&](int, int, bool) -> bool { ++n_pairs; return true; });
   if (!wait_bar(&sc->kv_full, items & 1u, p, sc, SITE_KV)) { sc->abort = 1; return; }
-  tc_fence_after();
-  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
-  bool first = true;
-  for_each_pair(p, it, [&](int, int, bool) -> bool {
-    const uint32_t qb = qcnt % 2, ph = (qcnt / 2) & 1u;
-    const uint32_t sQ = sbase + C::OFF_Q + qb * 2 * C::TILE, sDO = sQ + C::TILE;
-    if (!wait_bar(&sc->q_full[qb], ph, p, sc, SITE_Q_FULL)) return false;
+  auto issue_s = [&](uint32_t c) -> bool {  // S^T of the pair with load index c
+    if (!wait_bar(&sc->q_full[c % 2], (c / 2) & 1u, p, sc, SITE_Q_FULL)) return false;
     tc_fence_after();
-    // S^T = K Q^T (its columns held P^T of the previous pair, read by that pair's dV MMA)
+    const uint32_t sQ = sbase + C::OFF_Q + (c % 2) * C::TILE;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       mma_ss_w(tm + C::COL_S, kmaj_lo(sK, kk), kHi, kmaj_lo(sQ, kk), kHi, I_SS, kk > 0 ? 1u : 0u);
     mma_commit(&sc->s_full);
-    // dP^T = V dO^T, once the previous pair's dQ has been read out of these columns
-    if (jg > 0 && !wait_bar(&sc->dq_empty, (jg - 1) & 1u, p, sc, SITE_DQ_EMPTY)) return false;
-    tc_fence_after();
+    return true;
+  };
+  if (!issue_s(qcnt)) { sc->abort = 1; return; }
+  int i = 0;
+  for_each_q(p, it, [&](int, int, bool) -> bool {
+    const uint32_t qb = qcnt % 2;
+    const uint32_t sQ = sbase + C::OFF_Q + qb * C::TILE, sDO = sbase + C::OFF_DO + qb * C::TILE;
+    // dP^T = V dO^T (its columns held dS^T of the previous tile, read by that tile's dK MMA)
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       mma_ss_w(tm + C::COL_DP, kmaj_lo(sV, kk), kHi, kmaj_lo(sDO, kk), kHi, I_SS, kk > 0 ? 1u : 0u);
     mma_commit(&sc->dp_full);
-    // dV += P^T dO
     if (!wait_bar(&sc->p_ready, jg & 1u, p, sc, SITE_P)) return false;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk)
-      mma_ts_w(tm + C::COL_DV, tm + C::COL_S + kk * 8, mnmaj_lo(sDO, kk), kHi, I_TS, (first && kk == 0) ? 0u : 1u);
-    // dK += dS^T Q
+      mma_ts_w(tm + C::COL_DV, tm + C::COL_S + kk * 8, mnmaj_lo(sDO, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
+    if (i + 1 < n_pairs && !issue_s(qcnt + 1)) return false;
     if (!wait_bar(&sc->ds_ready, jg & 1u, p, sc, SITE_DS)) return false;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk)
-      mma_ts_w(tm + C::COL_DK, tm + C::COL_DP + kk * 8, mnmaj_lo(sQ, kk), kHi, I_TS, (first && kk == 0) ? 0u : 1u);
-    mma_commit(&sc->q_empty[qb]);  // Q and dO of this pair are read
-    // dQ_t = dS K into the dP^T columns (after the dK MMA has read dS^T from them)
-#pragma unroll
-    for (int kk = 0; kk < kRows / 16; ++kk)
-      mma_ss_w(tm + C::COL_DP, mnmaj_lo(sDS, kk), kHi, mnmaj_lo(sK, kk), kHi, I_DQ, kk > 0 ? 1u : 0u);
-    mma_commit(&sc->dq_full);
-    mma_commit(&sc->ds_free);
-    first = false;
+      mma_ts_w(tm + C::COL_DK, tm + C::COL_DP + kk * 8, mnmaj_lo(sQ, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
+    mma_commit(&sc->q_empty[qb]);  // Q, dO of this tile are read (LSE, D: the warpgroups are past them)
     ++qcnt;
     ++jg;
+    ++i;
     return true;
   });
+  if (i != n_pairs) { sc->abort = 1; return; }
   mma_commit(&sc->acc_full);
 }
 
-// The warpgroup whose threads own the K/V tile's rows (tensor-memory lanes 0..127).
+// Warpgroup w (warps 4..7: w = 0, warps 8..11: w = 1): the K/V tile's rows on the lanes, query
+// columns [64w, 64w + 64).
 template <int D>
-__device__ void softmax_wg(const BParams& p, BSmem* sc, uint8_t* smem, const Item& it, uint32_t items,
-                           uint32_t& jg) {
-  using C = BCfg<D>;
+__device__ void kv_elementwise(const BParams& p, KvSmem* sc, const uint8_t* smem, const KvItem& it, uint32_t items,
+                               uint32_t& jg, uint32_t& meet) {
+  using C = KvCfg<D>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int w = warp >= 8 ? 1 : 0;
   const int quarter = warp % 4;
   const int row = quarter * 32 + lane;  // K/V row of the tile
   const uint32_t lanes = sc->tmem_base + ((uint32_t)(quarter * 32) << 16);
-  uint8_t* ds_row = smem + C::OFF_DS + row * 128;
   bool ok = true;
-  for_each_pair(p, it, [&](int hq, int gq, bool diag) -> bool {
-    const size_t qrow0 = (size_t)(it.b * p.Hq + hq) * p.S + (size_t)gq * kRows;
-    ok = __all_sync(0xffffffffu, wait_bar(&sc->s_full, jg & 1u, p, sc, SITE_S));
+  for_each_q(p, it, [&](int, int, bool diag) -> bool {
+    const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LD + (jg % 2) * 1024) + 64 * w;
+    const float* d_s = lse_s + 128;
+    ok = __all_sync(0xffffffffu, wait_bar(&sc->q_full[jg % 2], (jg / 2) & 1u, p, sc, SITE_Q_FULL));
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(&sc->s_full, jg & 1u, p, sc, SITE_S));
     if (!ok) return false;
     tc_fence_after();
-    uint32_t pk[64];  // P^T of this row, bf16 pairs
+    uint32_t pk[32];  // P^T of this row over the warpgroup's 64 query columns, bf16 pairs
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t s[32];
-      tmem_ld32(lanes + C::COL_S + 32 * c, s);
+      tmem_ld32(lanes + C::COL_S + 64 * w + 32 * c, s);
       tmem_ld_wait();
-      const float4* l4 = reinterpret_cast<const float4*>(p.lse + qrow0 + 32 * c);
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 l = __ldg(l4 + e4);
-        const float lv[4] = {l.x, l.y, l.z, l.w};
-        float pv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int col = 32 * c + 4 * e4 + u;  // query row of the tile
-          const float x = __uint_as_float(s[4 * e4 + u]) * p.sl2 - lv[u] * kLog2e;
-          pv[u] = (diag && col < row) ? 0.0f : ex2_approx(x);
-        }
-        pk[16 * c + 2 * e4] = pack_bf16x2(pv[0], pv[1]);
-        pk[16 * c + 2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
+      for (int e = 0; e < 32; e += 2) {
+        const int col = 64 * w + 32 * c + e;  // query row of the tile
+        float p0 = ex2_approx(__uint_as_float(s[e]) * p.sl2 - lse_s[32 * c + e] * kLog2e);
+        float p1 = ex2_approx(__uint_as_float(s[e + 1]) * p.sl2 - lse_s[32 * c + e + 1] * kLog2e);
+        if (diag && col < row) p0 = 0.0f;       // key after query: masked
+        if (diag && col + 1 < row) p1 = 0.0f;
+        pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
       }
-      tmem_st16(lanes + C::COL_S + 16 * c, &pk[16 * c]);
     }
+    // both warpgroups have read their fp32 columns; the bf16 P^T (query q at column q/2) may
+    // now overwrite the lower half of the S^T columns
+    if (!wg_meet(&sc->wg_sync, meet, p, sc)) { ok = false; return false; }
+    tmem_st16(lanes + C::COL_S + 32 * w, pk);
+    tmem_st16(lanes + C::COL_S + 32 * w + 16, pk + 16);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sc->p_ready);
     ok = __all_sync(0xffffffffu, wait_bar(&sc->dp_full, jg & 1u, p, sc, SITE_DP));
-    if (ok && jg > 0) ok = __all_sync(0xffffffffu, wait_bar(&sc->ds_free, (jg - 1) & 1u, p, sc, SITE_DS_FREE));
     if (!ok) return false;
     tc_fence_after();
+    uint32_t ds[32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t dp[32];
-      tmem_ld32(lanes + C::COL_DP + 32 * c, dp);
+      tmem_ld32(lanes + C::COL_DP + 64 * w + 32 * c, dp);
       tmem_ld_wait();
-      const float4* d4 = reinterpret_cast<const float4*>(p.delta + qrow0 + 32 * c);
-      uint32_t ds[16];
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 dd = __ldg(d4 + e4);
-        float p0, p1, p2, p3;
-        unpack_bf16x2(pk[16 * c + 2 * e4], p0, p1);
-        unpack_bf16x2(pk[16 * c + 2 * e4 + 1], p2, p3);
-        ds[2 * e4] = pack_bf16x2(p0 * (__uint_as_float(dp[4 * e4]) - dd.x), p1 * (__uint_as_float(dp[4 * e4 + 1]) - dd.y));
-        ds[2 * e4 + 1] =
-            pack_bf16x2(p2 * (__uint_as_float(dp[4 * e4 + 2]) - dd.z), p3 * (__uint_as_float(dp[4 * e4 + 3]) - dd.w));
-      }
-      // dS^T over the dP^T columns already read (columns 16c .. 16c+15 of the bf16 pairs)
-      tmem_st16(lanes + C::COL_DP + 16 * c, ds);
-      // dS into shared memory as the MN-major A operand of dQ = dS K: row = key, 64 queries per
-      // 128-byte row of a 16 KiB box, 16-byte chunks swizzled with the row
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int chunk = (c % 2) * 4 + i;
-        uint4 v;
-        v.x = ds[4 * i];
-        v.y = ds[4 * i + 1];
-        v.z = ds[4 * i + 2];
-        v.w = ds[4 * i + 3];
-        *reinterpret_cast<uint4*>(ds_row + (c / 2) * 16384 + ((chunk ^ (row & 7)) * 16)) = v;
+      for (int e = 0; e < 32; e += 2) {
+        float p0, p1;
+        unpack_bf16x2(pk[16 * c + e / 2], p0, p1);
+        ds[16 * c + e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - d_s[32 * c + e]),
+                                         p1 * (__uint_as_float(dp[e + 1]) - d_s[32 * c + e + 1]));
       }
     }
+    if (!wg_meet(&sc->wg_sync, meet, p, sc)) { ok = false; return false; }
+    tmem_st16(lanes + C::COL_DP + 32 * w, ds);
+    tmem_st16(lanes + C::COL_DP + 32 * w + 16, ds + 16);
     tmem_st_wait();
-    fence_proxy_async_smem();  // the generic dS stores before the MMA's reads
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sc->ds_ready);
@@ -307,75 +308,40 @@ __device__ void softmax_wg(const BParams& p, BSmem* sc, uint8_t* smem, const Ite
     return true;
   });
   if (!ok) { sc->abort = 1; return; }
-  // the item's dK and dV rows
+  // the item's dK and dV rows: this warpgroup's half of the columns
   ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full, items & 1u, p, sc, SITE_ACC));
   if (!ok) { sc->abort = 1; return; }
   tc_fence_after();
   const size_t out_row = ((size_t)(it.b * p.Hkv + it.kvh) * p.S + (size_t)it.gk * kRows + row) * D;
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
-    const uint32_t col = which ? C::COL_DK : C::COL_DV;
+    const uint32_t col = (which ? C::COL_DK : C::COL_DV) + w * (D / 2);
     const float mul = which ? p.scale : 1.0f;
-    uint16_t* dst = (which ? p.dk : p.dv) + out_row;
+    uint16_t* dst = (which ? p.dk : p.dv) + out_row + w * (D / 2);
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t v[32];
+    for (int c = 0; c < D / 64; ++c) {
+      uint32_t v[32], o[16];
       tmem_ld32(lanes + col + 32 * c, v);
       tmem_ld_wait();
-      uint4 o[4];
-      uint32_t* w = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+      for (int e = 0; e < 16; ++e) o[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) reinterpret_cast<uint4*>(dst + 32 * c)[e] = o[e];
+      for (int e = 0; e < 4; ++e)
+        reinterpret_cast<uint4*>(dst + 32 * c)[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
     }
   }
 }
 
-// The warpgroup that reads each pair's dQ_t (query rows on the lanes) and adds it to dQ_acc.
-template <int D>
-__device__ void dq_wg(const BParams& p, BSmem* sc, const Item& it, uint32_t& jg) {
-  using C = BCfg<D>;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int quarter = warp % 4;
-  const int row = quarter * 32 + lane;
-  const uint32_t lanes = sc->tmem_base + ((uint32_t)(quarter * 32) << 16);
-  bool ok = true;
-  for_each_pair(p, it, [&](int hq, int gq, bool) -> bool {
-    ok = __all_sync(0xffffffffu, wait_bar(&sc->dq_full, jg & 1u, p, sc, SITE_DQ_FULL));
-    if (!ok) return false;
-    tc_fence_after();
-    float* dst = p.dq_acc + ((size_t)(it.b * p.Hq + hq) * p.S + (size_t)gq * kRows + row) * D;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(lanes + C::COL_DP + 32 * c, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        red_add_v4(dst + 32 * c + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sc->dq_empty);
-    ++jg;
-    return true;
-  });
-  if (!ok) sc->abort = 1;
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    ring_attn_bwd_kernel(const __grid_constant__ BParams p, const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v) {
+    bwd_kv_kernel(const __grid_constant__ BParams p, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ BSmem sc;
+  __shared__ KvSmem sc;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sbase - raw);
+  const uint8_t* smem = smem_raw + (sbase - raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(&sc.kv_full, 1);
@@ -385,11 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sc.s_full, 1);
     mbar_init(&sc.dp_full, 1);
-    mbar_init(&sc.p_ready, 4);   // the four warps of the softmax warpgroup
-    mbar_init(&sc.ds_ready, 4);
-    mbar_init(&sc.dq_full, 1);
-    mbar_init(&sc.dq_empty, 4);  // the four warps of the dQ warpgroup
-    mbar_init(&sc.ds_free, 1);
+    mbar_init(&sc.p_ready, 8);   // the eight warps of the two elementwise warpgroups
+    mbar_init(&sc.ds_ready, 8);
+    mbar_init(&sc.wg_sync, 8);
     mbar_init(&sc.acc_full, 1);
     mbar_init(&sc.drain, 1);
     sc.abort = 0;
@@ -406,29 +370,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-
-  uint32_t items = 0, qcnt_p = 0, qcnt_m = 0, jg_m = 0, jg_s = 0, jg_q = 0;
+  uint32_t items = 0, qcnt_p = 0, qcnt_m = 0, jg_m = 0, jg_e = 0, meet = 0;
   while (true) {
     if (threadIdx.x == 0) {
       int n = -1;
       if (!sc.abort && !ld_relaxed(&p.ctrl->abort)) {
         const uint32_t t = atomicAdd(&p.ctrl->item_next, 1u);
-        if (t < (uint32_t)p.n_items) n = (int)t;
+        if (t < (uint32_t)p.n_items_kv) n = (int)t;
       }
       sc.arg = n;
     }
     __syncthreads();
     const int n = sc.arg;
     if (n < 0) break;
-    const Item it = item_of(p, n);
+    const KvItem it = kv_item_of(p, n);
     if (warp == 0 && lane == 0) {
-      producer<D>(p, &sc, sbase, it, &tm_q, &tm_do, &tm_k, &tm_v, qcnt_p);
+      kv_producer<D>(p, &sc, sbase, it, &tm_q, &tm_do, &tm_k, &tm_v, qcnt_p);
     } else if (warp == 1 && lane == 0) {
-      mma_issuer<D>(p, &sc, sbase, it, items, qcnt_m, jg_m);
-    } else if (warp >= 4 && warp < 8) {
-      softmax_wg<D>(p, &sc, smem, it, items, jg_s);
-    } else if (warp >= 8) {
-      dq_wg<D>(p, &sc, it, jg_q);
+      kv_mma<D>(p, &sc, sbase, it, items, qcnt_m, jg_m);
+    } else if (warp >= 4) {
+      kv_elementwise<D>(p, &sc, smem, it, items, jg_e, meet);
     }
     tc_fence_before();
     __syncthreads();
@@ -437,8 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++items;
     if (sc.abort) break;
   }
-  // drain (bounded): every MMA has completed and every TMA load has landed before TMEM and
-  // shared memory are released
+  // drain (bounded): every MMA has completed and every TMA load has landed
   if (warp == 1 && lane == 0) {
     mma_commit(&sc.drain);
     const uint64_t t0 = globaltimer_ns();
@@ -453,6 +413,300 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t b = 0; b < 2 && b < qcnt_p; ++b) {
       const uint32_t fills = (qcnt_p - b + 1) / 2;
       while (!mbar_try_wait(&sc.q_full[b], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(sc.tmem_base, 512);
+}
+
+// ================================================================================================
+// dQ: Q-stationary
+// ================================================================================================
+template <int D>
+struct QCfg {
+  static constexpr int TILE = kRows * D * 2;
+  static constexpr int OFF_Q = 0, OFF_DO = TILE;
+  static constexpr int OFF_K = 2 * TILE;      // + kb * 2 * TILE
+  static constexpr int OFF_V = 3 * TILE;      // + kb * 2 * TILE
+  static constexpr int SMEM = 1024 + 6 * TILE;
+  static constexpr uint32_t COL_S = 0;        // + (tile % 2) * 128: S double-buffered
+  static constexpr uint32_t COL_DP = 256, COL_DQ = 384;
+  static_assert(SMEM <= 232448 - 1024, "shared memory");
+};
+
+struct QSmem {
+  uint64_t qd_full, kv_full[2], kv_empty[2], s_full[2], dp_full, ds_ready, wg_sync, acc_full, drain;
+  uint32_t tmem_base;
+  int arg;
+  volatile uint32_t abort;
+};
+
+struct QItem {
+  int b, hq, gq;  // batch, query head, query tile (global 128-row index)
+};
+__device__ inline QItem q_item_of(const BParams& p, int n) {
+  QItem it;
+  const int per = p.B * p.Hq;
+  it.gq = (p.causal ? (p.S / kRows - 1 - n / per) : n / per);  // causal: the last query tiles (most keys) first
+  const int rest = n % per;
+  it.b = rest / p.Hq;
+  it.hq = rest % p.Hq;
+  return it;
+}
+
+// The item's K/V tiles in the forward's ring order: the query shard r's own chunk first, then
+// r-1, r-2, ... (mod P); under the causal mask only K/V tiles at or before the query tile.
+template <class F>
+__device__ __forceinline__ void for_each_kv(const BParams& p, const QItem& it, F&& f) {
+  const int r = it.gq / p.tiles_per_shard;
+  for (int t = 0; t < p.P; ++t) {
+    const int j = ((r - t) % p.P + p.P) % p.P;
+    if (p.causal && j > r) continue;
+    for (int kt = 0; kt < p.tiles_per_shard; ++kt) {
+      const int gk = j * p.tiles_per_shard + kt;
+      if (p.causal && gk > it.gq) continue;
+      if (!f(gk, p.causal && gk == it.gq)) return;
+    }
+  }
+}
+
+template <int D>
+__device__ void q_producer(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& it, const CUtensorMap* tq,
+                           const CUtensorMap* tdo, const CUtensorMap* tk, const CUtensorMap* tv, uint32_t& kcnt) {
+  using C = QCfg<D>;
+  const int q_row = (it.b * p.Hq + it.hq) * p.S + it.gq * kRows;
+  mbar_expect_tx(&sc->qd_full, 2 * C::TILE);
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    tma_load_2d(sbase + C::OFF_Q + h * 16384, tq, 64 * h, q_row, &sc->qd_full);
+    tma_load_2d(sbase + C::OFF_DO + h * 16384, tdo, 64 * h, q_row, &sc->qd_full);
+  }
+  const int kv_base = (it.b * p.Hkv + it.hq / p.gqa) * p.S;
+  for_each_kv(p, it, [&](int gk, bool) -> bool {
+    const uint32_t kb = kcnt % 2, fill = kcnt / 2;
+    if (fill > 0 && !wait_bar(&sc->kv_empty[kb], (fill - 1) & 1u, p, sc, SITE_KV_EMPTY)) return false;
+    mbar_expect_tx(&sc->kv_full[kb], 2 * C::TILE);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_2d(sbase + C::OFF_K + kb * 2 * C::TILE + h * 16384, tk, 64 * h, kv_base + gk * kRows, &sc->kv_full[kb]);
+      tma_load_2d(sbase + C::OFF_V + kb * 2 * C::TILE + h * 16384, tv, 64 * h, kv_base + gk * kRows, &sc->kv_full[kb]);
+    }
+    ++kcnt;
+    return true;
+  });
+}
+
+// Order per K/V tile j: S(j+1) (into the other S buffer, as soon as its K has landed), dQ(j)
+// (after the warpgroups have written dS(j) over dP(j)), dP(j+1).
+template <int D>
+__device__ void q_mma(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& it, uint32_t items, uint32_t& kcnt,
+                      uint32_t& jg) {
+  using C = QCfg<D>;
+  constexpr uint32_t I_SS = idesc_ab(128, 128, false, false);  // S, dP
+  constexpr uint32_t I_TS = idesc_ab(128, D, false, true);     // dQ: A = dS in TMEM, B = K MN-major
+  constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+  const uint32_t tm = sc->tmem_base;
+  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO;
+  int n_kv = 0;
+  for_each_kv(p, it, [&](int, bool) -> bool { ++n_kv; return true; });
+  if (!wait_bar(&sc->qd_full, items & 1u, p, sc, SITE_Q_FULL)) { sc->abort = 1; return; }
+  auto k_of = [&](uint32_t c) { return sbase + C::OFF_K + (c % 2) * 2 * C::TILE; };
+  auto v_of = [&](uint32_t c) { return sbase + C::OFF_V + (c % 2) * 2 * C::TILE; };
+  auto issue_s = [&](uint32_t c, uint32_t j) -> bool {  // S of K/V load c into S buffer j % 2
+    if (!wait_bar(&sc->kv_full[c % 2], (c / 2) & 1u, p, sc, SITE_KV)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_ss_w(tm + C::COL_S + (j % 2) * 128, kmaj_lo(sQ, kk), kHi, kmaj_lo(k_of(c), kk), kHi, I_SS, kk > 0 ? 1u : 0u);
+    mma_commit(&sc->s_full[j % 2]);
+    return true;
+  };
+  auto issue_dp = [&](uint32_t c) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_ss_w(tm + C::COL_DP, kmaj_lo(sDO, kk), kHi, kmaj_lo(v_of(c), kk), kHi, I_SS, kk > 0 ? 1u : 0u);
+    mma_commit(&sc->dp_full);
+  };
+  tc_fence_after();
+  if (!issue_s(kcnt, jg)) { sc->abort = 1; return; }
+  issue_dp(kcnt);
+  int i = 0;
+  for_each_kv(p, it, [&](int, bool) -> bool {
+    if (i + 1 < n_kv && !issue_s(kcnt + 1, jg + 1)) return false;
+    if (!wait_bar(&sc->ds_ready, jg & 1u, p, sc, SITE_DS)) return false;
+    tc_fence_after();
+    const uint32_t sK = k_of(kcnt);
+#pragma unroll
+    for (int kk = 0; kk < kRows / 16; ++kk)
+      mma_ts_w(tm + C::COL_DQ, tm + C::COL_DP + kk * 8, mnmaj_lo(sK, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
+    mma_commit(&sc->kv_empty[kcnt % 2]);  // K, V of this tile are read
+    if (i + 1 < n_kv) issue_dp(kcnt + 1);  // dP(j+1) over dS(j), after the dQ MMA has read it
+    ++kcnt;
+    ++jg;
+    ++i;
+    return true;
+  });
+  if (i != n_kv) { sc->abort = 1; return; }
+  mma_commit(&sc->acc_full);
+}
+
+// Warpgroup w: the query tile's rows on the lanes, K/V columns [64w, 64w + 64).
+template <int D>
+__device__ void q_elementwise(const BParams& p, QSmem* sc, const QItem& it, uint32_t items, uint32_t& jg,
+                              uint32_t& meet) {
+  using C = QCfg<D>;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int w = warp >= 8 ? 1 : 0;
+  const int quarter = warp % 4;
+  const int row = quarter * 32 + lane;  // query row of the tile
+  const uint32_t lanes = sc->tmem_base + ((uint32_t)(quarter * 32) << 16);
+  const size_t qrow = (size_t)(it.b * p.Hq + it.hq) * p.S + (size_t)it.gq * kRows + row;
+  const float lse2 = p.lse[qrow] * kLog2e;
+  const float dlt = p.delta[qrow];
+  bool ok = true;
+  for_each_kv(p, it, [&](int, bool diag) -> bool {
+    ok = __all_sync(0xffffffffu, wait_bar(&sc->s_full[jg % 2], (jg / 2) & 1u, p, sc, SITE_S));
+    if (!ok) return false;
+    tc_fence_after();
+    float pv[64];  // P over the warpgroup's 64 key columns
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t s[32];
+      tmem_ld32(lanes + C::COL_S + (jg % 2) * 128 + 64 * w + 32 * c, s);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int col = 64 * w + 32 * c + e;  // key row of the K/V tile
+        const float x = ex2_approx(__uint_as_float(s[e]) * p.sl2 - lse2);
+        pv[32 * c + e] = (diag && col > row) ? 0.0f : x;
+      }
+    }
+    ok = __all_sync(0xffffffffu, wait_bar(&sc->dp_full, jg & 1u, p, sc, SITE_DP));
+    if (!ok) return false;
+    tc_fence_after();
+    uint32_t ds[32];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t dp[32];
+      tmem_ld32(lanes + C::COL_DP + 64 * w + 32 * c, dp);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; e += 2)
+        ds[16 * c + e / 2] = pack_bf16x2(pv[32 * c + e] * (__uint_as_float(dp[e]) - dlt),
+                                         pv[32 * c + e + 1] * (__uint_as_float(dp[e + 1]) - dlt));
+    }
+    // both warpgroups have read their fp32 dP columns; dS (key k at column k/2) may now
+    // overwrite the lower half of them
+    if (!wg_meet(&sc->wg_sync, meet, p, sc)) { ok = false; return false; }
+    tmem_st16(lanes + C::COL_DP + 32 * w, ds);
+    tmem_st16(lanes + C::COL_DP + 32 * w + 16, ds + 16);
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sc->ds_ready);
+    ++jg;
+    return true;
+  });
+  if (!ok) { sc->abort = 1; return; }
+  ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full, items & 1u, p, sc, SITE_ACC));
+  if (!ok) { sc->abort = 1; return; }
+  tc_fence_after();
+  uint16_t* dst = p.dq + qrow * D + w * (D / 2);
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t v[32], o[16];
+    tmem_ld32(lanes + C::COL_DQ + w * (D / 2) + 32 * c, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      o[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * p.scale, __uint_as_float(v[2 * e + 1]) * p.scale);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      reinterpret_cast<uint4*>(dst + 32 * c)[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_q_kernel(const __grid_constant__ BParams p, const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ QSmem sc;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(&sc.qd_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sc.kv_full[b], 1);
+      mbar_init(&sc.kv_empty[b], 1);
+      mbar_init(&sc.s_full[b], 1);
+    }
+    mbar_init(&sc.dp_full, 1);
+    mbar_init(&sc.ds_ready, 8);
+    mbar_init(&sc.wg_sync, 8);
+    mbar_init(&sc.acc_full, 1);
+    mbar_init(&sc.drain, 1);
+    sc.abort = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sc.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  uint32_t items = 0, kcnt_p = 0, kcnt_m = 0, jg_m = 0, jg_e = 0, meet = 0;
+  while (true) {
+    if (threadIdx.x == 0) {
+      int n = -1;
+      if (!sc.abort && !ld_relaxed(&p.ctrl->abort)) {
+        const uint32_t t = atomicAdd(&p.ctrl->init_next, 1u);
+        if (t < (uint32_t)p.n_items_q) n = (int)t;
+      }
+      sc.arg = n;
+    }
+    __syncthreads();
+    const int n = sc.arg;
+    if (n < 0) break;
+    const QItem it = q_item_of(p, n);
+    if (warp == 0 && lane == 0) {
+      q_producer<D>(p, &sc, sbase, it, &tm_q, &tm_do, &tm_k, &tm_v, kcnt_p);
+    } else if (warp == 1 && lane == 0) {
+      q_mma<D>(p, &sc, sbase, it, items, kcnt_m, jg_m);
+    } else if (warp >= 4) {
+      q_elementwise<D>(p, &sc, it, items, jg_e, meet);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0 && !sc.abort) atomicAdd(&p.ctrl->compute_items, 1ull);
+    ++items;
+    if (sc.abort) break;
+  }
+  if (warp == 1 && lane == 0) {
+    mma_commit(&sc.drain);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&sc.drain, 0) && globaltimer_ns() - t0 < 100000000ull) {
+    }
+  }
+  if (warp == 0 && lane == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    if (items > 0)
+      while (!mbar_try_wait(&sc.qd_full, (items - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    for (uint32_t b = 0; b < 2 && b < kcnt_p; ++b) {
+      const uint32_t fills = (kcnt_p - b + 1) / 2;
+      while (!mbar_try_wait(&sc.kv_full[b], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
   }
@@ -483,22 +737,12 @@ __global__ void delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __r
   }
 }
 
-// dQ = scale * dQ_acc, rounded to bf16 (four elements per thread)
-__global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, float scale, long long n4) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-    const float4 v = acc[i];
-    uint2 w;
-    w.x = pack_bf16x2(v.x * scale, v.y * scale);
-    w.y = pack_bf16x2(v.z * scale, v.w * scale);
-    dq[i] = w;
-  }
-}
 
 // ------------------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------------------
 struct BLayout {
-  size_t ctrl, delta, dq_acc, total;
+  size_t ctrl, delta, total;
 };
 
 static size_t au(size_t x) { return (x + 255) / 256 * 256; }
@@ -513,7 +757,7 @@ static int check_shape(const psr_shape* sh) {
   if (sh->Hq % sh->Hkv != 0 || sh->S % sh->P != 0 || (sh->S / sh->P) % kRows != 0) return PSR_ERR_UNSUPPORTED;
   const long long rows = (long long)sh->B * sh->Hq * sh->S;
   if (rows >= (1LL << 31) || rows * sh->d >= (1LL << 40)) return PSR_ERR_UNSUPPORTED;
-  if ((long long)sh->B * sh->Hkv * (sh->S / kRows) >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
+  if ((long long)sh->B * sh->Hq * (sh->S / kRows) >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   return PSR_OK;
 }
 
@@ -524,7 +768,6 @@ static BLayout layout(const psr_shape* sh) {
   l.ctrl = off; off += 256;
   off = au(off + (size_t)kTrajMax * 8);  // the shared workspace prefix (stats and trajectory)
   l.delta = off; off = au(off + rows * 4);
-  l.dq_acc = off; off = au(off + rows * sh->d * 4);
   l.total = off;
   return l;
 }
@@ -534,11 +777,15 @@ static cudaError_t launch_bwd(const BParams& kp, const CUtensorMap* maps, int n_
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(ring_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    BCfg<D>::SMEM);
+    attr_err = cudaFuncSetAttribute(bwd_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(bwd_q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<D>::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  ring_attn_bwd_kernel<D><<<n_cta, kThreads, BCfg<D>::SMEM, st>>>(kp, maps[0], maps[1], maps[2], maps[3]);
+  bwd_kv_kernel<D><<<n_cta, kThreads, KvCfg<D>::SMEM, st>>>(kp, maps[0], maps[1], maps[2], maps[3]);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_q_kernel<D><<<n_cta, kThreads, QCfg<D>::SMEM, st>>>(kp, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
 }
 
@@ -580,13 +827,14 @@ int psr_ring_attn_bwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.gqa = sh->Hq / sh->Hkv;
   kp.causal = sh->causal;
   kp.tiles_per_shard = kp.L / kRows;
-  kp.n_items = sh->B * sh->Hkv * (sh->S / kRows);
+  kp.n_items_kv = sh->B * sh->Hkv * (sh->S / kRows);
+  kp.n_items_q = sh->B * sh->Hq * (sh->S / kRows);
   const float scale = sh->scale > 0.0f ? sh->scale : 1.0f / std::sqrt((float)sh->d);
   kp.scale = scale;
   kp.sl2 = scale * kLog2e;
   kp.lse = lse;
   kp.delta = reinterpret_cast<const float*>(ws + L.delta);
-  kp.dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+  kp.dq = static_cast<uint16_t*>(dq);
   kp.dk = static_cast<uint16_t*>(dk);
   kp.dv = static_cast<uint16_t*>(dv);
   kp.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
@@ -602,7 +850,6 @@ int psr_ring_attn_bwd(const psr_shape* sh, const void* q, const void* k, const v
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, L.delta, st) != cudaSuccess) return PSR_ERR_CUDA;  // control block and log
-  if (cudaMemsetAsync(ws + L.dq_acc, 0, (size_t)rows_q * sh->d * 4, st) != cudaSuccess) return PSR_ERR_CUDA;
   const int dgrid = n_cta * 8;
   if (sh->d == 128)
     delta_kernel<128><<<dgrid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
@@ -616,9 +863,6 @@ int psr_ring_attn_bwd(const psr_shape* sh, const void* q, const void* k, const v
     cudaGetLastError();
     return PSR_ERR_CUDA;
   }
-  dq_convert_kernel<<<n_cta * 8, 256, 0, st>>>(reinterpret_cast<const float4*>(ws + L.dq_acc),
-                                               static_cast<uint2*>(dq), scale, rows_q * sh->d / 4);
-  if (cudaGetLastError() != cudaSuccess) return PSR_ERR_CUDA;
   return PSR_OK;
 }
 

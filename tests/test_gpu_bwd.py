@@ -74,7 +74,7 @@ def test_bwd_every_element(psr, w):
     ref = ob.for_workload(w, q, k, v, do)
     dq, dk, dv, st = run_bwd(psr, w, q, k, v, do)
     assert st["status"] == 0, st
-    assert st["compute_items"] == w.B * w.Hkv * w.S // 128
+    assert st["compute_items"] == (w.B * w.Hkv + w.B * w.Hq) * w.S // 128  # K/V items + query items
     check(w.name, (dq, dk, dv), ref)
 
 
