@@ -817,6 +817,8 @@ def run_bwd(args):
     peaks = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     base = ri.WORKLOADS["h32_s32k_c"]
+    if args.heads:  # a smaller same-kernel case (profiling): fewer heads, same S, P, d
+        base = base.with_(Hq=args.heads, Hkv=args.heads)
     q_h, k_h, v_h = ri.generate(base)
     do_h = ri.generate_dout(base)
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
@@ -825,7 +827,7 @@ def run_bwd(args):
     passes = []
     clk = None
     for name in ("h32_s32k_c", "h32_s32k_nc"):
-        w = ri.WORKLOADS[name]
+        w = ri.WORKLOADS[name].with_(Hq=base.Hq, Hkv=base.Hkv)
         o, lse, _ = psr.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, scale=w.scale)
         dq, dk, dv, ws = psr.ring_attn_bwd(q, k, v, o, lse, do, P=w.P, causal=w.causal, scale=w.scale)
 
@@ -853,7 +855,7 @@ def run_bwd(args):
         passes.append({"workload": name, "causal": bool(w.causal), "ms": round(ms, 4),
                        "tflops": round(bwd_flops(w) / (ms / 1e3) / 1e12, 2),
                        "pct_peak": round(100 * bwd_flops(w) / (ms / 1e3) / 1e12 / peak, 2), "clocks": c})
-    w = ri.WORKLOADS["h32_s32k_c"]
+    w = ri.WORKLOADS["h32_s32k_c"].with_(Hq=base.Hq, Hkv=base.Hkv)
     ms = passes[0]["ms"]
     value = bwd_flops(w) / (ms / 1e3) / 1e12
     cpu = None if args.no_cpu_baseline else bwd_cpu_baseline(w, q_h, k_h, v_h, do_h, args.cpu_budget)
