@@ -220,8 +220,8 @@ PSR_API size_t psr_ring_attn_bwd_workspace_bytes(const psr_shape* shape);
  *   timeout_ms: bound on every device wait (<= 0: 2000 ms); stream: a cudaStream_t.
  * All pointers 16-byte aligned.  Asynchronous: enqueues a workspace reset, the
  * D kernel, one persistent launch and the dQ rounding on `stream`; a device
- * timeout is reported by psr_get_stats.  Supported: d in {64, 128}; causal 0 or
- * 1 (PSR_CAUSAL_BALANCED: PSR_ERR_UNSUPPORTED); L = S/P a multiple of 128;
+ * timeout is reported by psr_get_stats.  Supported: d in {64, 128}; causal 0, 1 or
+ * PSR_CAUSAL_BALANCED; L = S/P a multiple of 128 (of 256 with PSR_CAUSAL_BALANCED);
  * Hq % Hkv == 0; sm_103 device. */
 PSR_API int psr_ring_attn_bwd(const psr_shape* shape, const void* q, const void* k, const void* v, const void* o,
                               const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,

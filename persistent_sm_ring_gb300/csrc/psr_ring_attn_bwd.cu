@@ -49,6 +49,7 @@ enum : uint32_t { SITE_KV = 21, SITE_Q_FULL = 22, SITE_Q_EMPTY = 23, SITE_S = 24
 
 struct BParams {
   int B, Hq, Hkv, S, P, L, gqa, causal;
+  int balanced;         // causal over load-balanced shards (shard r holds half-chunks r and 2P-1-r)
   int tiles_per_shard;  // L / 128
   int n_items_kv;       // B * Hkv * (S / 128)
   int n_items_q;        // B * Hq * (S / 128)
@@ -62,6 +63,20 @@ struct BParams {
   Ctrl* ctrl;
   unsigned long long timeout_ns;
 };
+
+// Global position (in 128-row tiles) of stored tile g, and its inverse.  Contiguous shards: g
+// itself.  Load-balanced shards: local tiles [0, T/2) of shard r are half-chunk r, local tiles
+// [T/2, T) half-chunk 2P-1-r (T = tiles per shard); positions rise inside a tile and a shard.
+__device__ __forceinline__ int tile_pos(const BParams& p, int g) {
+  if (!p.balanced) return g;
+  const int T = p.tiles_per_shard, h = T / 2, r = g / T, lt = g % T;
+  return lt < h ? r * h + lt : (2 * p.P - 1 - r) * h + (lt - h);
+}
+__device__ __forceinline__ int tile_at_pos(const BParams& p, int pos) {
+  if (!p.balanced) return pos;
+  const int T = p.tiles_per_shard, h = T / 2, c = pos / h, o = pos % h;
+  return c < p.P ? c * T + o : (2 * p.P - 1 - c) * T + h + o;
+}
 
 __host__ __device__ constexpr uint32_t idesc_ab(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
   return idesc_bf16_f32(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
@@ -125,7 +140,7 @@ struct KvItem {
 };
 __device__ inline KvItem kv_item_of(const BParams& p, int n) {
   KvItem it;
-  it.gk = n / (p.B * p.Hkv);  // the earliest K/V tiles have the most causal work: dispensed first
+  it.gk = tile_at_pos(p, n / (p.B * p.Hkv));  // the earliest positions have the most causal work: first
   const int rest = n % (p.B * p.Hkv);
   it.b = rest / p.Hkv;
   it.kvh = rest % p.Hkv;
@@ -133,19 +148,22 @@ __device__ inline KvItem kv_item_of(const BParams& p, int n) {
 }
 
 // The item's (query head, query tile) pairs in ring order: shard j of the K/V tile first, then
-// j+1, j+2, ... (mod P); under the causal mask only query tiles at or after the K/V tile.
+// j+1, j+2, ... (mod P); under the causal mask only query tiles at or after the K/V tile's
+// position (with contiguous shards no tile of a shard before j qualifies).
 template <class F>
 __device__ __forceinline__ void for_each_q(const BParams& p, const KvItem& it, F&& f) {
   const int j = it.gk / p.tiles_per_shard;
+  const int kpos = tile_pos(p, it.gk);
   for (int t = 0; t < p.P; ++t) {
     const int r = (j + t) % p.P;
-    if (p.causal && r < j) continue;
+    if (p.causal && !p.balanced && r < j) continue;
     for (int h = 0; h < p.gqa; ++h) {
       const int hq = it.kvh * p.gqa + h;
       for (int qt = 0; qt < p.tiles_per_shard; ++qt) {
         const int gq = r * p.tiles_per_shard + qt;
-        if (p.causal && gq < it.gk) continue;
-        if (!f(hq, gq, p.causal && gq == it.gk)) return;
+        const int qpos = tile_pos(p, gq);
+        if (p.causal && qpos < kpos) continue;
+        if (!f(hq, gq, p.causal && qpos == kpos)) return;
       }
     }
   }
@@ -450,7 +468,8 @@ struct QItem {
 __device__ inline QItem q_item_of(const BParams& p, int n) {
   QItem it;
   const int per = p.B * p.Hq;
-  it.gq = (p.causal ? (p.S / kRows - 1 - n / per) : n / per);  // causal: the last query tiles (most keys) first
+  // causal: the last query positions (most keys) first
+  it.gq = tile_at_pos(p, p.causal ? (p.S / kRows - 1 - n / per) : n / per);
   const int rest = n % per;
   it.b = rest / p.Hq;
   it.hq = rest % p.Hq;
@@ -458,17 +477,20 @@ __device__ inline QItem q_item_of(const BParams& p, int n) {
 }
 
 // The item's K/V tiles in the forward's ring order: the query shard r's own chunk first, then
-// r-1, r-2, ... (mod P); under the causal mask only K/V tiles at or before the query tile.
+// r-1, r-2, ... (mod P); under the causal mask only K/V tiles at or before the query tile's
+// position.
 template <class F>
 __device__ __forceinline__ void for_each_kv(const BParams& p, const QItem& it, F&& f) {
   const int r = it.gq / p.tiles_per_shard;
+  const int qpos = tile_pos(p, it.gq);
   for (int t = 0; t < p.P; ++t) {
     const int j = ((r - t) % p.P + p.P) % p.P;
-    if (p.causal && j > r) continue;
+    if (p.causal && !p.balanced && j > r) continue;
     for (int kt = 0; kt < p.tiles_per_shard; ++kt) {
       const int gk = j * p.tiles_per_shard + kt;
-      if (p.causal && gk > it.gq) continue;
-      if (!f(gk, p.causal && gk == it.gq)) return;
+      const int kpos = tile_pos(p, gk);
+      if (p.causal && kpos > qpos) continue;
+      if (!f(gk, p.causal && kpos == qpos)) return;
     }
   }
 }
@@ -752,9 +774,9 @@ static int check_shape(const psr_shape* sh) {
   if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->P < 1) return PSR_ERR_ARG;
   if (sh->causal < 0 || sh->causal > PSR_CAUSAL_BALANCED) return PSR_ERR_ARG;
   if (!(sh->scale == sh->scale)) return PSR_ERR_ARG;
-  if (sh->causal == PSR_CAUSAL_BALANCED) return PSR_ERR_UNSUPPORTED;
   if (sh->d != 64 && sh->d != 128) return PSR_ERR_UNSUPPORTED;
   if (sh->Hq % sh->Hkv != 0 || sh->S % sh->P != 0 || (sh->S / sh->P) % kRows != 0) return PSR_ERR_UNSUPPORTED;
+  if (sh->causal == PSR_CAUSAL_BALANCED && (sh->S / sh->P) % (2 * kRows) != 0) return PSR_ERR_UNSUPPORTED;
   const long long rows = (long long)sh->B * sh->Hq * sh->S;
   if (rows >= (1LL << 31) || rows * sh->d >= (1LL << 40)) return PSR_ERR_UNSUPPORTED;
   if ((long long)sh->B * sh->Hq * (sh->S / kRows) >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
@@ -825,7 +847,8 @@ int psr_ring_attn_bwd(const psr_shape* sh, const void* q, const void* k, const v
   kp.B = sh->B; kp.Hq = sh->Hq; kp.Hkv = sh->Hkv; kp.S = sh->S; kp.P = sh->P;
   kp.L = sh->S / sh->P;
   kp.gqa = sh->Hq / sh->Hkv;
-  kp.causal = sh->causal;
+  kp.causal = sh->causal ? 1 : 0;
+  kp.balanced = sh->causal == PSR_CAUSAL_BALANCED ? 1 : 0;
   kp.tiles_per_shard = kp.L / kRows;
   kp.n_items_kv = sh->B * sh->Hkv * (sh->S / kRows);
   kp.n_items_q = sh->B * sh->Hq * (sh->S / kRows);

@@ -90,3 +90,26 @@ def test_bwd_full_size_sampled_rows(psr):
     kr = np.unique(np.concatenate([[0, 127, 128, w.S - 1, w.S], rng.choice(w.B * w.Hkv * w.S, 60, replace=False)]))
     rq, rk, rv = ob.attn_bwd_rows(q, k, v, do, causal=True, scale=w.scale, bh_rows=qr, kv_rows=kr)
     check(w.name, (dq.reshape(-1, w.d)[qr], dk.reshape(-1, w.d)[kr], dv.reshape(-1, w.d)[kr]), (rq, rk, rv))
+
+
+def _balanced_order(S, P):
+    """Natural position held by each stored row: shard r holds half-chunks r and 2P-1-r."""
+    h = S // P // 2
+    return np.concatenate([np.arange(c * h, (c + 1) * h) for r in range(P) for c in (r, 2 * P - 1 - r)])
+
+
+@pytest.mark.parametrize("w", [BASE.with_(name="bwd_cb_d64", S=2048, P=4, causal=2, seed=98),
+                               BASE.with_(name="bwd_cb_gqa_d128", B=1, Hq=4, Hkv=2, S=4096, P=4, d=128, causal=2,
+                                          seed=99)], ids=lambda w: w.name)
+def test_bwd_balanced_shards(psr, w):
+    # the sequence stored in balanced shard order: the reference is the pinned oracle's causal
+    # gradient of the same sequence in natural order, re-ordered the same way
+    q, k, v = ri.generate(w)
+    do = ri.generate_dout(w)
+    pos = _balanced_order(w.S, w.P)  # stored row i holds natural row pos[i]
+    nat = lambda a: a[:, :, np.argsort(pos)]
+    rq, rk, rv = ob.attn_bwd(nat(q), nat(k), nat(v), nat(do), causal=True, scale=w.scale)
+    ref = tuple(g[:, :, pos] for g in (rq, rk, rv))
+    dq, dk, dv, st = run_bwd(psr, w, q, k, v, do)
+    assert st["status"] == 0, st
+    check(w.name, (dq, dk, dv), ref)
