@@ -55,8 +55,8 @@ struct BParams {
   int n_items_q;        // B * Hq * (S / 128)
   float sl2;            // scale * log2(e)
   float scale;
-  const float* lse;     // [B][Hq][S] natural-log LSE of the forward
-  const float* delta;   // [B][Hq][S] D = rowsum(dO * O)
+  const float* nlse2;   // [B][Hq][S] -LSE * log2(e) (LSE: the forward's natural-log log-sum-exp)
+  const float* ndelta;  // [B][Hq][S] -D = -rowsum(dO * O)
   uint16_t* dq;         // [B][Hq][S][d] bf16
   uint16_t* dk;         // [B][Hkv][S][d] bf16
   uint16_t* dv;
@@ -94,6 +94,11 @@ __device__ __forceinline__ void unpack_bf16x2(uint32_t v, float& lo, float& hi) 
   lo = __uint_as_float(v << 16);
   hi = __uint_as_float(v & 0xFFFF0000u);
 }
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // The two elementwise warpgroups (warps 4..11) meet here before either overwrites fp32 columns
 // that the other still reads: an mbarrier with bounded waits (a plain bar.sync would wait
@@ -122,7 +127,7 @@ struct KvCfg {
   static constexpr int OFF_K = 0, OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;      // + qb * TILE
   static constexpr int OFF_DO = 4 * TILE;     // + qb * TILE
-  static constexpr int OFF_LD = 6 * TILE;     // + qb * 1024: LSE[128] then D[128] (fp32)
+  static constexpr int OFF_LD = 6 * TILE;     // + qb * 1024: -LSE*log2(e)[128] then -D[128] (fp32)
   static constexpr int SMEM = 1024 + OFF_LD + 2 * 1024;
   static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
   static_assert(SMEM <= 232448 - 1024, "shared memory");
@@ -191,8 +196,8 @@ __device__ void kv_producer(const BParams& p, KvSmem* sc, uint32_t sbase, const 
       tma_load_2d(sbase + C::OFF_Q + qb * C::TILE + h * 16384, tq, 64 * h, q_row, &sc->q_full[qb]);
       tma_load_2d(sbase + C::OFF_DO + qb * C::TILE + h * 16384, tdo, 64 * h, q_row, &sc->q_full[qb]);
     }
-    bulk_load(ld, p.lse + q_row, 512, &sc->q_full[qb]);
-    bulk_load(ld + 512, p.delta + q_row, 512, &sc->q_full[qb]);
+    bulk_load(ld, p.nlse2 + q_row, 512, &sc->q_full[qb]);
+    bulk_load(ld + 512, p.ndelta + q_row, 512, &sc->q_full[qb]);
     ++qcnt;
     return true;
   });
@@ -267,13 +272,15 @@ __device__ void kv_elementwise(const BParams& p, KvSmem* sc, const uint8_t* smem
   const uint32_t lanes = sc->tmem_base + ((uint32_t)(quarter * 32) << 16);
   bool ok = true;
   for_each_q(p, it, [&](int, int, bool diag) -> bool {
-    const float* lse_s = reinterpret_cast<const float*>(smem + C::OFF_LD + (jg % 2) * 1024) + 64 * w;
-    const float* d_s = lse_s + 128;
+    // -LSE*log2(e) and -D of this warpgroup's 64 query columns, as fp32 pairs
+    const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(smem + C::OFF_LD + (jg % 2) * 1024) + 32 * w;
+    const uint64_t* nd2 = nl2 + 64;
     ok = __all_sync(0xffffffffu, wait_bar(&sc->q_full[jg % 2], (jg / 2) & 1u, p, sc, SITE_Q_FULL));
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(&sc->s_full, jg & 1u, p, sc, SITE_S));
     if (!ok) return false;
     tc_fence_after();
     uint32_t pk[32];  // P^T of this row over the warpgroup's 64 query columns, bf16 pairs
+    const uint64_t sl2 = f2_pack(p.sl2, p.sl2);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       uint32_t s[32];
@@ -281,12 +288,18 @@ __device__ void kv_elementwise(const BParams& p, KvSmem* sc, const uint8_t* smem
       tmem_ld_wait();
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
-        const int col = 64 * w + 32 * c + e;  // query row of the tile
-        float p0 = ex2_approx(__uint_as_float(s[e]) * p.sl2 - lse_s[32 * c + e] * kLog2e);
-        float p1 = ex2_approx(__uint_as_float(s[e + 1]) * p.sl2 - lse_s[32 * c + e + 1] * kLog2e);
-        if (diag && col < row) p0 = 0.0f;       // key after query: masked
-        if (diag && col + 1 < row) p1 = 0.0f;
-        pk[16 * c + e / 2] = pack_bf16x2(p0, p1);
+        // log2-domain exponent of the pair: s * scale * log2(e) - LSE * log2(e)
+        float x0, x1;
+        f2_unpack(fma2(f2_pack(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2, nl2[16 * c + e / 2]), x0, x1);
+        pk[16 * c + e / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+      }
+      if (diag) {  // diagonal tile: keys after the query are masked (query column < key row)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = 64 * w + 32 * c + e;
+          if (col + 1 < row) pk[16 * c + e / 2] = 0u;
+          else if (col < row) pk[16 * c + e / 2] &= 0xFFFF0000u;
+        }
       }
     }
     // both warpgroups have read their fp32 columns; the bf16 P^T (query q at column q/2) may
@@ -309,10 +322,13 @@ __device__ void kv_elementwise(const BParams& p, KvSmem* sc, const uint8_t* smem
       tmem_ld_wait();
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
-        float p0, p1;
+        float p0, p1, d0, d1;
         unpack_bf16x2(pk[16 * c + e / 2], p0, p1);
-        ds[16 * c + e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - d_s[32 * c + e]),
-                                         p1 * (__uint_as_float(dp[e + 1]) - d_s[32 * c + e + 1]));
+        // dS = P (dP - D) for the pair
+        f2_unpack(mul2(f2_pack(p0, p1), add2(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                             nd2[16 * c + e / 2])),
+                  d0, d1);
+        ds[16 * c + e / 2] = pack_bf16x2(d0, d1);
       }
     }
     if (!wg_meet(&sc->wg_sync, meet, p, sc)) { ok = false; return false; }
@@ -586,8 +602,8 @@ __device__ void q_elementwise(const BParams& p, QSmem* sc, const QItem& it, uint
   const int row = quarter * 32 + lane;  // query row of the tile
   const uint32_t lanes = sc->tmem_base + ((uint32_t)(quarter * 32) << 16);
   const size_t qrow = (size_t)(it.b * p.Hq + it.hq) * p.S + (size_t)it.gq * kRows + row;
-  const float lse2 = p.lse[qrow] * kLog2e;
-  const float dlt = p.delta[qrow];
+  const float nlse2 = p.nlse2[qrow];  // -LSE * log2(e) of this query row
+  const float ndlt = p.ndelta[qrow];  // -D
   bool ok = true;
   for_each_kv(p, it, [&](int, bool diag) -> bool {
     ok = __all_sync(0xffffffffu, wait_bar(&sc->s_full[jg % 2], (jg / 2) & 1u, p, sc, SITE_S));
@@ -600,10 +616,11 @@ __device__ void q_elementwise(const BParams& p, QSmem* sc, const QItem& it, uint
       tmem_ld32(lanes + C::COL_S + (jg % 2) * 128 + 64 * w + 32 * c, s);
       tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int col = 64 * w + 32 * c + e;  // key row of the K/V tile
-        const float x = ex2_approx(__uint_as_float(s[e]) * p.sl2 - lse2);
-        pv[32 * c + e] = (diag && col > row) ? 0.0f : x;
+      for (int e = 0; e < 32; ++e) pv[32 * c + e] = ex2_approx(fmaf(__uint_as_float(s[e]), p.sl2, nlse2));
+      if (diag) {  // diagonal tile: keys after the query are masked (key column > query row)
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (64 * w + 32 * c + e > row) pv[32 * c + e] = 0.0f;
       }
     }
     ok = __all_sync(0xffffffffu, wait_bar(&sc->dp_full, jg & 1u, p, sc, SITE_DP));
@@ -615,10 +632,15 @@ __device__ void q_elementwise(const BParams& p, QSmem* sc, const QItem& it, uint
       uint32_t dp[32];
       tmem_ld32(lanes + C::COL_DP + 64 * w + 32 * c, dp);
       tmem_ld_wait();
+      const uint64_t nd2 = f2_pack(ndlt, ndlt);
 #pragma unroll
-      for (int e = 0; e < 32; e += 2)
-        ds[16 * c + e / 2] = pack_bf16x2(pv[32 * c + e] * (__uint_as_float(dp[e]) - dlt),
-                                         pv[32 * c + e + 1] * (__uint_as_float(dp[e + 1]) - dlt));
+      for (int e = 0; e < 32; e += 2) {
+        float d0, d1;
+        f2_unpack(mul2(f2_pack(pv[32 * c + e], pv[32 * c + e + 1]),
+                       add2(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2)),
+                  d0, d1);
+        ds[16 * c + e / 2] = pack_bf16x2(d0, d1);
+      }
     }
     // both warpgroups have read their fp32 dP columns; dS (key k at column k/2) may now
     // overwrite the lower half of them
@@ -738,9 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(sc.tmem_base, 512);
 }
 
-// D = rowsum(dO * O) in fp32, one warp per row
+// -D = -rowsum(dO * O) in fp32 (one warp per row), and -LSE * log2(e)
 template <int D>
-__global__ void delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout, float* __restrict__ delta,
+__global__ void delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                             const float* __restrict__ lse, float* __restrict__ ndelta, float* __restrict__ nlse2,
                              long long rows) {
   const int lane = threadIdx.x % 32;
   const long long warps = (long long)gridDim.x * (blockDim.x / 32);
@@ -755,7 +778,10 @@ __global__ void delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __r
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) delta[r] = s;
+    if (lane == 0) {
+      ndelta[r] = -s;
+      nlse2[r] = -lse[r] * kLog2e;
+    }
   }
 }
 
@@ -764,7 +790,7 @@ __global__ void delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __r
 // Host side
 // ------------------------------------------------------------------------------------------------
 struct BLayout {
-  size_t ctrl, delta, total;
+  size_t ctrl, delta, nlse2, total;
 };
 
 static size_t au(size_t x) { return (x + 255) / 256 * 256; }
@@ -790,6 +816,7 @@ static BLayout layout(const psr_shape* sh) {
   l.ctrl = off; off += 256;
   off = au(off + (size_t)kTrajMax * 8);  // the shared workspace prefix (stats and trajectory)
   l.delta = off; off = au(off + rows * 4);
+  l.nlse2 = off; off = au(off + rows * 4);
   l.total = off;
   return l;
 }
@@ -855,8 +882,8 @@ int psr_ring_attn_bwd(const psr_shape* sh, const void* q, const void* k, const v
   const float scale = sh->scale > 0.0f ? sh->scale : 1.0f / std::sqrt((float)sh->d);
   kp.scale = scale;
   kp.sl2 = scale * kLog2e;
-  kp.lse = lse;
-  kp.delta = reinterpret_cast<const float*>(ws + L.delta);
+  kp.nlse2 = reinterpret_cast<const float*>(ws + L.nlse2);
+  kp.ndelta = reinterpret_cast<const float*>(ws + L.delta);
   kp.dq = static_cast<uint16_t*>(dq);
   kp.dk = static_cast<uint16_t*>(dk);
   kp.dv = static_cast<uint16_t*>(dv);
@@ -875,11 +902,13 @@ int psr_ring_attn_bwd(const psr_shape* sh, const void* q, const void* k, const v
   if (cudaMemsetAsync(ws, 0, L.delta, st) != cudaSuccess) return PSR_ERR_CUDA;  // control block and log
   const int dgrid = n_cta * 8;
   if (sh->d == 128)
-    delta_kernel<128><<<dgrid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                            reinterpret_cast<float*>(ws + L.delta), rows_q);
+    delta_kernel<128><<<dgrid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
+                                            reinterpret_cast<float*>(ws + L.delta),
+                                            reinterpret_cast<float*>(ws + L.nlse2), rows_q);
   else
-    delta_kernel<64><<<dgrid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                           reinterpret_cast<float*>(ws + L.delta), rows_q);
+    delta_kernel<64><<<dgrid, 256, 0, st>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
+                                           reinterpret_cast<float*>(ws + L.delta),
+                                           reinterpret_cast<float*>(ws + L.nlse2), rows_q);
   if (cudaGetLastError() != cudaSuccess) return PSR_ERR_CUDA;
   cudaError_t e = sh->d == 128 ? launch_bwd<128>(kp, maps, n_cta, st) : launch_bwd<64>(kp, maps, n_cta, st);
   if (e != cudaSuccess) {
