@@ -23,7 +23,9 @@
 // ~1.6 TB/s and bounded the whole pass, 2x slower than recomputing.  In each kernel one thread
 // issues every MMA; tensor-core instructions of one thread run in order, so an MMA that
 // overwrites columns another MMA reads is simply issued after it.  Two warpgroups share the
-// elementwise work, each on half of the columns.
+// elementwise work, each on half of the columns, and each writes its bf16 results over its own
+// fp32 columns (the MMAs take the operand from the two column ranges), so they never wait for
+// each other.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -45,7 +47,7 @@ constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : uint32_t { SITE_KV = 21, SITE_Q_FULL = 22, SITE_Q_EMPTY = 23, SITE_S = 24, SITE_DP = 25, SITE_P = 26,
-                  SITE_DS = 27, SITE_WG = 28, SITE_ACC = 29, SITE_KV_EMPTY = 30 };
+                  SITE_DS = 27, SITE_ACC = 29, SITE_KV_EMPTY = 30 };
 
 struct BParams {
   int B, Hq, Hkv, S, P, L, gqa, causal;
@@ -90,6 +92,11 @@ __device__ __forceinline__ uint32_t kmaj_lo(uint32_t tile, int kk) {
 }
 __device__ __forceinline__ uint32_t mnmaj_lo(uint32_t tile, int kk) { return sdesc_lo(tile + kk * 2048, 16384); }
 
+// TMEM column of the bf16 A operand (P^T, dS^T or dS) for the 16-element K step kk: warpgroup w
+// writes its 64 elements as 32 bf16 pairs into the low half of its own 64 fp32 columns
+// [64w, 64w + 64), so neither warpgroup overwrites columns the other still reads.
+__device__ __forceinline__ uint32_t bf16_col(int kk) { return (kk / 4) * 64 + (kk % 4) * 8; }
+
 __device__ __forceinline__ void unpack_bf16x2(uint32_t v, float& lo, float& hi) {
   lo = __uint_as_float(v << 16);
   hi = __uint_as_float(v & 0xFFFF0000u);
@@ -98,24 +105,6 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
-}
-
-// The two elementwise warpgroups (warps 4..11) meet here before either overwrites fp32 columns
-// that the other still reads: an mbarrier with bounded waits (a plain bar.sync would wait
-// forever if the other warpgroup had left on a timeout).
-template <class KP, class SC>
-__device__ __forceinline__ bool wg_meet(uint64_t* bar, uint32_t& phase, const KP& p, SC* sc) {
-  __syncwarp();
-  if ((threadIdx.x % 32) == 0) mbar_arrive(bar);
-  const bool ok = __all_sync(0xffffffffu, wait_bar(bar, phase & 1u, p, sc, SITE_WG));
-  ++phase;
-  return ok;
-}
-
-// Store 64 bf16 values (32 pairs) of this thread's row to global memory.
-__device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t* w) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
 }
 
 // ================================================================================================
@@ -134,7 +123,7 @@ struct KvCfg {
 };
 
 struct KvSmem {
-  uint64_t kv_full, q_full[2], q_empty[2], s_full, dp_full, p_ready, ds_ready, wg_sync, acc_full, drain;
+  uint64_t kv_full, q_full[2], q_empty[2], s_full, dp_full, p_ready, ds_ready, acc_full, drain;
   uint32_t tmem_base;
   int arg;
   volatile uint32_t abort;
@@ -242,13 +231,13 @@ __device__ void kv_mma(const BParams& p, KvSmem* sc, uint32_t sbase, const KvIte
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk)
-      mma_ts_w(tm + C::COL_DV, tm + C::COL_S + kk * 8, mnmaj_lo(sDO, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
+      mma_ts_w(tm + C::COL_DV, tm + C::COL_S + bf16_col(kk), mnmaj_lo(sDO, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
     if (i + 1 < n_pairs && !issue_s(qcnt + 1)) return false;
     if (!wait_bar(&sc->ds_ready, jg & 1u, p, sc, SITE_DS)) return false;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk)
-      mma_ts_w(tm + C::COL_DK, tm + C::COL_DP + kk * 8, mnmaj_lo(sQ, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
+      mma_ts_w(tm + C::COL_DK, tm + C::COL_DP + bf16_col(kk), mnmaj_lo(sQ, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
     mma_commit(&sc->q_empty[qb]);  // Q, dO of this tile are read (LSE, D: the warpgroups are past them)
     ++qcnt;
     ++jg;
@@ -263,7 +252,7 @@ __device__ void kv_mma(const BParams& p, KvSmem* sc, uint32_t sbase, const KvIte
 // columns [64w, 64w + 64).
 template <int D>
 __device__ void kv_elementwise(const BParams& p, KvSmem* sc, const uint8_t* smem, const KvItem& it, uint32_t items,
-                               uint32_t& jg, uint32_t& meet) {
+                               uint32_t& jg) {
   using C = KvCfg<D>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int w = warp >= 8 ? 1 : 0;
@@ -302,11 +291,9 @@ __device__ void kv_elementwise(const BParams& p, KvSmem* sc, const uint8_t* smem
         }
       }
     }
-    // both warpgroups have read their fp32 columns; the bf16 P^T (query q at column q/2) may
-    // now overwrite the lower half of the S^T columns
-    if (!wg_meet(&sc->wg_sync, meet, p, sc)) { ok = false; return false; }
-    tmem_st16(lanes + C::COL_S + 32 * w, pk);
-    tmem_st16(lanes + C::COL_S + 32 * w + 16, pk + 16);
+    // P^T as bf16 pairs over the low half of this warpgroup's own S^T columns
+    tmem_st16(lanes + C::COL_S + 64 * w, pk);
+    tmem_st16(lanes + C::COL_S + 64 * w + 16, pk + 16);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -331,9 +318,9 @@ __device__ void kv_elementwise(const BParams& p, KvSmem* sc, const uint8_t* smem
         ds[16 * c + e / 2] = pack_bf16x2(d0, d1);
       }
     }
-    if (!wg_meet(&sc->wg_sync, meet, p, sc)) { ok = false; return false; }
-    tmem_st16(lanes + C::COL_DP + 32 * w, ds);
-    tmem_st16(lanes + C::COL_DP + 32 * w + 16, ds + 16);
+    // dS^T as bf16 pairs over the low half of this warpgroup's own dP^T columns
+    tmem_st16(lanes + C::COL_DP + 64 * w, ds);
+    tmem_st16(lanes + C::COL_DP + 64 * w + 16, ds + 16);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -387,7 +374,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sc.dp_full, 1);
     mbar_init(&sc.p_ready, 8);   // the eight warps of the two elementwise warpgroups
     mbar_init(&sc.ds_ready, 8);
-    mbar_init(&sc.wg_sync, 8);
     mbar_init(&sc.acc_full, 1);
     mbar_init(&sc.drain, 1);
     sc.abort = 0;
@@ -404,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  uint32_t items = 0, qcnt_p = 0, qcnt_m = 0, jg_m = 0, jg_e = 0, meet = 0;
+  uint32_t items = 0, qcnt_p = 0, qcnt_m = 0, jg_m = 0, jg_e = 0;
   while (true) {
     if (threadIdx.x == 0) {
       int n = -1;
@@ -423,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && lane == 0) {
       kv_mma<D>(p, &sc, sbase, it, items, qcnt_m, jg_m);
     } else if (warp >= 4) {
-      kv_elementwise<D>(p, &sc, smem, it, items, jg_e, meet);
+      kv_elementwise<D>(p, &sc, smem, it, items, jg_e);
     }
     tc_fence_before();
     __syncthreads();
@@ -472,7 +458,7 @@ struct QCfg {
 };
 
 struct QSmem {
-  uint64_t qd_full, kv_full[2], kv_empty[2], s_full[2], dp_full, ds_ready, wg_sync, acc_full, drain;
+  uint64_t qd_full, kv_full[2], kv_empty[2], s_full[2], dp_full, ds_ready, acc_full, drain;
   uint32_t tmem_base;
   int arg;
   volatile uint32_t abort;
@@ -579,7 +565,7 @@ __device__ void q_mma(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& 
     const uint32_t sK = k_of(kcnt);
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk)
-      mma_ts_w(tm + C::COL_DQ, tm + C::COL_DP + kk * 8, mnmaj_lo(sK, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
+      mma_ts_w(tm + C::COL_DQ, tm + C::COL_DP + bf16_col(kk), mnmaj_lo(sK, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
     mma_commit(&sc->kv_empty[kcnt % 2]);  // K, V of this tile are read
     if (i + 1 < n_kv) issue_dp(kcnt + 1);  // dP(j+1) over dS(j), after the dQ MMA has read it
     ++kcnt;
@@ -593,8 +579,7 @@ __device__ void q_mma(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& 
 
 // Warpgroup w: the query tile's rows on the lanes, K/V columns [64w, 64w + 64).
 template <int D>
-__device__ void q_elementwise(const BParams& p, QSmem* sc, const QItem& it, uint32_t items, uint32_t& jg,
-                              uint32_t& meet) {
+__device__ void q_elementwise(const BParams& p, QSmem* sc, const QItem& it, uint32_t items, uint32_t& jg) {
   using C = QCfg<D>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int w = warp >= 8 ? 1 : 0;
@@ -642,11 +627,9 @@ __device__ void q_elementwise(const BParams& p, QSmem* sc, const QItem& it, uint
         ds[16 * c + e / 2] = pack_bf16x2(d0, d1);
       }
     }
-    // both warpgroups have read their fp32 dP columns; dS (key k at column k/2) may now
-    // overwrite the lower half of them
-    if (!wg_meet(&sc->wg_sync, meet, p, sc)) { ok = false; return false; }
-    tmem_st16(lanes + C::COL_DP + 32 * w, ds);
-    tmem_st16(lanes + C::COL_DP + 32 * w + 16, ds + 16);
+    // dS as bf16 pairs over the low half of this warpgroup's own dP columns
+    tmem_st16(lanes + C::COL_DP + 64 * w, ds);
+    tmem_st16(lanes + C::COL_DP + 64 * w + 16, ds + 16);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -692,7 +675,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sc.dp_full, 1);
     mbar_init(&sc.ds_ready, 8);
-    mbar_init(&sc.wg_sync, 8);
     mbar_init(&sc.acc_full, 1);
     mbar_init(&sc.drain, 1);
     sc.abort = 0;
@@ -709,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  uint32_t items = 0, kcnt_p = 0, kcnt_m = 0, jg_m = 0, jg_e = 0, meet = 0;
+  uint32_t items = 0, kcnt_p = 0, kcnt_m = 0, jg_m = 0, jg_e = 0;
   while (true) {
     if (threadIdx.x == 0) {
       int n = -1;
@@ -728,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && lane == 0) {
       q_mma<D>(p, &sc, sbase, it, items, kcnt_m, jg_m);
     } else if (warp >= 4) {
-      q_elementwise<D>(p, &sc, it, items, jg_e, meet);
+      q_elementwise<D>(p, &sc, it, items, jg_e);
     }
     tc_fence_before();
     __syncthreads();
