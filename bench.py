@@ -826,7 +826,7 @@ def run_bwd(args):
     stream = torch.cuda.current_stream()
     passes = []
     clk = None
-    for name in ("h32_s32k_c", "h32_s32k_nc"):
+    for name in ("h32_s32k_c", "h32_s32k_nc", "h32_s32k_cb"):
         w = ri.WORKLOADS[name].with_(Hq=base.Hq, Hkv=base.Hkv)
         o, lse, _ = psr.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, scale=w.scale)
         dq, dk, dv, ws = psr.ring_attn_bwd(q, k, v, o, lse, do, P=w.P, causal=w.causal, scale=w.scale)
@@ -852,12 +852,37 @@ def run_bwd(args):
         if st["status"] != 0:
             raise RuntimeError(f"device status {st['status']} site {st['error_site']}")
         ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
-        passes.append({"workload": name, "causal": bool(w.causal), "ms": round(ms, 4),
+        passes.append({"workload": name, "causal": {0: False, 1: True, 2: "balanced shards"}[int(w.causal)],
+                       "ms": round(ms, 4),
                        "tflops": round(bwd_flops(w) / (ms / 1e3) / 1e12, 2),
                        "pct_peak": round(100 * bwd_flops(w) / (ms / 1e3) / 1e12 / peak, 2), "clocks": c})
     w = ri.WORKLOADS["h32_s32k_c"].with_(Hq=base.Hq, Hkv=base.Hkv)
     ms = passes[0]["ms"]
     value = bwd_flops(w) / (ms / 1e3) / 1e12
+
+    # e2e: pinned host Q, K, V, O, LSE, dO in and dQ, dK, dV out around the public call
+    o, lse, _ = psr.ring_attn_fwd(q, k, v, P=w.P, causal=True, scale=w.scale)
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, o, lse, do)]
+    dev_in = [torch.empty_like(t) for t in (q, k, v, o, lse, do)]
+    dq, dk, dv, ws = psr.ring_attn_bwd(q, k, v, o, lse, do, P=w.P, causal=True, scale=w.scale)
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in (dq, dk, dv)]
+
+    def e2e_step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        psr.ring_attn_bwd(*dev_in, P=w.P, causal=True, scale=w.scale, workspace=ws, dq=dq, dk=dk, dv=dv,
+                          stream=stream)
+        for h, d in zip(host_out, (dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize()
+
+    e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / 3
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
     cpu = None if args.no_cpu_baseline else bwd_cpu_baseline(w, q_h, k_h, v_h, do_h, args.cpu_budget)
     print(json.dumps({
         "metric": BWD_METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
@@ -870,6 +895,8 @@ def run_bwd(args):
                      "frac": round(value / peak, 4), "traffic": None,
                      "peak_source": f"{peaks.get('source')} bf16_tflops (burst)"},
         "cpu_baseline": cpu,
+        "e2e": {"value": round(bwd_flops(w) / e2e_s / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "passes": passes,

@@ -64,6 +64,7 @@ SMALL = [
     BASE.with_(name="bwd_gqa_c", B=2, Hq=4, Hkv=2, S=1024, P=2, d=128, causal=True, seed=94),
     BASE.with_(name="bwd_p1_nc_d128", S=512, P=1, d=128, seed=95),
     BASE.with_(name="bwd_p8_c", Hq=1, Hkv=1, S=2048, P=8, d=128, causal=True, seed=96),
+    BASE.with_(name="bwd_mqa_d64_l256", Hq=4, Hkv=1, S=2048, P=8, d=64, causal=True, seed=90, qmul=2.0, kmul=2.0),
 ]
 
 
