@@ -216,18 +216,19 @@ __device__ long long producer(const Params& p, Smem* sc, uint32_t smem_base, con
 }
 
 // One warpgroup per 128-row half of the tile: accumulator -> bf16 -> C_r.
-__device__ void epilogue(const Params& p, Smem* sc, const Item& it, int i, const Counters& cnt, bool& ok) {
+__device__ void epilogue(const Params& p, Smem* sc, uint8_t* smem, const Item& it, int i, const Counters& cnt,
+                         bool& ok) {
   const Geo& g = p.g;
-  const size_t grow0 = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + i * 128;
-  ok = read_tile(p, sc, i, cnt, SITE_ACC, [&](int row, int cb, const uint32_t(&v)[64]) {
-    uint16_t* crow = p.c + ((size_t)it.r * g.M + grow0 + row) * g.Ns + (size_t)it.nb * kBN;
-    uint4 o[8];
-    uint32_t* w = reinterpret_cast<uint32_t*>(o);
+  const int warp = threadIdx.x / 32;
+  const size_t grow0 = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + i * 128 + (warp % 4) * 32;
+  // the stage area is idle during the epilogue (every MMA of the tile has completed): 4 KiB per warp
+  uint8_t* stage = smem + (warp - 4) * 4096;
+  uint8_t* rows = reinterpret_cast<uint8_t*>(p.c + ((size_t)it.r * g.M + grow0) * g.Ns + (size_t)it.nb * kBN);
+  ok = read_tile(p, sc, i, cnt, SITE_ACC, [&](int, int cb, const uint32_t(&v)[64]) {
+    uint32_t w[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-    uint4* dst = reinterpret_cast<uint4*>(crow + cb * 64);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dst[e] = o[e];
+    warp_store_rows<32>(stage, w, rows + cb * 128, (size_t)g.Ns * 2);
   });
 }
 
@@ -280,18 +281,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cmd = sc.cmd, arg = sc.arg;
     if (cmd == CMD_EXIT) break;
     if (cmd == CMD_STAGE) {
-      if (threadIdx.x == 0) run_staging(p, &sc, smem_base, arg, stg_phase);
+      if (threadIdx.x == 0) {
+        fence_proxy_async_smem();  // the previous epilogue's generic stores to the copy buffers
+        run_staging(p, &sc, smem_base, arg, stg_phase);
+      }
     } else if (cmd == CMD_COMPUTE) {
       const Item it = item_of(p.g, arg);
       bool ok = true;
       if (warp == 0 && lane == 0) {
         Counters c2 = cnt;
+        fence_proxy_async_smem();  // the previous epilogue's generic stores to the stage area
         starved = producer(p, &sc, smem_base, it, &tm_a, &tm_g, &tm_w, c2, ok);
       } else if (warp == 1 && lane == 0) {
         Counters c2 = cnt;
         mma_tile(p, &sc, smem_base, p.g.K / kBK, c2, SITE_KV_FULL);
       } else if (warp >= 4) {
-        epilogue(p, &sc, it, warp < 8 ? 0 : 1, cnt, ok);
+        epilogue(p, &sc, smem_raw + (smem_base - smem_u32(smem_raw)), it, warp < 8 ? 0 : 1, cnt, ok);
       }
       cnt.fills += (uint32_t)(p.g.K / kBK);
       cnt.items++;

@@ -208,15 +208,15 @@ __device__ void run_reduce(const Params& p, Smem* sc, uint32_t smem_base, const 
 // ------------------------------------------------------------------------------------------------
 // Compute task: producer (TMA), MMA issuer (tcgen05), epilogue warpgroups -> fp32 partial tile
 // ------------------------------------------------------------------------------------------------
-__device__ void epilogue(const Params& p, Smem* sc, const Item& it, int i, const Counters& cnt) {
+__device__ void epilogue(const Params& p, Smem* sc, uint8_t* smem, const Item& it, int i, const Counters& cnt) {
   const Geo& g = p.g;
+  const int warp = threadIdx.x / 32;
   float* tile = p.part + ((size_t)it.r * g.n_out + it.o) * kTileElems + (size_t)i * 128 * kBN;
-  const bool ok = read_tile(p, sc, i, cnt, SITE_ACC, [&](int row, int cb, const uint32_t(&v)[64]) {
-    float4* dst = reinterpret_cast<float4*>(tile + (size_t)row * kBN + cb * 64);
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-      dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
-                           __uint_as_float(v[4 * e + 3]));
+  // the stage area is idle during the epilogue (every MMA of the tile has completed): 8 KiB per warp
+  uint8_t* stage = smem + (warp - 4) * 8192;
+  uint8_t* rows = reinterpret_cast<uint8_t*>(tile + (size_t)((warp % 4) * 32) * kBN);
+  const bool ok = read_tile(p, sc, i, cnt, SITE_ACC, [&](int, int cb, const uint32_t(&v)[64]) {
+    warp_store_rows<64>(stage, v, rows + cb * 256, (size_t)kBN * 4);
   });
   if (!ok) return;
   // this warp's 32 rows are written: publish them (each thread's stores before lane 0's release)
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Counters c2 = cnt;
         mma_tile(p, &sc, smem_base, n_k, c2, SITE_KV_FULL);
       } else if (warp >= 4) {
-        epilogue(p, &sc, it, warp < 8 ? 0 : 1, cnt);
+        epilogue(p, &sc, smem_raw + (smem_base - raw), it, warp < 8 ? 0 : 1, cnt);
       }
       cnt.fills += (uint32_t)n_k;
       cnt.items++;

@@ -120,6 +120,32 @@ __device__ __forceinline__ bool read_tile(const KP& p, Smem* sc, int i, const Co
   return true;
 }
 
+// Coalesced store of one 64-column block of a warp's 32 rows (the 32x32b tensor-memory load gives
+// each thread one row).  Each thread hands W 32-bit words of its row (W = 64: fp32; W = 32: bf16
+// pairs); the warp writes them into its shared-memory staging area (32 x 4W bytes) with the
+// 16-byte chunks XOR-swizzled by row, reads them back row-contiguous, and stores whole 4W-byte row
+// segments: 16 (fp32) or 8 (bf16) lanes per row instead of one lane per row.  Both shared-memory
+// passes are free of bank conflicts.  `gbase` is the byte address of the block in the warp's
+// first row, `stride` the row pitch in bytes.
+template <int W>
+__device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t* words, uint8_t* gbase, size_t stride) {
+  constexpr int R = W / 4;        // 16-byte chunks per row segment
+  constexpr int RPI = 32 / R;     // rows per read-back instruction
+  const int lane = threadIdx.x % 32;
+#pragma unroll
+  for (int j = 0; j < R; ++j)
+    *reinterpret_cast<uint4*>(stage + lane * (4 * W) + ((j ^ (lane % R)) * 16)) =
+        make_uint4(words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int r = k * RPI + lane / R, c = lane % R;
+    const uint4 v = *reinterpret_cast<const uint4*>(stage + r * (4 * W) + ((c ^ (r % R)) * 16));
+    *reinterpret_cast<uint4*>(gbase + (size_t)r * stride + c * 16) = v;
+  }
+  __syncwarp();  // the staging area is reused for the next block
+}
+
 // End of the kernel (all threads): every tcgen05 op has completed and every TMA load into
 // the stages has landed (bounded waits) before tensor memory is released.
 __device__ __forceinline__ void drain_and_release(Smem* sc, const Counters& cnt) {
