@@ -28,8 +28,6 @@ from __future__ import annotations
 
 import numpy as np
 
-LOG2E = 1.4426950408889634
-
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> float64, exactly."""

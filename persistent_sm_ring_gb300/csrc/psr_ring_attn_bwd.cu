@@ -20,7 +20,8 @@
 //
 // dQ could also be accumulated by the first kernel with atomic adds, saving the second
 // kernel's S and dP products; on GB300 those fp32 atomics (64 KiB per tile pair) ran at
-// ~1.6 TB/s and bounded the whole pass, 2x slower than recomputing.  In each kernel one thread
+// ~1.6 TB/s and bounded the whole pass (41 ms per causal B1 H32 S32768 pass, against 27.5 ms
+// with the second kernel).  In each kernel one thread
 // issues every MMA; tensor-core instructions of one thread run in order, so an MMA that
 // overwrites columns another MMA reads is simply issued after it.  Two warpgroups share the
 // elementwise work, each on half of the columns, and each writes its bf16 results over its own
