@@ -1,7 +1,7 @@
 // Control block, partition controller and bounded waits shared by the persistent kernels
 // (Ring Attention, AllGather+GEMM).  A kernel's parameter struct provides: ctrl, traj,
-// timeout_ns, mode, n_s_init, n_stage_total, n_tiles_total, c_s0, c_p0, n_min, n_max; its
-// shared control struct provides a volatile `abort` word.
+// timeout_ns, mode, n_s_init, n_stage_total, n_tiles_total, c_s0, c_p0, n_min, n_max,
+// n_wave_items, n_wave_cap; its shared control struct provides a volatile `abort` word.
 #pragma once
 #include <cstdint>
 
@@ -113,6 +113,15 @@ constexpr double kStarveWeight = PSR_STARVE_WEIGHT / 100.0;
 #endif
 constexpr double kUpdateHeadroom = PSR_UPDATE_HEADROOM / 100.0;  // staging headroom in the updates
 
+#ifndef PSR_WAVE_MARGIN
+#define PSR_WAVE_MARGIN 110
+#endif
+// Staging capacity (over the balanced split) that the wave cap keeps: the cap is the largest
+// split with the compute waves of the rule's split at this headroom.
+constexpr double kWaveMargin = PSR_WAVE_MARGIN / 100.0;
+// Shortest ring step (KV tiles) for which the wave cap is applied.
+constexpr int kWaveMinTiles = 8;
+
 // The initial split stands until this fraction of the compute tiles is done: it covers the
 // ring's fill, when every active group needs its first staged steps at once and measured
 // costs are still dominated by start-up.
@@ -141,6 +150,9 @@ __device__ void controller_update(const KP& p) {
   const double C_s = (scy + kStarveWeight * (double)sv + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
   const double C_p = (ccy + (double)p.c_p0 * 64.0) / ((double)td + 64.0);
   int n = controller_rule((int)gridDim.x, R_s, kUpdateHeadroom * C_s, R_p, C_p, p.n_min, p.n_max);
+  // equal-length compute items: the launch's wave cap holds while items remain unclaimed (a
+  // CTA taken from compute then delays one of its items to an extra wave)
+  if (n > p.n_wave_cap && ld_relaxed(&c->item_next) < p.n_wave_items) n = p.n_wave_cap;
   const int cur = current_target(p);
   // hysteresis (move only by a margin unless the staging work is finished) and a rate
   // limit (each evaluation moves the target by at most max(2, cur/8) CTAs): a CTA changes

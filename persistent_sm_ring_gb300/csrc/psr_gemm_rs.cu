@@ -68,6 +68,8 @@ struct Params {
   unsigned long long timeout_ns;
   unsigned long long n_tiles_total, n_stage_total;
   int mode, n_s_init, n_min, n_max, fault;
+  uint32_t n_wave_items;  // no wave cap here (0): the tasks' waves are many and short
+  int n_wave_cap;
   float c_s0, c_p0;
 };
 

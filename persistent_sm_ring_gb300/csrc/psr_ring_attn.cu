@@ -117,6 +117,8 @@ struct KParams {
   int mode;           // PSR_STATIC / PSR_ADAPTIVE
   int n_s_init;
   int n_min, n_max;   // effective clamp
+  uint32_t n_wave_items;  // items under the wave cap (0: none)
+  int n_wave_cap;     // adaptive target bound while items remain unclaimed
   int fault;
   int lookahead;      // static list: groups ahead of the dispense frontier
   int ctrl_period;    // tasks between controller evaluations
@@ -1346,6 +1348,24 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
     else {
       if (n_s < n_min) n_s = n_min;
       if (n_s > n_max) n_s = n_max;
+    }
+    // Equal-length items (no causal mask, single CTAs), staging paced by compute (steps
+    // beyond the static list) and ring steps of at least kWaveMinTiles KV tiles: cap the
+    // target at the largest split with the compute waves of the rule's split at the wave
+    // margin, for the initial split and for every update while items remain unclaimed.  The
+    // compute CTAs of the first wave fix the wave structure of the launch, so the cap has to
+    // hold from the start.  With shorter steps an item's time is bound by the latency of its
+    // ring steps and grows as staging capacity shrinks, so item time is not a constant and
+    // the cap is not applied.
+    if (any_staging && !G.causal && cg == 1 && kp.n_dyn > 0 && pt.n_staging <= 0 && G.kv_tiles >= kWaveMinTiles) {
+      const int n_need = controller_rule(n_cta, (double)kp.n_stage_total, kWaveMargin * kp.c_s0,
+                                         (double)kp.n_tiles_total, kp.c_p0, n_min, n_max);
+      const int cap = wave_cap(n_cta, n_need, G.n_items);
+      if (cap < n_max) {
+        kp.n_wave_items = (uint32_t)G.n_items;
+        kp.n_wave_cap = cap < n_min ? n_min : cap;
+        if (n_s > kp.n_wave_cap) n_s = kp.n_wave_cap;
+      }
     }
   }
   kp.n_s_init = n_s;

@@ -294,4 +294,19 @@ PSR_HD int controller_rule(int n_cta, double R_s, double C_s, double R_p, double
   return n;
 }
 
+// Compute waves.  When every compute item takes the same time (non-causal attention), the
+// compute role finishes in ceil(U / (N - n)) waves of whole items for U items and n staging
+// CTAs, so compute time is flat between wave boundaries and jumps by one item at each
+// boundary.  Given the smallest split n_need that still gives staging its capacity, the
+// largest split with the same number of waves is
+//   N - ceil(U / w),  w = ceil(U / (N - n_need)):
+// any split up to it costs the compute role nothing, one above it costs a whole item.
+// Returns n_cta (no cap) when there is nothing to cap.
+PSR_HD int wave_cap(int n_cta, int n_need, long long U) {
+  if (U <= 0 || n_need < 0 || n_need >= n_cta) return n_cta;
+  const long long nc = n_cta - n_need;
+  const long long w = (U + nc - 1) / nc;
+  return n_cta - (int)((U + w - 1) / w);
+}
+
 }  // namespace psr

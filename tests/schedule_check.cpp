@@ -11,11 +11,13 @@
 //  * flag / consumed indices stay below n_groups * P and the dynamic queue
 //    receives exactly dynamic_staging_tasks() pushes;
 //  * total_tiles(), total_staging_tasks() and the piece counts agree with direct enumeration.
+// Usage: schedule_check wave   -> checks the controller's wave cap against enumeration.
 // Usage: schedule_check B Hq Hkv S P d causal max_group [cg]   -> prints "OK ..." or "FAIL ..."
 // (causal: 0, 1, or 2 = load-balanced shards; cg: CTAs per compute unit, 1 or 2; default 1)
 #include <cstdio>
 #include <algorithm>
 #include <cstdlib>
+#include <string>
 #include <vector>
 
 #include "../persistent_sm_ring_gb300/csrc/psr_schedule.h"
@@ -40,7 +42,27 @@ static long long pos_of(const Geometry& G, int r, long long i) {
     }                                 \
   } while (0)
 
+// wave_cap against its definition by enumeration: the largest split n in [n_need, N-1] whose
+// compute waves ceil(U / (N - n)) equal those of n_need.
+static int check_wave_cap() {
+  for (int N = 2; N <= 160; N += (N < 20 ? 1 : 7))
+    for (int need = 0; need < N; ++need)
+      for (long long U = 1; U <= 5000; U += (U < 300 ? 1 : 37)) {
+        auto waves = [&](int n) { return (U + (N - n) - 1) / (N - n); };
+        int best = need;
+        for (int n = need; n < N; ++n)
+          if (waves(n) == waves(need)) best = n;
+        const int cap = wave_cap(N, need, U);
+        CHECK(cap == best, "wave_cap N=%d need=%d U=%lld: %d, enumeration %d", N, need, U, cap, best);
+      }
+  CHECK(wave_cap(152, 20, 0) == 152 && wave_cap(152, 152, 100) == 152, "wave_cap without a cap");
+  CHECK(wave_cap(152, 21, 1024) == 24 && wave_cap(152, 41, 1024) == 49, "wave_cap examples");
+  std::printf("OK wave_cap\n");
+  return 0;
+}
+
 int main(int argc, char** argv) {
+  if (argc == 2 && std::string(argv[1]) == "wave") return check_wave_cap();
   if (argc != 9 && argc != 10) return 2;
   int a[9] = {0, 0, 0, 0, 0, 0, 0, 0, 1};
   for (int i = 0; i < argc - 1; ++i) a[i] = std::atoi(argv[i + 1]);

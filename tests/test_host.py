@@ -129,6 +129,11 @@ def test_schedule_bounds_and_coverage(schedule_check, shape):
     assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
 
 
+def test_wave_cap_matches_enumeration(schedule_check):
+    out = subprocess.run([schedule_check, "wave"], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
+
+
 # CTA-pair items (512 query rows): shards whose length is a multiple of 512
 PAIR_SHAPES = [s for s in SHAPES if (s[3] // s[4]) % (1024 if s[6] == 2 else 512) == 0] + [
     (1, 2, 2, 2048, 2, 128, 1), (2, 8, 2, 3072, 3, 128, 1), (1, 2, 2, 2048, 2, 128, 2)]
