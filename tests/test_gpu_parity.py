@@ -188,6 +188,26 @@ def test_static_and_adaptive_agree(psr):
         check(o, lse, outs[0][0], outs[0][1], "across partitions")
 
 
+def test_initial_split_keeps_compute_waves(psr):
+    """The adaptive launch's initial split on a 152-SM GB300.  B1 H16 S16384 has 1024 equal
+    (non-causal) items: at P = 16 the rule with its staging headroom asks for ~30 staging CTAs,
+    which leaves 122 compute CTAs and 9 waves; 24 is the largest split with 8 waves (1024 / 128),
+    so the launch starts there.  P = 32 (4-tile ring steps) and d = 128, P = 16 (the rule's 32 is
+    below the 9-wave cap of 38) start at the rule's split."""
+    torch = _torch()
+    if psr.num_ctas() != 152:
+        pytest.skip("expected splits are for 152 SMs")
+    assert -(-1024 // (152 - 24)) == 8 and -(-1024 // (152 - 25)) == 9
+    for name, want in (("sweep_d64_P16", 24), ("sweep_d64_P32", 51), ("sweep_d128_P16", 32)):
+        w = ri.WORKLOADS[name]
+        sh = (w.B, w.Hq, w.S, w.d)
+        q = torch.zeros(sh, dtype=torch.bfloat16, device="cuda")
+        k = torch.zeros((w.B, w.Hkv, w.S, w.d), dtype=torch.bfloat16, device="cuda")
+        o, lse, ws = psr.ring_attn_fwd(q, k, k, P=w.P, causal=w.causal, scale=w.scale)
+        st = psr.get_stats(ws)
+        assert st["status"] == 0 and st["n_s_initial"] == want, (name, st)
+
+
 # ------------------------------------------------------------------------------------------------
 # host-buffer entry point and failure reporting
 # ------------------------------------------------------------------------------------------------
