@@ -11,12 +11,16 @@
  * shard r consumes KV chunk (r - t) mod P while the next chunk is moved into
  * its receive buffer, and the per-chunk partial results are merged exactly
  * through the running max and log-sum-exp.  Here the P ranks are P shards in
- * one GPU's HBM: "staging" CTAs copy each chunk into a double-buffered ring
- * slot with TMA and publish a readiness flag (pwwt.cn §2.2 Figure 2 readiness
- * flag; §2.5: the flag names the completed payload), "compute" CTAs run the
- * FlashAttention pass on tcgen05 tensor cores, and an on-GPU controller
- * re-splits CTAs between the two roles with the pwwt.cn §2.4 rule
+ * one GPU's HBM: "staging" CTAs copy each chunk into a ring slot (three per
+ * group of items that read the same chunks) with TMA and publish a readiness
+ * flag (pwwt.cn §2.2 Figure 2 readiness flag; §2.5: the flag names the
+ * completed payload), "compute" CTAs run the FlashAttention pass on tcgen05
+ * tensor cores, and an on-GPU controller re-splits CTAs between the two roles
+ * with the pwwt.cn §2.4 rule
  *     n_s* = N * (R_s*C_s) / (R_p*C_p + R_s*C_s).
+ * Without a causal mask every compute item takes the same time, and the
+ * adaptive target is capped at the largest split that keeps the compute
+ * waves ceil(items / compute CTAs) of the split the staging work needs.
  *
  * Result: O = softmax(scale * Q K^T [+ causal mask over global positions]) V,
  * rounded to bf16, and LSE = natural-log log-sum-exp of the scaled scores per
