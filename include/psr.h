@@ -140,10 +140,12 @@ PSR_API int psr_ring_attn_fwd(const psr_shape* shape, const void* q, const void*
  * to the caller's device buffers dq, dk, dv (same layouts and sizes as the
  * device entry's q, k, v, o, lse), runs the attention, copies O and LSE back
  * to o_host / lse_host, and returns when they are there.  Shapes of 64 MB of
- * Q or more run in up to 4 slices of whole batches (B > 1) or of whole
- * KV-head groups with their query heads (B = 1): the copies in of slice c+1
- * and out of slice c-1 overlap the kernel of slice c (two internal streams,
- * created once per device; one launch per slice on `stream`).  The workspace
+ * Q or more run in up to 16 slices of whole batches (B > 1) or of whole
+ * KV-head groups with their query heads (B = 1), sized 1, 2, 4, ... units
+ * and back down to 1, so that only the first slice's copy in and the last
+ * slice's copy out are exposed: the copies in of slice c+1 and out of slice
+ * c-1 overlap the kernel of slice c (two internal streams, created once per
+ * device; one launch per slice on `stream`).  The workspace
  * is sized for the whole shape.  psr_get_stats afterwards describes the last
  * slice's launch.  Returns the first failing status, or PSR_ERR_TIMEOUT if a
  * slice's launch reported a device timeout. */

@@ -1186,7 +1186,7 @@ static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta,
 // Streams and events of the host-buffer entry point, one set per device and process (created on
 // first use, never freed); calls on one device serialise on a mutex.  err_host is pinned host
 // memory that receives each slice's error word.
-constexpr int kHostSlices = 4;
+constexpr int kHostSlices = 16;  // most slices of one call
 struct HostPipe {
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t ev_start = nullptr, ev_in[kHostSlices] = {}, ev_out[kHostSlices] = {};
@@ -1419,20 +1419,29 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
     if (rc != PSR_OK) return rc;
     if (ws_bytes < ws_layout(G).total) return PSR_ERR_ARG;
   }
-  // Slices: contiguous batches, or (one batch) contiguous KV-head groups with their query heads.
-  // Slice c+1 is copied in while slice c computes and slice c-1 is copied out.
+  // Slices: contiguous batches, or (one batch) contiguous KV-head groups with their query heads,
+  // sized by host_slice_plan (1, 2, 4, ... units and back down to 1).  Slice c+1 is copied in
+  // while slice c computes and slice c-1 is copied out.
   const size_t row_b = (size_t)sh->S * sh->d * 2;  // bytes of one head's Q/K/V/O rows
   const size_t q_bytes = (size_t)sh->B * sh->Hq * row_b;
-  const int units = sh->B > 1 ? sh->B : sh->Hkv;
+  const bool by_batch = sh->B > 1;
+  const int units = by_batch ? sh->B : sh->Hkv;
+  int plan[kHostSlices];
   int n_sl = 1;
-  if (q_bytes >= ((size_t)64 << 20))
-    for (int c = kHostSlices; c >= 2; --c)
-      if (units % c == 0) { n_sl = c; break; }
-  psr_shape ss = *sh;
-  if (sh->B > 1) ss.B = sh->B / n_sl;
-  else { ss.Hkv = sh->Hkv / n_sl; ss.Hq = sh->Hq / n_sl; }
-  const size_t q_sl = (size_t)ss.B * ss.Hq * row_b, kv_sl = (size_t)ss.B * ss.Hkv * row_b;
-  const size_t l_sl = (size_t)ss.B * ss.Hq * sh->S * 4;
+  plan[0] = units;
+  if (q_bytes >= ((size_t)64 << 20)) n_sl = host_slice_plan(units, plan, kHostSlices);
+  // per unit: query rows, KV rows and LSE entries of one batch (or of one KV-head group)
+  const size_t q_u = (by_batch ? (size_t)sh->Hq : (size_t)(sh->Hq / sh->Hkv)) * row_b;
+  const size_t kv_u = (by_batch ? (size_t)sh->Hkv : (size_t)1) * row_b;
+  const size_t l_u = (by_batch ? (size_t)sh->Hq : (size_t)(sh->Hq / sh->Hkv)) * sh->S * 4;
+  auto slice_shape = [&](int c) {
+    psr_shape ss = *sh;
+    if (by_batch) ss.B = plan[c];
+    else { ss.Hkv = plan[c]; ss.Hq = plan[c] * (sh->Hq / sh->Hkv); }
+    return ss;
+  };
+  size_t u0[kHostSlices];  // first unit of each slice
+  for (int c = 0, u = 0; c < n_sl; u += plan[c], ++c) u0[c] = (size_t)u;
 
   HostPipe* hp = host_pipe();
   if (!hp) return PSR_ERR_CUDA;
@@ -1446,27 +1455,28 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
                            cudaMemcpyHostToDevice, hp->h2d);
   };
   for (int c = 0; c < n_sl; ++c) {
-    if (cp_in(dq, q_host, c * q_sl, q_sl) != cudaSuccess || cp_in(dk, k_host, c * kv_sl, kv_sl) != cudaSuccess ||
-        cp_in(dv, v_host, c * kv_sl, kv_sl) != cudaSuccess || cudaEventRecord(hp->ev_in[c], hp->h2d) != cudaSuccess)
+    const size_t qo = u0[c] * q_u, ko = u0[c] * kv_u, qn = plan[c] * q_u, kn = plan[c] * kv_u;
+    if (cp_in(dq, q_host, qo, qn) != cudaSuccess || cp_in(dk, k_host, ko, kn) != cudaSuccess ||
+        cp_in(dv, v_host, ko, kn) != cudaSuccess || cudaEventRecord(hp->ev_in[c], hp->h2d) != cudaSuccess)
       return PSR_ERR_CUDA;
   }
   for (int c = 0; c < n_sl; ++c) {
+    const size_t qo = u0[c] * q_u, ko = u0[c] * kv_u, lo = u0[c] * l_u, qn = plan[c] * q_u, ln = plan[c] * l_u;
+    const psr_shape ss = slice_shape(c);
     if (cudaStreamWaitEvent(st, hp->ev_in[c], 0) != cudaSuccess) return PSR_ERR_CUDA;
-    const int rc = psr_ring_attn_fwd(&ss, static_cast<const uint8_t*>(dq) + c * q_sl,
-                                     static_cast<const uint8_t*>(dk) + c * kv_sl,
-                                     static_cast<const uint8_t*>(dv) + c * kv_sl, static_cast<uint8_t*>(d_o) + c * q_sl,
-                                     reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(d_lse) + c * l_sl), workspace,
+    const int rc = psr_ring_attn_fwd(&ss, static_cast<const uint8_t*>(dq) + qo, static_cast<const uint8_t*>(dk) + ko,
+                                     static_cast<const uint8_t*>(dv) + ko, static_cast<uint8_t*>(d_o) + qo,
+                                     reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(d_lse) + lo), workspace,
                                      ws_bytes, part, st);
     if (rc != PSR_OK) return rc;
     // this slice's error word, before the next launch resets the control block
     if (cudaMemcpyAsync(hp->err_host + c, static_cast<uint8_t*>(workspace) + offsetof(Ctrl, error), 4,
                         cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaEventRecord(hp->ev_out[c], st) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->ev_out[c], 0) != cudaSuccess ||
-        cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + c * q_sl, static_cast<const uint8_t*>(d_o) + c * q_sl, q_sl,
+        cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + qo, static_cast<const uint8_t*>(d_o) + qo, qn,
                         cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess ||
-        cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + c * l_sl,
-                        reinterpret_cast<const uint8_t*>(d_lse) + c * l_sl, l_sl, cudaMemcpyDeviceToHost,
-                        hp->d2h) != cudaSuccess)
+        cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + lo, reinterpret_cast<const uint8_t*>(d_lse) + lo, ln,
+                        cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
       return PSR_ERR_CUDA;
   }
   if (cudaStreamSynchronize(hp->d2h) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) return PSR_ERR_CUDA;

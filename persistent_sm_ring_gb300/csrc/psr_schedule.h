@@ -309,4 +309,37 @@ PSR_HD int wave_cap(int n_cta, int n_need, long long U) {
   return n_cta - (int)((U + w - 1) / w);
 }
 
+// Slice sizes (in units: batches, or KV-head groups) of the host-buffer pipeline, in order.  The
+// copies in of slice c+1 and out of slice c-1 overlap the kernel of slice c, so only the first
+// slice's upload and the last slice's download are exposed: the sizes ramp up from one unit by
+// doubling (an upload of twice a slice's units still hides behind its kernel) and mirror back
+// down to one unit; what is left over goes to the middle, beside the largest slices.  Returns
+// the slice count (at most max_slices, at least 1); the sizes sum to `units`.
+PSR_HD int host_slice_plan(int units, int* sizes, int max_slices) {
+  if (units <= 1 || max_slices < 3) {
+    sizes[0] = units;
+    return 1;
+  }
+  int up[32];
+  int nu = 0, sum = 0;
+  for (int sz = 1; nu < 32 && 2 * nu + 3 <= max_slices && 2 * (sum + sz) <= units; sz *= 2) {
+    up[nu++] = sz;
+    sum += sz;
+  }
+  const int last = up[nu - 1];
+  int rest = units - 2 * sum;
+  int n = 0;
+  for (int i = 0; i < nu; ++i) sizes[n++] = up[i];
+  if (rest > 0 && rest <= last) {
+    // widen the two middle slices (the later one first)
+    sizes[n - 1] += rest / 2;
+    for (int i = nu - 1; i >= 0; --i) sizes[n++] = up[i];
+    sizes[nu] += (rest + 1) / 2;
+    return n;
+  }
+  if (rest > 0) sizes[n++] = rest;  // one middle slice (at most ~4x the largest ramp slice)
+  for (int i = nu - 1; i >= 0; --i) sizes[n++] = up[i];
+  return n;
+}
+
 }  // namespace psr

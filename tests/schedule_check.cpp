@@ -12,6 +12,7 @@
 //    receives exactly dynamic_staging_tasks() pushes;
 //  * total_tiles(), total_staging_tasks() and the piece counts agree with direct enumeration.
 // Usage: schedule_check wave   -> checks the controller's wave cap against enumeration.
+//        schedule_check slices -> checks the host-buffer pipeline's slice plan.
 // Usage: schedule_check B Hq Hkv S P d causal max_group [cg]   -> prints "OK ..." or "FAIL ..."
 // (causal: 0, 1, or 2 = load-balanced shards; cg: CTAs per compute unit, 1 or 2; default 1)
 #include <cstdio>
@@ -61,8 +62,37 @@ static int check_wave_cap() {
   return 0;
 }
 
+// host_slice_plan: the sizes cover the units exactly, stay within the slice budget, start at one
+// unit, grow at most ~3x from one slice to the next (2x, plus the widened middle pair) and reach
+// the largest by at most ~4x unless the slice budget is what stopped the ramp, and only shrink
+// after it.
+static int check_slice_plan() {
+  for (int max_slices = 1; max_slices <= 16; ++max_slices)
+    for (int units = 1; units <= 400; ++units) {
+      int sz[64];
+      const int n = host_slice_plan(units, sz, max_slices);
+      CHECK(n >= 1 && n <= (max_slices < 1 ? 1 : max_slices), "slice count %d (units %d, max %d)", n, units, max_slices);
+      int sum = 0, peak = 0;
+      for (int i = 0; i < n; ++i) {
+        CHECK(sz[i] >= 1, "empty slice (units %d)", units);
+        sum += sz[i];
+        if (sz[i] > sz[peak]) peak = i;
+      }
+      CHECK(sum == units, "slices sum to %d, not %d", sum, units);
+      if (n > 1) CHECK(sz[0] == 1, "first slice %d (units %d)", sz[0], units);
+      for (int i = 1; i <= peak; ++i)
+        CHECK(sz[i] >= sz[i - 1] && (i == peak || sz[i] <= 3 * sz[i - 1] + 1) &&
+                  (i < peak || n >= max_slices - 1 || sz[i] <= 4 * sz[i - 1] + 4),
+              "ramp up at slice %d (units %d, max %d)", i, units, max_slices);
+      for (int i = peak + 1; i < n; ++i) CHECK(sz[i] <= sz[i - 1], "ramp down at slice %d (units %d)", i, units);
+    }
+  std::printf("OK host_slice_plan\n");
+  return 0;
+}
+
 int main(int argc, char** argv) {
   if (argc == 2 && std::string(argv[1]) == "wave") return check_wave_cap();
+  if (argc == 2 && std::string(argv[1]) == "slices") return check_slice_plan();
   if (argc != 9 && argc != 10) return 2;
   int a[9] = {0, 0, 0, 0, 0, 0, 0, 0, 1};
   for (int i = 0; i < argc - 1; ++i) a[i] = std::atoi(argv[i + 1]);
