@@ -222,6 +222,155 @@ def cpu_baseline(workloads, inputs, budget_s=12.0):
 
 
 # ------------------------------------------------------------------------------------------------
+# every workload: the five configurations, each timed on its own
+# ------------------------------------------------------------------------------------------------
+
+# (configuration, workloads): 1 the small case, 2 the headline (both passes), 3 GQA causal, 4 the
+# long causal sequence with outlier keys, 5 the partition-stress grid (adaptive partition)
+CONFIGS = (("1", ("small",)), ("2", ("h32_s32k_nc", "h32_s32k_c")), ("3", ("gqa_s64k_c",)),
+           ("4", ("long_s128k_c",)),
+           ("5", tuple(f"sweep_d{d}_P{P}" for d in (64, 128) for P in (2, 4, 8, 16, 32, 64))))
+
+
+def algorithmic_bytes(w) -> int:
+    """HBM bytes a pass must move: Q, K, V read once, O and LSE written once, and every ring
+    transfer read from the chunk's home and written into its slot."""
+    return 2 * (w.n_q + 2 * w.n_kv) + 2 * w.n_q + 4 * w.B * w.Hq * w.S + 2 * w.staging_bytes()
+
+
+def roofline_of(w, ms, peaks):
+    """Roofline time of a pass (tensor flops at the measured bf16 peak, or its bytes at the measured
+    HBM bandwidth, whichever is longer) over its measured time."""
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    t_flops = w.flops() / (peak * 1e12)
+    t_bytes = algorithmic_bytes(w) / (hbm * 1e9)
+    bound = "tensor" if t_flops >= t_bytes else "hbm"
+    return bound, max(t_flops, t_bytes) / (ms / 1e3)
+
+
+def time_configs(psr, torch, peaks, passes_small=50, budget_ms=400.0):
+    """Median CUDA-event time of each configuration's pass (adaptive partition, inputs resident in
+    HBM), with TFLOP/s, the fraction of the measured bf16 peak, the roofline fraction and the
+    staging rate.  One input set is resident at a time."""
+    import ring_inputs as ri
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    stream = torch.cuda.current_stream()
+    part = psr.make_partition(psr.ADAPTIVE)
+    out = []
+    key_now, tensors = None, None
+    for cfg, names in CONFIGS:
+        for name in names:
+            w = ri.WORKLOADS[name]
+            key = (w.B, w.Hq, w.Hkv, w.S, w.d, w.seed, w.qmul, w.kmul, w.outlier_frac)
+            if key != key_now:
+                tensors = None
+                torch.cuda.empty_cache()
+                host = [torch.empty(shape, dtype=torch.int16).pin_memory()
+                        for shape in ((w.B, w.Hq, w.S, w.d), (w.B, w.Hkv, w.S, w.d), (w.B, w.Hkv, w.S, w.d))]
+                ri.generate(w, *(t.data_ptr() for t in host))
+                tensors = [t.cuda().view(torch.bfloat16) for t in host]
+                del host
+                key_now = key
+            q, k, v = tensors
+            o = torch.empty_like(q)
+            lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=q.device)
+            ws = torch.empty(psr.workspace_bytes(psr.make_shape(w.B, w.Hq, w.Hkv, w.S, w.P, w.d, w.causal)),
+                             dtype=torch.uint8, device=q.device)
+
+            def one():
+                psr.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, scale=w.scale, partition=part, workspace=ws,
+                                  out=o, lse=lse, stream=stream)
+            for _ in range(3):
+                one()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            one()
+            torch.cuda.synchronize()
+            est_ms = 1e3 * (time.perf_counter() - t0)
+            reps = passes_small if est_ms < 1.0 else int(min(20, max(5, budget_ms / max(est_ms, 1e-3))))
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                one()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            st = psr.get_stats(ws)
+            if st["status"] != 0:
+                raise RuntimeError(f"{name}: device status {st['status']} site {st['error_site']}")
+            times = sorted(e0.elapsed_time(e1) for e0, e1 in ev)
+            ms = statistics.median(times)
+            bound, frac = roofline_of(w, ms, peaks)
+            out.append({"config": cfg, "workload": name,
+                        "shape": f"B{w.B} Hq{w.Hq} Hkv{w.Hkv} S{w.S} P{w.P} d{w.d}",
+                        "causal": {0: False, 1: True, 2: "balanced shards"}[int(w.causal)],
+                        "ms": round(ms, 4), "ms_min_max": [round(times[0], 4), round(times[-1], 4)], "passes": reps,
+                        "tflops": round(w.flops() / (ms / 1e3) / 1e12, 2),
+                        "pct_bf16_peak": round(100 * w.flops() / (ms / 1e3) / 1e12 / peak, 2),
+                        "roofline": {"bound": bound, "frac": round(frac, 4)},
+                        "staging_GBps": round(2 * st["staging_bytes"] / (ms / 1e3) / 1e9, 1),
+                        "n_s": [st["n_s_initial"], st["n_s_min"], st["n_s_max"], st["n_s_final"]]})
+            del o, lse, ws
+    tensors = None
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline_cases(cores):
+    """The fp64 oracle on each configuration: full runs of the small case and of the
+    partition-stress grid (its result does not depend on P: once per d), and rows per second on
+    the sampled rows of the large configurations with the full-configuration time extrapolated from
+    the sample's algorithmic flops."""
+    import numpy as np
+
+    import oracle
+    import ring_inputs as ri
+    cases = []
+    for name, full in (("small", True), ("sweep_d64_P2", True), ("sweep_d128_P2", True), ("h32_s32k_nc", False),
+                       ("h32_s32k_c", False), ("gqa_s64k_c", False), ("long_s128k_c", False)):
+        w = ri.WORKLOADS[name]
+        q, k, v = ri.generate(w)
+        rows = None if full else ri.sample_rows(w)
+        t0 = time.perf_counter()
+        oracle.for_workload(w, q, k, v, rows=rows, n_threads=cores)
+        dt = time.perf_counter() - t0
+        if full:
+            cases.append({"workload": name if not name.startswith("sweep") else f"sweep_d{w.d} (every P)",
+                          "rows": w.B * w.Hq * w.S, "seconds": round(dt, 3), "kind": "full run",
+                          "tflops": round(w.flops() / dt / 1e12, 5)})
+        else:
+            fl = oracle_rows_flops(w, rows)
+            cases.append({"workload": name, "rows": int(len(rows)), "seconds": round(dt, 3),
+                          "rows_per_s": round(len(rows) / dt, 1), "tflops": round(fl / dt / 1e12, 5),
+                          "full_seconds_extrapolated": round(w.flops() / (fl / dt), 1)})
+        del q, k, v
+    return {"cores": cores, "kind": "oracle", "cases": cases}
+
+
+def run_configs(args):
+    import torch
+
+    import oracle
+    import persistent_sm_ring_gb300 as psr
+    psr.build()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    rows = time_configs(psr, torch, peaks)
+    clk = clocks.stop()
+    for r in rows:
+        print(json.dumps(r), flush=True)
+    cpu = None
+    if not args.no_cpu_baseline:
+        oracle.build()
+        cpu = cpu_baseline_cases(oracle.default_threads())
+    print(json.dumps({"configs": len(rows), "clocks": clk, "peak_source": peaks.get("source"),
+                      "cpu_baseline_cases": cpu}), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------
 
@@ -352,6 +501,13 @@ def run_ours(args):
                    "n_s": [st["n_s_initial"], st["n_s_min"], st["n_s_max"], st["n_s_final"]],
                    "timed_in_step": False})
 
+    # every configuration, each timed on its own (not part of the headline step)
+    configs = None
+    if not args.no_configs and not args.heads:
+        configs = [{k2: r[k2] for k2 in ("config", "workload", "ms", "tflops", "pct_bf16_peak", "staging_GBps")}
+                   | {"roofline_frac": r["roofline"]["frac"], "bound": r["roofline"]["bound"]}
+                   for r in time_configs(psr, torch, peaks)]
+
     # e2e: host buffers through the C ABI (H2D + kernel + D2H, synchronised, per pass)
     o_h = torch.empty(host[0].shape, dtype=torch.int16).pin_memory()
     l_h = torch.empty(tuple(host[0].shape[:3]), dtype=torch.float32).pin_memory()
@@ -400,6 +556,7 @@ def run_ours(args):
             "gpu_launches": args.steps * len(wls),
             "clocks": clk,
             "passes": passes,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -913,6 +1070,9 @@ def main():
     ap.add_argument("--ag-gemm", action="store_true", help="the AllGather+GEMM path instead of attention")
     ap.add_argument("--gemm-rs", action="store_true", help="the GEMM+ReduceScatter path instead of attention")
     ap.add_argument("--bwd", action="store_true", help="the Ring Attention backward instead of the forward")
+    ap.add_argument("--configs", action="store_true",
+                    help="time all five configurations and run the oracle's CPU-baseline cases")
+    ap.add_argument("--no-configs", action="store_true", help="leave the per-configuration table out of the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=96)
@@ -927,6 +1087,8 @@ def main():
         run_rs(args)
     elif args.bwd:
         run_bwd(args)
+    elif args.configs:
+        run_configs(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -178,16 +178,28 @@ PSR_API int psr_controller_target(int n_cta, double R_s, double C_s, double R_p,
  * PSR_NOALLOC_SCRATCH_BYTES held by every GPU that loads the library until the
  * process exits.  The library allocates nothing (no cudaMalloc, cudaFree or
  * allocating library call).
- *   - Returns PSR_ERR_UNSUPPORTED when psr_workspace_bytes(shape) exceeds
- *     PSR_NOALLOC_SCRATCH_BYTES (or the shape is unsupported).
+ *   - Checks in the order of psr_ring_attn_fwd, with the same status codes:
+ *     null or misaligned q, k, v, o, lse -> PSR_ERR_ARG; the device; the shape
+ *     (PSR_ERR_ARG / PSR_ERR_UNSUPPORTED).  Only then, a supported shape whose
+ *     psr_workspace_bytes(shape) exceeds PSR_NOALLOC_SCRATCH_BYTES ->
+ *     PSR_ERR_UNSUPPORTED.
  *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     device current (and looks it up again after the device's context was
+ *     reset); make that first call before any stream capture.
  *   - All calls on a device share the array and each call clears its control
  *     words first; calls whose launches overlap on the GPU race on it, so order
- *     them (one stream, or events). */
+ *     them (one stream, or events).
+ *   - A device-side timeout is not reported here: read it with
+ *     psr_noalloc_get_stats after the call (before the next no-alloc call). */
 #define PSR_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 PSR_API int psr_ring_attn_fwd_noalloc(const psr_shape* shape, const void* q, const void* k, const void* v, void* o,
                                       float* lse, const psr_partition* part, void* stream);
+
+/* psr_get_stats for the allocation-free entry: synchronises `stream`, reads the
+ * control block of the last psr_ring_attn_fwd_noalloc launch on the current
+ * device from the fixed scratch and fills *out.  Returns out->status (PSR_OK or
+ * PSR_ERR_TIMEOUT), or PSR_ERR_ARG / PSR_ERR_CUDA.  Allocates nothing. */
+PSR_API int psr_noalloc_get_stats(psr_stats* out, void* stream);
 
 /* Human-readable name of a status code (static string). */
 PSR_API const char* psr_status_string(int status);
@@ -204,16 +216,17 @@ PSR_API int psr_num_ctas(void);
  *     dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
  * (dK, dV summed over the query heads that share the KV head).  In the ring
  * each KV chunk travels with its dK/dV partial sums while the queries stay;
- * on one GPU each persistent CTA holds one 128-row K/V tile and its dK/dV
- * accumulators in tensor memory while it visits the query shards in ring
- * order, and dQ is accumulated in fp32 (vector atomic adds) and rounded at the
- * end.  All matrix products run on tcgen05 with bf16 operands (P and dS
- * rounded to bf16) and fp32 accumulation. */
+ * on one GPU a first persistent kernel gives each task one 128-row K/V tile
+ * whose dK/dV accumulators stay in tensor memory while it visits the query
+ * shards in ring order, and a second, query-stationary one gives each task one
+ * 128-row query tile whose dQ accumulator stays in tensor memory while it
+ * visits the K/V tiles (it recomputes S and dP; no atomics).  All matrix
+ * products run on tcgen05 with bf16 operands (P and dS rounded to bf16) and
+ * fp32 accumulation. */
 
 /* Bytes of device workspace psr_ring_attn_bwd needs: the control block (the
- * shared prefix, read by psr_get_stats), D ([B][Hq][S] fp32) and the dQ
- * accumulator ([B][Hq][S][d] fp32).  Returns 0 for an invalid or unsupported
- * shape. */
+ * shared prefix, read by psr_get_stats), D = rowsum(dO * O) and -LSE*log2(e)
+ * ([B][Hq][S] fp32 each).  Returns 0 for an invalid or unsupported shape. */
 PSR_API size_t psr_ring_attn_bwd_workspace_bytes(const psr_shape* shape);
 
 /* Ring Attention backward.
@@ -225,7 +238,7 @@ PSR_API size_t psr_ring_attn_bwd_workspace_bytes(const psr_shape* shape);
  *   workspace:  device, >= psr_ring_attn_bwd_workspace_bytes(shape), 256-byte aligned.
  *   timeout_ms: bound on every device wait (<= 0: 2000 ms); stream: a cudaStream_t.
  * All pointers 16-byte aligned.  Asynchronous: enqueues a workspace reset, the
- * D kernel, one persistent launch and the dQ rounding on `stream`; a device
+ * D kernel and the two persistent launches (dK/dV, then dQ) on `stream`; a device
  * timeout is reported by psr_get_stats.  Supported: d in {64, 128}; causal 0, 1 or
  * PSR_CAUSAL_BALANCED; L = S/P a multiple of 128 (of 256 with PSR_CAUSAL_BALANCED);
  * Hq % Hkv == 0; sm_103 device. */

@@ -29,7 +29,7 @@ CAUSAL, CAUSAL_BALANCED = 1, 2
 
 EXPORTED = ("psr_workspace_bytes", "psr_ring_attn_fwd", "psr_ring_attn_fwd_host", "psr_get_stats",
             "psr_get_trajectory", "psr_controller_target", "psr_status_string", "psr_num_ctas",
-            "psr_ring_attn_fwd_noalloc", "psr_ag_gemm_workspace_bytes", "psr_ag_gemm", "psr_gemm_rs_workspace_bytes",
+            "psr_ring_attn_fwd_noalloc", "psr_noalloc_get_stats", "psr_ag_gemm_workspace_bytes", "psr_ag_gemm", "psr_gemm_rs_workspace_bytes",
             "psr_gemm_rs", "psr_ring_attn_bwd_workspace_bytes", "psr_ring_attn_bwd")
 
 
@@ -128,6 +128,10 @@ def load(trace: bool = False, variant: str = "") -> ctypes.CDLL:
         lib.psr_gemm_rs_workspace_bytes.restype = sz
         lib.psr_gemm_rs.argtypes = [P_rs, vp, vp, vp, vp, sz, P_part, vp]
         lib.psr_gemm_rs.restype = ctypes.c_int
+        lib.psr_ring_attn_fwd_noalloc.argtypes = [P_shape, vp, vp, vp, vp, vp, P_part, vp]
+        lib.psr_ring_attn_fwd_noalloc.restype = ctypes.c_int
+        lib.psr_noalloc_get_stats.argtypes = [ctypes.POINTER(Stats), vp]
+        lib.psr_noalloc_get_stats.restype = ctypes.c_int
         lib.psr_num_ctas.argtypes = []
         lib.psr_num_ctas.restype = ctypes.c_int
         _lib = lib
@@ -186,6 +190,24 @@ def _check_tensor(t, name, shape, dtype):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_host(t, name, shape, dtypes):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must be one of {dtypes}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _same_device(tensors, what):
+    devs = {t.device for t in tensors}
+    if len(devs) != 1:
+        raise ValueError(f"{what}: all device tensors must be on one GPU, got {sorted(map(str, devs))}")
+
+
 def ring_attn_fwd(q, k, v, *, P, causal, scale=None, partition=None, workspace=None, out=None, lse=None,
                   stream=None):
     """Ring Attention forward over P shards held on this GPU.
@@ -208,8 +230,8 @@ def ring_attn_fwd(q, k, v, *, P, causal, scale=None, partition=None, workspace=N
     need = workspace_bytes(shape)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    elif workspace.numel() * workspace.element_size() < need:
-        raise ValueError(f"workspace too small: need {need} bytes")
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -218,6 +240,7 @@ def ring_attn_fwd(q, k, v, *, P, causal, scale=None, partition=None, workspace=N
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     else:
         _check_tensor(lse, "lse", (B, Hq, S), torch.float32)
+    _same_device((q, k, v, out, lse, workspace), "ring_attn_fwd")
     part = partition if partition is not None else make_partition()
     rc = lib.psr_ring_attn_fwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                lse.data_ptr(), workspace.data_ptr(), need, ctypes.byref(part),
@@ -230,15 +253,42 @@ def ring_attn_fwd(q, k, v, *, P, causal, scale=None, partition=None, workspace=N
 def ring_attn_fwd_host(q_host, k_host, v_host, o_host, lse_host, dq, dk, dv, d_o, d_lse, *, P, causal, scale=None,
                        partition=None, workspace=None, stream=None):
     """Host-buffer variant: copies in, runs, copies out and synchronises (one C call; large shapes
-    run in slices whose copies overlap the kernels)."""
+    run in slices whose copies overlap the kernels).
+
+    q_host, o_host: [B, Hq, S, d]; k_host, v_host: [B, Hkv, S, d] -- pinned host tensors holding
+    bf16 values (dtype bfloat16, or int16 carrying the bf16 bit patterns); lse_host: [B, Hq, S]
+    fp32, pinned.  dq, d_o: [B, Hq, S, d] and dk, dv: [B, Hkv, S, d] bf16, d_lse: [B, Hq, S] fp32 --
+    the device buffers the copies land in (CUDA, contiguous, one GPU)."""
     import torch
     lib = load()
+    if not isinstance(q_host, torch.Tensor) or q_host.dim() != 4 or not isinstance(k_host, torch.Tensor) \
+            or k_host.dim() != 4:
+        raise ValueError("q_host, k_host, v_host must be 4-d [B, H, S, d] tensors")
     B, Hq, S, d = q_host.shape
     Hkv = k_host.shape[1]
+    bits = (torch.bfloat16, torch.int16)
+    _check_host(q_host, "q_host", (B, Hq, S, d), bits)
+    _check_host(k_host, "k_host", (B, Hkv, S, d), bits)
+    _check_host(v_host, "v_host", (B, Hkv, S, d), bits)
+    _check_host(o_host, "o_host", (B, Hq, S, d), bits)
+    _check_host(lse_host, "lse_host", (B, Hq, S), (torch.float32,))
+    _check_tensor(dq, "dq", (B, Hq, S, d), torch.bfloat16)
+    _check_tensor(dk, "dk", (B, Hkv, S, d), torch.bfloat16)
+    _check_tensor(dv, "dv", (B, Hkv, S, d), torch.bfloat16)
+    _check_tensor(d_o, "d_o", (B, Hq, S, d), torch.bfloat16)
+    _check_tensor(d_lse, "d_lse", (B, Hq, S), torch.float32)
+    _same_device((dq, dk, dv, d_o, d_lse), "ring_attn_fwd_host")
+    for t, name in ((q_host, "q_host"), (k_host, "k_host"), (v_host, "v_host"), (o_host, "o_host"),
+                    (lse_host, "lse_host")):
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be in pinned host memory (tensor.pin_memory()): the copies run "
+                             f"asynchronously on the library's streams")
     shape = make_shape(B, Hq, Hkv, S, P, d, causal, scale)
     need = workspace_bytes(shape)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dq.device)
+    elif not workspace.is_cuda or workspace.device != dq.device or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor on {dq.device} of at least {need} bytes")
     part = partition if partition is not None else make_partition()
     rc = lib.psr_ring_attn_fwd_host(ctypes.byref(shape), q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(),
                                     o_host.data_ptr(), lse_host.data_ptr(), dq.data_ptr(), dk.data_ptr(),
@@ -261,20 +311,25 @@ def ag_gemm(a, w, *, P, partition=None, workspace=None, out=None, stream=None):
     w [P][Ns][K] bf16 -> c [P][M][Ns] bf16, C_r = gather(A) @ W_r^T.  Returns (c, workspace)."""
     import torch
     lib = load()
+    if a.dim() != 2 or w.dim() != 3:
+        raise ValueError("ag_gemm: a must be [M, K] and w [P, Ns, K]")
     M, K = a.shape
     Ns = w.shape[1]
     shape = AgShape(int(M), int(K), int(Ns), int(P))
     need = ag_gemm_workspace_bytes(M, K, Ns, P)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    _check_tensor(a, "a", (M, K), torch.bfloat16)
+    _check_tensor(w, "w", (P, Ns, K), torch.bfloat16)
     if out is None:
         out = torch.empty((P, M, Ns), dtype=torch.bfloat16, device=a.device)
-    for t in (a, w, out):
-        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError("ag_gemm: a, w and out must be contiguous bf16 CUDA tensors")
+    _check_tensor(out, "out", (P, M, Ns), torch.bfloat16)
+    _same_device((a, w, out), "ag_gemm")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"ag_gemm: workspace must be a CUDA tensor of at least {need} bytes")
     part = partition if partition is not None else make_partition()
     rc = lib.psr_ag_gemm(ctypes.byref(shape), a.data_ptr(), w.data_ptr(), out.data_ptr(), workspace.data_ptr(),
-                         workspace.numel(), ctypes.byref(part), _stream_handle(stream))
+                         workspace.numel() * workspace.element_size(), ctypes.byref(part), _stream_handle(stream))
     if rc != OK:
         raise PsrError(rc, "psr_ag_gemm")
     return out, workspace
@@ -293,23 +348,29 @@ def ring_attn_bwd(q, k, v, o, lse, dout, *, P, causal, scale=None, workspace=Non
     (bf16), lse [B][Hq][S] fp32 (the forward's) -> (dq, dk, dv, workspace)."""
     import torch
     lib = load()
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("ring_attn_bwd: q, k, v must be 4-d [B, H, S, d]")
     B, Hq, S, d = q.shape
     Hkv = k.shape[1]
     shape = make_shape(B, Hq, Hkv, S, P, d, causal, scale)
     need = ring_attn_bwd_workspace_bytes(shape)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for t in (q, k, v, o, dout, dq, dk, dv):
-        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError("ring_attn_bwd: q, k, v, o, dout, dq, dk, dv must be contiguous bf16 CUDA tensors")
-    if lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
-        raise ValueError("ring_attn_bwd: lse must be a contiguous fp32 CUDA tensor")
+    for t, name in ((q, "q"), (o, "o"), (dout, "dout"), (dq, "dq")):
+        _check_tensor(t, name, (B, Hq, S, d), torch.bfloat16)
+    for t, name in ((k, "k"), (v, "v"), (dk, "dk"), (dv, "dv")):
+        _check_tensor(t, name, (B, Hkv, S, d), torch.bfloat16)
+    _check_tensor(lse, "lse", (B, Hq, S), torch.float32)
+    _same_device((q, k, v, o, lse, dout, dq, dk, dv), "ring_attn_bwd")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"ring_attn_bwd: workspace must be a CUDA tensor of at least {need} bytes")
     rc = lib.psr_ring_attn_bwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                               workspace.data_ptr(), workspace.numel(), int(timeout_ms), _stream_handle(stream))
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(), int(timeout_ms),
+                               _stream_handle(stream))
     if rc != OK:
         raise PsrError(rc, "psr_ring_attn_bwd")
     return dq, dk, dv, workspace
@@ -328,22 +389,25 @@ def gemm_rs(a, w, *, partition=None, workspace=None, out=None, stream=None):
     q*M/P .. belonging to rank q.  Returns (out, workspace)."""
     import torch
     lib = load()
+    if a.dim() != 3 or w.dim() != 3:
+        raise ValueError("gemm_rs: a must be [P, M, Ks] and w [P, N, Ks]")
     P, M, Ks = a.shape
     N = w.shape[1]
     shape = RsShape(int(M), int(N), int(Ks), int(P))
     need = gemm_rs_workspace_bytes(M, N, Ks, P)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    _check_tensor(a, "a", (P, M, Ks), torch.bfloat16)
+    _check_tensor(w, "w", (P, N, Ks), torch.bfloat16)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
-    for t in (a, w, out):
-        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError("gemm_rs: a, w and out must be contiguous bf16 CUDA tensors")
-    if tuple(w.shape) != (P, N, Ks) or tuple(out.shape) != (M, N):
-        raise ValueError("gemm_rs: shapes a [P][M][Ks], w [P][N][Ks], out [M][N]")
+    _check_tensor(out, "out", (M, N), torch.bfloat16)
+    _same_device((a, w, out), "gemm_rs")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"gemm_rs: workspace must be a CUDA tensor of at least {need} bytes")
     part = partition if partition is not None else make_partition()
     rc = lib.psr_gemm_rs(ctypes.byref(shape), a.data_ptr(), w.data_ptr(), out.data_ptr(), workspace.data_ptr(),
-                         workspace.numel(), ctypes.byref(part), _stream_handle(stream))
+                         workspace.numel() * workspace.element_size(), ctypes.byref(part), _stream_handle(stream))
     if rc != OK:
         raise PsrError(rc, "psr_gemm_rs")
     return out, workspace

@@ -16,7 +16,7 @@ VARIANTS = {"": ([], LIB), "trace": (["-DPSR_TRACE=1"], LIB_TRACE), "pairs": (["
 SOURCES = [os.path.join(CSRC, f) for f in ("psr_ring_attn.cu", "psr_ring_attn_bwd.cu", "psr_ag_gemm.cu", "psr_gemm_rs.cu",
                                             "psr_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f)
-                  for f in ("psr_device.cuh", "psr_schedule.h", "psr_control.cuh", "psr_gemm_tile.cuh")] + [
+                  for f in ("psr_device.cuh", "psr_schedule.h", "psr_control.cuh", "psr_gemm_tile.cuh", "psr_internal.h")] + [
     os.path.join(ROOT, "include", "psr.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 _lock = threading.Lock()

@@ -461,25 +461,4 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// 2^x for a pair, on the FMA/ALU pipes instead of MUFU (Cody-Waite range
-// reduction x = n + f, n = round(x), |f| <= 1/2, and a degree-3 minimax
-// polynomial for 2^f; coefficients and error bound from
-// persistent_sm_ring_gb300/exp2_poly.py: max relative error 7.5e-5).
-// Inputs must be >= -125 (callers clamp), so 2^n stays a normal number.
-__device__ __forceinline__ void exp2_poly_pair(float x0, float x1, float& y0, float& y1) {
-  const uint64_t x = f2_pack(x0, x1);
-  const float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer in the low mantissa bits
-  const uint64_t t = add2(x, f2_pack(kMagic, kMagic));
-  const uint64_t n = add2(t, f2_pack(-kMagic, -kMagic));
-  const uint64_t f = fma2(n, f2_pack(-1.0f, -1.0f), x);
-  uint64_t p = fma2(f, f2_pack(0x1.c3f76p-5f, 0x1.c3f76p-5f), f2_pack(0x1.f0de1ap-3f, 0x1.f0de1ap-3f));
-  p = fma2(p, f, f2_pack(0x1.62f31ap-1f, 0x1.62f31ap-1f));
-  p = fma2(p, f, f2_pack(0x1.fff692p-1f, 0x1.fff692p-1f));
-  float p0, p1, t0, t1;
-  f2_unpack(p, p0, p1);
-  f2_unpack(t, t0, t1);
-  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-}
-
 }  // namespace psr

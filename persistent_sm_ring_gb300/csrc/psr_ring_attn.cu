@@ -37,6 +37,7 @@
 #include "psr_device.cuh"
 #include "psr_schedule.h"
 #include "psr_control.cuh"
+#include "psr_internal.h"
 
 #ifndef PSR_TRACE
 #define PSR_TRACE 0  // 1: accumulate per-role wait/compute cycles into the control block
@@ -45,24 +46,6 @@
 namespace psr {
 
 constexpr bool kTrace = PSR_TRACE != 0;
-#ifndef PSR_POLY_EVERY
-#define PSR_POLY_EVERY 0
-#endif
-// One in kPolyEvery exponential pairs of an off-diagonal tile uses the FMA-pipe
-// polynomial instead of MUFU (0: none).  Off by default: measured on GB300, the
-// polynomial's dense FMA-pipe instruction stream starves the warp that issues
-// tcgen05.mma on the same SM sub-partition (issue rate halves under dense FMA
-// neighbours, not under MUFU-bound ones), which costs more than it saves.
-constexpr int kPolyEvery = PSR_POLY_EVERY;
-#ifndef PSR_P_PARTS
-#define PSR_P_PARTS 1
-#endif
-// P of a query tile is published in this many parts (key ranges of 128 / kPParts), so
-// that the PV MMAs of the first keys can run while the softmax computes the rest.  One part
-// by default: measured on GB300 (single CTAs), the per-part store waits and arrivals cost
-// more than the overlap gains (1249 / 1185 / 1077 TFLOP/s for 1 / 2 / 4 parts).
-constexpr int kPParts = PSR_P_PARTS;
-static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P parts: 1, 2 or 4");
 __device__ __forceinline__ long long trace_clock() { return kTrace ? clock64() : 0; }
 
 // ------------------------------------------------------------------------------------------------
@@ -166,7 +149,7 @@ struct SmemCtl {
   uint64_t kv_full[16];
   uint64_t kv_empty[16];
   uint64_t s_full[2];
-  uint64_t p_full[2][4];  // [query tile][part]: that part of P is in tensor memory (in every CTA)
+  uint64_t p_full[2];     // [query tile]: P is in tensor memory (in every CTA)
   uint64_t o_full[2];
   uint64_t stg[16];
   uint64_t drain;
@@ -585,20 +568,17 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
     mma_commit_cg<CG>(&sc->s_full[i]);
     mma_commit_cg<CG>(&sc->kv_empty[kstage]);
   };
-  // PV_i(j) part by part: the K = 16 steps over the keys of each published part of P
+  // PV_i(j): the K = 16 steps over the 128 keys of P_i(j)
   auto issue_pv = [&](int i, uint32_t vstage, bool first, uint32_t parity) -> bool {
     // V share MN-major: 64-column halves 16 KB apart (a pair's CTA holds one half)
     const uint32_t b_lo = sdesc_lo(sStage + vstage * C::KVB, 16384);
     const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
     const uint32_t tO = sc->tmem_base + (i ? C::COL_O1 : C::COL_O0);
+    if (!wait_bar<CG == 2>(&sc->p_full[i], parity, p, sc, SITE_P_FULL)) return false;
+    tc_fence_after();
 #pragma unroll
-    for (int part = 0; part < kPParts; ++part) {
-      if (!wait_bar<CG == 2>(&sc->p_full[i][part], parity, p, sc, SITE_P_FULL)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = part * (8 / kPParts); kk < (part + 1) * (8 / kPParts); ++kk)
-        mma_ts_cg<CG>(tO, tS + kk * 8, b_lo + kk * (2048 >> 4), kHi, IPV, (first && kk == 0) ? 0u : 1u);
-    }
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ts_cg<CG>(tO, tS + kk * 8, b_lo + kk * (2048 >> 4), kHi, IPV, (first && kk == 0) ? 0u : 1u);
     mma_commit_cg<CG>(&sc->o_full[i]);
     mma_commit_cg<CG>(&sc->kv_empty[vstage]);
     return true;
@@ -652,9 +632,8 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
 
 // p = 2^(s*sl2 - m) for scores [32*B0, 32*B1) of a row, written as bf16 pairs into TMEM
 // columns [16*B0, 16*B1) at tP (16 columns at a time, so few packed values are live);
-// the fp32 sums of p accumulate in acc.  When POLY, one in kPolyEvery pairs takes the
-// FMA-pipe polynomial instead of MUFU (off-diagonal tiles only: no -inf there).
-template <bool POLY, int B0, int B1>
+// the fp32 sums of p accumulate in acc.
+template <int B0, int B1>
 __device__ __forceinline__ void exp_blocks(const float (&s)[128], float sl2, float m, uint32_t tP, uint64_t (&acc)[4]) {
   const uint64_t scale2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m, -m);
 #pragma unroll
@@ -664,15 +643,9 @@ __device__ __forceinline__ void exp_blocks(const float (&s)[128], float sl2, flo
     for (int q = 0; q < 16; ++q) {
       const int e = blk * 16 + q;
       const uint64_t x = fma2(f2_pack(s[2 * e], s[2 * e + 1]), scale2, negm2);
-      float x0, x1, y0, y1;
+      float x0, x1;
       f2_unpack(x, x0, x1);
-      constexpr int kEvery = kPolyEvery > 0 ? kPolyEvery : 1;
-      if (POLY && kPolyEvery > 0 && (e % kEvery) == kEvery - 1) {
-        exp2_poly_pair(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f), y0, y1);
-      } else {
-        y0 = ex2_approx(x0);
-        y1 = ex2_approx(x1);
-      }
+      const float y0 = ex2_approx(x0), y1 = ex2_approx(x1);
       acc[e & 3] = add2(acc[e & 3], f2_pack(y0, y1));
       pk[q] = pack_bf16x2(y0, y1);
     }
@@ -699,20 +672,20 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
   const int row = quarter * 32 + lane;  // TMEM lane = tile row
   const int tile = it.qp * G.item_qt + 2 * (int)rank + i;  // query tile within the shard
   const int q_local = tile * kTileRows + row;               // position within the shard
-  // P ready, per part: one arrival per warp; in a pair the odd CTA's warps signal the even
-  // CTA's barrier with a 4-byte st.async each (16 bytes that its warp 0 expects)
-  const uint32_t p_full_cl = CG == 2 ? mapa_shared(smem_u32(&sc->p_full[i][0]), 0) : 0u;
+  // P ready: one arrival per warp; in a pair the odd CTA's warps signal the even CTA's
+  // barrier with a 4-byte st.async each (16 bytes that its warp 0 expects)
+  const uint32_t p_full_cl = CG == 2 ? mapa_shared(smem_u32(&sc->p_full[i]), 0) : 0u;
   const uint32_t p_sink_cl = CG == 2 ? mapa_shared(smem_u32(&sc->p_sink[quarter]), 0) : 0u;
-  auto publish = [&](int part) {
+  auto publish = [&]() {
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
       if (CG == 1 || rank == 0) {
-        if (CG == 2 && quarter == 0) mbar_expect_tx(&sc->p_full[i][part], 16);
-        else mbar_arrive(&sc->p_full[i][part]);
+        if (CG == 2 && quarter == 0) mbar_expect_tx(&sc->p_full[i], 16);
+        else mbar_arrive(&sc->p_full[i]);
       } else {
-        st_async_signal(p_sink_cl, 1u, p_full_cl + 8u * (uint32_t)part);
+        st_async_signal(p_sink_cl, 1u, p_full_cl);
       }
     }
   };
@@ -778,26 +751,8 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
       m_run = m_new;
       const float m_use = m_run == -INFINITY ? 0.0f : m_run;
       uint64_t acc[4] = {0, 0, 0, 0};
-      constexpr int BP = 4 / kPParts;  // 32-key blocks per part
-      if (diag) {
-        exp_blocks<false, 0, BP>(s, sl2, m_use, tS, acc);
-      } else {
-        exp_blocks<true, 0, BP>(s, sl2, m_use, tS, acc);
-      }
-      publish(0);
-      if constexpr (kPParts >= 2) {
-        if (diag) exp_blocks<false, BP, 2 * BP>(s, sl2, m_use, tS, acc);
-        else exp_blocks<true, BP, 2 * BP>(s, sl2, m_use, tS, acc);
-        publish(1);
-      }
-      if constexpr (kPParts == 4) {
-        if (diag) exp_blocks<false, 2, 3>(s, sl2, m_use, tS, acc);
-        else exp_blocks<true, 2, 3>(s, sl2, m_use, tS, acc);
-        publish(2);
-        if (diag) exp_blocks<false, 3, 4>(s, sl2, m_use, tS, acc);
-        else exp_blocks<true, 3, 4>(s, sl2, m_use, tS, acc);
-        publish(3);
-      }
+      exp_blocks<0, 4>(s, sl2, m_use, tS, acc);
+      publish();
       l_run += acc_sum(acc);
       tr_busy += trace_clock() - c1;
     }
@@ -876,9 +831,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sc.q_full[i], 1);
       mbar_init(&sc.s_full[i], 1);
-      // one arrival per softmax warp of tile i per part (in a pair, the even CTA's four
-      // warps, the first with the 16 bytes the odd CTA's warps send)
-      for (int part = 0; part < 4; ++part) mbar_init(&sc.p_full[i][part], 4);
+      // one arrival per softmax warp of tile i (in a pair, the even CTA's four warps, the
+      // first with the 16 bytes the odd CTA's warps send)
+      mbar_init(&sc.p_full[i], 4);
       mbar_init(&sc.o_full[i], 1);
     }
     for (int s = 0; s < C::NSTAGE; ++s) {
@@ -1257,17 +1212,35 @@ size_t psr_workspace_bytes(const psr_shape* sh) {
   return ws_layout(G).total;
 }
 
-int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const void* v, void* o, float* lse,
-                      void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
-  if (!sh || !q || !k || !v || !o || !lse || !workspace) return PSR_ERR_ARG;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PSR_ERR_ARG;
-  for (const void* ptr : {q, k, v, (const void*)o, (const void*)lse})
+// The forward's argument checks short of the workspace, in the order the entry points apply
+// them: null or misaligned tensors (PSR_ERR_ARG), the device (PSR_ERR_CUDA / PSR_ERR_UNSUPPORTED),
+// then the shape (PSR_ERR_ARG / PSR_ERR_UNSUPPORTED).
+static int fwd_prepare(const psr_shape* sh, const void* q, const void* k, const void* v, const void* o,
+                       const void* lse, DeviceInfo& di, Geometry& G) {
+  if (!sh || !q || !k || !v || !o || !lse) return PSR_ERR_ARG;
+  for (const void* ptr : {q, k, v, o, lse})
     if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return PSR_ERR_ARG;
-  DeviceInfo di;
   if (!device_info(di)) return PSR_ERR_CUDA;
   if (di.cc_major != 10 || di.cc_minor != 3) return PSR_ERR_UNSUPPORTED;
+  return shape_geometry(sh, G, di.n_sm);
+}
+
+int psr_internal_fwd_check(const psr_shape* sh, const void* q, const void* k, const void* v, const void* o,
+                           const void* lse, size_t* ws_need) {
+  DeviceInfo di;
   Geometry G;
-  int rc = shape_geometry(sh, G, di.n_sm);
+  const int rc = fwd_prepare(sh, q, k, v, o, lse, di, G);
+  if (rc == PSR_OK && ws_need) *ws_need = ws_layout(G).total;
+  return rc;
+}
+
+int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const void* v, void* o, float* lse,
+                      void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
+  if (!workspace) return PSR_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PSR_ERR_ARG;
+  DeviceInfo di;
+  Geometry G;
+  int rc = fwd_prepare(sh, q, k, v, o, lse, di, G);
   if (rc != PSR_OK) return rc;
   const int cg = G.cg;
   const int n_cta = di.n_sm / cg * cg;  // whole pairs
@@ -1409,6 +1382,9 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
   if (!sh || !q_host || !k_host || !v_host || !o_host || !lse_host) return PSR_ERR_ARG;
   if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->d < 1) return PSR_ERR_ARG;
   if (!dq || !dk || !dv || !d_o || !d_lse || !workspace) return PSR_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PSR_ERR_ARG;
+  for (const void* ptr : {(const void*)dq, (const void*)dk, (const void*)dv, (const void*)d_o, (const void*)d_lse})
+    if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return PSR_ERR_ARG;
   if (sh->Hq % sh->Hkv != 0) return PSR_ERR_UNSUPPORTED;
   // The whole shape must be launchable (validates the shape and the workspace size once).
   {
@@ -1442,14 +1418,35 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
   };
   size_t u0[kHostSlices];  // first unit of each slice
   for (int c = 0, u = 0; c < n_sl; u += plan[c], ++c) u0[c] = (size_t)u;
+  // every slice's launch must be valid before any copy is queued
+  {
+    DeviceInfo di;
+    if (!device_info(di)) return PSR_ERR_CUDA;
+    for (int c = 0; c < n_sl; ++c) {
+      const psr_shape ss = slice_shape(c);
+      Geometry Gc;
+      const int rc = shape_geometry(&ss, Gc, di.n_sm);
+      if (rc != PSR_OK) return rc;
+      if (ws_bytes < ws_layout(Gc).total) return PSR_ERR_ARG;
+    }
+  }
 
   HostPipe* hp = host_pipe();
   if (!hp) return PSR_ERR_CUDA;
   std::lock_guard<std::mutex> lk(hp->mu);  // the pipeline's streams, events and error words are per device
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Every failure after the first enqueue ends here: the copies already queued still read the
+  // caller's host buffers (or write o_host / lse_host), so they are drained before returning.
+  auto fail = [&](int status) {
+    cudaStreamSynchronize(hp->h2d);
+    cudaStreamSynchronize(st);
+    cudaStreamSynchronize(hp->d2h);
+    cudaGetLastError();
+    return status;
+  };
   // the copies must not overtake work already queued on the caller's stream
   if (cudaEventRecord(hp->ev_start, st) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0) != cudaSuccess)
-    return PSR_ERR_CUDA;
+    return fail(PSR_ERR_CUDA);
   auto cp_in = [&](void* dst, const void* src, size_t off, size_t n) {
     return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + off, static_cast<const uint8_t*>(src) + off, n,
                            cudaMemcpyHostToDevice, hp->h2d);
@@ -1458,17 +1455,17 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
     const size_t qo = u0[c] * q_u, ko = u0[c] * kv_u, qn = plan[c] * q_u, kn = plan[c] * kv_u;
     if (cp_in(dq, q_host, qo, qn) != cudaSuccess || cp_in(dk, k_host, ko, kn) != cudaSuccess ||
         cp_in(dv, v_host, ko, kn) != cudaSuccess || cudaEventRecord(hp->ev_in[c], hp->h2d) != cudaSuccess)
-      return PSR_ERR_CUDA;
+      return fail(PSR_ERR_CUDA);
   }
   for (int c = 0; c < n_sl; ++c) {
     const size_t qo = u0[c] * q_u, ko = u0[c] * kv_u, lo = u0[c] * l_u, qn = plan[c] * q_u, ln = plan[c] * l_u;
     const psr_shape ss = slice_shape(c);
-    if (cudaStreamWaitEvent(st, hp->ev_in[c], 0) != cudaSuccess) return PSR_ERR_CUDA;
+    if (cudaStreamWaitEvent(st, hp->ev_in[c], 0) != cudaSuccess) return fail(PSR_ERR_CUDA);
     const int rc = psr_ring_attn_fwd(&ss, static_cast<const uint8_t*>(dq) + qo, static_cast<const uint8_t*>(dk) + ko,
                                      static_cast<const uint8_t*>(dv) + ko, static_cast<uint8_t*>(d_o) + qo,
                                      reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(d_lse) + lo), workspace,
                                      ws_bytes, part, st);
-    if (rc != PSR_OK) return rc;
+    if (rc != PSR_OK) return fail(rc);
     // this slice's error word, before the next launch resets the control block
     if (cudaMemcpyAsync(hp->err_host + c, static_cast<uint8_t*>(workspace) + offsetof(Ctrl, error), 4,
                         cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -1477,9 +1474,10 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
                         cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess ||
         cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + lo, reinterpret_cast<const uint8_t*>(d_lse) + lo, ln,
                         cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
-      return PSR_ERR_CUDA;
+      return fail(PSR_ERR_CUDA);
   }
-  if (cudaStreamSynchronize(hp->d2h) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) return PSR_ERR_CUDA;
+  if (cudaStreamSynchronize(hp->d2h) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return fail(PSR_ERR_CUDA);
   for (int c = 0; c < n_sl; ++c)
     if (hp->err_host[c] != 0) return PSR_ERR_TIMEOUT;
   return PSR_OK;

@@ -57,3 +57,29 @@ def test_reference_arm_other_ranks_exit_quietly():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                           "--warmup", "0"], capture_output=True, text=True, timeout=120, env=env)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_config_roofline_arithmetic():
+    # the per-configuration roofline: flops and bytes worked out by hand for the headline shape
+    sys.path.insert(0, ROOT)
+    import bench
+    import ring_inputs as ri
+    w = ri.WORKLOADS["h32_s32k_nc"]
+    assert w.flops() == 4 * 128 * 32768 * 32768 * 32  # 1.759e13
+    # Q, K, V read, O written (32 heads x 32768 rows x 128 x 2 B each), LSE 32 x 32768 x 4 B, and the
+    # 240 ring transfers of a 2048-row chunk of K and V (1 MiB per head) read and written
+    tensor = 32 * 32768 * 128 * 2
+    staged = 16 * 15 * 32 * (2 * 2048 * 128 * 2)
+    assert bench.algorithmic_bytes(w) == 4 * tensor + 32 * 32768 * 4 + 2 * staged
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}
+    bound, frac = bench.roofline_of(w, 1e3 * w.flops() / 1e15, peaks)  # a pass at 1000 TFLOP/s
+    assert bound == "tensor" and abs(frac - 0.5) < 1e-12
+    # the large-P sweep point moves more bytes than its flops take at these peaks: HBM-bound
+    w64 = ri.WORKLOADS["sweep_d64_P64"]
+    bound, frac = bench.roofline_of(w64, 1.0, peaks)
+    assert bound == "hbm"
+    assert abs(frac - bench.algorithmic_bytes(w64) / 8e12 / 1e-3) < 1e-9
+    # every configuration is covered, each workload once
+    names = [n for _, ns in bench.CONFIGS for n in ns]
+    assert len(names) == len(set(names)) == 1 + 2 + 1 + 1 + 12
+    assert all(n in ri.WORKLOADS for n in names)
