@@ -514,19 +514,33 @@ def run_ours(args):
     dq, dk, dv = (torch.empty_like(t) for t in devt)
     h2d = sum(t.numel() * 2 for t in host) * len(wls)
     d2h = (o_h.numel() * 2 + l_h.numel() * 4) * len(wls)
-    e2e_steps = max(1, min(args.steps, 3))
+    e2e_steps = max(10, args.steps)
     for w in wls:  # warm the host path once
         psr.ring_attn_fwd_host(*host, o_h, l_h, dq, dk, dv, o, lse, P=w.P, causal=w.causal, scale=w.scale,
                                partition=part, workspace=ws, stream=stream)
-    dist_barrier(world)
+    # plain pinned-copy bandwidth of this machine, for reading the e2e figure (not part of the metric)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    dq.view(torch.int16).copy_(host[0], non_blocking=True)
+    torch.cuda.synchronize()
+    h2d_gbps = host[0].numel() * 2 / (time.perf_counter() - t0) / 1e9
+    t0 = time.perf_counter()
+    o_h.copy_(dq.view(torch.int16), non_blocking=True)
+    torch.cuda.synchronize()
+    d2h_gbps = o_h.numel() * 2 / (time.perf_counter() - t0) / 1e9
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    e2e_times = []
+    t_all = time.perf_counter()
     for _ in range(e2e_steps):
+        t0 = time.perf_counter()
         for w in wls:
             psr.ring_attn_fwd_host(*host, o_h, l_h, dq, dk, dv, o, lse, P=w.P, causal=w.causal, scale=w.scale,
                                    partition=part, workspace=ws, stream=stream)
-    e2e_s = dist_max((time.perf_counter() - t0) / e2e_steps, world)
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = dist_max((time.perf_counter() - t_all) / e2e_steps, world)
     e2e_value = dist_sum(flops_step, world) / e2e_s / 1e12
+    e2e_sorted = sorted(e2e_times)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -552,7 +566,10 @@ def run_ours(args):
                          "frac_of_sustained": round(kern_achieved / peak_sus, 4)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step_median": round(1e3 * statistics.median(e2e_times), 3),
+                    "ms_per_step_min_max": [round(1e3 * e2e_sorted[0], 3), round(1e3 * e2e_sorted[-1], 3)],
+                    "pinned_copy_GBps": {"h2d": round(h2d_gbps, 1), "d2h": round(d2h_gbps, 1)}},
             "gpu_launches": args.steps * len(wls),
             "clocks": clk,
             "passes": passes,
@@ -621,7 +638,7 @@ def run_sweep(args):
     psr.build()
     torch.cuda.set_device(0)
     ds = [args.sweep] if args.sweep in (64, 128) else [64, 128]
-    statics = [2, 4, 6, 8, 12, 16, 24, 32, 48, 64]
+    statics = [2, 4, 6, 8, 12, 16, 24, 32, 48, 64, 76]  # 76 = N/2, the adaptive mode's default upper clamp
     rows = []
     for d in ds:
         base = ri.WORKLOADS[f"sweep_d{d}_P2"]

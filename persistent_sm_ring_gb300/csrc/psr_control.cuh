@@ -119,8 +119,16 @@ constexpr double kUpdateHeadroom = PSR_UPDATE_HEADROOM / 100.0;  // staging head
 // Staging capacity (over the balanced split) that the wave cap keeps: the cap is the largest
 // split with the compute waves of the rule's split at this headroom.
 constexpr double kWaveMargin = PSR_WAVE_MARGIN / 100.0;
-// Shortest ring step (KV tiles) for which the wave cap is applied.
-constexpr int kWaveMinTiles = 8;
+#ifndef PSR_WAVE_MIN_TILES
+#define PSR_WAVE_MIN_TILES 4
+#endif
+// Shortest ring step (KV tiles) for which the wave cap is applied.  Measured on GB300 (partition
+// sweep, P = 32: 4-tile steps): once the staging tasks' control path stopped waiting on chains of
+// L2 round trips, compute items there were no longer bound by step latency, the static optimum sat
+// at the compute-wave boundary (48 of 152 stagers: the largest split with 10 waves), and the
+// adaptive target without the cap rose to 72-75 (1.10-1.16x the best static time).  Two-tile steps
+// (P = 64) are left out: there the cap does not bind under the default upper clamp anyway.
+constexpr int kWaveMinTiles = PSR_WAVE_MIN_TILES;
 
 // The initial split stands until this fraction of the compute tiles is done: it covers the
 // ring's fill, when every active group needs its first staged steps at once and measured
@@ -132,7 +140,7 @@ __device__ void controller_update(const KP& p) {
   Ctrl* c = p.ctrl;
   {
     const unsigned long long now = globaltimer_ns();
-    const unsigned long long last = atomicAdd(&c->last_eval_ns, 0ull);
+    const unsigned long long last = ld_relaxed64(&c->last_eval_ns);
     if (now - last < kCtrlMinIntervalNs) return;
     if (atomicCAS(&c->last_eval_ns, last, now) != last) return;  // another CTA evaluates now
   }
@@ -175,6 +183,18 @@ __device__ void controller_update(const KP& p) {
     p.traj[2 * k] = (uint32_t)((now > t0 ? now - t0 : 0) / 1000ull);
     p.traj[2 * k + 1] = (uint32_t)n;
   }
+}
+
+// Called by thread 0 of a CTA at its task boundaries: each CTA offers an evaluation at most
+// every kCtrlMinIntervalNs of its own (no shared counter on the task path); controller_update
+// then lets one CTA evaluate per interval.
+template <class KP>
+__device__ __forceinline__ void controller_tick(const KP& p, unsigned long long& next_offer_ns) {
+  if (p.mode != PSR_ADAPTIVE) return;
+  const unsigned long long now = globaltimer_ns();
+  if (now < next_offer_ns) return;
+  next_offer_ns = now + kCtrlMinIntervalNs;
+  controller_update(p);
 }
 
 }  // namespace psr

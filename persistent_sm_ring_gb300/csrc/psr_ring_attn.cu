@@ -104,7 +104,6 @@ struct KParams {
   int n_wave_cap;     // adaptive target bound while items remain unclaimed
   int fault;
   int lookahead;      // static list: groups ahead of the dispense frontier
-  int ctrl_period;    // tasks between controller evaluations
   float c_s0, c_p0;   // prior costs (cycles per staging task / per tile) before measurements exist
 };
 
@@ -180,15 +179,20 @@ struct StageTicket {
   bool done = false; // every queue entry has been handed out
 };
 
+// i0 / frontier_item: init_next and item_next as the caller last read them (its first attempt
+// uses them; later attempts read again).
 template <int BAL>
-__device__ int claim_static_piece(const KParams& p) {
+__device__ int claim_static_piece(const KParams& p, uint32_t i0, uint32_t frontier_item) {
   Ctrl* c = p.ctrl;
   const Geometry& G = p.geo;
   for (int attempt = 0; attempt < 8; ++attempt) {
-    const uint32_t i0 = ld_relaxed(&c->init_next);
+    if (attempt > 0) {
+      i0 = ld_relaxed(&c->init_next);
+      frontier_item = ld_relaxed(&c->item_next);
+    }
     if (i0 >= (uint32_t)p.n_init) return -1;
     const int g0 = (int)(i0 / ((uint32_t)kRingSlots * G.n_pieces));
-    const int frontier = (int)(ld_relaxed(&c->item_next) / (uint32_t)G.Gs);
+    const int frontier = (int)(frontier_item / (uint32_t)G.Gs);
     if (g0 > frontier + p.lookahead) return -1;
     const uint32_t i = atomicAdd(&c->init_next, 1u);
     if (i >= (uint32_t)p.n_init) return -1;
@@ -205,20 +209,34 @@ __device__ int claim_static_piece(const KParams& p) {
   return -1;
 }
 
+// sc != nullptr: a single staging CTA claiming its next piece while the current one's loads are in
+// flight; it claims only while it is still a stager (the controller's target, or a held entry).
 template <int BAL>
-__device__ int try_claim_staging(const KParams& p, StageTicket& tk) {
+__device__ int try_claim_staging(const KParams& p, StageTicket& tk, const SmemCtl* sc = nullptr) {
   Ctrl* c = p.ctrl;
-  if (tk.held >= 0) {
-    const uint32_t e = ld_acquire(&p.queue[tk.held]);
-    if (e != 0) {
-      tk.held = -1;
-      return (int)(e - 1);
-    }
+  // every word the branches below may read, loaded together: one round trip to L2 instead of
+  // a chain of dependent ones (a staging task is a few microseconds, so this latency counts)
+  const bool want_ticket = tk.held < 0 && !tk.done;
+  const uint32_t e_held = tk.held >= 0 ? ld_relaxed(&p.queue[tk.held]) : 0u;
+  const uint32_t i0 = ld_relaxed(&c->init_next);
+  const uint32_t item = ld_relaxed(&c->item_next);
+  const uint32_t qh = want_ticket ? ld_relaxed(&c->q_head) : 0u;
+  if (sc != nullptr) {
+    const uint32_t w_abort = ld_relaxed(&c->abort);
+    const uint32_t w_target = p.mode == PSR_STATIC ? 0u : ld_relaxed(&c->target_ns);
+    const int n_s = p.mode == PSR_STATIC ? p.n_s_init : (w_target ? (int)(w_target - 1) : p.n_s_init);
+    if (sc->abort || w_abort) return -1;
+    if ((int)blockIdx.x >= n_s && tk.held < 0) return -1;
   }
-  const int t = claim_static_piece<BAL>(p);
+  if (e_held != 0) {
+    fence_acq_rel_gpu();  // the entry was published with release: acquire it
+    tk.held = -1;
+    return (int)(e_held - 1);
+  }
+  const int t = claim_static_piece<BAL>(p, i0, item);
   if (t >= 0) return t;
-  if (tk.held < 0 && !tk.done) {
-    if (ld_relaxed(&c->q_head) >= (uint32_t)p.n_dyn) {
+  if (want_ticket) {
+    if (qh >= (uint32_t)p.n_dyn) {
       tk.done = true;
     } else {
       const uint32_t h = atomicAdd(&c->q_head, 1u);
@@ -237,19 +255,20 @@ __device__ int try_claim_staging(const KParams& p, StageTicket& tk) {
   return -1;
 }
 
-// every static-list entry and every ready-queue ticket has been handed out
-__device__ bool staging_all_claimed(const KParams& p) {
-  return ld_relaxed(&p.ctrl->init_next) >= (uint32_t)p.n_init && ld_relaxed(&p.ctrl->q_head) >= (uint32_t)p.n_dyn;
-}
-
 // Role of the compute unit for its next task: CMD_STAGE (each CTA of the unit then claims a
 // piece, or idles when none is claimable), CMD_COMPUTE with item `arg`, or CMD_EXIT.
 // Unit u stages while u * CG < n_s (the controller's target counts CTAs).
 template <int CG>
 __device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging, const StageTicket& tk) {
   Ctrl* c = p.ctrl;
-  if (sc->abort || ld_relaxed(&c->abort)) { sc->cmd = CMD_EXIT; return; }
-  const int n_s = current_target(p);
+  // every control word the decision reads, loaded together (one round trip to L2)
+  const uint32_t w_abort = ld_relaxed(&c->abort);
+  const uint32_t w_target = p.mode == PSR_STATIC ? 0u : ld_relaxed(&c->target_ns);
+  const uint32_t w_init = ld_relaxed(&c->init_next);
+  const uint32_t w_qhead = ld_relaxed(&c->q_head);
+  const uint32_t w_item = ld_relaxed(&c->item_next);
+  if (sc->abort || w_abort) { sc->cmd = CMD_EXIT; return; }
+  const int n_s = p.mode == PSR_STATIC ? p.n_s_init : (w_target ? (int)(w_target - 1) : p.n_s_init);
   const int unit = (int)blockIdx.x / CG;
   // a unit whose CTA owns a queue entry stages until that entry is served
   const bool held = tk.held >= 0 || (CG == 2 && sc->peer_held != 0);
@@ -258,13 +277,13 @@ __device__ void decide(const KParams& p, SmemCtl* sc, bool& was_staging, const S
     atomicAdd(&c->role_switches, 1ull);
     was_staging = staging_role;
   }
-  const bool all_claimed = !held && staging_all_claimed(p);
+  const bool all_claimed = !held && w_init >= (uint32_t)p.n_init && w_qhead >= (uint32_t)p.n_dyn;
   if (staging_role) {
     if (!all_claimed) { sc->cmd = CMD_STAGE; return; }
     if (p.mode == PSR_STATIC) { sc->cmd = CMD_EXIT; return; }
     // adaptive: nothing left to stage; fall through to compute
   }
-  if (ld_relaxed(&c->item_next) < (uint32_t)p.geo.n_items) {
+  if (w_item < (uint32_t)p.geo.n_items) {
     const uint32_t n = atomicAdd(&c->item_next, 1u);
     if (n < (uint32_t)p.geo.n_items) { sc->cmd = CMD_COMPUTE; sc->arg = (int)n; return; }
   }
@@ -296,9 +315,11 @@ __device__ __forceinline__ void publish_pending(StagePending& pend) {
   pend.flag = nullptr;
 }
 
+// tk != nullptr: once this piece's first loads are in flight, claim the next piece into *next
+// (-1 if none), so that the claim's round trips to L2 overlap the copy.
 template <int D, int CG, int BAL>
 __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, int task, uint32_t (&stg_phase)[16],
-                            StagePending& pend) {
+                            StagePending& pend, StageTicket* tk, int* next) {
   using C = Cfg<D, CG>;
   const Geometry& G = p.geo;
   const int chunk = task / G.n_pieces, piece = task % G.n_pieces;
@@ -332,6 +353,7 @@ __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, i
   for (int u = 0; u < pre; ++u) issue_load(u);
   int issued = pre;
   publish_pending(pend);  // the previous piece's stores complete while these loads are in flight
+  if (tk != nullptr) *next = try_claim_staging<BAL>(p, *tk, sc);
   bool ok = true;
   for (int u = 0; u < n_u; ++u) {
     const int bi = u % NB;
@@ -878,6 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long t_task = 0;
     Starved starved;
     uint64_t idle_since = 0;  // first idle poll of the current idle stretch (0 = not idle)
+    unsigned long long next_offer_ns = 0;  // thread 0: next time this CTA may offer a controller evaluation
     while (true) {
       if (threadIdx.x == 0) {
         if (rank == 0) decide<CG>(p, &sc, was_staging, ticket);
@@ -887,14 +910,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cmd, arg;
       read_cmd<CG>(sc, rank, cmd, arg);
       if (cmd == CMD_EXIT) break;
-      int done_kind = cmd;  // thread 0: CMD_STAGE (a piece was staged), CMD_COMPUTE or CMD_IDLE
+      int done_kind = cmd;  // thread 0: CMD_COMPUTE (accounted at the boundary below) or CMD_IDLE
       // a deferred publication waits only while this CTA goes straight on to another piece
       if (threadIdx.x == 0 && cmd != CMD_STAGE) publish_pending(pend);
       if (cmd == CMD_STAGE) {
         if (threadIdx.x == 0) {
-          const int task = try_claim_staging<BAL>(p, ticket);
+          int task = try_claim_staging<BAL>(p, ticket);
           if (task >= 0) {
-            run_staging<D, CG, BAL>(p, &sc, smem_base, task, stg_phase, pend);
+            // Consecutive pieces without returning to the task boundary (the CTA's other threads
+            // wait there): a single CTA claims its next piece while the current one's loads are in
+            // flight, and every piece is accounted for the controller as it ends.
+            while (task >= 0) {
+              int next = -1;
+              run_staging<D, CG, BAL>(p, &sc, smem_base, task, stg_phase, pend, CG == 1 ? &ticket : nullptr, &next);
+              const long long now = clock64();
+              atomicAdd(&p.ctrl->stage_cycles, (unsigned long long)(now - t_task));
+              atomicAdd(&p.ctrl->stage_done, 1ull);
+              t_task = now;
+              controller_tick(p, next_offer_ns);
+              task = next;
+            }
+            done_kind = CMD_IDLE;  // accounted piece by piece above
             idle_since = 0;
           } else {
             publish_pending(pend);
@@ -930,20 +966,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicAdd(&p.ctrl->starve_cycles, (unsigned long long)(starved.late > 0 ? starved.late : 0));  // ... charged to staging
         }
         const unsigned long long dt = (unsigned long long)(busy > 0 ? busy : 0);
-        if (done_kind == CMD_STAGE) {
-          atomicAdd(&p.ctrl->stage_cycles, dt);
-          atomicAdd(&p.ctrl->stage_done, 1ull);
-        } else {
-          // cycles from every CTA of the unit (the cost of a tile in CTA-cycles); tiles and items once
-          atomicAdd(&p.ctrl->compute_cycles, dt);
-          if (rank == 0) {
-            const ItemCoord it = item_coord<BAL>(p.geo, arg);
-            atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles<BAL>(p.geo, it));
-            atomicAdd(&p.ctrl->compute_items, 1ull);
-          }
+        // cycles from every CTA of the unit (the cost of a tile in CTA-cycles); tiles and items once
+        atomicAdd(&p.ctrl->compute_cycles, dt);
+        if (rank == 0) {
+          const ItemCoord it = item_coord<BAL>(p.geo, arg);
+          atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles<BAL>(p.geo, it));
+          atomicAdd(&p.ctrl->compute_items, 1ull);
         }
-        const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
-        if (p.mode == PSR_ADAPTIVE && (tick % (uint32_t)p.ctrl_period) == 0) controller_update(p);
+        controller_tick(p, next_offer_ns);
       }
     }
     // drain: every tcgen05 op issued by this CTA has completed before TMEM is released
@@ -1333,7 +1363,7 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
     if (any_staging && !G.causal && cg == 1 && kp.n_dyn > 0 && pt.n_staging <= 0 && G.kv_tiles >= kWaveMinTiles) {
       const int n_need = controller_rule(n_cta, (double)kp.n_stage_total, kWaveMargin * kp.c_s0,
                                          (double)kp.n_tiles_total, kp.c_p0, n_min, n_max);
-      const int cap = wave_cap(n_cta, n_need, G.n_items);
+      const int cap = wave_cap_groups(n_cta, n_need, wave_cap(n_cta, n_need, G.n_items), G.Gs);
       if (cap < n_max) {
         kp.n_wave_items = (uint32_t)G.n_items;
         kp.n_wave_cap = cap < n_min ? n_min : cap;
@@ -1343,7 +1373,6 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   }
   kp.n_s_init = n_s;
   kp.lookahead = n_units / G.Gs + 2;
-  kp.ctrl_period = n_cta / 8 > 1 ? n_cta / 8 : 1;
 
   CUtensorMap maps[5];
   const long long rows_q = (long long)G.B * G.Hq * G.S, rows_kv = (long long)G.B * G.Hkv * G.S;

@@ -309,6 +309,18 @@ PSR_HD int wave_cap(int n_cta, int n_need, long long U) {
   return n_cta - (int)((U + w - 1) / w);
 }
 
+// The wave cap made to hold whole groups: the items of one group share their ring slots, and a
+// slot can be refilled only once every item of the group has loaded it, so a group whose items
+// straddle a wave boundary holds its first items back by up to a whole item.  Returns the largest
+// split n in [n_need, cap] whose compute CTAs N - n are a multiple of the group size Gs, or cap
+// when there is none.
+PSR_HD int wave_cap_groups(int n_cta, int n_need, int cap, int Gs) {
+  if (Gs <= 1) return cap;
+  for (int n = cap; n >= n_need && n >= 0; --n)
+    if ((n_cta - n) % Gs == 0) return n;
+  return cap;
+}
+
 // Slice sizes (in units: batches, or KV-head groups) of the host-buffer pipeline, in order.  The
 // copies in of slice c+1 and out of slice c-1 overlap the kernel of slice c, so only the first
 // slice's upload and the last slice's download are exposed: the sizes ramp up from one unit by

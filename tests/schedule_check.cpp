@@ -58,6 +58,18 @@ static int check_wave_cap() {
       }
   CHECK(wave_cap(152, 20, 0) == 152 && wave_cap(152, 152, 100) == 152, "wave_cap without a cap");
   CHECK(wave_cap(152, 21, 1024) == 24 && wave_cap(152, 41, 1024) == 49, "wave_cap examples");
+  // wave_cap_groups against its definition: the largest n in [need, cap] with N - n a multiple of Gs
+  for (int N = 2; N <= 160; N += 3)
+    for (int need = 0; need < N; need += 2)
+      for (int cap = need; cap < N; cap += 3)
+        for (int Gs = 1; Gs <= 9; ++Gs) {
+          int want = cap;
+          for (int n = need; n <= cap; ++n)
+            if ((N - n) % Gs == 0) want = n;
+          const int got = wave_cap_groups(N, need, cap, Gs);
+          CHECK(got == want, "wave_cap_groups N=%d need=%d cap=%d Gs=%d: %d, enumeration %d", N, need, cap, Gs, got, want);
+        }
+  CHECK(wave_cap_groups(152, 41, 49, 2) == 48 && wave_cap_groups(152, 21, 24, 4) == 24, "wave_cap_groups examples");
   std::printf("OK wave_cap\n");
   return 0;
 }

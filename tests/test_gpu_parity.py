@@ -192,13 +192,17 @@ def test_initial_split_keeps_compute_waves(psr):
     """The adaptive launch's initial split on a 152-SM GB300.  B1 H16 S16384 has 1024 equal
     (non-causal) items: at P = 16 the rule with its staging headroom asks for ~30 staging CTAs,
     which leaves 122 compute CTAs and 9 waves; 24 is the largest split with 8 waves (1024 / 128),
-    so the launch starts there.  P = 32 (4-tile ring steps) and d = 128, P = 16 (the rule's 32 is
-    below the 9-wave cap of 38) start at the rule's split."""
+    so the launch starts there.  At P = 32 (4-tile ring steps) the rule asks for 51 (d = 64) and
+    54 (d = 128); the split the staging work needs (41 and 43 at the wave margin) leaves 10
+    waves, 49 is the largest split with 10 (152 - ceil(1024 / 10)), and 48 the largest whose
+    compute CTAs hold whole two-item groups.  d = 128, P = 16 (the rule's 32 is below the
+    group-aligned 9-wave cap of 36) starts at the rule's split."""
     torch = _torch()
     if psr.num_ctas() != 152:
         pytest.skip("expected splits are for 152 SMs")
     assert -(-1024 // (152 - 24)) == 8 and -(-1024 // (152 - 25)) == 9
-    for name, want in (("sweep_d64_P16", 24), ("sweep_d64_P32", 51), ("sweep_d128_P16", 32)):
+    assert -(-1024 // (152 - 49)) == 10 and -(-1024 // (152 - 50)) == 11 and (152 - 48) % 2 == 0
+    for name, want in (("sweep_d64_P16", 24), ("sweep_d64_P32", 48), ("sweep_d128_P32", 48), ("sweep_d128_P16", 32)):
         w = ri.WORKLOADS[name]
         sh = (w.B, w.Hq, w.S, w.d)
         q = torch.zeros(sh, dtype=torch.bfloat16, device="cuda")
