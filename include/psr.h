@@ -139,16 +139,17 @@ PSR_API int psr_ring_attn_fwd(const psr_shape* shape, const void* q, const void*
 /* Same operation with HOST buffers: copies q, k, v (host; pinned for overlap)
  * to the caller's device buffers dq, dk, dv (same layouts and sizes as the
  * device entry's q, k, v, o, lse), runs the attention, copies O and LSE back
- * to o_host / lse_host, and returns when they are there.  Shapes of 64 MB of
- * Q or more run in up to 16 slices of whole batches (B > 1) or of whole
- * KV-head groups with their query heads (B = 1), sized 1, 2, 4, ... units
- * and back down to 1, so that only the first slice's copy in and the last
- * slice's copy out are exposed: the copies in of slice c+1 and out of slice
- * c-1 overlap the kernel of slice c (two internal streams, created once per
- * device; one launch per slice on `stream`).  The workspace
- * is sized for the whole shape.  psr_get_stats afterwards describes the last
- * slice's launch.  Returns the first failing status, or PSR_ERR_TIMEOUT if a
- * slice's launch reported a device timeout. */
+ * to o_host / lse_host, and returns when they are there.  One persistent
+ * launch covers the whole shape; the inputs are uploaded unit by unit (a unit
+ * is one batch when B > 1, else one KV head with its query heads) on an
+ * internal stream that marks each unit ready in the workspace, the launch
+ * dispenses its items unit by unit and each item waits (bounded by
+ * part->timeout_ms) for its unit, and a second internal stream copies each
+ * unit's O and LSE out as soon as all of its items are done.  So only the first
+ * unit's upload and the last unit's download are exposed.  The workspace is
+ * psr_workspace_bytes(shape); psr_get_stats afterwards describes the launch.
+ * Returns the first failing status, or PSR_ERR_TIMEOUT if the launch reported
+ * a device timeout (for instance an upload slower than the wait bound). */
 PSR_API int psr_ring_attn_fwd_host(const psr_shape* shape, const void* q_host, const void* k_host, const void* v_host,
                            void* o_host, float* lse_host, void* dq, void* dk, void* dv, void* d_o, float* d_lse,
                            void* workspace, size_t workspace_bytes, const psr_partition* part, void* stream);

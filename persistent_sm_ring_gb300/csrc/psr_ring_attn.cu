@@ -53,7 +53,7 @@ __device__ __forceinline__ long long trace_clock() { return kTrace ? clock64() :
 // ------------------------------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t ctrl, flags, consumed, queue, traj, slot_k, slot_v, total, reset_bytes;
+  size_t ctrl, flags, consumed, queue, io, traj, slot_k, slot_v, total, reset_bytes;
 };
 
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -67,6 +67,7 @@ static WsLayout ws_layout(const Geometry& G) {
   w.flags = off; off = align_up(off + n_fc * G.n_pieces * 4, 256);  // per (group, step, piece)
   w.consumed = off; off = align_up(off + n_fc * 4, 256);
   w.queue = off; off = align_up(off + (size_t)(dynamic_staging_pieces(G) + 1) * 4, 256);
+  w.io = off; off = align_up(off + (size_t)2 * unit_count(G) * 4, 256);  // per unit: inputs ready, items done
   w.reset_bytes = off;  // everything above is zeroed before each launch
   const size_t slot_elems = (size_t)kRingSlots * G.n_groups * G.L * G.d;
   w.slot_k = off; off = align_up(off + slot_elems * 2, 256);
@@ -105,6 +106,12 @@ struct KParams {
   int fault;
   int lookahead;      // static list: groups ahead of the dispense frontier
   float c_s0, c_p0;   // prior costs (cycles per staging task / per tile) before measurements exist
+  // Host-buffer entry only (nullptr otherwise): per unit (a batch, or a KV head with its query
+  // heads), a word the upload stream sets once the unit's Q, K, V are in device memory, and the
+  // count of the unit's items whose O and LSE are written (the download stream waits on it).
+  const uint32_t* in_ready;
+  uint32_t* out_done;
+  int n_units;
 };
 
 // Warpgroup 0: warp 0 = TMA producer / staging / scheduler thread, warp 1 = MMA issuer (in a
@@ -132,6 +139,9 @@ struct Cfg {
   static constexpr uint32_t KBLK = (kTileRows / CG) * 128;  // bytes of one 64-column block of the K share
   static_assert(NB * QT <= 2 * QT + NSTAGE * KVB, "staging buffers must fit in the compute region");
   static_assert(NB <= 16, "staging barriers");
+  // the MMA issuer acquires K_{j+1} before issuing PV(j): K_{j+1}'s stage was last used by load
+  // 2j+2-NSTAGE, which must be released by MMAs already issued (V_{j-1} at the latest)
+  static_assert(NSTAGE >= 3, "K/V stages");
   static_assert(SMEM <= 232448 - 512, "shared memory");
 };
 
@@ -140,8 +150,11 @@ enum : int { CMD_EXIT = 0, CMD_COMPUTE = 1, CMD_STAGE = 2, CMD_IDLE = 3 };
 // error sites
 enum : uint32_t {
   SITE_NONE = 0, SITE_FLAG = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_S_FULL = 4, SITE_P_FULL = 5,
-  SITE_O_FULL = 6, SITE_Q_FULL = 7, SITE_STAGE_LOAD = 8, SITE_DRAIN = 9, SITE_QUEUE = 10, SITE_IDLE = 11
+  SITE_O_FULL = 6, SITE_Q_FULL = 7, SITE_STAGE_LOAD = 8, SITE_DRAIN = 9, SITE_QUEUE = 10, SITE_IDLE = 11,
+  SITE_INPUT = 12
 };
+
+
 
 struct SmemCtl {
   uint64_t q_full[2];
@@ -158,6 +171,18 @@ struct SmemCtl {
   uint32_t peer_held;  // pair: the odd CTA holds a ready-queue ticket (written by that CTA)
   uint32_t p_sink[4];  // pair: landing words of the odd CTA's P-ready signals (never read)
 };
+
+// Host-buffer entry: bounded wait until the unit's inputs are in device memory (the upload
+// stream's write follows a system-wide fence after the copies), then order the async proxy's
+// reads after it.
+__device__ __forceinline__ bool wait_inputs(const KParams& p, SmemCtl* sc, int b, int kvh) {
+  if (p.in_ready == nullptr) return true;
+  uint32_t seen = 0;
+  if (!wait_flag(p.in_ready + unit_of(p.geo, b, kvh), 1u, seen, p, sc, SITE_INPUT)) return false;
+  fence_proxy_async_global();
+  return true;
+}
+
 
 
 // ------------------------------------------------------------------------------------------------
@@ -334,6 +359,10 @@ __device__ void run_staging(const KParams& p, SmemCtl* sc, uint32_t smem_base, i
   const size_t src_off = ((size_t)(b * G.Hkv + kvh) * G.S + (size_t)j * G.L + (size_t)kt0 * kTileRows) * D;
   const size_t slot_off = (((size_t)slot_of(step) * G.n_groups + g) * (size_t)G.L + (size_t)kt0 * kTileRows) * D;
   uint32_t* flag = p.flags + (size_t)chunk * G.n_pieces + piece;
+  if (!wait_inputs(p, sc, b, kvh)) {
+    sc->abort = 1;
+    return;
+  }
   const bool drop = (p.fault == PSR_FAULT_DROP_FIRST_FLAG) && (atomicAdd(&p.ctrl->fault_count, 1u) == 0u);
   if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
   // staging "acquire": queue entries were published with release after the slot's
@@ -456,6 +485,11 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
   const bool leader = rank == 0;
   const uint32_t sQ = smem_base, sStage = smem_base + 2 * C::QT;
   auto bar_cl = [](uint64_t* b) -> uint32_t { return CG == 2 ? mapa_shared(smem_u32(b), 0) : 0u; };
+  Starved starved;
+  if (!wait_inputs(p, sc, it.b, it.kvh)) {
+    sc->abort = 1;
+    return starved;
+  }
   // Q tiles (the barrier phase of q_full is the item count)
   const int q_row = (it.b * G.Hq + it.hq) * G.S + it.r * G.L + it.qp * G.item_rows + (int)rank * kCtaRows;
   for (int i = 0; i < 2; ++i) {
@@ -493,7 +527,6 @@ __device__ Starved producer(const KParams& p, SmemCtl* sc, uint32_t smem_base, c
   };
   bool ok = true;
   unsigned long long tr_empty = 0;
-  Starved starved;
   for (int t = 0; t < it.n_steps && ok; ++t) {
     const int j = ((it.r - t) % G.P + G.P) % G.P;
     const int n_kt = tiles_at_step<BAL>(G, it, t);
@@ -614,20 +647,20 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
   if (!wait_bar(&sc->kv_full[stage_of(ck)], par_of(ck), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
   tc_fence_after();
   for (int i = 0; i < 2; ++i) issue_s(i, stage_of(ck));
+  // K_{j+1} is acquired together with V_j, before the first block of the step: a wait between the
+  // PV and QK^T halves of a block would let the tensor core's short queue run dry (measured on
+  // GB300: each pause of the issuing thread costs the pipeline's refill on top of the wait).
   for (uint32_t jt = 0; jt < n; ++jt, ck += 2) {
     const uint32_t cv = ck + 1, cn = ck + 2;  // V_j, K_{j+1}
+    const bool more = jt + 1 < n;
     const long long a0 = trace_clock();
     if (!wait_bar(&sc->kv_full[stage_of(cv)], par_of(cv), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
+    if (more && !wait_bar(&sc->kv_full[stage_of(cn)], par_of(cn), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
     tr_kv += trace_clock() - a0;
     for (int i = 0; i < 2; ++i) {
       const long long a2 = trace_clock();
       if (!issue_pv(i, stage_of(cv), jt == 0, (cnt.tiles + jt) & 1u)) { sc->abort = 1; return; }
-      if (jt + 1 < n) {
-        const long long b0 = trace_clock();
-        if (!wait_bar(&sc->kv_full[stage_of(cn)], par_of(cn), p, sc, SITE_KV_FULL)) { sc->abort = 1; return; }
-        tr_kv += trace_clock() - b0;
-        issue_s(i, stage_of(cn));
-      }
+      if (more) issue_s(i, stage_of(cn));
       tr_issue += trace_clock() - a2;
     }
   }
@@ -972,6 +1005,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const ItemCoord it = item_coord<BAL>(p.geo, arg);
           atomicAdd(&p.ctrl->compute_tiles, (unsigned long long)item_tiles<BAL>(p.geo, it));
           atomicAdd(&p.ctrl->compute_items, 1ull);
+          // the item's O and LSE rows (stored by the softmax warps before the unit barrier) are
+          // released at system scope to the download stream
+          if (p.out_done != nullptr && !sc.abort) red_add_release_sys(p.out_done + unit_of(p.geo, it.b, it.kvh), 1u);
         }
         controller_tick(p, next_offer_ns);
       }
@@ -985,6 +1021,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (threadIdx.x == 0) {
+      // a launch that gave up releases every unit's completion word, so that a download stream
+      // waiting on one of them never waits for items that will not finish
+      if (p.out_done != nullptr && (sc.abort || ld_relaxed(&p.ctrl->abort)))
+        for (int u = 0; u < p.n_units; ++u) st_release_sys(p.out_done + u, 0x40000000u);
       publish_pending(pend);
       bulk_wait<0>();
       // every TMA load of a compute item has landed (normally already true); a pair's
@@ -1168,13 +1208,12 @@ static cudaError_t launch(const KParams& kp, const CUtensorMap* maps, int n_cta,
   return e;
 }
 
-// Streams and events of the host-buffer entry point, one set per device and process (created on
-// first use, never freed); calls on one device serialise on a mutex.  err_host is pinned host
-// memory that receives each slice's error word.
-constexpr int kHostSlices = 16;  // most slices of one call
+// Streams of the host-buffer entry point, one set per device and process (created on first use,
+// never freed); calls on one device serialise on a mutex.  err_host is pinned host memory that
+// receives the launch's error word.
 struct HostPipe {
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_in[kHostSlices] = {}, ev_out[kHostSlices] = {};
+  cudaEvent_t ev_start = nullptr;
   uint32_t* err_host = nullptr;
   std::mutex mu;
 };
@@ -1190,17 +1229,37 @@ static HostPipe* host_pipe() {
   bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&hp.ev_start, cudaEventDisableTiming) == cudaSuccess;
-  for (int c = 0; ok && c < kHostSlices; ++c)
-    ok = cudaEventCreateWithFlags(&hp.ev_in[c], cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&hp.ev_out[c], cudaEventDisableTiming) == cudaSuccess;
   void* pinned = nullptr;
-  ok = ok && cudaHostAlloc(&pinned, kHostSlices * sizeof(uint32_t), cudaHostAllocDefault) == cudaSuccess;
+  ok = ok && cudaHostAlloc(&pinned, sizeof(uint32_t), cudaHostAllocDefault) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     return nullptr;
   }
   hp.err_host = static_cast<uint32_t*>(pinned);
   return &hp;
+}
+
+// The driver's stream memory operations: a stream writes a word once its earlier copies have
+// completed (with a system-wide fence before the write), or waits until a word reaches a value.
+struct StreamMemOps {
+  PFN_cuStreamWriteValue32_v11070 write = nullptr;
+  PFN_cuStreamWaitValue32_v11070 wait = nullptr;
+};
+
+static const StreamMemOps& stream_mem_ops() {
+  static StreamMemOps ops;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &f, 11070, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      ops.write = reinterpret_cast<PFN_cuStreamWriteValue32_v11070>(f);
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &f, 11070, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      ops.wait = reinterpret_cast<PFN_cuStreamWaitValue32_v11070>(f);
+  });
+  return ops;
 }
 
 }  // namespace psr
@@ -1264,8 +1323,18 @@ int psr_internal_fwd_check(const psr_shape* sh, const void* q, const void* k, co
   return rc;
 }
 
-int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const void* v, void* o, float* lse,
-                      void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
+// Everything a forward launch needs, checked and encoded on the host (no CUDA work enqueued).
+struct FwdLaunch {
+  KParams kp;
+  CUtensorMap tmaps[5];
+  int n_cta = 0, cg = 1, d = 0;
+  bool bal = false;
+  uint8_t* ws = nullptr;
+  WsLayout L;
+};
+
+static int fwd_setup(const psr_shape* sh, const void* q, const void* k, const void* v, void* o, float* lse,
+                     void* workspace, size_t ws_bytes, const psr_partition* part, FwdLaunch& F) {
   if (!workspace) return PSR_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PSR_ERR_ARG;
   DeviceInfo di;
@@ -1274,9 +1343,10 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   if (rc != PSR_OK) return rc;
   const int cg = G.cg;
   const int n_cta = di.n_sm / cg * cg;  // whole pairs
-  const int n_units = n_cta / cg;
+  const int n_cunits = n_cta / cg;  // compute units (CTAs, or CTA pairs)
   const WsLayout L = ws_layout(G);
   if (ws_bytes < L.total) return PSR_ERR_ARG;
+  KParams& kp = F.kp;
 
   psr_partition pt;
   if (part) pt = *part;
@@ -1284,9 +1354,9 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   if (pt.mode != PSR_STATIC && pt.mode != PSR_ADAPTIVE) return PSR_ERR_ARG;
   if (pt.fault < 0 || pt.fault > PSR_FAULT_SLOW_STAGING) return PSR_ERR_ARG;
 
-  KParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.geo = G;
+  kp.n_units = unit_count(G);
   const double scale = sh->scale > 0.0f ? (double)sh->scale : 1.0 / std::sqrt((double)sh->d);
   kp.scale_log2 = (float)(scale * 1.4426950408889634);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1337,7 +1407,7 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
     if (!any_staging) n_s = 0;
     else if (n_s < 1 || n_s > n_cta - 1) return PSR_ERR_ARG;
     // a group could never be fully resident
-    if (any_staging && n_units - (n_s + cg - 1) / cg < G.Gs) return PSR_ERR_ARG;
+    if (any_staging && n_cunits - (n_s + cg - 1) / cg < G.Gs) return PSR_ERR_ARG;
   } else {
     // initial split: the rule on the prior costs with the staging cost raised by the headroom.  At launch every
     // active group needs its first staged steps at once, and later a group's staging can run
@@ -1372,9 +1442,9 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
     }
   }
   kp.n_s_init = n_s;
-  kp.lookahead = n_units / G.Gs + 2;
+  kp.lookahead = n_cunits / G.Gs + 2;
 
-  CUtensorMap maps[5];
+  CUtensorMap* maps = F.tmaps;
   const long long rows_q = (long long)G.B * G.Hq * G.S, rows_kv = (long long)G.B * G.Hkv * G.S;
   const long long rows_slot = (long long)kRingSlots * G.n_groups * G.L;
   // K maps: a pair's CTA loads 64 of every 128 K rows
@@ -1383,21 +1453,28 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
       !make_tmap(&maps[2], v, rows_kv, G.d) || !make_tmap(&maps[3], kp.slot_k, rows_slot, G.d, k_box) ||
       !make_tmap(&maps[4], kp.slot_v, rows_slot, G.d))
     return PSR_ERR_CUDA;
+  F.n_cta = n_cta;
+  F.cg = cg;
+  F.d = G.d;
+  F.bal = G.balanced != 0;
+  F.ws = ws;
+  F.L = L;
+  return PSR_OK;
+}
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
-  // one kernel per (d, compute unit, shard layout); CTA-pair kernels only in a library built with pairs
-  const bool bal = G.balanced != 0;
+// The persistent launch itself (one kernel per d, compute unit and shard layout; CTA-pair kernels
+// only in a library built with pairs).  The control words must have been cleared before it.
+static int fwd_enqueue(const FwdLaunch& F, cudaStream_t st) {
   cudaError_t e;
 #if PSR_PAIRS
-  if (cg == 2)
-    e = bal ? launch<128, 2, 1>(kp, maps, n_cta, st) : launch<128, 2, 0>(kp, maps, n_cta, st);
+  if (F.cg == 2)
+    e = F.bal ? launch<128, 2, 1>(F.kp, F.tmaps, F.n_cta, st) : launch<128, 2, 0>(F.kp, F.tmaps, F.n_cta, st);
   else
 #endif
-  if (G.d == 128)
-    e = bal ? launch<128, 1, 1>(kp, maps, n_cta, st) : launch<128, 1, 0>(kp, maps, n_cta, st);
+  if (F.d == 128)
+    e = F.bal ? launch<128, 1, 1>(F.kp, F.tmaps, F.n_cta, st) : launch<128, 1, 0>(F.kp, F.tmaps, F.n_cta, st);
   else
-    e = bal ? launch<64, 1, 1>(kp, maps, n_cta, st) : launch<64, 1, 0>(kp, maps, n_cta, st);
+    e = F.bal ? launch<64, 1, 1>(F.kp, F.tmaps, F.n_cta, st) : launch<64, 1, 0>(F.kp, F.tmaps, F.n_cta, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PSR_ERR_CUDA;
@@ -1405,67 +1482,47 @@ int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const v
   return PSR_OK;
 }
 
+int psr_ring_attn_fwd(const psr_shape* sh, const void* q, const void* k, const void* v, void* o, float* lse,
+                      void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
+  FwdLaunch F;
+  const int rc = fwd_setup(sh, q, k, v, o, lse, workspace, ws_bytes, part, F);
+  if (rc != PSR_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(F.ws, 0, F.L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
+  return fwd_enqueue(F, st);
+}
+
 int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* k_host, const void* v_host,
                            void* o_host, float* lse_host, void* dq, void* dk, void* dv, void* d_o, float* d_lse,
                            void* workspace, size_t ws_bytes, const psr_partition* part, void* stream) {
   if (!sh || !q_host || !k_host || !v_host || !o_host || !lse_host) return PSR_ERR_ARG;
-  if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 1 || sh->d < 1) return PSR_ERR_ARG;
-  if (!dq || !dk || !dv || !d_o || !d_lse || !workspace) return PSR_ERR_ARG;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PSR_ERR_ARG;
-  for (const void* ptr : {(const void*)dq, (const void*)dk, (const void*)dv, (const void*)d_o, (const void*)d_lse})
-    if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return PSR_ERR_ARG;
-  if (sh->Hq % sh->Hkv != 0) return PSR_ERR_UNSUPPORTED;
-  // The whole shape must be launchable (validates the shape and the workspace size once).
-  {
-    Geometry G;
-    DeviceInfo di;
-    if (!device_info(di)) return PSR_ERR_CUDA;
-    const int rc = shape_geometry(sh, G, di.n_sm);
-    if (rc != PSR_OK) return rc;
-    if (ws_bytes < ws_layout(G).total) return PSR_ERR_ARG;
-  }
-  // Slices: contiguous batches, or (one batch) contiguous KV-head groups with their query heads,
-  // sized by host_slice_plan (1, 2, 4, ... units and back down to 1).  Slice c+1 is copied in
-  // while slice c computes and slice c-1 is copied out.
-  const size_t row_b = (size_t)sh->S * sh->d * 2;  // bytes of one head's Q/K/V/O rows
-  const size_t q_bytes = (size_t)sh->B * sh->Hq * row_b;
-  const bool by_batch = sh->B > 1;
-  const int units = by_batch ? sh->B : sh->Hkv;
-  int plan[kHostSlices];
-  int n_sl = 1;
-  plan[0] = units;
-  if (q_bytes >= ((size_t)64 << 20)) n_sl = host_slice_plan(units, plan, kHostSlices);
-  // per unit: query rows, KV rows and LSE entries of one batch (or of one KV-head group)
-  const size_t q_u = (by_batch ? (size_t)sh->Hq : (size_t)(sh->Hq / sh->Hkv)) * row_b;
-  const size_t kv_u = (by_batch ? (size_t)sh->Hkv : (size_t)1) * row_b;
-  const size_t l_u = (by_batch ? (size_t)sh->Hq : (size_t)(sh->Hq / sh->Hkv)) * sh->S * 4;
-  auto slice_shape = [&](int c) {
-    psr_shape ss = *sh;
-    if (by_batch) ss.B = plan[c];
-    else { ss.Hkv = plan[c]; ss.Hq = plan[c] * (sh->Hq / sh->Hkv); }
-    return ss;
-  };
-  size_t u0[kHostSlices];  // first unit of each slice
-  for (int c = 0, u = 0; c < n_sl; u += plan[c], ++c) u0[c] = (size_t)u;
-  // every slice's launch must be valid before any copy is queued
-  {
-    DeviceInfo di;
-    if (!device_info(di)) return PSR_ERR_CUDA;
-    for (int c = 0; c < n_sl; ++c) {
-      const psr_shape ss = slice_shape(c);
-      Geometry Gc;
-      const int rc = shape_geometry(&ss, Gc, di.n_sm);
-      if (rc != PSR_OK) return rc;
-      if (ws_bytes < ws_layout(Gc).total) return PSR_ERR_ARG;
-    }
-  }
+  // the launch over the device buffers (checks the shape, the device pointers and the workspace)
+  FwdLaunch F;
+  int rc = fwd_setup(sh, dq, dk, dv, d_o, d_lse, workspace, ws_bytes, part, F);
+  if (rc != PSR_OK) return rc;
+  const StreamMemOps& mem_ops = stream_mem_ops();
+  if (!mem_ops.write || !mem_ops.wait) return PSR_ERR_UNSUPPORTED;
+  const Geometry& G = F.kp.geo;
+  // Units: one batch (B > 1), or one KV head with its query heads (B = 1).  Each unit's Q, K, V is
+  // one contiguous block of each tensor, and so is its O and LSE.
+  const int n_units = unit_count(G);
+  const size_t row_b = (size_t)G.S * G.d * 2;  // bytes of one head's rows of Q, K, V or O
+  const size_t q_u = (size_t)(G.B > 1 ? G.Hq : G.gqa) * row_b;
+  const size_t kv_u = (size_t)(G.B > 1 ? G.Hkv : 1) * row_b;
+  const size_t l_u = (size_t)(G.B > 1 ? G.Hq : G.gqa) * G.S * 4;
+  const uint32_t items_per_unit = (uint32_t)(G.n_items / n_units);
+  uint32_t* in_ready = reinterpret_cast<uint32_t*>(F.ws + F.L.io);
+  uint32_t* out_done = in_ready + n_units;
+  F.kp.in_ready = in_ready;
+  F.kp.out_done = out_done;
 
   HostPipe* hp = host_pipe();
   if (!hp) return PSR_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(hp->mu);  // the pipeline's streams, events and error words are per device
+  std::lock_guard<std::mutex> lk(hp->mu);  // the pipeline's streams and error word are per device
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Every failure after the first enqueue ends here: the copies already queued still read the
-  // caller's host buffers (or write o_host / lse_host), so they are drained before returning.
+  // Every failure after the first enqueue ends here: copies already queued still read the caller's
+  // host buffers (or write o_host / lse_host), so they are drained before returning.  A launch
+  // that gave up releases every unit's completion word, so the download stream's waits end too.
   auto fail = [&](int status) {
     cudaStreamSynchronize(hp->h2d);
     cudaStreamSynchronize(st);
@@ -1473,43 +1530,49 @@ int psr_ring_attn_fwd_host(const psr_shape* sh, const void* q_host, const void* 
     cudaGetLastError();
     return status;
   };
-  // the copies must not overtake work already queued on the caller's stream
+  // control words (and the units' words) cleared on the caller's stream; the uploads start after
+  // that and after any work already queued there
+  if (cudaMemsetAsync(F.ws, 0, F.L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
   if (cudaEventRecord(hp->ev_start, st) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0) != cudaSuccess)
     return fail(PSR_ERR_CUDA);
-  auto cp_in = [&](void* dst, const void* src, size_t off, size_t n) {
-    return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + off, static_cast<const uint8_t*>(src) + off, n,
-                           cudaMemcpyHostToDevice, hp->h2d);
-  };
-  for (int c = 0; c < n_sl; ++c) {
-    const size_t qo = u0[c] * q_u, ko = u0[c] * kv_u, qn = plan[c] * q_u, kn = plan[c] * kv_u;
-    if (cp_in(dq, q_host, qo, qn) != cudaSuccess || cp_in(dk, k_host, ko, kn) != cudaSuccess ||
-        cp_in(dv, v_host, ko, kn) != cudaSuccess || cudaEventRecord(hp->ev_in[c], hp->h2d) != cudaSuccess)
+  // one launch for the whole shape: its items wait (bounded) for their unit's inputs
+  rc = fwd_enqueue(F, st);
+  if (rc != PSR_OK) return fail(rc);
+  // Backstop behind the launch on the same stream: once the kernel has finished, every unit's
+  // completion word is set far above its item count (bytes 0x40: 0x40404040), so the download
+  // stream's waits end even if a launch that gave up had not released them.  After a normal
+  // launch the words are already complete and the copies read finished results either way.
+  if (cudaMemsetAsync(out_done, 0x40, (size_t)n_units * 4, st) != cudaSuccess) return fail(PSR_ERR_CUDA);
+  for (int u = 0; u < n_units; ++u) {
+    const size_t qo = (size_t)u * q_u, ko = (size_t)u * kv_u;
+    if (cudaMemcpyAsync(static_cast<uint8_t*>(dq) + qo, static_cast<const uint8_t*>(q_host) + qo, q_u,
+                        cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(dk) + ko, static_cast<const uint8_t*>(k_host) + ko, kv_u,
+                        cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(dv) + ko, static_cast<const uint8_t*>(v_host) + ko, kv_u,
+                        cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+        mem_ops.write(reinterpret_cast<CUstream>(hp->h2d), reinterpret_cast<CUdeviceptr>(in_ready + u), 1u,
+                      CU_STREAM_WRITE_VALUE_DEFAULT) != CUDA_SUCCESS)
       return fail(PSR_ERR_CUDA);
   }
-  for (int c = 0; c < n_sl; ++c) {
-    const size_t qo = u0[c] * q_u, ko = u0[c] * kv_u, lo = u0[c] * l_u, qn = plan[c] * q_u, ln = plan[c] * l_u;
-    const psr_shape ss = slice_shape(c);
-    if (cudaStreamWaitEvent(st, hp->ev_in[c], 0) != cudaSuccess) return fail(PSR_ERR_CUDA);
-    const int rc = psr_ring_attn_fwd(&ss, static_cast<const uint8_t*>(dq) + qo, static_cast<const uint8_t*>(dk) + ko,
-                                     static_cast<const uint8_t*>(dv) + ko, static_cast<uint8_t*>(d_o) + qo,
-                                     reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(d_lse) + lo), workspace,
-                                     ws_bytes, part, st);
-    if (rc != PSR_OK) return fail(rc);
-    // this slice's error word, before the next launch resets the control block
-    if (cudaMemcpyAsync(hp->err_host + c, static_cast<uint8_t*>(workspace) + offsetof(Ctrl, error), 4,
-                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaEventRecord(hp->ev_out[c], st) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->ev_out[c], 0) != cudaSuccess ||
-        cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + qo, static_cast<const uint8_t*>(d_o) + qo, qn,
+  // each unit's results are copied out as soon as all of its items are done
+  for (int u = 0; u < n_units; ++u) {
+    const size_t qo = (size_t)u * q_u, lo = (size_t)u * l_u;
+    if (mem_ops.wait(reinterpret_cast<CUstream>(hp->d2h), reinterpret_cast<CUdeviceptr>(out_done + u),
+                     items_per_unit, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + qo, static_cast<const uint8_t*>(d_o) + qo, q_u,
                         cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess ||
-        cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + lo, reinterpret_cast<const uint8_t*>(d_lse) + lo, ln,
+        cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + lo, reinterpret_cast<const uint8_t*>(d_lse) + lo, l_u,
                         cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
       return fail(PSR_ERR_CUDA);
   }
-  if (cudaStreamSynchronize(hp->d2h) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+  // the launch's error word, once it has finished
+  if (cudaMemcpyAsync(hp->err_host, F.ws + offsetof(Ctrl, error), 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return fail(PSR_ERR_CUDA);
-  for (int c = 0; c < n_sl; ++c)
-    if (hp->err_host[c] != 0) return PSR_ERR_TIMEOUT;
-  return PSR_OK;
+  if (cudaStreamSynchronize(hp->d2h) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaStreamSynchronize(hp->h2d) != cudaSuccess)
+    return fail(PSR_ERR_CUDA);
+  return *hp->err_host != 0 ? PSR_ERR_TIMEOUT : PSR_OK;
 }
 
 int psr_get_stats(const void* workspace, psr_stats* out, void* stream) {

@@ -160,15 +160,31 @@ PSR_HD int shard_of_rank(const Geometry& G, int rr) { return skewed<kBal>(G) ? (
 template <int kBal = -1>
 PSR_HD int steps_of_shard(const Geometry& G, int r) { return skewed<kBal>(G) ? (r + 1) : G.P; }
 
+// Groups are dispensed unit by unit -- a unit is one batch (B > 1) or one KV head with its query
+// heads (B = 1), the blocks in which the host-buffer entry uploads the inputs and downloads the
+// results -- and inside a unit shard by shard in rank order (longest shards first under the causal
+// mask), so that compute follows the upload and each unit's results are complete as early as
+// possible.
 template <int kBal = -1>
 PSR_HD void group_coord(const Geometry& G, int g, int& r, int& b, int& kvh, int& sub) {
   sub = g % G.n_sub;
   int rest = g / G.n_sub;
-  kvh = rest % G.Hkv;
-  rest /= G.Hkv;
-  b = rest % G.B;
-  r = shard_of_rank<kBal>(G, rest / G.B);
+  if (G.B > 1) {  // unit = batch: shard by shard, every KV head of the batch at each shard
+    kvh = rest % G.Hkv;
+    rest /= G.Hkv;
+    r = shard_of_rank<kBal>(G, rest % G.P);
+    b = rest / G.P;
+  } else {  // unit = KV head
+    r = shard_of_rank<kBal>(G, rest % G.P);
+    kvh = rest / G.P;
+    b = 0;
+  }
 }
+
+// Units: the blocks of the input the host-buffer entry uploads (and of the output it downloads)
+// one at a time.
+PSR_HD int unit_count(const Geometry& G) { return G.B > 1 ? G.B : G.Hkv; }
+PSR_HD int unit_of(const Geometry& G, int b, int kvh) { return G.B > 1 ? b : kvh; }
 
 template <int kBal = -1>
 PSR_HD int group_steps(const Geometry& G, int g) {
@@ -319,39 +335,6 @@ PSR_HD int wave_cap_groups(int n_cta, int n_need, int cap, int Gs) {
   for (int n = cap; n >= n_need && n >= 0; --n)
     if ((n_cta - n) % Gs == 0) return n;
   return cap;
-}
-
-// Slice sizes (in units: batches, or KV-head groups) of the host-buffer pipeline, in order.  The
-// copies in of slice c+1 and out of slice c-1 overlap the kernel of slice c, so only the first
-// slice's upload and the last slice's download are exposed: the sizes ramp up from one unit by
-// doubling (an upload of twice a slice's units still hides behind its kernel) and mirror back
-// down to one unit; what is left over goes to the middle, beside the largest slices.  Returns
-// the slice count (at most max_slices, at least 1); the sizes sum to `units`.
-PSR_HD int host_slice_plan(int units, int* sizes, int max_slices) {
-  if (units <= 1 || max_slices < 3) {
-    sizes[0] = units;
-    return 1;
-  }
-  int up[32];
-  int nu = 0, sum = 0;
-  for (int sz = 1; nu < 32 && 2 * nu + 3 <= max_slices && 2 * (sum + sz) <= units; sz *= 2) {
-    up[nu++] = sz;
-    sum += sz;
-  }
-  const int last = up[nu - 1];
-  int rest = units - 2 * sum;
-  int n = 0;
-  for (int i = 0; i < nu; ++i) sizes[n++] = up[i];
-  if (rest > 0 && rest <= last) {
-    // widen the two middle slices (the later one first)
-    sizes[n - 1] += rest / 2;
-    for (int i = nu - 1; i >= 0; --i) sizes[n++] = up[i];
-    sizes[nu] += (rest + 1) / 2;
-    return n;
-  }
-  if (rest > 0) sizes[n++] = rest;  // one middle slice (at most ~4x the largest ramp slice)
-  for (int i = nu - 1; i >= 0; --i) sizes[n++] = up[i];
-  return n;
 }
 
 }  // namespace psr

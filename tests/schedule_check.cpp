@@ -74,37 +74,8 @@ static int check_wave_cap() {
   return 0;
 }
 
-// host_slice_plan: the sizes cover the units exactly, stay within the slice budget, start at one
-// unit, grow at most ~3x from one slice to the next (2x, plus the widened middle pair) and reach
-// the largest by at most ~4x unless the slice budget is what stopped the ramp, and only shrink
-// after it.
-static int check_slice_plan() {
-  for (int max_slices = 1; max_slices <= 16; ++max_slices)
-    for (int units = 1; units <= 400; ++units) {
-      int sz[64];
-      const int n = host_slice_plan(units, sz, max_slices);
-      CHECK(n >= 1 && n <= (max_slices < 1 ? 1 : max_slices), "slice count %d (units %d, max %d)", n, units, max_slices);
-      int sum = 0, peak = 0;
-      for (int i = 0; i < n; ++i) {
-        CHECK(sz[i] >= 1, "empty slice (units %d)", units);
-        sum += sz[i];
-        if (sz[i] > sz[peak]) peak = i;
-      }
-      CHECK(sum == units, "slices sum to %d, not %d", sum, units);
-      if (n > 1) CHECK(sz[0] == 1, "first slice %d (units %d)", sz[0], units);
-      for (int i = 1; i <= peak; ++i)
-        CHECK(sz[i] >= sz[i - 1] && (i == peak || sz[i] <= 3 * sz[i - 1] + 1) &&
-                  (i < peak || n >= max_slices - 1 || sz[i] <= 4 * sz[i - 1] + 4),
-              "ramp up at slice %d (units %d, max %d)", i, units, max_slices);
-      for (int i = peak + 1; i < n; ++i) CHECK(sz[i] <= sz[i - 1], "ramp down at slice %d (units %d)", i, units);
-    }
-  std::printf("OK host_slice_plan\n");
-  return 0;
-}
-
 int main(int argc, char** argv) {
   if (argc == 2 && std::string(argv[1]) == "wave") return check_wave_cap();
-  if (argc == 2 && std::string(argv[1]) == "slices") return check_slice_plan();
   if (argc != 9 && argc != 10) return 2;
   int a[9] = {0, 0, 0, 0, 0, 0, 0, 0, 1};
   for (int i = 0; i < argc - 1; ++i) a[i] = std::atoi(argv[i + 1]);
@@ -128,8 +99,19 @@ int main(int argc, char** argv) {
       }
   }
   long long tiles = 0;
+  // items are dispensed unit by unit, the same number per unit, and inside a unit (contiguous
+  // causal shards) longest shards first
+  const int n_units = unit_count(G);
+  CHECK(G.n_items % n_units == 0, "items per unit");
+  const int per_unit = G.n_items / n_units;
   for (int n = 0; n < G.n_items; ++n) {
     ItemCoord c = item_coord(G, n);
+    CHECK(unit_of(G, c.b, c.kvh) == n / per_unit, "item %d in unit %d, dispensed as unit %d", n,
+          unit_of(G, c.b, c.kvh), n / per_unit);
+    if (n > 0 && (n % per_unit) != 0 && G.causal && !G.balanced) {
+      const ItemCoord pc = item_coord(G, n - 1);
+      CHECK(pc.r >= c.r, "item %d: shard %d after shard %d inside a unit", n, c.r, pc.r);
+    }
     CHECK(c.g >= 0 && c.g < G.n_groups, "group %d", c.g);
     CHECK(c.b >= 0 && c.b < G.B && c.hq >= 0 && c.hq < G.Hq && c.r >= 0 && c.r < G.P, "coords item %d", n);
     CHECK(c.kvh == c.hq / G.gqa, "gqa mapping item %d", n);

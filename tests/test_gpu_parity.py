@@ -236,14 +236,14 @@ def test_host_buffer_entry_point(psr):
 
 
 @pytest.mark.parametrize("shape", [(1, 8, 8, 32768, 16, False), (2, 8, 2, 16384, 8, True)],
-                         ids=["head_slices", "batch_slices_gqa_causal"])
+                         ids=["kv_head_units", "batch_units_gqa_causal"])
 def test_host_buffer_entry_point_pipelined(psr, shape):
-    """Shapes with >= 64 MB of Q run through the host entry in slices (KV-head groups when
-    B = 1, batches otherwise) whose copies overlap the kernels; the result equals the
-    device entry's on the same inputs and matches the oracle on sampled rows."""
+    """The host entry streams the inputs in and the results out unit by unit (KV heads when
+    B = 1, batches otherwise) around one launch whose items wait for their unit; the result
+    equals the device entry's on the same inputs and matches the oracle on sampled rows."""
     torch = _torch()
     B, H, Hkv, S, P, causal = shape
-    w = ri.WORKLOADS["small"].with_(name="host_sliced", B=B, Hq=H, Hkv=Hkv, S=S, P=P, d=128, causal=causal, seed=43)
+    w = ri.WORKLOADS["small"].with_(name="host_streamed", B=B, Hq=H, Hkv=Hkv, S=S, P=P, d=128, causal=causal, seed=43)
     q, k, v = inputs(w)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
     qh, kh, vh = pin(q), pin(k), pin(v)
@@ -264,7 +264,34 @@ def test_host_buffer_entry_point_pipelined(psr, shape):
     rows = ri.sample_rows(w, n_random=1024)
     o_ref, lse_ref = oracle.for_workload(w, q, k, v, rows=rows)
     o = ri.bf16_bits_to_f64(oh.numpy().view(np.uint16)).reshape(-1, w.d)[rows]
-    check(o, lh.numpy().astype(np.float64).reshape(-1)[rows], o_ref, lse_ref, "host entry, sliced")
+    check(o, lh.numpy().astype(np.float64).reshape(-1)[rows], o_ref, lse_ref, "host entry, streamed")
+
+
+def test_host_entry_reports_a_device_timeout_and_recovers(psr):
+    """A dropped readiness flag inside the host entry's single launch: the call returns
+    PSR_ERR_TIMEOUT (the launch releases the units' completion words, so the download stream
+    does not wait for items that never finish), and the next call is correct."""
+    torch = _torch()
+    w = ri.WORKLOADS["small"].with_(name="host_fault", Hq=4, Hkv=4, S=2048, P=8, seed=47)
+    q, k, v = inputs(w)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+    qh, kh, vh = pin(q), pin(k), pin(v)
+    oh = torch.empty(q.shape, dtype=torch.int16).pin_memory()
+    lh = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device="cuda")
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, device="cuda")
+    do = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    dl = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    bufs = (qh, kh, vh, oh, lh, dq, dk, dv, do, dl)
+    faulty = psr.make_partition(psr.ADAPTIVE, fault=psr.FAULT_DROP_FIRST_FLAG, timeout_ms=200)
+    with pytest.raises(psr.PsrError) as e:
+        psr.ring_attn_fwd_host(*bufs, P=w.P, causal=False, scale=w.scale, partition=faulty)
+    assert e.value.status == psr.ERR_TIMEOUT
+    psr.ring_attn_fwd_host(*bufs, P=w.P, causal=False, scale=w.scale)
+    o_ref, lse_ref = oracle.for_workload(w, q, k, v)
+    o = ri.bf16_bits_to_f64(oh.numpy().view(np.uint16)).reshape(-1, w.d)
+    check(o, lh.numpy().astype(np.float64).reshape(-1), o_ref, lse_ref, "host entry after a timeout")
 
 
 @pytest.mark.parametrize("d", [64, 128])

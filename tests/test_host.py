@@ -129,11 +129,6 @@ def test_schedule_bounds_and_coverage(schedule_check, shape):
     assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
 
 
-def test_host_slice_plan(schedule_check):
-    out = subprocess.run([schedule_check, "slices"], capture_output=True, text=True)
-    assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
-
-
 def test_wave_cap_matches_enumeration(schedule_check):
     out = subprocess.run([schedule_check, "wave"], capture_output=True, text=True)
     assert out.returncode == 0 and out.stdout.startswith("OK"), out.stdout + out.stderr
