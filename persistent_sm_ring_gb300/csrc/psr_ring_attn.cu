@@ -621,10 +621,14 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
       mma_ss_cg<CG>(tS, q_lo + a_off, kHi, b_lo + b_off, kHi, IQK, kk > 0 ? 1u : 0u);
     }
     mma_commit_cg<CG>(&sc->s_full[i]);
-    mma_commit_cg<CG>(&sc->kv_empty[kstage]);
+    // a commit tracks every earlier MMA of this thread: one per K/V stage, after the second tile's
+    // reads, releases the stage for both
+    if (i == 1) mma_commit_cg<CG>(&sc->kv_empty[kstage]);
   };
   // PV_i(j): the K = 16 steps over the 128 keys of P_i(j)
-  auto issue_pv = [&](int i, uint32_t vstage, bool first, uint32_t parity) -> bool {
+  // O_i is only waited for at the end of the item (the rescale of a tile waits for that tile's S,
+  // whose commit also tracks the previous PV_i), so only the item's last PV commits o_full
+  auto issue_pv = [&](int i, uint32_t vstage, bool first, bool last, uint32_t parity) -> bool {
     // V share MN-major: 64-column halves 16 KB apart (a pair's CTA holds one half)
     const uint32_t b_lo = sdesc_lo(sStage + vstage * C::KVB, 16384);
     const uint32_t tS = sc->tmem_base + (i ? C::COL_S1 : C::COL_S0);
@@ -634,8 +638,8 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       mma_ts_cg<CG>(tO, tS + kk * 8, b_lo + kk * (2048 >> 4), kHi, IPV, (first && kk == 0) ? 0u : 1u);
-    mma_commit_cg<CG>(&sc->o_full[i]);
-    mma_commit_cg<CG>(&sc->kv_empty[vstage]);
+    if (last) mma_commit_cg<CG>(&sc->o_full[i]);
+    if (i == 1) mma_commit_cg<CG>(&sc->kv_empty[vstage]);
     return true;
   };
   const uint32_t n = (uint32_t)item_tiles<BAL>(G, it);
@@ -659,7 +663,7 @@ __device__ void mma_issuer(const KParams& p, SmemCtl* sc, uint32_t smem_base, co
     tr_kv += trace_clock() - a0;
     for (int i = 0; i < 2; ++i) {
       const long long a2 = trace_clock();
-      if (!issue_pv(i, stage_of(cv), jt == 0, (cnt.tiles + jt) & 1u)) { sc->abort = 1; return; }
+      if (!issue_pv(i, stage_of(cv), jt == 0, !more, (cnt.tiles + jt) & 1u)) { sc->abort = 1; return; }
       if (more) issue_s(i, stage_of(cn));
       tr_issue += trace_clock() - a2;
     }
@@ -788,8 +792,7 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
       const float m_new = need ? fmaxf(m_run, m_tile) : m_run;
       if (jglob > 0 && __any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-        ok = __all_sync(0xffffffffu, wait_bar(&sc->o_full[i], (cnt.tiles + jglob - 1) & 1u, p, sc, SITE_O_FULL));
-        if (!ok) break;
+        // PV_i of the previous tile has completed: the commit this tile's S was waited on tracks it
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -816,11 +819,10 @@ __device__ void softmax_wg(const KParams& p, SmemCtl* sc, const ItemCoord& it, i
     atomicAdd(&p.ctrl->tr_softmax_wait, tr_wait);
     atomicAdd(&p.ctrl->tr_softmax_busy, tr_busy);
   }
-  const uint32_t n = jglob;
   ok = __all_sync(0xffffffffu, ok);
   if (ok) {
     // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
-    ok = __all_sync(0xffffffffu, wait_bar(&sc->o_full[i], (cnt.tiles + n - 1) & 1u, p, sc, SITE_O_FULL));
+    ok = __all_sync(0xffffffffu, wait_bar(&sc->o_full[i], cnt.items & 1u, p, sc, SITE_O_FULL));  // one phase per item
   }
   if (ok) {
     tc_fence_after();
@@ -893,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&sc.kv_full[s], 1);
-      mbar_init(&sc.kv_empty[s], 2);  // both query tiles' MMAs commit their reads of every K/V tile
+      mbar_init(&sc.kv_empty[s], 1);  // committed once per fill, after both query tiles' reads
     }
     for (int s = 0; s < C::NB; ++s) mbar_init(&sc.stg[s], 1);
     mbar_init(&sc.drain, 1);

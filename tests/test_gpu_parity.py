@@ -212,6 +212,24 @@ def test_initial_split_keeps_compute_waves(psr):
         assert st["status"] == 0 and st["n_s_initial"] == want, (name, st)
 
 
+@pytest.mark.parametrize("causal,d", [(False, 64), (False, 128), (True, 128)])
+def test_running_max_rescale_path(psr, causal, d):
+    """Keys of later chunks scaled up by 8 (exact in bf16): the running maximum of the rows whose
+    first tiles hold unscaled keys is far below the scores of the later ring steps (up to ~25 more
+    in log2 units), so the softmax takes its rare path there (the tile's sum of exponentials
+    exceeds 2^16: row maximum, rescale of O and l, exponentials again)."""
+    w = ri.WORKLOADS["small"].with_(name=f"rescale_{'c' if causal else 'nc'}_d{d}", S=2048, P=8, d=d,
+                                    causal=causal, seed=91)
+    q, k, v = ri.generate(w)
+    kf = ri.bf16_bits_to_f32(k).reshape(w.B, w.Hkv, w.S, w.d)
+    # keys from position 512 on (chunks 2..7): x8
+    kf[:, :, 512:, :] *= np.float32(8.0)
+    k = ri.f32_to_bf16_bits(kf).reshape(k.shape)
+    o_ref, lse_ref = oracle.for_workload(w, q, k, v)
+    o, lse, st = gpu_run(psr, w, q, k, v)
+    check(o, lse, o_ref, lse_ref, w.name)
+
+
 # ------------------------------------------------------------------------------------------------
 # host-buffer entry point and failure reporting
 # ------------------------------------------------------------------------------------------------
