@@ -7,17 +7,20 @@
 // HBM: rank r owns rows [r*Ms, (r+1)*Ms) of A (Ms = M/P) and the weight slice W_r
 // ([Ns][K], K-major), and produces C_r = gather(A) @ W_r^T.
 //
-//  * staging CTAs copy a peer shard's rows, in pieces of >= 512 KiB, into rank r's gather
-//    buffer (the same row positions) with TMA bulk copies through shared memory, and publish
-//    a per-piece readiness flag with a gpu-scope release once the stores are complete;
-//  * compute CTAs each produce one 256 x 256 output tile of one rank per task: two 128-row
-//    A tiles against one 256-row W tile per 64-wide K step, on tcgen05 (M = 128, N = 256)
-//    with both accumulators in tensor memory; the rank's own shard is read in place, a
-//    peer's only after acquiring the piece flags that cover the tile's rows;
+//  * the CTAs work in pairs (clusters of two); a pair takes either role;
+//  * a staging pair's two CTAs each copy a piece of a peer shard's rows (>= 512 KiB) into rank
+//    r's gather buffer (the same row positions) with TMA bulk copies through shared memory,
+//    and publish a per-piece readiness flag with a gpu-scope release once the stores are
+//    complete;
+//  * a compute pair produces one 256 x 256 output tile of one rank per task (the pair tile of
+//    psr_gemm_tile.cuh: each CTA 128 rows, tcgen05 cta_group::2, double-buffered
+//    accumulators); the rank's own shard is read in place, a peer's only after each CTA has
+//    acquired the piece flags that cover its 128 rows;
 //  * each rank's tasks run in availability order: its local tiles first, then the tiles of
 //    shard r+1, r+2, ... (the order in which staging delivers them); ranks run one after
 //    another, so that a rank's weight slice is read from HBM once;
-//  * the shared controller re-splits CTAs between the roles with the pages' rule.
+//  * the shared controller re-splits the pairs between the roles with the pages' rule (a
+//    target of n staging CTAs gives ceil(n/2) staging pairs).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -41,8 +44,7 @@ constexpr int kNCopyBuf = kStageArea / kCopyUnit;
 constexpr int kPieceMinBytes = 512 * 1024;
 static_assert(kNCopyBuf <= 16, "staging barriers");
 
-enum : uint32_t { SITE_FLAG = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_ACC = 4, SITE_STAGE_LOAD = 8, SITE_IDLE = 11 };
-enum : int { CMD_EXIT = 0, CMD_COMPUTE = 1, CMD_STAGE = 2, CMD_IDLE = 3 };
+enum : uint32_t { SITE_FLAG = 1, SITE_STAGE_LOAD = 8 };
 
 struct Geo {
   int M, K, Ns, P, Ms;
@@ -99,39 +101,59 @@ __device__ inline void stage_of(const Geo& g, long long idx, int& r, int& j, int
 }
 
 // ------------------------------------------------------------------------------------------------
-// Task selection (thread 0)
+// Task selection (the even CTA's thread 0, for its pair)
 // ------------------------------------------------------------------------------------------------
-__device__ void decide(const Params& p, Smem* sc, bool& was_staging) {
+// A staging task gives each CTA of the pair its own piece (arg, arg1).  With `ahead` (called
+// while the current compute task's last loads are in flight) only a compute task is claimed;
+// otherwise the result is CMD_NONE and the pair decides again once those loads are issued.
+__device__ void decide(const Params& p, Smem* sc, Task& t, bool& was_staging, bool ahead) {
   Ctrl* c = p.ctrl;
-  if (sc->abort || ld_relaxed(&c->abort)) { sc->cmd = CMD_EXIT; return; }
+  const Geo& g = p.g;
+  t.cmd = ahead ? CMD_NONE : CMD_EXIT;
+  t.arg = -1;
+  t.arg1 = -1;
+  t.pad = 0;
+  if (sc->abort || ld_relaxed(&c->abort)) return;
   const int n_s = current_target(p);
-  const bool staging_role = (int)blockIdx.x < n_s;
+  const bool staging_role = 2 * (int)(blockIdx.x / 2) < n_s;
   if (staging_role != was_staging) {
     atomicAdd(&c->role_switches, 1ull);
     was_staging = staging_role;
   }
-  const bool all_claimed = ld_relaxed(&c->init_next) >= (uint32_t)p.g.n_stage;
+  auto claim_pieces = [&]() -> bool {
+    const uint32_t k = atomicAdd(&c->init_next, 2u);
+    if (k >= (uint32_t)g.n_stage) return false;
+    t.cmd = CMD_COMM;
+    t.arg = (int)k;
+    t.arg1 = k + 1 < (uint32_t)g.n_stage ? (int)k + 1 : -1;
+    return true;
+  };
+  const bool all_claimed = ld_relaxed(&c->init_next) >= (uint32_t)g.n_stage;
   if (staging_role && !all_claimed) {
-    const uint32_t t = atomicAdd(&c->init_next, 1u);
-    if (t < (uint32_t)p.g.n_stage) { sc->cmd = CMD_STAGE; sc->arg = (int)t; return; }
+    if (ahead) return;
+    if (claim_pieces()) return;
   }
-  if (staging_role && p.mode == PSR_STATIC) { sc->cmd = CMD_EXIT; return; }
-  if (ld_relaxed(&c->item_next) < (uint32_t)p.g.n_items) {
+  if (staging_role && p.mode == PSR_STATIC) return;
+  if (ld_relaxed(&c->item_next) < (uint32_t)g.n_items) {
     const uint32_t n = atomicAdd(&c->item_next, 1u);
-    if (n < (uint32_t)p.g.n_items) { sc->cmd = CMD_COMPUTE; sc->arg = (int)n; return; }
+    if (n < (uint32_t)g.n_items) {
+      t.cmd = CMD_COMPUTE;
+      t.arg = (int)n;
+      return;
+    }
   }
+  if (ahead) return;
   // no compute left: help with staging while any piece is unclaimed
-  if (p.mode == PSR_ADAPTIVE && ld_relaxed(&c->init_next) < (uint32_t)p.g.n_stage) {
-    const uint32_t t = atomicAdd(&c->init_next, 1u);
-    if (t < (uint32_t)p.g.n_stage) { sc->cmd = CMD_STAGE; sc->arg = (int)t; return; }
-  }
-  sc->cmd = CMD_EXIT;
+  if (p.mode == PSR_ADAPTIVE && ld_relaxed(&c->init_next) < (uint32_t)g.n_stage && claim_pieces()) return;
+  t.cmd = CMD_EXIT;
 }
 
 // ------------------------------------------------------------------------------------------------
-// Staging task (thread 0): a piece of shard j's rows -> rank r's gather buffer, same rows
+// Staging task (thread 0 of a CTA): a piece of shard j's rows -> rank r's gather buffer, same rows
 // ------------------------------------------------------------------------------------------------
-__device__ void run_staging(const Params& p, Smem* sc, uint32_t smem_base, int task, uint32_t (&phase)[16]) {
+// The stage area is free (wait_stages_free) when it starts; every copy has completed when it
+// returns.  False on timeout or abort.
+__device__ bool run_staging(const Params& p, Smem* sc, uint32_t smem_base, int task, uint32_t (&phase)[16]) {
   const Geo& g = p.g;
   int r, j, piece;
   stage_of(g, task, r, j, piece);
@@ -183,50 +205,54 @@ __device__ void run_staging(const Params& p, Smem* sc, uint32_t smem_base, int t
     st_release(flag, 1u);
   }
   atomicAdd(&p.ctrl->stage_bytes, (unsigned long long)bytes);
+  return ok;
 }
 
 // ------------------------------------------------------------------------------------------------
-// Compute task: producer (TMA), MMA issuer (tcgen05), epilogue warpgroups
+// Compute task: producer (thread 0 of each CTA), epilogue warps (both CTAs)
 // ------------------------------------------------------------------------------------------------
-// Returns the cycles spent waiting for readiness flags.
-__device__ long long producer(const Params& p, Smem* sc, uint32_t smem_base, const Item& it, const CUtensorMap* tm_a,
-                              const CUtensorMap* tm_g, const CUtensorMap* tm_w, Counters& cnt, bool& ok) {
+// This CTA's 128 rows of the tile's A and W.  `starved` accumulates the cycles spent waiting
+// for readiness flags.  False on timeout or abort.
+template <class Ahead>
+__device__ bool produce_tile(const Params& p, Smem* sc, uint32_t smem_base, uint32_t rank, const Item& it,
+                             const CUtensorMap* tm_a, const CUtensorMap* tm_g, const CUtensorMap* tm_w,
+                             uint32_t& fills, long long& starved, Ahead&& ahead) {
   const Geo& g = p.g;
-  long long waited = 0;
+  const int srow = it.mb * kBM + (int)rank * kRows;  // this CTA's first row inside the shard
   const CUtensorMap* ma = tm_a;
-  int arow = it.j * g.Ms + it.mb * kBM;  // rows of A (local) ...
+  int arow = it.j * g.Ms + srow;  // rows of A (local) ...
   if (it.j != it.r) {
-    // ... or of rank r's gather buffer, once the pieces covering the tile's rows are there
+    // ... or of rank r's gather buffer, once the pieces covering these rows are there
     ma = tm_g;
-    const int p0 = (it.mb * kBM) / g.piece_rows, p1 = (it.mb * kBM + kBM - 1) / g.piece_rows;
+    const int p0 = srow / g.piece_rows, p1 = (srow + kRows - 1) / g.piece_rows;
     const uint32_t* f = p.flags + ((size_t)it.r * g.P + it.j) * g.n_pieces;
-    for (int pc = p0; pc <= p1 && ok; ++pc) {
+    for (int pc = p0; pc <= p1; ++pc) {
       uint32_t seen = ld_acquire(f + pc);
       if (seen < 1u) {
         const long long f0 = clock64();
-        if (!wait_flag(f + pc, 1u, seen, p, sc, SITE_FLAG)) ok = false;
-        waited += clock64() - f0;
+        const bool ok = wait_flag(f + pc, 1u, seen, p, sc, SITE_FLAG);
+        starved += clock64() - f0;
+        if (!ok) return false;
       }
     }
     fence_proxy_async_global();  // acquire (generic) before the async-proxy reads of the buffer
-    arow = it.r * g.M + it.j * g.Ms + it.mb * kBM;
+    arow = it.r * g.M + it.j * g.Ms + srow;
   }
-  const int wrow = it.r * g.Ns + it.nb * kBN;
-  if (ok && !load_tile(p, sc, smem_base, ma, arow, tm_w, wrow, g.K / kBK, cnt, SITE_KV_EMPTY)) ok = false;
-  if (!ok) sc->abort = 1;
-  return waited;
+  const int n_k = g.K / kBK;
+  const int wrow = it.r * g.Ns + it.nb * kBN + (int)rank * kRows;
+  return load_tile(p, sc, smem_base, rank, ma, arow, tm_w, wrow, n_k, fills, n_k > kNStage ? n_k - kNStage : 0,
+                   ahead);
 }
 
-// One warpgroup per 128-row half of the tile: accumulator -> bf16 -> C_r.
-__device__ void epilogue(const Params& p, Smem* sc, uint8_t* smem, const Item& it, int i, const Counters& cnt,
-                         bool& ok) {
+// Epilogue warp: its 32 rows x 128 columns of the tile, accumulator -> bf16 -> C_r.
+__device__ bool epilogue(const Params& p, Smem* sc, uint8_t* epi, uint32_t rank, const Item& it, uint32_t item) {
   const Geo& g = p.g;
   const int warp = threadIdx.x / 32;
-  const size_t grow0 = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + i * 128 + (warp % 4) * 32;
-  // the stage area is idle during the epilogue (every MMA of the tile has completed): 4 KiB per warp
-  uint8_t* stage = smem + (warp - 4) * 4096;
-  uint8_t* rows = reinterpret_cast<uint8_t*>(p.c + ((size_t)it.r * g.M + grow0) * g.Ns + (size_t)it.nb * kBN);
-  ok = read_tile(p, sc, i, cnt, SITE_ACC, [&](int, int cb, const uint32_t(&v)[64]) {
+  const size_t grow0 = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + rank * kRows + (warp % 4) * 32;
+  const size_t col0 = (size_t)it.nb * kBN + ((warp - 4) / 4) * 128;
+  uint8_t* stage = epi + (warp - 4) * kEpiWarpBytes;
+  uint8_t* rows = reinterpret_cast<uint8_t*>(p.c + ((size_t)it.r * g.M + grow0) * g.Ns + col0);
+  return read_acc(p, sc, rank, item, [&](int cb, const uint32_t* v) {
     uint32_t w[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
@@ -239,17 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_w) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Smem sc;
-  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t smem_base = (raw + 1023u) & ~1023u;
+  uint8_t* epi = smem_raw + (smem_base - raw) + kStageArea;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNStage; ++s) {
-      mbar_init(&sc.full[s], 1);
-      mbar_init(&sc.empty[s], 1);
-    }
-    mbar_init(&sc.acc_full, 1);
+    init_barriers(&sc);
     for (int b = 0; b < 16; ++b) mbar_init(&sc.stg[b], 1);
-    mbar_init(&sc.drain, 1);
-    sc.abort = 0;
     fence_barrier_init();
     if (blockIdx.x == 0) {
       unsigned long long z = 0;
@@ -262,71 +285,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_g);
     prefetch_tmap(&tm_w);
   }
-  if (warp == 1) {
-    tmem_alloc(&sc.tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  setup_pair(&sc);
 
-  Counters cnt{0, 0};
-  uint32_t stg_phase[16] = {};
-  bool was_staging = false;
-  long long t_task = 0, starved = 0;
-  while (true) {
-    if (threadIdx.x == 0) {
-      decide(p, &sc, was_staging);
-      t_task = clock64();
-    }
-    __syncthreads();
-    const int cmd = sc.cmd, arg = sc.arg;
-    if (cmd == CMD_EXIT) break;
-    if (cmd == CMD_STAGE) {
-      if (threadIdx.x == 0) {
-        fence_proxy_async_smem();  // the previous epilogue's generic stores to the copy buffers
-        run_staging(p, &sc, smem_base, arg, stg_phase);
-      }
-    } else if (cmd == CMD_COMPUTE) {
-      const Item it = item_of(p.g, arg);
-      bool ok = true;
-      if (warp == 0 && lane == 0) {
-        Counters c2 = cnt;
-        fence_proxy_async_smem();  // the previous epilogue's generic stores to the stage area
-        starved = producer(p, &sc, smem_base, it, &tm_a, &tm_g, &tm_w, c2, ok);
-      } else if (warp == 1 && lane == 0) {
-        Counters c2 = cnt;
-        mma_tile(p, &sc, smem_base, p.g.K / kBK, c2, SITE_KV_FULL);
-      } else if (warp >= 4) {
-        epilogue(p, &sc, smem_raw + (smem_base - smem_u32(smem_raw)), it, warp < 8 ? 0 : 1, cnt, ok);
-      }
-      cnt.fills += (uint32_t)(p.g.K / kBK);
-      cnt.items++;
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (threadIdx.x == 0 && cmd != CMD_IDLE) {
-      long long busy = clock64() - t_task;
-      if (cmd == CMD_COMPUTE) {
-        busy -= starved;
-        atomicAdd(&p.ctrl->starve_cycles, (unsigned long long)(starved > 0 ? starved : 0));
-        starved = 0;
-      }
-      const unsigned long long dt = (unsigned long long)(busy > 0 ? busy : 0);
-      if (cmd == CMD_STAGE) {
-        atomicAdd(&p.ctrl->stage_cycles, dt);
-        atomicAdd(&p.ctrl->stage_done, 1ull);
+  uint32_t fills = 0;  // thread 0: the stage fills this CTA issued
+  const int n_k = p.g.K / kBK;
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stg_phase[16] = {};
+      long long starved = 0;
+      if (rank == 0) {
+        // the pair's scheduler, and the even CTA's producer
+        bool was_staging = false;
+        unsigned long long next_offer_ns = 0;
+        Task next;
+        next.cmd = CMD_NONE;
+        int prev_cmd = CMD_NONE, prev_pieces = 0;
+        long long t_prev = 0;
+        for (uint32_t k = 0;; ++k) {
+          Task t = next;
+          next.cmd = CMD_NONE;
+          if (t.cmd == CMD_NONE) decide(p, &sc, t, was_staging, false);
+          // the previous task's cost, in CTA-cycles (both CTAs of the pair)
+          const long long now = clock64();
+          long long busy = now - t_prev;
+          if (prev_cmd == CMD_COMPUTE) {
+            busy -= starved;
+            atomicAdd(&p.ctrl->starve_cycles, (unsigned long long)(starved > 0 ? starved : 0));
+            atomicAdd(&p.ctrl->compute_cycles, 2ull * (unsigned long long)(busy > 0 ? busy : 0));
+            atomicAdd(&p.ctrl->compute_tiles, 1ull);
+            atomicAdd(&p.ctrl->compute_items, 1ull);
+          } else if (prev_cmd == CMD_COMM) {
+            atomicAdd(&p.ctrl->stage_cycles, (unsigned long long)(busy > 0 ? busy : 0) * prev_pieces);
+            atomicAdd(&p.ctrl->stage_done, (unsigned long long)prev_pieces);
+          }
+          controller_tick(p, next_offer_ns);
+          if (!post_task(p, &sc, k, t)) { sc.abort = 1; break; }
+          if (t.cmd == CMD_EXIT) break;
+          prev_cmd = t.cmd;
+          t_prev = clock64();
+          starved = 0;
+          bool ok;
+          if (t.cmd == CMD_COMPUTE) {
+            ok = produce_tile(p, &sc, smem_base, 0, item_of(p.g, t.arg), &tm_a, &tm_g, &tm_w, fills, starved,
+                              [&] { decide(p, &sc, next, was_staging, true); });
+          } else {
+            prev_pieces = t.arg1 >= 0 ? 2 : 1;
+            ok = wait_stages_free(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg, stg_phase);
+          }
+          if (!ok) { sc.abort = 1; break; }
+        }
       } else {
-        atomicAdd(&p.ctrl->compute_cycles, dt);
-        atomicAdd(&p.ctrl->compute_tiles, 1ull);
-        atomicAdd(&p.ctrl->compute_items, 1ull);
+        // the odd CTA's producer
+        for (uint32_t k = 0;; ++k) {
+          Task t;
+          if (!take_task(p, &sc, k, t)) { sc.abort = 1; break; }
+          release_task(&sc, k, 1);
+          if (t.cmd == CMD_EXIT) break;
+          bool ok = true;
+          if (t.cmd == CMD_COMPUTE)
+            ok = produce_tile(p, &sc, smem_base, 1, item_of(p.g, t.arg), &tm_a, &tm_g, &tm_w, fills, starved, [] {});
+          else if (t.arg1 >= 0)
+            ok = wait_stages_free(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg1, stg_phase);
+          if (!ok) { sc.abort = 1; break; }
+        }
       }
-      const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
-      if (p.mode == PSR_ADAPTIVE && (tick % 16u) == 0) controller_update(p);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // the pair's MMA issuer
+      uint32_t mfills = 0, items = 0;
+      for (uint32_t k = 0;; ++k) {
+        Task t;
+        if (!take_task(p, &sc, k, t)) { sc.abort = 1; break; }
+        release_task(&sc, k, 0);
+        if (t.cmd == CMD_EXIT) break;
+        if (t.cmd != CMD_COMPUTE) continue;
+        if (!mma_tile(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
+        ++items;
+      }
+    }
+  } else if (warp >= 4) {
+    uint32_t items = 0;
+    for (uint32_t k = 0;; ++k) {
+      Task t;
+      const bool ok = __all_sync(0xffffffffu, take_task(p, &sc, k, t));
+      if (!ok) { sc.abort = 1; break; }
+      __syncwarp();
+      if (lane == 0) release_task(&sc, k, rank);
+      if (t.cmd == CMD_EXIT) break;
+      if (t.cmd != CMD_COMPUTE) continue;
+      if (!epilogue(p, &sc, epi, rank, item_of(p.g, t.arg), items)) break;
+      ++items;
     }
   }
-  drain_and_release(&sc, cnt);
+  drain_pair(&sc, rank, fills);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -398,7 +450,8 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   cudaDeviceProp prop;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PSR_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return PSR_ERR_UNSUPPORTED;
-  const int n_cta = prop.multiProcessorCount;
+  const int n_cta = pair_ctas(ag_gemm_kernel, prop.multiProcessorCount);  // whole CTA pairs
+  if (n_cta < 4) return PSR_ERR_CUDA;
   Geo g;
   int rc = geometry(sh, g);
   if (rc != PSR_OK) return rc;
@@ -430,7 +483,7 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   const double piece_cycles = (double)g.piece_rows * g.K * 2 / 50e9 * 1.95e9;
   kp.c_s0 = (float)(piece_cycles > 6500.0 ? piece_cycles : 6500.0);
   kp.c_p0 = (float)(2.0 * kBM * kBN * (double)g.K / (0.6 * 8192.0));
-  const int hard_max = n_cta - 1;
+  const int hard_max = n_cta - 2;  // at least one compute pair
   int n_max = pt.n_max > 0 ? pt.n_max : n_cta / 2;
   if (n_max > hard_max) n_max = hard_max;
   int n_min = pt.n_min > 0 ? pt.n_min : 1;
@@ -441,7 +494,7 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   int n_s;
   if (pt.mode == PSR_STATIC) {
     n_s = any_staging ? pt.n_staging : 0;
-    if (any_staging && (n_s < 1 || n_s > n_cta - 1)) return PSR_ERR_ARG;
+    if (any_staging && (n_s < 1 || n_s > hard_max)) return PSR_ERR_ARG;
   } else {
     n_s = pt.n_staging > 0 ? pt.n_staging
                            : controller_rule(n_cta, (double)g.n_stage, kStageHeadroom * kp.c_s0, (double)g.n_items,
@@ -455,29 +508,14 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   kp.n_s_init = n_s;
 
   CUtensorMap ma, mg, mw;
-  if (!tmap_kmajor(&ma, a, g.M, g.K, 128) || !tmap_kmajor(&mg, kp.gbuf, (long long)g.P * g.M, g.K, 128) ||
-      !tmap_kmajor(&mw, w, (long long)g.P * g.Ns, g.K, kBN))
+  if (!tmap_kmajor(&ma, a, g.M, g.K, kRows) || !tmap_kmajor(&mg, kp.gbuf, (long long)g.P * g.M, g.K, kRows) ||
+      !tmap_kmajor(&mw, w, (long long)g.P * g.Ns, g.K, kRows))
     return PSR_ERR_CUDA;
 
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(ag_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  });
-  if (attr_err != cudaSuccess) return PSR_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)n_cta);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: compute waits on staging
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, ag_gemm_kernel, kp, ma, mg, mw) != cudaSuccess) {
+  // all pairs co-resident: compute waits on staging
+  if (launch_pairs(ag_gemm_kernel, n_cta, st, kp, ma, mg, mw) != cudaSuccess) {
     cudaGetLastError();
     return PSR_ERR_CUDA;
   }

@@ -47,9 +47,12 @@ __device__ __forceinline__ void raise_error(const KP& p, uint32_t site) {
 }
 
 // Bounded mbarrier wait: false on timeout or abort.  CL: the acquire also covers
-// arrivals released by the other CTA of a pair.
+// arrivals released by the other CTA of a pair.  `slack` multiplies the timeout, so that a
+// wait downstream of another (a pipeline stage waiting for its producer) gives the root
+// cause the first chance to be reported.
 template <bool CL = false, class KP, class SC>
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KP& p, SC* sc, uint32_t site) {
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const KP& p, SC* sc, uint32_t site,
+                                         uint32_t slack = 1) {
   auto poll = [&]() { return CL ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -59,7 +62,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const K
     if ((++it & 15u) == 0) {
       if (sc->abort) return false;
       if (ld_relaxed(&p.ctrl->abort)) { sc->abort = 1; return false; }
-      if (globaltimer_ns() - t0 > p.timeout_ns) { raise_error(p, site); sc->abort = 1; return false; }
+      if (globaltimer_ns() - t0 > p.timeout_ns * slack) { raise_error(p, site); sc->abort = 1; return false; }
     }
   }
 }

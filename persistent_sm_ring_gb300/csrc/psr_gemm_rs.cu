@@ -9,17 +9,20 @@
 // forwarded to its owner as soon as its partials exist.  On one GPU the P ranks are emulated
 // in HBM:
 //
-//  * compute CTAs produce one 256 x 256 partial tile of one rank per task on tcgen05 (the
-//    shared tile of psr_gemm_tile.cuh) and write it in fp32 to that rank's partial buffer;
-//    the epilogue warp that completes the last of an output tile's P partials enqueues the
-//    tile for reduction (a gpu-scope release, like the ring's readiness flags);
-//  * reduce CTAs (the communication role) take enqueued tiles, stream the P partials through
-//    shared memory with TMA bulk copies, sum them in rank order (fixed, so the result does not
-//    depend on timing) and write the owner's bf16 rows;
+//  * the CTAs work in pairs (clusters of two); a pair takes either role;
+//  * a compute pair produces one 256 x 256 partial tile of one rank per task (the pair tile of
+//    psr_gemm_tile.cuh: each CTA 128 rows, tcgen05 cta_group::2, double-buffered accumulators)
+//    and writes it in fp32 to that rank's partial buffer; the epilogue warp that completes the
+//    last of an output tile's P partials enqueues the tile for reduction (a gpu-scope release,
+//    like the ring's readiness flags);
+//  * each CTA of a reduce pair (the communication role) takes enqueued tiles, streams the P
+//    partials through shared memory with TMA bulk copies, sums them in rank order (fixed, so
+//    the result does not depend on timing) and writes the owner's bf16 rows;
 //  * compute tasks run window by window (up to 8 x 8 output tiles, every rank's partials of the
 //    window before the next window), so reductions start one window after the launch and a
 //    window's partials are still in L2 when they are reduced;
-//  * the shared controller splits CTAs between the roles with the pages' rule.  Compute feeds
+//  * the shared controller splits the pairs between the roles with the pages' rule (a target of
+//    n reduce CTAs gives ceil(n/2) reduce pairs).  Compute feeds
 //    communication here, so the launch starts with no reduce CTA (pwwt.cn §2.4: the data
 //    dependence decides the initial allocation) and the controller adds them as tiles complete.
 #include <cuda.h>
@@ -44,9 +47,7 @@ constexpr int kRoundBytes = kStageArea / 3;      // one reduce round: P partial 
 constexpr int kMaxP = kRoundBytes / (kBN * 4);   // at least one 256-column fp32 row per rank
 static_assert(kRoundBytes % 1024 == 0, "reduce round");
 
-enum : uint32_t { SITE_FLAG = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_ACC = 4, SITE_REDUCE_LOAD = 8,
-                  SITE_REDUCE_FREE = 9, SITE_QUEUE = 10 };
-enum : int { CMD_EXIT = 0, CMD_COMPUTE = 1, CMD_REDUCE = 2 };
+enum : uint32_t { SITE_FLAG = 1, SITE_REDUCE_LOAD = 8, SITE_REDUCE_FREE = 9, SITE_QUEUE = 10 };
 
 struct Geo {
   int M, N, Ks, P, Mq;
@@ -94,147 +95,190 @@ __device__ __host__ inline Item item_of(const Geo& g, long long idx) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Task selection (thread 0)
+// Task selection (the even CTA's thread 0, for its pair)
 // ------------------------------------------------------------------------------------------------
-// Reduce tickets are claimed in completion order.  In the adaptive mode a CTA claims one only
-// when an enqueued tile is waiting (or when no compute task is left), so a ticket holder waits
-// only for tiles whose compute tasks are running; at most n_max < N CTAs hold tickets.
-__device__ void decide(const Params& p, Smem* sc, bool& was_reducing) {
+// Reduce tickets are claimed in completion order; a reduce task carries the queue positions of
+// the even CTA's ticket (arg) and of the odd CTA's (arg1, or -1).  In the adaptive mode a pair
+// claims a ticket only when an enqueued tile is waiting (or when no compute task is left), and
+// a second one only when a second tile is waiting, so a ticket holder waits only for tiles whose
+// compute tasks are running; at most n_max < N CTAs hold tickets.  With `ahead` (called while
+// the current compute task's last loads are in flight) only a compute task is claimed: a ticket
+// may wait for that very task.
+__device__ void decide(const Params& p, Smem* sc, Task& t, bool& was_reducing, bool ahead) {
   Ctrl* c = p.ctrl;
   const Geo& g = p.g;
-  if (sc->abort || ld_relaxed(&c->abort)) { sc->cmd = CMD_EXIT; return; }
+  t.cmd = ahead ? CMD_NONE : CMD_EXIT;
+  t.arg = -1;
+  t.arg1 = -1;
+  t.pad = 0;
+  if (sc->abort || ld_relaxed(&c->abort)) return;
   const int n_s = current_target(p);
-  const bool reduce_role = (int)blockIdx.x < n_s;
+  const bool reduce_role = 2 * (int)(blockIdx.x / 2) < n_s;
   if (reduce_role != was_reducing) {
     atomicAdd(&c->role_switches, 1ull);
     was_reducing = reduce_role;
   }
   const bool fixed = p.mode == PSR_STATIC;
-  auto take_ticket = [&]() -> bool {
+  const bool compute_left = ld_relaxed(&c->item_next) < (uint32_t)g.n_items;
+  auto take_tickets = [&]() -> bool {
     const uint32_t h = atomicAdd(&c->q_head, 1u);
     if (h >= (uint32_t)g.n_out) return false;
     uint32_t seen = 0;
-    if (!wait_flag(p.queue + h, 1u, seen, p, sc, SITE_FLAG)) { sc->cmd = CMD_EXIT; return true; }
-    sc->cmd = CMD_REDUCE;
-    sc->arg = (int)(seen - 1u);
+    if (!wait_flag(p.queue + h, 1u, seen, p, sc, SITE_FLAG)) return true;  // CMD_EXIT
+    t.cmd = CMD_COMM;
+    t.arg = (int)h;
+    if (fixed || !compute_left || ld_relaxed(&c->q_tail) > h + 1) {
+      const uint32_t h1 = atomicAdd(&c->q_head, 1u);
+      if (h1 < (uint32_t)g.n_out) {
+        if (!wait_flag(p.queue + h1, 1u, seen, p, sc, SITE_FLAG)) {
+          t.cmd = CMD_EXIT;
+          return true;
+        }
+        t.arg1 = (int)h1;
+      }
+    }
     return true;
   };
-  const bool compute_left = ld_relaxed(&c->item_next) < (uint32_t)g.n_items;
   if (reduce_role) {
     const uint32_t head = ld_relaxed(&c->q_head);
-    if (head < (uint32_t)g.n_out) {
-      if ((fixed || !compute_left || ld_relaxed(&c->q_tail) > head) && take_ticket()) return;
+    if (head < (uint32_t)g.n_out && (fixed || !compute_left || ld_relaxed(&c->q_tail) > head)) {
+      if (ahead) return;
+      if (take_tickets()) return;
     }
-    if (fixed) { sc->cmd = CMD_EXIT; return; }
+    if (fixed) return;
   }
-  if (!(fixed && reduce_role) && compute_left) {
+  if (compute_left) {
     const uint32_t n = atomicAdd(&c->item_next, 1u);
-    if (n < (uint32_t)g.n_items) { sc->cmd = CMD_COMPUTE; sc->arg = (int)n; return; }
+    if (n < (uint32_t)g.n_items) {
+      t.cmd = CMD_COMPUTE;
+      t.arg = (int)n;
+      return;
+    }
   }
+  if (ahead) return;
   // no compute task left: help with the reductions (adaptive)
-  if (!fixed && ld_relaxed(&c->q_head) < (uint32_t)g.n_out && take_ticket()) return;
-  sc->cmd = CMD_EXIT;
+  if (!fixed && ld_relaxed(&c->q_head) < (uint32_t)g.n_out && take_tickets()) return;
+  t.cmd = CMD_EXIT;
 }
 
 // ------------------------------------------------------------------------------------------------
-// Reduce task: output tile o = sum over ranks of its partial tiles, rounded to bf16
+// Reduce task (one CTA): output tile o = sum over ranks of its partial tiles, rounded to bf16
 // ------------------------------------------------------------------------------------------------
 // Round k of the task carries rows k*cr .. k*cr+cr-1 of every rank's partial (P bulk copies of
 // cr KiB into one third of the stage area); thread 0 issues the copies, the eight epilogue warps
 // sum and store.  Three rounds are in flight; stg[s] counts a round's bytes, stg[3 + s] the
-// eight consumer warps that have read it.  `rounds` is the CTA's lifetime round count.
-__device__ void run_reduce(const Params& p, Smem* sc, uint32_t smem_base, const uint8_t* smem, int o,
-                           uint32_t& rounds) {
+// eight consumer warps that have read it.  `rounds` is the CTA's lifetime round count, kept by
+// both sides.  `h` is the ticket's queue position (its entry is already published: the
+// scheduler waited for it).
+//
+// Producer side.  The stage area is free of MMA reads first (wait_stages_free), and the
+// consumers have read the last rounds before it returns, so that later TMA fills may overwrite
+// the area.  False on timeout or abort.
+__device__ bool reduce_loads(const Params& p, Smem* sc, uint32_t smem_base, int h, uint32_t& rounds, uint32_t fills) {
   const Geo& g = p.g;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int o = (int)ld_acquire(p.queue + h) - 1;
   const int n_rounds = kBM / g.cr;
   const uint32_t rank_bytes = (uint32_t)g.cr * kBN * 4;
+  if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
+  const uint32_t r0 = rounds;
+  rounds += (uint32_t)n_rounds;
+  if (!wait_stages_free(p, sc, fills)) return false;
+  // the partials were written by other CTAs (generic proxy) and published with a release that
+  // the acquire above observed; order those writes before the bulk copies
+  fence_proxy_async_global();
+  for (int k = 0; k < n_rounds; ++k) {
+    const uint32_t u = r0 + (uint32_t)k;
+    const uint32_t s = u % 3, use = u / 3;
+    if (use > 0) {
+      if (!wait_bar(&sc->stg[3 + s], (use - 1) & 1u, p, sc, SITE_REDUCE_FREE)) return false;
+      fence_proxy_async_smem();  // the consumers' generic reads of the buffer before the copies into it
+    }
+    mbar_expect_tx(&sc->stg[s], rank_bytes * (uint32_t)g.P);
+    for (int r = 0; r < g.P; ++r) {
+      const float* src = p.part + ((size_t)r * g.n_out + o) * kTileElems + (size_t)k * g.cr * kBN;
+      bulk_load(smem_base + s * kRoundBytes + (uint32_t)r * rank_bytes, src, rank_bytes, &sc->stg[s]);
+    }
+  }
+  atomicAdd(&p.ctrl->stage_bytes, (unsigned long long)rank_bytes * g.P * n_rounds);
+  const uint32_t first = rounds >= 3u ? rounds - 3u : 0u;
+  for (uint32_t u = first; u < rounds; ++u)
+    if (!wait_bar(&sc->stg[3 + u % 3], (u / 3) & 1u, p, sc, SITE_REDUCE_FREE)) return false;
+  fence_proxy_async_smem();
+  return true;
+}
+
+// Consumer side (the eight epilogue warps).  False on timeout or abort.
+__device__ bool reduce_sums(const Params& p, Smem* sc, const uint8_t* smem, int h, uint32_t& rounds) {
+  const Geo& g = p.g;
+  const int lane = threadIdx.x % 32;
+  const int o = (int)ld_acquire(p.queue + h) - 1;
   const int mb = o / g.n_nb, nb = o % g.n_nb;
-  if (threadIdx.x == 0) {
-    if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
-    // the partials were written by other CTAs (generic proxy) and published with a release
-    // that the ticket's acquire observed; order those writes, and this CTA's earlier generic
-    // reads of the stage area, before the bulk copies
-    fence_proxy_async_global();
-    fence_proxy_async_smem();
-    bool ok = true;
-    for (int k = 0; k < n_rounds && ok; ++k) {
-      const uint32_t u = rounds + (uint32_t)k;
-      const uint32_t s = u % 3, use = u / 3;
-      if (use > 0) {
-        if (!wait_bar(&sc->stg[3 + s], (use - 1) & 1u, p, sc, SITE_REDUCE_FREE)) { ok = false; break; }
-        fence_proxy_async_smem();  // the consumers' generic reads of the buffer before the copies into it
-      }
-      mbar_expect_tx(&sc->stg[s], rank_bytes * (uint32_t)g.P);
-      for (int r = 0; r < g.P; ++r) {
-        const float* src = p.part + ((size_t)r * g.n_out + o) * kTileElems + (size_t)k * g.cr * kBN;
-        bulk_load(smem_base + s * kRoundBytes + (uint32_t)r * rank_bytes, src, rank_bytes, &sc->stg[s]);
-      }
-    }
-    if (!ok) sc->abort = 1;
-    atomicAdd(&p.ctrl->stage_bytes, (unsigned long long)rank_bytes * g.P * n_rounds);
-  } else if (warp >= 4) {
-    const int t = threadIdx.x - 128;  // 0..255
-    const int per_round = g.cr * (kBN / 4);  // float4 elements of one rank's rows in a round
-    bool ok = true;
-    for (int k = 0; k < n_rounds; ++k) {
-      const uint32_t u = rounds + (uint32_t)k;
-      const uint32_t s = u % 3, use = u / 3;
-      if (ok) ok = __all_sync(0xffffffffu, wait_bar(&sc->stg[s], use & 1u, p, sc, SITE_REDUCE_LOAD));
-      if (ok) {
-        const float4* base = reinterpret_cast<const float4*>(smem + s * kRoundBytes);
-        for (int e = t; e < per_round; e += 256) {
-          float4 acc = base[e];
-          for (int r = 1; r < g.P; ++r) {
-            const float4 x = base[r * per_round + e];
-            acc.x += x.x;
-            acc.y += x.y;
-            acc.z += x.z;
-            acc.w += x.w;
-          }
-          const int row = k * g.cr + e / (kBN / 4), col = (e % (kBN / 4)) * 4;
-          uint2 v;
-          v.x = pack_bf16x2(acc.x, acc.y);
-          v.y = pack_bf16x2(acc.z, acc.w);
-          *reinterpret_cast<uint2*>(p.out + (size_t)(mb * kBM + row) * g.N + (size_t)nb * kBN + col) = v;
+  const int n_rounds = kBM / g.cr;
+  const int t = threadIdx.x - 128;            // 0..255
+  const int per_round = g.cr * (kBN / 4);     // float4 elements of one rank's rows in a round
+  bool ok = true;
+  for (int k = 0; k < n_rounds; ++k) {
+    const uint32_t u = rounds + (uint32_t)k;
+    const uint32_t s = u % 3, use = u / 3;
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(&sc->stg[s], use & 1u, p, sc, SITE_REDUCE_LOAD, kSlack));
+    if (ok) {
+      const float4* base = reinterpret_cast<const float4*>(smem + s * kRoundBytes);
+      for (int e = t; e < per_round; e += 256) {
+        float4 acc = base[e];
+        for (int r = 1; r < g.P; ++r) {
+          const float4 x = base[r * per_round + e];
+          acc.x += x.x;
+          acc.y += x.y;
+          acc.z += x.z;
+          acc.w += x.w;
         }
+        const int row = k * g.cr + e / (kBN / 4), col = (e % (kBN / 4)) * 4;
+        uint2 v;
+        v.x = pack_bf16x2(acc.x, acc.y);
+        v.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(p.out + (size_t)(mb * kBM + row) * g.N + (size_t)nb * kBN + col) = v;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sc->stg[3 + s]);  // also on abort: the issuer's waits stay bounded
     }
-    if (!ok) sc->abort = 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sc->stg[3 + s]);  // also on abort: the issuer's waits stay bounded
   }
   rounds += (uint32_t)n_rounds;
+  if (!ok) sc->abort = 1;
+  return ok;
 }
 
 // ------------------------------------------------------------------------------------------------
-// Compute task: producer (TMA), MMA issuer (tcgen05), epilogue warpgroups -> fp32 partial tile
+// Compute task epilogue (each epilogue warp of both CTAs) -> fp32 partial tile
 // ------------------------------------------------------------------------------------------------
-__device__ void epilogue(const Params& p, Smem* sc, uint8_t* smem, const Item& it, int i, const Counters& cnt) {
+// The warp's 32 rows x 128 columns of the partial tile; then its arrival on the tile's count
+// (16 warps per partial), and the last arrival of the output tile's P partials enqueues it.
+__device__ bool epilogue(const Params& p, Smem* sc, uint8_t* epi, uint32_t rank, const Item& it, uint32_t item) {
   const Geo& g = p.g;
   const int warp = threadIdx.x / 32;
-  float* tile = p.part + ((size_t)it.r * g.n_out + it.o) * kTileElems + (size_t)i * 128 * kBN;
-  // the stage area is idle during the epilogue (every MMA of the tile has completed): 8 KiB per warp
-  uint8_t* stage = smem + (warp - 4) * 8192;
-  uint8_t* rows = reinterpret_cast<uint8_t*>(tile + (size_t)((warp % 4) * 32) * kBN);
-  const bool ok = read_tile(p, sc, i, cnt, SITE_ACC, [&](int, int cb, const uint32_t(&v)[64]) {
-    warp_store_rows<64>(stage, v, rows + cb * 256, (size_t)kBN * 4);
+  float* tile = p.part + ((size_t)it.r * g.n_out + it.o) * kTileElems;
+  const int row0 = (int)rank * kRows + (warp % 4) * 32, col0 = ((warp - 4) / 4) * 128;
+  uint8_t* rows = reinterpret_cast<uint8_t*>(tile + (size_t)row0 * kBN + col0);
+  uint8_t* stage = epi + (warp - 4) * kEpiWarpBytes;
+  const bool ok = read_acc(p, sc, rank, item, [&](int cb, const uint32_t* v) {
+    warp_store_rows<32>(stage, v, rows + cb * 256, (size_t)kBN * 4);
+    warp_store_rows<32>(stage, v + 32, rows + cb * 256 + 128, (size_t)kBN * 4);
   });
-  if (!ok) return;
-  // this warp's 32 rows are written: publish them (each thread's stores before lane 0's release)
+  if (!ok) return false;
+  // this warp's rows are written: publish them (each thread's stores before lane 0's release)
   __threadfence();
   __syncwarp();
   if ((threadIdx.x % 32) == 0) {
     const bool drop = (p.fault == PSR_FAULT_DROP_FIRST_FLAG) && (atomicAdd(&p.ctrl->fault_count, 1u) == 0u);
     if (!drop) {
       const uint32_t old = atom_add_acq_rel(p.count + it.o, 1u);
-      if (old + 1u == 8u * (uint32_t)g.P) {
+      if (old + 1u == 2u * kEpiWarps * (uint32_t)g.P) {
         const uint32_t k = atomicAdd(&p.ctrl->q_tail, 1u);
         if (k < (uint32_t)g.n_out) st_release(p.queue + k, (uint32_t)it.o + 1u);
         else raise_error(p, SITE_QUEUE);
       }
     }
   }
+  return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -244,20 +288,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Smem sc;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t smem_base = (raw + 1023u) & ~1023u;
-  const uint8_t* smem = smem_raw + (smem_base - raw);
+  uint8_t* smem = smem_raw + (smem_base - raw);
+  uint8_t* epi = smem + kStageArea;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNStage; ++s) {
-      mbar_init(&sc.full[s], 1);
-      mbar_init(&sc.empty[s], 1);
-    }
-    mbar_init(&sc.acc_full, 1);
+    init_barriers(&sc);
     for (int s = 0; s < 3; ++s) {
-      mbar_init(&sc.stg[s], 1);      // a reduce round's bytes have landed
-      mbar_init(&sc.stg[3 + s], 8);  // the eight consumer warps have read it
+      mbar_init(&sc.stg[s], 1);              // a reduce round's bytes have landed
+      mbar_init(&sc.stg[3 + s], kEpiWarps);  // the eight consumer warps have read it
     }
-    mbar_init(&sc.drain, 1);
-    sc.abort = 0;
     fence_barrier_init();
     if (blockIdx.x == 0) {
       unsigned long long z = 0;
@@ -269,62 +309,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_w);
   }
-  if (warp == 1) {
-    tmem_alloc(&sc.tmem_base, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  setup_pair(&sc);
 
-  Counters cnt{0, 0};
-  uint32_t rounds = 0;
-  bool was_reducing = false;
-  long long t_task = 0;
-  const int n_k = p.g.Ks / kBK;
-  while (true) {
-    if (threadIdx.x == 0) {
-      decide(p, &sc, was_reducing);
-      t_task = clock64();
-    }
-    __syncthreads();
-    const int cmd = sc.cmd, arg = sc.arg;
-    if (cmd == CMD_EXIT) break;
-    if (cmd == CMD_REDUCE) {
-      run_reduce(p, &sc, smem_base, smem, arg, rounds);
-    } else {
-      const Item it = item_of(p.g, arg);
-      if (warp == 0 && lane == 0) {
-        Counters c2 = cnt;
-        fence_proxy_async_smem();  // earlier generic reads of the stage area (a reduce task)
-        if (!load_tile(p, &sc, smem_base, &tm_a, it.r * p.g.M + it.mb * kBM, &tm_w, it.r * p.g.N + it.nb * kBN, n_k,
-                       c2, SITE_KV_EMPTY))
-          sc.abort = 1;
-      } else if (warp == 1 && lane == 0) {
-        Counters c2 = cnt;
-        mma_tile(p, &sc, smem_base, n_k, c2, SITE_KV_FULL);
-      } else if (warp >= 4) {
-        epilogue(p, &sc, smem_raw + (smem_base - raw), it, warp < 8 ? 0 : 1, cnt);
-      }
-      cnt.fills += (uint32_t)n_k;
-      cnt.items++;
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (threadIdx.x == 0) {
-      long long busy = clock64() - t_task;
-      const unsigned long long dt = (unsigned long long)(busy > 0 ? busy : 0);
-      if (cmd == CMD_REDUCE) {
-        atomicAdd(&p.ctrl->stage_cycles, dt);
-        atomicAdd(&p.ctrl->stage_done, 1ull);
+  const Geo& g = p.g;
+  const int n_k = g.Ks / kBK;
+  uint32_t fills = 0;   // thread 0: the stage fills this CTA issued
+  uint32_t rounds = 0;  // thread 0 and the epilogue warps: reduce rounds of this CTA
+  // This CTA's share of a compute task's loads.
+  auto produce = [&](const Task& t, int ahead_at, auto&& ahead) {
+    const Item it = item_of(g, t.arg);
+    return load_tile(p, &sc, smem_base, rank, &tm_a, it.r * g.M + it.mb * kBM + (int)rank * kRows, &tm_w,
+                     it.r * g.N + it.nb * kBN + (int)rank * kRows, n_k, fills, ahead_at, ahead);
+  };
+  if (warp == 0) {
+    if (lane == 0) {
+      if (rank == 0) {
+        // the pair's scheduler, and the even CTA's producer
+        bool was_reducing = false;
+        unsigned long long next_offer_ns = 0;
+        Task next;
+        next.cmd = CMD_NONE;
+        int prev_cmd = CMD_NONE, prev_tickets = 0;
+        long long t_prev = 0;
+        for (uint32_t k = 0;; ++k) {
+          Task t = next;
+          next.cmd = CMD_NONE;
+          if (t.cmd == CMD_NONE) decide(p, &sc, t, was_reducing, false);
+          // the previous task's cost, in CTA-cycles (both CTAs of the pair)
+          const long long now = clock64();
+          const unsigned long long busy = (unsigned long long)(now > t_prev ? now - t_prev : 0);
+          if (prev_cmd == CMD_COMPUTE) {
+            atomicAdd(&p.ctrl->compute_cycles, 2ull * busy);
+            atomicAdd(&p.ctrl->compute_tiles, 1ull);
+            atomicAdd(&p.ctrl->compute_items, 1ull);
+          } else if (prev_cmd == CMD_COMM) {
+            atomicAdd(&p.ctrl->stage_cycles, busy * (unsigned long long)prev_tickets);
+            atomicAdd(&p.ctrl->stage_done, (unsigned long long)prev_tickets);
+          }
+          controller_tick(p, next_offer_ns);
+          if (!post_task(p, &sc, k, t)) { sc.abort = 1; break; }
+          if (t.cmd == CMD_EXIT) break;
+          prev_cmd = t.cmd;
+          t_prev = clock64();
+          bool ok;
+          if (t.cmd == CMD_COMPUTE) {
+            ok = produce(t, n_k > kNStage ? n_k - kNStage : 0, [&] { decide(p, &sc, next, was_reducing, true); });
+          } else {
+            prev_tickets = t.arg1 >= 0 ? 2 : 1;
+            ok = reduce_loads(p, &sc, smem_base, t.arg, rounds, fills);
+          }
+          if (!ok) { sc.abort = 1; break; }
+        }
       } else {
-        atomicAdd(&p.ctrl->compute_cycles, dt);
-        atomicAdd(&p.ctrl->compute_tiles, 1ull);
-        atomicAdd(&p.ctrl->compute_items, 1ull);
+        // the odd CTA's producer
+        for (uint32_t k = 0;; ++k) {
+          Task t;
+          if (!take_task(p, &sc, k, t)) { sc.abort = 1; break; }
+          release_task(&sc, k, 1);
+          if (t.cmd == CMD_EXIT) break;
+          bool ok = true;
+          if (t.cmd == CMD_COMPUTE) ok = produce(t, -1, [] {});
+          else if (t.arg1 >= 0) ok = reduce_loads(p, &sc, smem_base, t.arg1, rounds, fills);
+          if (!ok) { sc.abort = 1; break; }
+        }
       }
-      const uint32_t tick = atomicAdd(&p.ctrl->ticks, 1u);
-      if (p.mode == PSR_ADAPTIVE && (tick % 16u) == 0) controller_update(p);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // the pair's MMA issuer
+      uint32_t mfills = 0, items = 0;
+      for (uint32_t k = 0;; ++k) {
+        Task t;
+        if (!take_task(p, &sc, k, t)) { sc.abort = 1; break; }
+        release_task(&sc, k, 0);
+        if (t.cmd == CMD_EXIT) break;
+        if (t.cmd != CMD_COMPUTE) continue;
+        if (!mma_tile(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
+        ++items;
+      }
+    }
+  } else if (warp >= 4) {
+    uint32_t items = 0;
+    for (uint32_t k = 0;; ++k) {
+      Task t;
+      const bool ok = __all_sync(0xffffffffu, take_task(p, &sc, k, t));
+      if (!ok) { sc.abort = 1; break; }
+      __syncwarp();
+      if (lane == 0) release_task(&sc, k, rank);
+      if (t.cmd == CMD_EXIT) break;
+      if (t.cmd == CMD_COMPUTE) {
+        if (!epilogue(p, &sc, epi, rank, item_of(g, t.arg), items)) break;
+        ++items;
+      } else {
+        const int h = rank == 0 ? t.arg : t.arg1;
+        if (h >= 0 && !reduce_sums(p, &sc, smem, h, rounds)) break;
+      }
     }
   }
   // every bulk copy of a reduce round has landed before the CTA exits (bounded)
@@ -336,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  drain_and_release(&sc, cnt);
+  drain_pair(&sc, rank, fills);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -413,7 +492,8 @@ int psr_gemm_rs(const psr_rs_shape* sh, const void* a, const void* w, void* out,
   cudaDeviceProp prop;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PSR_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return PSR_ERR_UNSUPPORTED;
-  const int n_cta = prop.multiProcessorCount;
+  const int n_cta = pair_ctas(gemm_rs_kernel, prop.multiProcessorCount);  // whole CTA pairs
+  if (n_cta < 4) return PSR_ERR_CUDA;
   Geo g;
   int rc = geometry(sh, g);
   if (rc != PSR_OK) return rc;
@@ -444,7 +524,7 @@ int psr_gemm_rs(const psr_rs_shape* sh, const void* a, const void* w, void* out,
   // ~100 GB/s per SM; a compute task (2*256*256*Ks flops) at ~60 % of an SM's dense bf16 rate
   kp.c_s0 = (float)(((double)g.P * kTileElems * 4 + kTileElems * 2) / 100e9 * 1.95e9);
   kp.c_p0 = (float)(2.0 * kBM * kBN * (double)g.Ks / (0.6 * 8192.0));
-  const int hard_max = n_cta - 1;
+  const int hard_max = n_cta - 2;  // at least one compute pair
   int n_max = pt.n_max > 0 ? pt.n_max : n_cta / 2;
   if (n_max > hard_max) n_max = hard_max;
   int n_min = pt.n_min > 0 ? pt.n_min : 1;
@@ -454,7 +534,7 @@ int psr_gemm_rs(const psr_rs_shape* sh, const void* a, const void* w, void* out,
   int n_s;
   if (pt.mode == PSR_STATIC) {
     n_s = pt.n_staging;
-    if (n_s < 1 || n_s > n_cta - 1) return PSR_ERR_ARG;
+    if (n_s < 1 || n_s > hard_max) return PSR_ERR_ARG;
   } else {
     // compute feeds the reductions: nothing to reduce at launch, so every CTA starts computing
     n_s = pt.n_staging > 0 ? (pt.n_staging < n_max ? pt.n_staging : n_max) : 0;
@@ -462,28 +542,13 @@ int psr_gemm_rs(const psr_rs_shape* sh, const void* a, const void* w, void* out,
   kp.n_s_init = n_s;
 
   CUtensorMap ma, mw;
-  if (!tmap_kmajor(&ma, a, (long long)g.P * g.M, g.Ks, 128) || !tmap_kmajor(&mw, w, (long long)g.P * g.N, g.Ks, kBN))
+  if (!tmap_kmajor(&ma, a, (long long)g.P * g.M, g.Ks, kRows) || !tmap_kmajor(&mw, w, (long long)g.P * g.N, g.Ks, kRows))
     return PSR_ERR_CUDA;
 
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_rs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  });
-  if (attr_err != cudaSuccess) return PSR_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, L.reset_bytes, st) != cudaSuccess) return PSR_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)n_cta);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: reductions wait on compute
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gemm_rs_kernel, kp, ma, mw) != cudaSuccess) {
+  // all pairs co-resident: reductions wait on compute
+  if (launch_pairs(gemm_rs_kernel, n_cta, st, kp, ma, mw) != cudaSuccess) {
     cudaGetLastError();
     return PSR_ERR_CUDA;
   }

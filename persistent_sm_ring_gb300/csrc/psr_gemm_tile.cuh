@@ -1,14 +1,24 @@
 // The 256 x 256 output tile of the persistent GEMM kernels (AllGather+GEMM and
-// GEMM+ReduceScatter) on sm_103a.
+// GEMM+ReduceScatter) on sm_103a, computed by a pair of CTAs (a cluster of two SMs).
 //
-//  * a ring of kNStage shared-memory stages, each holding two 128-row A tiles and one 256-row
-//    W tile of one 64-wide K step (both K-major, loaded by TMA with the 128-byte swizzle);
-//  * one elected thread issues tcgen05.mma (M = 128, N = 256, K = 16) for both 128-row halves
-//    of the tile, with both fp32 accumulators in tensor memory (2 x 256 columns), and commits
-//    each stage back to the producer as soon as its MMAs have read it;
-//  * two warpgroups read the accumulators back with tcgen05.ld, one 128-row half each (tensor
-//    memory lane = tile row), in 64-column blocks handed to a kernel-specific store.
-// Each kernel adds its own task selection, data dependencies and epilogue destination.
+//  * each CTA of the pair loads 128 of the tile's A rows and 128 of its W rows (output columns
+//    128*rank ..), one 64-wide K step per stage, K-major with the 128-byte swizzle, into a ring
+//    of kNStage stages; both CTAs' TMA loads are counted on the even CTA's stage barrier;
+//  * one thread of the even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16):
+//    each SM accumulates its 128 rows x 256 columns in fp32 tensor memory, in one of two
+//    accumulator buffers (2 x 256 columns), so that a tile's epilogue runs while the next
+//    tile accumulates into the other buffer;
+//  * the even CTA's scheduling thread hands tasks to the roles of both CTAs through a ring of
+//    task slots in shared memory (the odd CTA's copy written with distributed stores), each
+//    slot released by an mbarrier: no role waits for another at a task boundary;
+//  * eight epilogue warps per CTA read the accumulators back with tcgen05.ld (warp w: tensor
+//    memory lanes 32*(w%4) .., columns 128*((w-4)/4) ..) and hand 64-column blocks to a
+//    kernel-specific store.
+// Shared-memory traffic per SM and 64-wide K step: the MMAs read 32 KiB (its A rows and its
+// half of W; the other half is read by the peer SM) and TMA writes 32 KiB, i.e. ~128 B/clk at
+// the tensor rate, against ~160 B/clk for one SM computing a whole 256 x 256 tile.
+// Each kernel adds its own task selection, data dependencies, communication role and epilogue
+// destination.
 #pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -23,114 +33,225 @@
 namespace psr {
 namespace gemm {
 
-constexpr int kBM = 256;          // output rows per tile (two 128-row A tiles)
-constexpr int kBN = 256;          // output columns per tile (one W tile)
-constexpr int kBK = 64;           // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int kNStage = 3;        // stages of A0 | A1 | W
-constexpr int kATile = 128 * kBK * 2;   // 16 KiB
-constexpr int kWTile = kBN * kBK * 2;   // 32 KiB
-constexpr int kStageBytes = 2 * kATile + kWTile;
-constexpr int kStageArea = kNStage * kStageBytes;  // also the scratch of the copy / reduce roles
-constexpr int kSmem = 1024 + kStageArea;
+constexpr int kBM = 256;    // output rows per tile (128 per CTA of the pair)
+constexpr int kBN = 256;    // output columns per tile (W rows; 128 loaded by each CTA)
+constexpr int kBK = 64;     // K per stage (one 128-byte swizzle atom of bf16)
+constexpr int kRows = 128;  // A rows and W rows one CTA loads per tile
+constexpr int kNStage = 6;
+constexpr int kHalf = kRows * kBK * 2;             // 16 KiB
+constexpr int kStageBytes = 2 * kHalf;             // this CTA's A and W rows of one K step
+constexpr int kStageArea = kNStage * kStageBytes;  // 192 KiB; also the scratch of the comm roles
+constexpr int kEpiWarps = 8;
+constexpr int kEpiWarpBytes = 4096;  // one warp's store staging: 32 rows x 128 bytes
+constexpr int kEpiArea = kEpiWarps * kEpiWarpBytes;
+constexpr int kSmem = 1024 + kStageArea + kEpiArea;
 constexpr int kWarps = 12, kThreads = kWarps * 32;
-static_assert(kSmem <= 232448 - 512, "shared memory");
+constexpr int kSlots = 4;  // task ring
+constexpr uint32_t kAccCols = 256;
+// readers of a task slot: the odd CTA's producer, the MMA issuer, the epilogue warps of both CTAs
+constexpr uint32_t kTaskReaders = 2 + 2 * kEpiWarps;
+// the waits inside the tile pipeline give up after kSlack timeouts: a stall there is a
+// consequence of a wait upstream (a readiness flag, a queue entry), which reports first
+constexpr uint32_t kSlack = 4;
+static_assert(kSmem + 1024 <= 232448, "shared memory");
+
+enum : uint32_t { SITE_FULL = 2, SITE_EMPTY = 3, SITE_ACC = 4, SITE_TASK = 12, SITE_ACC_EMPTY = 13 };
+enum : int { CMD_NONE = -1, CMD_EXIT = 0, CMD_COMPUTE = 1, CMD_COMM = 2 };
+
+// One task of the pair: a compute task (arg = its index) or a communication task (arg for the
+// even CTA, arg1 for the odd one; -1 = nothing for that CTA).
+struct Task {
+  int cmd, arg, arg1, pad;
+};
 
 // Shared control state of one CTA.
 struct Smem {
-  uint64_t full[kNStage], empty[kNStage];  // stage loaded (TMA bytes) / stage read by the MMAs
-  uint64_t acc_full;                       // accumulators of the current tile complete
-  uint64_t stg[16];                        // the other role's buffers (kernel-specific)
+  uint64_t full[kNStage], empty[kNStage];  // stage loaded (both CTAs' bytes; even CTA) / read by the MMAs
+  uint64_t acc_full[2], acc_empty[2];      // accumulator buffer complete / read back (even CTA)
+  uint64_t task_full[kSlots], task_empty[kSlots];  // task slot written / read by every reader (even CTA)
+  uint64_t stg[16];                        // the communication role's buffers (kernel-specific)
   uint64_t drain;
+  Task task[kSlots];
   uint32_t tmem_base;
-  int cmd, arg;
+  uint32_t peer_fills;  // the odd CTA's stage fills, reported at the end
   volatile uint32_t abort;
 };
 
-// Running counts over the CTA's lifetime; every role advances its own copy identically,
-// so mbarrier phases agree across roles.
-struct Counters {
-  uint32_t fills;  // stage fills issued (producer) / consumed (issuer)
-  uint32_t items;  // tiles completed (accumulator phase)
-};
+// Thread 0 of each CTA: the pipeline's barriers (the kernel initialises stg[] itself).
+__device__ __forceinline__ void init_barriers(Smem* sc) {
+  for (int s = 0; s < kNStage; ++s) {
+    mbar_init(&sc->full[s], 1);
+    mbar_init(&sc->empty[s], 1);
+  }
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(&sc->acc_full[b], 1);
+    mbar_init(&sc->acc_empty[b], 2 * kEpiWarps);
+  }
+  for (int k = 0; k < kSlots; ++k) {
+    mbar_init(&sc->task_full[k], 1);
+    mbar_init(&sc->task_empty[k], kTaskReaders);
+  }
+  mbar_init(&sc->drain, 1);
+  sc->peer_fills = 0;
+  sc->abort = 0;
+}
 
-// Producer (one thread): the K loop of one tile, A rows arow .. arow+255 of `ma` and W rows
-// wrow .. wrow+255 of `mw`, n_k steps of kBK.  False on timeout or abort.
+// Every thread of both CTAs, after init_barriers: tensor memory (512 columns per CTA, the pair's
+// allocation), and both CTAs' barriers visible before any remote arrival.
+__device__ __forceinline__ void setup_pair(Smem* sc) {
+  if (threadIdx.x / 32 == 1) {
+    tmem_alloc_cg<2>(&sc->tmem_base, 512);
+    tmem_relinquish_cg<2>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Task ring
+// ------------------------------------------------------------------------------------------------
+// Scheduling thread (even CTA): publish task k to both CTAs.  False on timeout or abort.
 template <class KP>
-__device__ __forceinline__ bool load_tile(const KP& p, Smem* sc, uint32_t smem_base, const CUtensorMap* ma, int arow,
-                                          const CUtensorMap* mw, int wrow, int n_k, Counters& cnt,
-                                          uint32_t site_empty) {
+__device__ __forceinline__ bool post_task(const KP& p, Smem* sc, uint32_t k, const Task& t) {
+  const uint32_t s = k % kSlots, use = k / kSlots;
+  if (use > 0 && !wait_bar<true>(&sc->task_empty[s], (use - 1) & 1u, p, sc, SITE_TASK, kSlack)) return false;
+  sc->task[s] = t;
+  const uint32_t remote = mapa_shared(smem_u32(&sc->task[s]), 1);
+  st_shared_cluster(remote, (uint32_t)t.cmd);
+  st_shared_cluster(remote + 4, (uint32_t)t.arg);
+  st_shared_cluster(remote + 8, (uint32_t)t.arg1);
+  mbar_arrive(&sc->task_full[s]);
+  mbar_arrive_cluster(mapa_shared(smem_u32(&sc->task_full[s]), 1));  // release: orders the stores above
+  return true;
+}
+
+// A reader: wait for task k and read it.  False on timeout or abort.
+template <class KP>
+__device__ __forceinline__ bool take_task(const KP& p, Smem* sc, uint32_t k, Task& t) {
+  const uint32_t s = k % kSlots;
+  if (!wait_bar<true>(&sc->task_full[s], (k / kSlots) & 1u, p, sc, SITE_TASK, kSlack)) return false;
+  const volatile Task* e = &sc->task[s];
+  t.cmd = e->cmd;
+  t.arg = e->arg;
+  t.arg1 = e->arg1;
+  t.pad = 0;
+  return true;
+}
+
+// A reader is done with slot k (release: its reads of the slot come first).
+__device__ __forceinline__ void release_task(Smem* sc, uint32_t k, uint32_t rank) {
+  const uint32_t s = k % kSlots;
+  if (rank == 0) mbar_arrive(&sc->task_empty[s]);
+  else mbar_arrive_cluster(mapa_shared(smem_u32(&sc->task_empty[s]), 0));
+}
+
+// ------------------------------------------------------------------------------------------------
+// Producer (thread 0 of each CTA), MMA issuer (one thread of the even CTA), epilogue warps
+// ------------------------------------------------------------------------------------------------
+// This CTA's share of a tile's K loop: A rows arow .. arow+127 of `ma` and W rows wrow ..
+// wrow+127 of `mw`, n_k steps of kBK.  `ahead()` runs once, after the loads of step `ahead_at`
+// are issued (the scheduler decides its next task there).  `fills` counts the stage fills
+// this CTA has issued.  False on timeout or abort.
+template <class KP, class Ahead>
+__device__ __forceinline__ bool load_tile(const KP& p, Smem* sc, uint32_t smem_base, uint32_t rank,
+                                          const CUtensorMap* ma, int arow, const CUtensorMap* mw, int wrow, int n_k,
+                                          uint32_t& fills, int ahead_at, Ahead&& ahead) {
   for (int ks = 0; ks < n_k; ++ks) {
-    const uint32_t c = cnt.fills++;
-    const uint32_t s = c % kNStage, fill = c / kNStage;
-    if (fill > 0 && !wait_bar(&sc->empty[s], (fill - 1) & 1u, p, sc, site_empty)) return false;
+    const uint32_t c = fills;
+    const uint32_t s = c % kNStage, use = c / kNStage;
+    if (use > 0 && !wait_bar(&sc->empty[s], (use - 1) & 1u, p, sc, SITE_EMPTY, kSlack)) return false;
+    if (rank == 0) mbar_expect_tx(&sc->full[s], 2 * kStageBytes);  // both CTAs' bytes
+    const uint32_t bar = mapa_shared(smem_u32(&sc->full[s]), 0);
     const uint32_t base = smem_base + s * kStageBytes;
-    mbar_expect_tx(&sc->full[s], kStageBytes);
-    tma_load_2d(base, ma, ks * kBK, arow, &sc->full[s]);
-    tma_load_2d(base + kATile, ma, ks * kBK, arow + 128, &sc->full[s]);
-    tma_load_2d(base + 2 * kATile, mw, ks * kBK, wrow, &sc->full[s]);
+    tma_load_2d_pair(base, ma, ks * kBK, arow, bar);
+    tma_load_2d_pair(base + kHalf, mw, ks * kBK, wrow, bar);
+    fills = c + 1;
+    if (ks == ahead_at) ahead();
   }
   return true;
 }
 
-// MMA issuer (one thread): n_k stages into the two accumulators, then acc_full.
+// Producer, before a communication task reuses the stage area: every stage this CTA filled
+// has been read by the MMAs.  False on timeout or abort.
 template <class KP>
-__device__ __forceinline__ void mma_tile(const KP& p, Smem* sc, uint32_t smem_base, int n_k, Counters& cnt,
-                                         uint32_t site_full) {
-  constexpr uint32_t ID = idesc_bf16_f32(128, kBN, false);
-  constexpr uint32_t kHi = sdesc_hi_sw128(1024);
+__device__ __forceinline__ bool wait_stages_free(const KP& p, Smem* sc, uint32_t fills) {
+  for (uint32_t s = 0; s < (uint32_t)kNStage && s < fills; ++s) {
+    const uint32_t last = s + ((fills - 1 - s) / kNStage) * kNStage;  // the stage's last fill
+    if (!wait_bar(&sc->empty[s], (last / kNStage) & 1u, p, sc, SITE_EMPTY, kSlack)) return false;
+  }
+  return true;
+}
+
+// MMA issuer: n_k stages into accumulator buffer (item & 1), then acc_full on both CTAs.
+// `fills` counts the stages consumed.  False on timeout or abort.
+template <class KP>
+__device__ __forceinline__ bool mma_tile(const KP& p, Smem* sc, uint32_t smem_base, int n_k, uint32_t& fills,
+                                         uint32_t item) {
+  constexpr uint32_t ID = idesc_bf16_f32(2 * kRows, kBN, false);
+  constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // 8-row groups 1024 B apart
+  const uint32_t b = item & 1u, use = item >> 1;
+  if (use > 0 && !wait_bar<true>(&sc->acc_empty[b], (use - 1) & 1u, p, sc, SITE_ACC_EMPTY, kSlack)) return false;
+  tc_fence_after();
+  const uint32_t tacc = sc->tmem_base + b * kAccCols;
   for (int ks = 0; ks < n_k; ++ks) {
-    const uint32_t c = cnt.fills++;
-    const uint32_t s = c % kNStage, fill = c / kNStage;
-    if (!wait_bar(&sc->full[s], fill & 1u, p, sc, site_full)) { sc->abort = 1; return; }
+    const uint32_t c = fills;
+    const uint32_t s = c % kNStage;
+    if (!wait_bar(&sc->full[s], (c / kNStage) & 1u, p, sc, SITE_FULL, kSlack)) return false;
     tc_fence_after();
     const uint32_t base = smem_base + s * kStageBytes;
-    const uint32_t w_lo = sdesc_lo(base + 2 * kATile, 16);
+    const uint32_t a_lo = sdesc_lo(base, 16), w_lo = sdesc_lo(base + kHalf, 16);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t a_lo = sdesc_lo(base + i * kATile, 16);
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        mma_ss_w(sc->tmem_base + i * kBN, a_lo + kk * 2, kHi, w_lo + kk * 2, kHi, ID, (ks > 0 || kk > 0) ? 1u : 0u);
-    }
-    mma_commit(&sc->empty[s]);
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      mma_ss_cg<2>(tacc, a_lo + kk * 2, kHi, w_lo + kk * 2, kHi, ID, (ks > 0 || kk > 0) ? 1u : 0u);
+    mma_commit_cg<2>(&sc->empty[s], 3);
+    fills = c + 1;
   }
-  mma_commit(&sc->acc_full);
-}
-
-// Epilogue warpgroup for 128-row half i of the tile: waits for the accumulators, then hands
-// each 64-column block of this thread's row (row = 0..127 inside the half) to
-// store(row, cb, v[64]) as raw fp32 bits.  False on timeout or abort.
-template <class KP, class Store>
-__device__ __forceinline__ bool read_tile(const KP& p, Smem* sc, int i, const Counters& cnt, uint32_t site_acc,
-                                          Store&& store) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int quarter = warp % 4;
-  const int row = quarter * 32 + lane;
-  const bool ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full, cnt.items & 1u, p, sc, site_acc));
-  if (!ok) { sc->abort = 1; return false; }
-  tc_fence_after();
-  const uint32_t tacc = sc->tmem_base + ((uint32_t)(quarter * 32) << 16) + i * kBN;
-#pragma unroll 1
-  for (int cb = 0; cb < kBN / 64; ++cb) {
-    uint32_t v[64];
-    tmem_ld64(tacc + cb * 64, v);
-    tmem_ld_wait();
-    store(row, cb, v);
-  }
+  mma_commit_cg<2>(&sc->acc_full[b], 3);
   return true;
 }
 
-// Coalesced store of one 64-column block of a warp's 32 rows (the 32x32b tensor-memory load gives
-// each thread one row).  Each thread hands W 32-bit words of its row (W = 64: fp32; W = 32: bf16
-// pairs); the warp writes them into its shared-memory staging area (32 x 4W bytes) with the
-// 16-byte chunks XOR-swizzled by row, reads them back row-contiguous, and stores whole 4W-byte row
-// segments: 16 (fp32) or 8 (bf16) lanes per row instead of one lane per row.  Both shared-memory
-// passes are free of bank conflicts.  `gbase` is the byte address of the block in the warp's
-// first row, `stride` the row pitch in bytes.
+// Epilogue warp: waits for accumulator buffer (item & 1), reads this warp's 32 rows x 128
+// columns as two 64-column blocks, releases the buffer once both are in registers, and hands
+// each block to store(cb, v[64]) (columns col0 + 64*cb, col0 = 128*((warp-4)/4), raw fp32
+// bits; the thread's row inside the CTA's 128 is 32*(warp%4) + lane).  False on timeout or
+// abort.
+template <class KP, class Store>
+__device__ __forceinline__ bool read_acc(const KP& p, Smem* sc, uint32_t rank, uint32_t item, Store&& store) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quarter = warp % 4, chalf = (warp - 4) / 4;
+  const uint32_t b = item & 1u;
+  const bool ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full[b], (item >> 1) & 1u, p, sc, SITE_ACC, kSlack));
+  if (!ok) { sc->abort = 1; return false; }
+  tc_fence_after();
+  const uint32_t tacc = sc->tmem_base + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + chalf * 128;
+  uint32_t v[64];
+  tmem_ld64(tacc, v);
+  tmem_ld_wait();
+  store(0, v);
+  tmem_ld64(tacc + 64, v);
+  tmem_ld_wait();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if (rank == 0) mbar_arrive(&sc->acc_empty[b]);
+    else mbar_arrive_cluster(mapa_shared(smem_u32(&sc->acc_empty[b]), 0));
+  }
+  store(1, v);
+  return true;
+}
+
+// Coalesced store of one block of a warp's 32 rows (the 32x32b tensor-memory load gives each
+// thread one row).  Each thread hands W 32-bit words of its row; the warp writes them into its
+// shared-memory staging area (32 x 4W bytes) with the 16-byte chunks XOR-swizzled by row,
+// reads them back row-contiguous, and stores whole 4W-byte row segments (W/4 lanes per row
+// instead of one lane per row).  Both shared-memory passes are free of bank conflicts.
+// `gbase` is the byte address of the block in the warp's first row, `stride` the row pitch.
 template <int W>
 __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t* words, uint8_t* gbase, size_t stride) {
-  constexpr int R = W / 4;        // 16-byte chunks per row segment
-  constexpr int RPI = 32 / R;     // rows per read-back instruction
+  constexpr int R = W / 4;     // 16-byte chunks per row segment
+  constexpr int RPI = 32 / R;  // rows per read-back instruction
   const int lane = threadIdx.x % 32;
 #pragma unroll
   for (int j = 0; j < R; ++j)
@@ -146,32 +267,46 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t* 
   __syncwarp();  // the staging area is reused for the next block
 }
 
-// End of the kernel (all threads): every tcgen05 op has completed and every TMA load into
-// the stages has landed (bounded waits) before tensor memory is released.
-__device__ __forceinline__ void drain_and_release(Smem* sc, const Counters& cnt) {
+// End of the kernel (every thread of both CTAs).  `fills` is thread 0's count of the stage
+// fills its CTA issued.  Every tcgen05 op has completed and every TMA load into either CTA's
+// stages has landed (bounded waits) before tensor memory is released and either CTA exits.
+// The loads of both CTAs count on the even CTA's barriers; after an abort the two producers
+// may have issued different numbers of fills (at most one apart per stage), so the even CTA
+// completes each stage's last phase itself: it arms a phase only the odd CTA loaded, and
+// accounts for the odd CTA's bytes of a phase that only it loaded.
+__device__ __forceinline__ void drain_pair(Smem* sc, uint32_t rank, uint32_t fills) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  if (warp == 1 && lane == 0) {
-    mma_commit(&sc->drain);
+  if (warp == 1 && lane == 0 && rank == 0) {
+    mma_commit_cg<2>(&sc->drain, 1);
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(&sc->drain, 0)) {
       if (globaltimer_ns() - t0 > 100000000ull) break;
     }
   }
-  if (threadIdx.x == 0) {
-    bulk_wait<0>();
+  if (threadIdx.x == 0 && rank == 1) st_shared_cluster(mapa_shared(smem_u32(&sc->peer_fills), 0), fills);
+  __syncthreads();
+  cluster_sync();
+  if (threadIdx.x == 0 && rank == 0) {
+    const uint32_t L = fills, Q = sc->peer_fills, F = L > Q ? L : Q;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t s = 0; s < (uint32_t)kNStage && s < cnt.fills; ++s) {
-      const uint32_t fills = (cnt.fills - s + kNStage - 1) / kNStage;
-      while (!mbar_try_wait(&sc->full[s], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+    for (uint32_t s = 0; s < (uint32_t)kNStage && s < F; ++s) {
+      const uint32_t m = s + ((F - 1 - s) / kNStage) * kNStage;  // the stage's last fill by either CTA
+      if (m >= L) mbar_expect_tx(&sc->full[s], kStageBytes);           // armed by no one: the odd CTA's bytes
+      else if (m >= Q) mbar_complete_tx(&sc->full[s], kStageBytes);    // the odd CTA's bytes will not come
+      while (!mbar_try_wait(&sc->full[s], (m / kNStage) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still signal it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(sc->tmem_base, 512);
+  if (warp == 1) tmem_dealloc_cg<2>(sc->tmem_base, 512);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------------
 // cuTensorMapEncodeTiled from the driver (looked up once), or null.
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -198,6 +333,66 @@ inline bool tmap_kmajor(CUtensorMap* m, const void* base, long long rows, int K,
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// CTAs of a pair kernel that can all be resident at once: whole pairs, no more than the SMs
+// and the device's co-resident clusters allow (0 on error).  Computed once per kernel.
+template <class Kern>
+inline int pair_ctas(Kern kern, int n_sm) {
+  static std::once_flag once;
+  static int n_ok = 0;
+  std::call_once(once, [kern, n_sm] {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_sm / 2 * 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    n_ok = 2 * max_clusters < n_sm / 2 * 2 ? 2 * max_clusters : n_sm / 2 * 2;
+  });
+  return n_ok;
+}
+
+// Launch n_cta CTAs (whole pairs, all co-resident: pair_ctas) as clusters of two: a
+// cooperative launch where the driver accepts one for clusters, else a plain cluster launch
+// (the occupancy bound of pair_ctas still holds every pair resident at once).
+template <class Kern, class... Args>
+inline cudaError_t launch_pairs(Kern kern, int n_cta, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_cta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, args...);
+  }
+  return e;
 }
 
 }  // namespace gemm
