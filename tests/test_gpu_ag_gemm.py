@@ -1,9 +1,10 @@
 """GPU parity of the AllGather + GEMM path (psr_ag_gemm through the C ABI) against the fp64
 oracle (oracle/ag_gemm.py).
 
-Bound: the result is the fp32-accumulated product rounded to bf16 (round to nearest even,
-relative error <= 2^-9); every compared element must satisfy
-|C - C_ref| <= 2^-8 |C_ref| + 2^-12 rms(C_ref), and ||C - C_ref||_2 / ||C_ref||_2 <= 3e-3.
+Bound: the result is the fp32-accumulated product rounded to bf16 (8 significant bits, round to
+nearest even: relative error <= 2^-8, the first term of the bound; the fp32 accumulation errors, a
+random walk of ~sqrt(K) roundings of 2^-24, stay far below the second); every compared element
+must satisfy |C - C_ref| <= 2^-8 |C_ref| + 2^-12 rms(C_ref), and ||C - C_ref||_2 / ||C_ref||_2 <= 3e-3.
 """
 import numpy as np
 import pytest

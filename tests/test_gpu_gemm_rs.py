@@ -2,9 +2,10 @@
 fp64 oracle (oracle/gemm_rs.py).
 
 Bound: each rank's partial is an fp32 tensor-core accumulation over Ks, the P partials are
-summed in fp32 in rank order and the sum is rounded to bf16 (round to nearest even, relative
-error <= 2^-9); every compared element must satisfy
-|out - ref| <= 2^-8 |ref| + 2^-12 rms(ref), and ||out - ref||_2 / ||ref||_2 <= 3e-3.
+summed in fp32 in rank order and the sum is rounded to bf16 (8 significant bits, round to
+nearest even: relative error <= 2^-8, the first term of the bound; the fp32 accumulation errors,
+a random walk of ~sqrt(K) roundings of 2^-24, stay far below the second); every compared element
+must satisfy |out - ref| <= 2^-8 |ref| + 2^-12 rms(ref), and ||out - ref||_2 / ||ref||_2 <= 3e-3.
 """
 import numpy as np
 import pytest

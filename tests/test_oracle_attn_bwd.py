@@ -174,3 +174,82 @@ def test_dq_rows_match_full():
         rows = np.array([0, 3, S - 1, S + 1, 2 * S + 30, B * Hq * S - 1])
         got = ob.attn_bwd_dq_rows(q, k, v, do, causal=causal, scale=0.4, bh_rows=rows)
         assert np.allclose(got, dq.reshape(-1, d)[rows], rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------------------------------------
+# The GPU parity bounds come from error_scales.  Pin it against an emulation of the roundings it
+# models (numpy, float64 between the bf16 roundings): the emulated gradients must stay inside the
+# worst-case bound, and their L2 deviation inside the independent-rounding bound.
+# ------------------------------------------------------------------------------------------------
+U = 2.0 ** -8  # relative rounding error of bf16 (8 significant bits, round to nearest)
+
+
+def _bf16(x):
+    """Round float64 to the nearest bf16 (via float32; ties to even), as float64."""
+    b = np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _emulated_bf16_path(q_bits, k_bits, v_bits, do_bits, causal, scale):
+    """Forward and backward with bf16 roundings where a bf16 tensor-core path makes them: P before
+    P V, O; P before P dO and before dS (the K/V side), dS before dS K and dS^T Q, the gradients.
+    The query side forms dS from the unrounded P, as the dQ pass does."""
+    f = ri.bf16_bits_to_f64
+    q, k, v, do = f(q_bits), f(k_bits), f(v_bits), f(do_bits)
+    B, Hq, S, d = q.shape
+    g = Hq // k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    mask = np.triu(np.ones((S, S), dtype=bool), 1) if causal else np.zeros((S, S), dtype=bool)
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, h // g], v[b, h // g]
+            s = np.where(mask, -np.inf, scale * q[b, h] @ kh.T)
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            l = e.sum(axis=1, keepdims=True)
+            o = _bf16((_bf16(e) @ vh) / l)
+            lse = m + np.log(l)
+            p = np.exp(s - lse)
+            pr = _bf16(p)
+            dp = do[b, h] @ vh.T
+            D = np.sum(do[b, h] * o, axis=1, keepdims=True)
+            dv[b, h // g] += pr.T @ do[b, h]
+            dk[b, h // g] += scale * (_bf16(pr * (dp - D)).T @ q[b, h])
+            dq[b, h] = _bf16(scale * (_bf16(p * (dp - D)) @ kh))
+    return dq, _bf16(dk), _bf16(dv)
+
+
+@pytest.mark.parametrize("causal,Hq,Hkv,seed", [(False, 2, 2, 31), (True, 2, 2, 32), (True, 4, 2, 33)])
+def test_error_scales_cover_emulated_bf16_roundings(causal, Hq, Hkv, seed):
+    rng = np.random.default_rng(seed)
+    S, d, scale = 256, 32, 0.3
+    q, k, v = _bits(rng, (1, Hq, S, d), 1.5), _bits(rng, (1, Hkv, S, d), 1.5), _bits(rng, (1, Hkv, S, d))
+    do = _bits(rng, (1, Hq, S, d))
+    exact = ob.attn_bwd(q, k, v, do, causal=causal, scale=scale)
+    emul = _emulated_bf16_path(q, k, v, do, causal, scale)
+    (E, T2) = ob.error_scales(q, k, v, do, causal=causal, scale=scale)
+    for g_em, g_ex, e, t2 in zip(emul, exact, E, T2):
+        err = np.abs(g_em - g_ex)
+        # worst case, first order in U (second-order terms are below 1 % of it)
+        assert np.all(err <= 1.01 * U * (e + np.abs(g_ex)) + 1e-300)
+        # independent roundings: L2 deviation within twice its RMS bound, plus the outputs' rounding
+        rms = U * np.sqrt(t2.sum() / 3.0)
+        assert np.linalg.norm(err) <= 2.0 * rms + U * np.linalg.norm(g_ex)
+        # and the bounds are not vacuous: the deviation is a visible share of them
+        assert np.linalg.norm(err) >= 0.1 * rms
+
+
+def test_error_scale_rows_match_full():
+    rng = np.random.default_rng(41)
+    q, k, v = _bits(rng, (1, 4, 64, 16), 1.5), _bits(rng, (1, 2, 64, 16), 1.5), _bits(rng, (1, 2, 64, 16))
+    do = _bits(rng, (1, 4, 64, 16))
+    for causal in (False, True):
+        (E, T2) = ob.error_scales(q, k, v, do, causal=causal, scale=0.3)
+        qr, kr = np.array([0, 9, 64 + 63, 3 * 64 + 5]), np.array([0, 17, 64 + 63])
+        _, e_rows, t_rows = ob.attn_bwd_rows(q, k, v, do, causal=causal, scale=0.3, bh_rows=qr, kv_rows=kr,
+                                             with_scales=True)
+        for got, full, rows in zip(e_rows + t_rows, E + T2, (qr, kr, kr, qr, kr, kr)):
+            assert np.allclose(got, full.reshape(-1, 16)[rows], rtol=1e-12, atol=1e-300)
