@@ -773,6 +773,9 @@ def run_ag(args):
         raise RuntimeError(f"device status {st['status']} site {st['error_site']}")
     ms = statistics.mean(ts)
     value = w.flops() / (ms / 1e3) / 1e12
+    if args.device_only:  # profiling: the timed launches only
+        print(json.dumps({"device_only": True, "ms_per_step": round(ms, 4), "tflops": round(value, 2)}), flush=True)
+        return
 
     statics = {}
     for n in (4, 8, 12, 16, 24):
@@ -784,7 +787,7 @@ def run_ag(args):
 
     # e2e: pinned host A, W in; C out; through the public binding
     c_h = torch.empty((w.P, w.M, w.Ns), dtype=torch.int16).pin_memory()
-    e2e_steps = 3
+    e2e_steps = 10
 
     def e2e_step():
         a.view(torch.int16).copy_(a_p, non_blocking=True)
@@ -794,10 +797,12 @@ def run_ag(args):
         torch.cuda.synchronize()
 
     e2e_step()
-    t0 = time.perf_counter()
+    e2e_times = []
     for _ in range(e2e_steps):
+        t0 = time.perf_counter()
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_times)
 
     cpu = None if args.no_cpu_baseline else ag_cpu_baseline(w, a_h, w_h, args.cpu_budget)
     print(json.dumps({
@@ -817,7 +822,9 @@ def run_ag(args):
         "cublas_no_gather_tflops": round(w.flops() / (t_lib / 1e3) / 1e12, 1),
         "cpu_baseline": cpu,
         "e2e": {"value": round(w.flops() / e2e_s / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": (w.n_a + w.n_w) * 2, "d2h_bytes_per_step": c_h.numel() * 2},
+                "h2d_bytes_per_step": (w.n_a + w.n_w) * 2, "d2h_bytes_per_step": c_h.numel() * 2, "steps": e2e_steps,
+                "per_step_ms_median_min_max": [round(1e3 * statistics.median(e2e_times), 3), round(1e3 * min(e2e_times), 3),
+                                               round(1e3 * max(e2e_times), 3)]},
         "gpu_launches": args.steps,
         "clocks": clk,
     }), flush=True)
@@ -895,6 +902,9 @@ def run_rs(args):
         raise RuntimeError(f"device status {st['status']} site {st['error_site']}")
     ms = statistics.mean(ts)
     value = w.flops() / (ms / 1e3) / 1e12
+    if args.device_only:  # profiling: the timed launches only
+        print(json.dumps({"device_only": True, "ms_per_step": round(ms, 4), "tflops": round(value, 2)}), flush=True)
+        return
 
     statics = {}
     for n in (4, 8, 12, 16, 24):
@@ -906,7 +916,7 @@ def run_rs(args):
 
     # e2e: pinned host A, W in; the reduced output out; through the public binding
     o_h = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
-    e2e_steps = 3
+    e2e_steps = 10
 
     def e2e_step():
         a.view(torch.int16).copy_(a_p, non_blocking=True)
@@ -916,10 +926,12 @@ def run_rs(args):
         torch.cuda.synchronize()
 
     e2e_step()
-    t0 = time.perf_counter()
+    e2e_times = []
     for _ in range(e2e_steps):
+        t0 = time.perf_counter()
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_times)
 
     cpu = None if args.no_cpu_baseline else rs_cpu_baseline(w, a_h, w_h, args.cpu_budget)
     print(json.dumps({
@@ -940,7 +952,9 @@ def run_rs(args):
         "cublas_bmm_then_sum_tflops": round(w.flops() / (t_lib / 1e3) / 1e12, 1),
         "cpu_baseline": cpu,
         "e2e": {"value": round(w.flops() / e2e_s / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": (w.n_a + w.n_w) * 2, "d2h_bytes_per_step": o_h.numel() * 2},
+                "h2d_bytes_per_step": (w.n_a + w.n_w) * 2, "d2h_bytes_per_step": o_h.numel() * 2, "steps": e2e_steps,
+                "per_step_ms_median_min_max": [round(1e3 * statistics.median(e2e_times), 3), round(1e3 * min(e2e_times), 3),
+                                               round(1e3 * max(e2e_times), 3)]},
         "gpu_launches": args.steps,
         "clocks": clk,
     }), flush=True)
