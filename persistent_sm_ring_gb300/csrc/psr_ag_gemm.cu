@@ -73,9 +73,11 @@ struct Params {
 };
 
 
-// task index -> (rank, shard, m-block, n-block): rank by rank (rank r's weight slice stays in L2
-// across its shards), shards in availability order jj = 0, 1, .. (shard = (rank + jj) mod P,
-// the local one first), then W tile by W tile with the m-blocks that share it
+// task index -> (rank, shard, m-block, n-block): rank by rank, shards in availability order
+// jj = 0, 1, .. (shard = (rank + jj) mod P, the local one first), then W tile by W tile with the
+// m-blocks that share it.  The W tiles run forward through even shards and backward through odd
+// ones, so that a shard starts on the W tiles its predecessor used last, which are still in L2
+// (a rank's weight slice is larger than the share of L2 it keeps).
 struct Item {
   int r, j, mb, nb;
 };
@@ -83,11 +85,12 @@ __device__ __host__ inline Item item_of(const Geo& g, long long idx) {
   Item it;
   it.mb = (int)(idx % g.n_mb);
   idx /= g.n_mb;
-  it.nb = (int)(idx % g.n_nb);
+  const int nbi = (int)(idx % g.n_nb);
   idx /= g.n_nb;
   const int jj = (int)(idx % g.P);
   it.r = (int)(idx / g.P);
   it.j = (it.r + jj) % g.P;
+  it.nb = (jj & 1) ? g.n_nb - 1 - nbi : nbi;
   return it;
 }
 // staging task index -> (rank, shard, piece), in the compute tasks' order (rank by rank, peers
@@ -269,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t smem_base = (raw + 1023u) & ~1023u;
   uint8_t* epi = smem_raw + (smem_base - raw) + kStageArea;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (!launched_as_pairs(p)) return;
   const uint32_t rank = cluster_ctarank();
   if (threadIdx.x == 0) {
     init_barriers(&sc);

@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (smem_base - raw);
   uint8_t* epi = smem + kStageArea;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (!launched_as_pairs(p)) return;
   const uint32_t rank = cluster_ctarank();
   if (threadIdx.x == 0) {
     init_barriers(&sc);

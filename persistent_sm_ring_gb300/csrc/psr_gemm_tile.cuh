@@ -55,7 +55,7 @@ constexpr uint32_t kTaskReaders = 2 + 2 * kEpiWarps;
 constexpr uint32_t kSlack = 4;
 static_assert(kSmem + 1024 <= 232448, "shared memory");
 
-enum : uint32_t { SITE_FULL = 2, SITE_EMPTY = 3, SITE_ACC = 4, SITE_TASK = 12, SITE_ACC_EMPTY = 13 };
+enum : uint32_t { SITE_FULL = 2, SITE_EMPTY = 3, SITE_ACC = 4, SITE_TASK = 12, SITE_ACC_EMPTY = 13, SITE_LAUNCH = 14 };
 enum : int { CMD_NONE = -1, CMD_EXIT = 0, CMD_COMPUTE = 1, CMD_COMM = 2 };
 
 // One task of the pair: a compute task (arg = its index) or a communication task (arg for the
@@ -94,6 +94,18 @@ __device__ __forceinline__ void init_barriers(Smem* sc) {
   mbar_init(&sc->drain, 1);
   sc->peer_fills = 0;
   sc->abort = 0;
+}
+
+// Every thread, first: the kernel runs in clusters of two CTAs.  A launch without them (which
+// no caller of launch_pairs makes) raises an error and returns before any distributed
+// shared-memory access or pair allocation.
+template <class KP>
+__device__ __forceinline__ bool launched_as_pairs(const KP& p) {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  if (n == 2u) return true;
+  if (threadIdx.x == 0) raise_error(p, SITE_LAUNCH);
+  return false;
 }
 
 // Every thread of both CTAs, after init_barriers: tensor memory (512 columns per CTA, the pair's
@@ -367,9 +379,9 @@ inline int pair_ctas(Kern kern, int n_sm) {
   return n_ok;
 }
 
-// Launch n_cta CTAs (whole pairs, all co-resident: pair_ctas) as clusters of two: a
-// cooperative launch where the driver accepts one for clusters, else a plain cluster launch
-// (the occupancy bound of pair_ctas still holds every pair resident at once).
+// Launch n_cta CTAs (whole pairs, all co-resident: pair_ctas) as clusters of two.  The grid is
+// no larger than the clusters the device holds at once, one CTA per SM, so every pair is resident
+// from the start (the roles wait on one another, with bounded waits).
 template <class Kern, class... Args>
 inline cudaError_t launch_pairs(Kern kern, int n_cta, cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg = {};
@@ -377,22 +389,14 @@ inline cudaError_t launch_pairs(Kern kern, int n_cta, cudaStream_t st, Args... a
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, args...);
-  }
-  return e;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace gemm
