@@ -18,9 +18,10 @@
 //  * each CTA of a reduce pair (the communication role) takes enqueued tiles, streams the P
 //    partials through shared memory with TMA bulk copies, sums them in rank order (fixed, so
 //    the result does not depend on timing) and writes the owner's bf16 rows;
-//  * compute tasks run window by window (up to 8 x 8 output tiles, every rank's partials of the
-//    window before the next window), so reductions start one window after the launch and a
-//    window's partials are still in L2 when they are reduced;
+//  * compute tasks run window by window (up to 16 x 16 output tiles, every rank's partials of
+//    the window before the next window), so reductions start one window after the launch, and a
+//    rank's A and W blocks of the window (16 + 16 of them) are read from HBM about once per
+//    window (8 x 8 windows read them twice as often: 6.1 GB of DRAM reads per launch against 4.6);
 //  * the shared controller splits the pairs between the roles with the pages' rule (a target of
 //    n reduce CTAs gives ceil(n/2) reduce pairs).  Compute feeds
 //    communication here, so the launch starts with no reduce CTA (pwwt.cn §2.4: the data
@@ -442,8 +443,8 @@ static int geometry(const psr_rs_shape* sh, Geo& g) {
   if ((long long)g.P * g.M >= (1LL << 31) || (long long)g.P * g.N >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   g.n_mb = g.M / kBM;
   g.n_nb = g.N / kBN;
-  g.wm = largest_divisor_upto(g.n_mb, 8);
-  g.wn = largest_divisor_upto(g.n_nb, 8);
+  g.wm = largest_divisor_upto(g.n_mb, 16);
+  g.wn = largest_divisor_upto(g.n_nb, 16);
   const long long n_out = (long long)g.n_mb * g.n_nb;
   if (n_out >= (1LL << 30) || n_out * g.P >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   g.n_out = (int)n_out;

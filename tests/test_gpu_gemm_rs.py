@@ -52,6 +52,7 @@ SMALL = [
     BASE.with_(name="rs_p8", M=2048, N=512, Ks=128, P=8, seed=803),
     BASE.with_(name="rs_p2_k64", M=512, N=1280, Ks=64, P=2, seed=804),  # one K step per tile
     BASE.with_(name="rs_p3", M=768, N=256, Ks=320, P=3, seed=805),      # P not a power of two
+    BASE.with_(name="rs_two_windows", M=8192, N=512, Ks=64, P=2, seed=806),  # 32 row blocks: two task windows
 ]
 
 
