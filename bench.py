@@ -384,7 +384,9 @@ def run_ours(args):
     rank, world, local = dist_init(args.gpus)
     psr.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    wls = [ri.WORKLOADS[n] for n in WORKLOADS]
+    # profiling: the causal pass next to the causal pass over load-balanced shards
+    names = ("h32_s32k_c", "h32_s32k_cb") if args.balanced else WORKLOADS
+    wls = [ri.WORKLOADS[n] for n in names]
     if args.heads:  # a smaller same-kernel case (profiling): fewer heads, same S, P, d
         wls = [w.with_(Hq=args.heads, Hkv=args.heads) for w in wls]
     flops_step = sum(w.flops() for w in wls)
@@ -1109,7 +1111,11 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--heads", type=int, default=0, help="profiling: run the same kernel with fewer heads")
     ap.add_argument("--device-only", action="store_true", help="profiling: timed device passes only")
+    ap.add_argument("--balanced", action="store_true",
+                    help="profiling (with --device-only): the causal pass and the causal pass over load-balanced shards")
     args = ap.parse_args()
+    if args.balanced and not args.device_only:
+        ap.error("--balanced is a profiling mode: use it with --device-only")
     if args.sweep is not None:
         run_sweep(args)
     elif args.ag_gemm:
