@@ -257,10 +257,12 @@ PSR_API int psr_ring_attn_bwd(const psr_shape* shape, const void* q, const void*
  *     C_r = gather(A) @ W_r^T      (fp32 accumulation, bf16 result, RNE),
  * the gathered A being the shards concatenated in rank order.  Staging CTAs
  * copy peer shards into each rank's gather buffer in the workspace (pieces of
- * >= 512 KiB, each published with a readiness flag); compute CTAs each produce
- * one 256 x 256 tile of one rank on tcgen05, reading the rank's own shard in
- * place and a peer's rows after acquiring their flags; the same controller as
- * the Ring Attention splits the CTAs between the two roles. */
+ * >= 512 KiB, each published with a readiness flag); compute CTAs work in
+ * pairs (clusters of two SMs), each pair producing one 256 x 256 tile of one
+ * rank with tcgen05 cta_group::2 MMAs, reading the rank's own shard in place and
+ * a peer's rows after acquiring their flags; the same controller as the Ring
+ * Attention splits the pairs between the two roles (a target of n staging CTAs
+ * gives ceil(n/2) staging pairs). */
 typedef struct {
   int M;   /* rows of the gathered A; M/P must be a multiple of 256 */
   int K;   /* contraction; a multiple of 128 */
@@ -280,9 +282,11 @@ PSR_API size_t psr_ag_gemm_workspace_bytes(const psr_ag_shape* shape);
  *   c: device, bf16, [P][M][Ns] contiguous (rank r's output)              (written)
  *   workspace: device, >= psr_ag_gemm_workspace_bytes(shape), 256-byte aligned, caller-owned.
  *   part: partition policy (NULL = adaptive); stream: a cudaStream_t (NULL = default).
- * Asynchronous (one flag reset and one persistent launch on `stream`); a
- * device timeout is reported by psr_get_stats.  PSR_ERR_UNSUPPORTED for shapes
- * outside the constraints above or a device other than sm_103. */
+ *   A static partition takes 1 <= n_staging <= (CTAs launched) - 2, so that at
+ *   least one pair computes; the launch is one CTA per SM in whole pairs.
+ * Asynchronous (one flag reset and one persistent launch of clusters of two on
+ * `stream`); a device timeout is reported by psr_get_stats.  PSR_ERR_UNSUPPORTED
+ * for shapes outside the constraints above or a device other than sm_103. */
 PSR_API int psr_ag_gemm(const psr_ag_shape* shape, const void* a, const void* w, void* c, void* workspace,
                         size_t workspace_bytes, const psr_partition* part, void* stream);
 
@@ -295,13 +299,15 @@ PSR_API int psr_ag_gemm(const psr_ag_shape* shape, const void* a, const void* w,
  * receives rows [q*M/P, (q+1)*M/P) of
  *     out = sum_r A_r @ W_r^T      (fp32 partials summed in rank order, bf16 result, RNE),
  * each output tile being reduced and forwarded as soon as its partials exist.
- * On one GPU the P ranks are emulated in HBM: compute CTAs each produce one
- * 256 x 256 fp32 partial tile of one rank on tcgen05 into the workspace, and
- * the completion of an output tile's P partials enqueues it; reduce CTAs (the
- * communication role) stream the P partials through shared memory with TMA
- * bulk copies and write the owner's rows.  The same controller splits the CTAs
- * between the roles; as compute feeds the reductions, the adaptive launch
- * starts with no reduce CTA (part->n_staging > 0 overrides). */
+ * On one GPU the P ranks are emulated in HBM: compute pairs (clusters of two
+ * SMs) each produce one 256 x 256 fp32 partial tile of one rank with tcgen05
+ * cta_group::2 MMAs into the workspace, and the completion of an output tile's
+ * P partials enqueues it; reduce CTAs (the communication role) stream the P
+ * partials through shared memory with TMA bulk copies and write the owner's
+ * rows.  The same controller splits the pairs between the roles (a target of n
+ * reduce CTAs gives ceil(n/2) reduce pairs); as compute feeds the reductions,
+ * the adaptive launch starts with no reduce CTA (part->n_staging > 0
+ * overrides). */
 typedef struct {
   int M;   /* output rows (tokens); M/P must be a multiple of 256 */
   int N;   /* output columns; a multiple of 256 */
@@ -320,10 +326,11 @@ PSR_API size_t psr_gemm_rs_workspace_bytes(const psr_rs_shape* shape);
  *   w:   device, bf16, [P][N][Ks] contiguous (rank r's weights, K-major)      (read)
  *   out: device, bf16, [M][N] contiguous (rows q*M/P .. belong to rank q)     (written)
  *   workspace: device, >= psr_gemm_rs_workspace_bytes(shape), 256-byte aligned, caller-owned.
- *   part: partition policy (NULL = adaptive; static needs n_staging >= 1 reduce CTAs).
+ *   part: partition policy (NULL = adaptive; static needs 1 <= n_staging <= (CTAs launched) - 2
+ *         reduce CTAs, so that at least one pair computes).
  *   stream: a cudaStream_t (NULL = default).
- * Asynchronous (one counter reset and one persistent launch on `stream`); a
- * device timeout is reported by psr_get_stats (staging_tasks counts the tile
+ * Asynchronous (one counter reset and one persistent launch of clusters of two
+ * on `stream`); a device timeout is reported by psr_get_stats (staging_tasks counts the tile
  * reductions, staging_bytes the partial bytes they read).  PSR_ERR_UNSUPPORTED
  * for shapes outside the constraints above or a device other than sm_103. */
 PSR_API int psr_gemm_rs(const psr_rs_shape* shape, const void* a, const void* w, void* out, void* workspace,
