@@ -144,16 +144,28 @@ __device__ inline KvItem kv_item_of(const BParams& p, int n) {
 
 // The item's (query head, query tile) pairs in ring order: shard j of the K/V tile first, then
 // j+1, j+2, ... (mod P); under the causal mask only query tiles at or after the K/V tile's
-// position (with contiguous shards no tile of a shard before j qualifies).
+// position (with contiguous shards no tile of a shard before j qualifies; with load-balanced
+// shards the qualifying tiles of each half-chunk are a suffix of it, visited directly).
 template <class F>
 __device__ __forceinline__ void for_each_q(const BParams& p, const KvItem& it, F&& f) {
   const int j = it.gk / p.tiles_per_shard;
   const int kpos = tile_pos(p, it.gk);
+  const int hh = p.tiles_per_shard / 2;
   for (int t = 0; t < p.P; ++t) {
     const int r = (j + t) % p.P;
     if (p.causal && !p.balanced && r < j) continue;
     for (int h = 0; h < p.gqa; ++h) {
       const int hq = it.kvh * p.gqa + h;
+      if (p.causal && p.balanced) {
+        // local tiles [0, hh) hold positions r*hh + o, tiles [hh, 2hh) positions (2P-1-r)*hh + o
+        for (int half = 0; half < 2; ++half) {
+          const int c = half ? 2 * p.P - 1 - r : r;
+          const int o0 = kpos - c * hh > 0 ? kpos - c * hh : 0;
+          for (int o = o0; o < hh; ++o)
+            if (!f(hq, r * p.tiles_per_shard + half * hh + o, c * hh + o == kpos)) return;
+        }
+        continue;
+      }
       for (int qt = 0; qt < p.tiles_per_shard; ++qt) {
         const int gq = r * p.tiles_per_shard + qt;
         const int qpos = tile_pos(p, gq);
@@ -481,14 +493,24 @@ __device__ inline QItem q_item_of(const BParams& p, int n) {
 
 // The item's K/V tiles in the forward's ring order: the query shard r's own chunk first, then
 // r-1, r-2, ... (mod P); under the causal mask only K/V tiles at or before the query tile's
-// position.
+// position (with load-balanced shards a prefix of each half-chunk, visited directly).
 template <class F>
 __device__ __forceinline__ void for_each_kv(const BParams& p, const QItem& it, F&& f) {
   const int r = it.gq / p.tiles_per_shard;
   const int qpos = tile_pos(p, it.gq);
+  const int hh = p.tiles_per_shard / 2;
   for (int t = 0; t < p.P; ++t) {
     const int j = ((r - t) % p.P + p.P) % p.P;
     if (p.causal && !p.balanced && j > r) continue;
+    if (p.causal && p.balanced) {
+      for (int half = 0; half < 2; ++half) {
+        const int c = half ? 2 * p.P - 1 - j : j;
+        const int o1 = qpos - c * hh + 1 < hh ? qpos - c * hh + 1 : hh;  // exclusive end
+        for (int o = 0; o < o1; ++o)
+          if (!f(j * p.tiles_per_shard + half * hh + o, c * hh + o == qpos)) return;
+      }
+      continue;
+    }
     for (int kt = 0; kt < p.tiles_per_shard; ++kt) {
       const int gk = j * p.tiles_per_shard + kt;
       const int kpos = tile_pos(p, gk);
