@@ -461,17 +461,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct QCfg {
   static constexpr int TILE = kRows * D * 2;
+  // K tiles in three buffers, V tiles in two: K(j) is read until dQ(j), V(j) only until dP(j),
+  // and the S product of a tile is issued a tile ahead, so a third K buffer lets each K load
+  // start a whole tile before it is needed
+  static constexpr int KST = 3, VST = 2;
   static constexpr int OFF_Q = 0, OFF_DO = TILE;
-  static constexpr int OFF_K = 2 * TILE;      // + kb * 2 * TILE
-  static constexpr int OFF_V = 3 * TILE;      // + kb * 2 * TILE
-  static constexpr int SMEM = 1024 + 6 * TILE;
+  static constexpr int OFF_K = 2 * TILE;           // + kb * TILE
+  static constexpr int OFF_V = (2 + KST) * TILE;   // + vb * TILE
+  static constexpr int SMEM = 1024 + (2 + KST + VST) * TILE;
   static constexpr uint32_t COL_S = 0;        // + (tile % 2) * 128: S double-buffered
   static constexpr uint32_t COL_DP = 256, COL_DQ = 384;
   static_assert(SMEM <= 232448 - 1024, "shared memory");
 };
 
 struct QSmem {
-  uint64_t qd_full, kv_full[2], kv_empty[2], s_full[2], dp_full, ds_ready, acc_full, drain;
+  uint64_t qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], dp_full, ds_ready, acc_full, drain;
   uint32_t tmem_base;
   int arg;
   volatile uint32_t abort;
@@ -522,7 +526,8 @@ __device__ __forceinline__ void for_each_kv(const BParams& p, const QItem& it, F
 
 template <int D>
 __device__ void q_producer(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& it, const CUtensorMap* tq,
-                           const CUtensorMap* tdo, const CUtensorMap* tk, const CUtensorMap* tv, uint32_t& kcnt) {
+                           const CUtensorMap* tdo, const CUtensorMap* tk, const CUtensorMap* tv, uint32_t& kcnt,
+                           uint32_t& vcnt) {
   using C = QCfg<D>;
   const int q_row = (it.b * p.Hq + it.hq) * p.S + it.gq * kRows;
   mbar_expect_tx(&sc->qd_full, 2 * C::TILE);
@@ -533,15 +538,21 @@ __device__ void q_producer(const BParams& p, QSmem* sc, uint32_t sbase, const QI
   }
   const int kv_base = (it.b * p.Hkv + it.hq / p.gqa) * p.S;
   for_each_kv(p, it, [&](int gk, bool) -> bool {
-    const uint32_t kb = kcnt % 2, fill = kcnt / 2;
-    if (fill > 0 && !wait_bar(&sc->kv_empty[kb], (fill - 1) & 1u, p, sc, SITE_KV_EMPTY)) return false;
-    mbar_expect_tx(&sc->kv_full[kb], 2 * C::TILE);
+    // kcnt and vcnt count the K and V loads issued (equal between tiles; both kept so that the
+    // end of the kernel waits for exactly the loads in flight after an abort)
+    const uint32_t kb = kcnt % C::KST, kfill = kcnt / C::KST, vb = vcnt % C::VST, vfill = vcnt / C::VST;
+    if (kfill > 0 && !wait_bar(&sc->k_empty[kb], (kfill - 1) & 1u, p, sc, SITE_KV_EMPTY)) return false;
+    mbar_expect_tx(&sc->k_full[kb], C::TILE);
 #pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-      tma_load_2d(sbase + C::OFF_K + kb * 2 * C::TILE + h * 16384, tk, 64 * h, kv_base + gk * kRows, &sc->kv_full[kb]);
-      tma_load_2d(sbase + C::OFF_V + kb * 2 * C::TILE + h * 16384, tv, 64 * h, kv_base + gk * kRows, &sc->kv_full[kb]);
-    }
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_2d(sbase + C::OFF_K + kb * C::TILE + h * 16384, tk, 64 * h, kv_base + gk * kRows, &sc->k_full[kb]);
     ++kcnt;
+    if (vfill > 0 && !wait_bar(&sc->v_empty[vb], (vfill - 1) & 1u, p, sc, SITE_KV_EMPTY)) return false;
+    mbar_expect_tx(&sc->v_full[vb], C::TILE);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+      tma_load_2d(sbase + C::OFF_V + vb * C::TILE + h * 16384, tv, 64 * h, kv_base + gk * kRows, &sc->v_full[vb]);
+    ++vcnt;
     return true;
   });
 }
@@ -560,10 +571,10 @@ __device__ void q_mma(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& 
   int n_kv = 0;
   for_each_kv(p, it, [&](int, bool) -> bool { ++n_kv; return true; });
   if (!wait_bar(&sc->qd_full, items & 1u, p, sc, SITE_Q_FULL)) { sc->abort = 1; return; }
-  auto k_of = [&](uint32_t c) { return sbase + C::OFF_K + (c % 2) * 2 * C::TILE; };
-  auto v_of = [&](uint32_t c) { return sbase + C::OFF_V + (c % 2) * 2 * C::TILE; };
-  auto issue_s = [&](uint32_t c, uint32_t j) -> bool {  // S of K/V load c into S buffer j % 2
-    if (!wait_bar(&sc->kv_full[c % 2], (c / 2) & 1u, p, sc, SITE_KV)) return false;
+  auto k_of = [&](uint32_t c) { return sbase + C::OFF_K + (c % C::KST) * C::TILE; };
+  auto v_of = [&](uint32_t c) { return sbase + C::OFF_V + (c % C::VST) * C::TILE; };
+  auto issue_s = [&](uint32_t c, uint32_t j) -> bool {  // S of K load c into S buffer j % 2
+    if (!wait_bar(&sc->k_full[c % C::KST], (c / C::KST) & 1u, p, sc, SITE_KV)) return false;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
@@ -571,15 +582,18 @@ __device__ void q_mma(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& 
     mma_commit(&sc->s_full[j % 2]);
     return true;
   };
-  auto issue_dp = [&](uint32_t c) {
+  auto issue_dp = [&](uint32_t c) -> bool {  // dP of V load c; V is then released
+    if (!wait_bar(&sc->v_full[c % C::VST], (c / C::VST) & 1u, p, sc, SITE_KV)) return false;
+    tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
       mma_ss_w(tm + C::COL_DP, kmaj_lo(sDO, kk), kHi, kmaj_lo(v_of(c), kk), kHi, I_SS, kk > 0 ? 1u : 0u);
     mma_commit(&sc->dp_full);
+    mma_commit(&sc->v_empty[c % C::VST]);
+    return true;
   };
   tc_fence_after();
-  if (!issue_s(kcnt, jg)) { sc->abort = 1; return; }
-  issue_dp(kcnt);
+  if (!issue_s(kcnt, jg) || !issue_dp(kcnt)) { sc->abort = 1; return; }
   int i = 0;
   for_each_kv(p, it, [&](int, bool) -> bool {
     if (i + 1 < n_kv && !issue_s(kcnt + 1, jg + 1)) return false;
@@ -589,8 +603,8 @@ __device__ void q_mma(const BParams& p, QSmem* sc, uint32_t sbase, const QItem& 
 #pragma unroll
     for (int kk = 0; kk < kRows / 16; ++kk)
       mma_ts_w(tm + C::COL_DQ, tm + C::COL_DP + bf16_col(kk), mnmaj_lo(sK, kk), kHi, I_TS, (i == 0 && kk == 0) ? 0u : 1u);
-    mma_commit(&sc->kv_empty[kcnt % 2]);  // K, V of this tile are read
-    if (i + 1 < n_kv) issue_dp(kcnt + 1);  // dP(j+1) over dS(j), after the dQ MMA has read it
+    mma_commit(&sc->k_empty[kcnt % C::KST]);  // K of this tile is read
+    if (i + 1 < n_kv && !issue_dp(kcnt + 1)) return false;  // dP(j+1) over dS(j), after the dQ MMA has read it
     ++kcnt;
     ++jg;
     ++i;
@@ -691,9 +705,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(&sc.qd_full, 1);
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(&sc.k_full[b], 1);
+      mbar_init(&sc.k_empty[b], 1);
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sc.kv_full[b], 1);
-      mbar_init(&sc.kv_empty[b], 1);
+      mbar_init(&sc.v_full[b], 1);
+      mbar_init(&sc.v_empty[b], 1);
       mbar_init(&sc.s_full[b], 1);
     }
     mbar_init(&sc.dp_full, 1);
@@ -714,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  uint32_t items = 0, kcnt_p = 0, kcnt_m = 0, jg_m = 0, jg_e = 0;
+  uint32_t items = 0, kcnt_p = 0, kcnt_v = 0, kcnt_m = 0, jg_m = 0, jg_e = 0;
   while (true) {
     if (threadIdx.x == 0) {
       int n = -1;
@@ -729,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n < 0) break;
     const QItem it = q_item_of(p, n);
     if (warp == 0 && lane == 0) {
-      q_producer<D>(p, &sc, sbase, it, &tm_q, &tm_do, &tm_k, &tm_v, kcnt_p);
+      q_producer<D>(p, &sc, sbase, it, &tm_q, &tm_do, &tm_k, &tm_v, kcnt_p, kcnt_v);
     } else if (warp == 1 && lane == 0) {
       q_mma<D>(p, &sc, sbase, it, items, kcnt_m, jg_m);
     } else if (warp >= 4) {
@@ -753,9 +771,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (items > 0)
       while (!mbar_try_wait(&sc.qd_full, (items - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
       }
-    for (uint32_t b = 0; b < 2 && b < kcnt_p; ++b) {
-      const uint32_t fills = (kcnt_p - b + 1) / 2;
-      while (!mbar_try_wait(&sc.kv_full[b], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+    // every K and V load has landed (the producer issued K before V for each tile, so the
+    // last fill of each buffer is the one to wait for)
+    for (uint32_t b = 0; b < (uint32_t)QCfg<D>::KST && b < kcnt_p; ++b) {
+      const uint32_t fills = (kcnt_p - b + QCfg<D>::KST - 1) / QCfg<D>::KST;
+      while (!mbar_try_wait(&sc.k_full[b], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+    for (uint32_t b = 0; b < (uint32_t)QCfg<D>::VST && b < kcnt_v; ++b) {
+      const uint32_t fills = (kcnt_v - b + QCfg<D>::VST - 1) / QCfg<D>::VST;
+      while (!mbar_try_wait(&sc.v_full[b], (fills - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
   }
