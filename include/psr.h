@@ -88,7 +88,9 @@ typedef struct {
   int n_min;      /* adaptive clamp, lower (<= 0: 1) */
   int n_max;      /* adaptive clamp, upper (<= 0: automatic) */
   int fault;      /* PSR_FAULT_* */
-  int timeout_ms; /* bound on every device wait (<= 0: 2000 ms) */
+  int timeout_ms; /* bound on every device wait (<= 0: 2000 ms); in the GEMM entries the waits
+                     inside the tile pipeline, which only follow an upstream wait, give up after
+                     4 x timeout_ms, so that the upstream wait reports the cause */
 } psr_partition;
 
 typedef struct {
