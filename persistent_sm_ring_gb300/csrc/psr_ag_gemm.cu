@@ -70,6 +70,7 @@ struct Params {
   uint32_t n_wave_items;  // no wave cap here (0): the tasks' waves are many and short
   int n_wave_cap;
   float c_s0, c_p0;
+  float update_headroom;
 };
 
 
@@ -482,6 +483,7 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   kp.n_stage_total = (unsigned long long)g.n_stage;
   kp.mode = pt.mode;
   kp.fault = pt.fault;
+  kp.update_headroom = (float)kUpdateHeadroom;
   // priors (CTA-cycles): a piece at ~50 GB/s per staging SM (no less than ~6500 cycles); a task
   // (2*256*256*K flops) at ~60 % of an SM's dense bf16 rate
   const double piece_cycles = (double)g.piece_rows * g.K * 2 / 50e9 * 1.95e9;

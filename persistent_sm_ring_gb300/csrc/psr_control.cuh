@@ -1,7 +1,8 @@
 // Control block, partition controller and bounded waits shared by the persistent kernels
 // (Ring Attention, AllGather+GEMM).  A kernel's parameter struct provides: ctrl, traj,
 // timeout_ns, mode, n_s_init, n_stage_total, n_tiles_total, c_s0, c_p0, n_min, n_max,
-// n_wave_items, n_wave_cap; its shared control struct provides a volatile `abort` word.
+// n_wave_items, n_wave_cap, update_headroom; its shared control struct provides a volatile
+// `abort` word.
 #pragma once
 #include <cstdint>
 
@@ -133,6 +134,18 @@ constexpr double kWaveMargin = PSR_WAVE_MARGIN / 100.0;
 // (P = 64) are left out: there the cap does not bind under the default upper clamp anyway.
 constexpr int kWaveMinTiles = PSR_WAVE_MIN_TILES;
 
+#ifndef PSR_SHORT_STEP_HEADROOM
+#define PSR_SHORT_STEP_HEADROOM 120
+#endif
+// Staging headroom, initial split and updates, on ring steps shorter than kWaveMinTiles KV tiles.
+// There a compute item is bound by the latency of its ring steps: the time it waits for staged
+// data is part of what it costs (it is not moved to the staging cost), and with that cost the
+// rule needs little headroom.  Measured on GB300 (partition sweep, P = 64: 2-tile steps): with the
+// waits moved to staging and 1.5x headroom the d = 64 point sat at the upper clamp, 1.04-1.07x the
+// best static split (64 stagers); with the waits kept in the compute cost, 1.0x headroom fit d = 64
+// (0.99x) but let d = 128 fall below its optimum (the clamp, 76: 1.11x), 1.2x held both within 1.04x.
+constexpr double kShortStepHeadroom = PSR_SHORT_STEP_HEADROOM / 100.0;
+
 // The initial split stands until this fraction of the compute tiles is done: it covers the
 // ring's fill, when every active group needs its first staged steps at once and measured
 // costs are still dominated by start-up.
@@ -160,7 +173,7 @@ __device__ void controller_update(const KP& p) {
   const unsigned long long sv = atomicAdd(&c->starve_cycles, 0ull);
   const double C_s = (scy + kStarveWeight * (double)sv + (double)p.c_s0 * 4.0) / ((double)sd + 4.0);
   const double C_p = (ccy + (double)p.c_p0 * 64.0) / ((double)td + 64.0);
-  int n = controller_rule((int)gridDim.x, R_s, kUpdateHeadroom * C_s, R_p, C_p, p.n_min, p.n_max);
+  int n = controller_rule((int)gridDim.x, R_s, (double)p.update_headroom * C_s, R_p, C_p, p.n_min, p.n_max);
   // equal-length compute items: the launch's wave cap holds while items remain unclaimed (a
   // CTA taken from compute then delays one of its items to an extra wave)
   if (n > p.n_wave_cap && ld_relaxed(&c->item_next) < p.n_wave_items) n = p.n_wave_cap;

@@ -73,6 +73,7 @@ struct Params {
   uint32_t n_wave_items;  // no wave cap here (0): the tasks' waves are many and short
   int n_wave_cap;
   float c_s0, c_p0;
+  float update_headroom;
 };
 
 // compute task index -> (rank, m-block, n-block): window by window, rank by rank inside a
@@ -522,6 +523,7 @@ int psr_gemm_rs(const psr_rs_shape* sh, const void* a, const void* w, void* out,
   kp.n_stage_total = (unsigned long long)g.n_out;
   kp.mode = pt.mode;
   kp.fault = pt.fault;
+  kp.update_headroom = (float)kUpdateHeadroom;
   // priors (CTA-cycles): a reduction streams P partial tiles in and one bf16 tile out at
   // ~100 GB/s per SM; a compute task (2*256*256*Ks flops) at ~60 % of an SM's dense bf16 rate
   kp.c_s0 = (float)(((double)g.P * kTileElems * 4 + kTileElems * 2) / 100e9 * 1.95e9);

@@ -101,6 +101,8 @@ struct KParams {
   int mode;           // PSR_STATIC / PSR_ADAPTIVE
   int n_s_init;
   int n_min, n_max;   // effective clamp
+  int starve_charge;      // compute waits for staged data: moved to the staging cost (1) or kept (0)
+  float update_headroom;  // staging headroom of the controller's updates
   uint32_t n_wave_items;  // items under the wave cap (0: none)
   int n_wave_cap;     // adaptive target bound while items remain unclaimed
   int fault;
@@ -996,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (threadIdx.x == 0 && done_kind != CMD_IDLE) {
         long long busy = clock64() - t_task;
-        if (done_kind == CMD_COMPUTE) {
+        if (done_kind == CMD_COMPUTE && p.starve_charge) {
           busy -= starved.all;  // compute cost excludes waiting for staged data ...
           atomicAdd(&p.ctrl->starve_cycles, (unsigned long long)(starved.late > 0 ? starved.late : 0));  // ... charged to staging
         }
@@ -1403,6 +1405,10 @@ static int fwd_setup(const psr_shape* sh, const void* q, const void* k, const vo
   kp.c_s0 = (float)(copy_cycles > 6500.0 ? copy_cycles : 6500.0);
   const double mma_cycles = 2.0 * 2.0 * 2.0 * 128.0 * 128.0 * G.d / (0.6 * 8192.0);
   kp.c_p0 = (float)(cg * (mma_cycles > 2800.0 ? mma_cycles : 2800.0));
+  // ring steps shorter than kWaveMinTiles tiles: items bound by their steps' latency (the
+  // controller keeps their waits for staged data in the compute cost, with less headroom)
+  const bool short_steps = G.kv_tiles < kWaveMinTiles;
+  const double stage_headroom = short_steps ? kShortStepHeadroom : kStageHeadroom;
   int n_s;
   if (pt.mode == PSR_STATIC) {
     n_s = pt.n_staging;
@@ -1417,7 +1423,7 @@ static int fwd_setup(const psr_shape* sh, const void* q, const void* k, const vo
     // rate (measured best static splits for P = 4..16 sit 1.2-3x above the balanced split); the
     // measured costs and starvation then move the target.
     n_s = pt.n_staging > 0 ? pt.n_staging
-                           : controller_rule(n_cta, (double)kp.n_stage_total, kStageHeadroom * kp.c_s0,
+                           : controller_rule(n_cta, (double)kp.n_stage_total, stage_headroom * kp.c_s0,
                                              (double)kp.n_tiles_total, kp.c_p0, n_min, n_max);
     if (!any_staging) n_s = 0;
     else {
@@ -1444,6 +1450,8 @@ static int fwd_setup(const psr_shape* sh, const void* q, const void* k, const vo
     }
   }
   kp.n_s_init = n_s;
+  kp.starve_charge = short_steps ? 0 : 1;
+  kp.update_headroom = (float)(short_steps ? kShortStepHeadroom : kUpdateHeadroom);
   kp.lookahead = n_cunits / G.Gs + 2;
 
   CUtensorMap* maps = F.tmaps;
