@@ -1067,10 +1067,12 @@ def run_bwd(args):
         torch.cuda.synchronize()
 
     e2e_step()
-    t0 = time.perf_counter()
-    for _ in range(3):
+    e2e_times = []
+    for _ in range(10):
+        t0 = time.perf_counter()
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / 3
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_times)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     cpu = None if args.no_cpu_baseline else bwd_cpu_baseline(w, q_h, k_h, v_h, do_h, args.cpu_budget)
@@ -1086,7 +1088,9 @@ def run_bwd(args):
                      "peak_source": f"{peaks.get('source')} bf16_tflops (burst)"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(bwd_flops(w) / e2e_s / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "steps": len(e2e_times),
+                "per_step_ms_median_min_max": [round(1e3 * statistics.median(e2e_times), 3),
+                                               round(1e3 * min(e2e_times), 3), round(1e3 * max(e2e_times), 3)]},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "passes": passes,
