@@ -571,6 +571,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "ms_per_step_median": round(1e3 * statistics.median(e2e_times), 3),
                     "ms_per_step_min_max": [round(1e3 * e2e_sorted[0], 3), round(1e3 * e2e_sorted[-1], 3)],
+                    "ms_per_step_all": [round(1e3 * t, 2) for t in e2e_times],
                     "pinned_copy_GBps": {"h2d": round(h2d_gbps, 1), "d2h": round(d2h_gbps, 1)}},
             "gpu_launches": args.steps * len(wls),
             "clocks": clk,
