@@ -260,9 +260,10 @@ PSR_API int psr_ring_attn_bwd(const psr_shape* shape, const void* q, const void*
  * the gathered A being the shards concatenated in rank order.  Staging CTAs
  * copy peer shards into each rank's gather buffer in the workspace (pieces of
  * >= 512 KiB, each published with a readiness flag); compute CTAs work in
- * pairs (clusters of two SMs), each pair producing one 256 x 256 tile of one
- * rank with tcgen05 cta_group::2 MMAs, reading the rank's own shard in place and
- * a peer's rows after acquiring their flags; the same controller as the Ring
+ * pairs (clusters of two SMs), each pair producing one 256 x 512 tile of one
+ * rank with tcgen05 cta_group::2 MMAs (a rank's last tile is 256 x 256 when Ns
+ * is an odd multiple of 256), reading the rank's own shard in place and a
+ * peer's rows after acquiring their flags; the same controller as the Ring
  * Attention splits the pairs between the two roles (a target of n staging CTAs
  * gives ceil(n/2) staging pairs). */
 typedef struct {

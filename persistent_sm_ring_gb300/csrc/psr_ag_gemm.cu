@@ -12,10 +12,11 @@
 //    r's gather buffer (the same row positions) with TMA bulk copies through shared memory,
 //    and publish a per-piece readiness flag with a gpu-scope release once the stores are
 //    complete;
-//  * a compute pair produces one 256 x 256 output tile of one rank per task (the pair tile of
-//    psr_gemm_tile.cuh: each CTA 128 rows, tcgen05 cta_group::2, double-buffered
-//    accumulators); the rank's own shard is read in place, a peer's only after each CTA has
-//    acquired the piece flags that cover its 128 rows;
+//  * a compute pair produces one 256 x 512 output tile of one rank per task (the pair tile of
+//    psr_gemm_tile.cuh with two accumulator halves: each CTA 128 rows x 512 columns, tcgen05
+//    cta_group::2); the rank's own shard is read in place, a peer's only after each CTA has
+//    acquired the piece flags that cover its 128 rows.  When Ns is an odd multiple of 256 a
+//    rank's last tile is half wide: its second half is computed and not stored;
 //  * each rank's tasks run in availability order: its local tiles first, then the tiles of
 //    shard r+1, r+2, ... (the order in which staging delivers them); ranks run one after
 //    another, so that a rank's weight slice is read from HBM once;
@@ -38,7 +39,9 @@
 namespace psr {
 namespace ag {
 
-using namespace gemm;  // the 256 x 256 tile: stages, MMA issue, accumulator read-back
+using namespace gemm;  // the pair tile: stages, MMA issue, accumulator read-back
+constexpr int kNH = 2;  // 256 x 512 tiles
+using TileT = Tile<kNH>;
 constexpr int kCopyUnit = 32768;  // staging copy unit
 constexpr int kNCopyBuf = kStageArea / kCopyUnit;
 constexpr int kPieceMinBytes = 512 * 1024;
@@ -49,7 +52,7 @@ enum : uint32_t { SITE_FLAG = 1, SITE_STAGE_LOAD = 8 };
 struct Geo {
   int M, K, Ns, P, Ms;
   int n_mb;          // 256-row blocks per shard
-  int n_nb;          // 256-column blocks per rank
+  int n_nb;          // 512-column blocks per rank (the last one half wide when Ns % 512 = 256)
   int piece_rows;    // rows per staging piece (a multiple of 128 dividing Ms)
   int n_pieces;      // pieces per shard
   long long n_items;   // compute tasks: P ranks x P shards x n_mb x n_nb
@@ -243,24 +246,29 @@ __device__ bool produce_tile(const Params& p, Smem* sc, uint32_t smem_base, uint
     arow = it.r * g.M + it.j * g.Ms + srow;
   }
   const int n_k = g.K / kBK;
-  const int wrow = it.r * g.Ns + it.nb * kBN + (int)rank * kRows;
-  return load_tile(p, sc, smem_base, rank, ma, arow, tm_w, wrow, n_k, fills, n_k > kNStage ? n_k - kNStage : 0,
-                   ahead);
+  // W rows of half h: wrow + 256h (past the rank's Ns in a half-wide tile: the next rank's rows,
+  // or the tensor map's zero fill past the last one; never stored)
+  const int wrow = it.r * g.Ns + it.nb * TileT::kCols + (int)rank * kRows;
+  return load_tile<kNH>(p, sc, smem_base, rank, ma, arow, tm_w, wrow, n_k, fills,
+                        n_k > TileT::kNStage ? n_k - TileT::kNStage : 0, ahead);
 }
 
-// Epilogue warp: its 32 rows x 128 columns of the tile, accumulator -> bf16 -> C_r.
+// Epilogue warp: its 32 rows x 128 columns of each half of the tile, accumulator -> bf16 -> C_r
+// (columns at or past Ns, the second half of a half-wide tile, are not stored).
 __device__ bool epilogue(const Params& p, Smem* sc, uint8_t* epi, uint32_t rank, const Item& it, uint32_t item) {
   const Geo& g = p.g;
   const int warp = threadIdx.x / 32;
   const size_t grow0 = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + rank * kRows + (warp % 4) * 32;
-  const size_t col0 = (size_t)it.nb * kBN + ((warp - 4) / 4) * 128;
+  const int col0 = it.nb * TileT::kCols + ((warp - 4) / 4) * 128;
   uint8_t* stage = epi + (warp - 4) * kEpiWarpBytes;
-  uint8_t* rows = reinterpret_cast<uint8_t*>(p.c + ((size_t)it.r * g.M + grow0) * g.Ns + col0);
-  return read_acc(p, sc, rank, item, [&](int cb, const uint32_t* v) {
+  uint16_t* rows = p.c + ((size_t)it.r * g.M + grow0) * g.Ns;
+  return read_acc<kNH>(p, sc, rank, item, [&](int cb, const uint32_t* v) {
+    const int col = col0 + (cb / 2) * kBN + (cb % 2) * 64;
+    if (col >= g.Ns) return;
     uint32_t w[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-    warp_store_rows<32>(stage, w, rows + cb * 128, (size_t)g.Ns * 2);
+    warp_store_rows<32>(stage, w, reinterpret_cast<uint8_t*>(rows + col), (size_t)g.Ns * 2);
   });
 }
 
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               [&] { decide(p, &sc, next, was_staging, true); });
           } else {
             prev_pieces = t.arg1 >= 0 ? 2 : 1;
-            ok = wait_stages_free(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg, stg_phase);
+            ok = wait_stages_free<kNH>(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg, stg_phase);
           }
           if (!ok) { sc.abort = 1; break; }
         }
@@ -350,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t.cmd == CMD_COMPUTE)
             ok = produce_tile(p, &sc, smem_base, 1, item_of(p.g, t.arg), &tm_a, &tm_g, &tm_w, fills, starved, [] {});
           else if (t.arg1 >= 0)
-            ok = wait_stages_free(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg1, stg_phase);
+            ok = wait_stages_free<kNH>(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg1, stg_phase);
           if (!ok) { sc.abort = 1; break; }
         }
       }
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_task(&sc, k, 0);
         if (t.cmd == CMD_EXIT) break;
         if (t.cmd != CMD_COMPUTE) continue;
-        if (!mma_tile(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
+        if (!mma_tile<kNH>(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
         ++items;
       }
     }
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++items;
     }
   }
-  drain_pair(&sc, rank, fills);
+  drain_pair<kNH>(&sc, rank, fills);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -402,7 +410,7 @@ static int geometry(const psr_ag_shape* sh, Geo& g) {
   if (g.Ms % kBM != 0 || g.Ns % kBN != 0 || g.K % 128 != 0) return PSR_ERR_UNSUPPORTED;
   if ((long long)g.P * g.M >= (1LL << 31) || (long long)g.P * g.Ns >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   g.n_mb = g.Ms / kBM;
-  g.n_nb = g.Ns / kBN;
+  g.n_nb = (g.Ns + TileT::kCols - 1) / TileT::kCols;
   // piece: >= 512 KiB of rows, a multiple of 128 rows dividing the shard
   const long long row_bytes = (long long)g.K * 2;
   int pr = 128;
@@ -485,10 +493,10 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   kp.fault = pt.fault;
   kp.update_headroom = (float)kUpdateHeadroom;
   // priors (CTA-cycles): a piece at ~50 GB/s per staging SM (no less than ~6500 cycles); a task
-  // (2*256*256*K flops) at ~60 % of an SM's dense bf16 rate
+  // (2*256*512*K flops) at ~60 % of an SM's dense bf16 rate
   const double piece_cycles = (double)g.piece_rows * g.K * 2 / 50e9 * 1.95e9;
   kp.c_s0 = (float)(piece_cycles > 6500.0 ? piece_cycles : 6500.0);
-  kp.c_p0 = (float)(2.0 * kBM * kBN * (double)g.K / (0.6 * 8192.0));
+  kp.c_p0 = (float)(2.0 * kBM * TileT::kCols * (double)g.K / (0.6 * 8192.0));
   const int hard_max = n_cta - 2;  // at least one compute pair
   int n_max = pt.n_max > 0 ? pt.n_max : n_cta / 2;
   if (n_max > hard_max) n_max = hard_max;

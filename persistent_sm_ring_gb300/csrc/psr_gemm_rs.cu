@@ -43,6 +43,7 @@ namespace psr {
 namespace rs {
 
 using namespace gemm;
+constexpr int kNH = 1;  // 256 x 256 tiles (partials reduced per tile), double-buffered accumulators
 constexpr int kTileElems = kBM * kBN;            // fp32 elements of one partial tile
 constexpr int kRoundBytes = kStageArea / 3;      // one reduce round: P partial row blocks
 constexpr int kMaxP = kRoundBytes / (kBN * 4);   // at least one 256-column fp32 row per rank
@@ -184,7 +185,7 @@ __device__ bool reduce_loads(const Params& p, Smem* sc, uint32_t smem_base, int 
   if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
   const uint32_t r0 = rounds;
   rounds += (uint32_t)n_rounds;
-  if (!wait_stages_free(p, sc, fills)) return false;
+  if (!wait_stages_free<kNH>(p, sc, fills)) return false;
   // the partials were written by other CTAs (generic proxy) and published with a release that
   // the acquire above observed; order those writes before the bulk copies
   fence_proxy_async_global();
@@ -261,7 +262,7 @@ __device__ bool epilogue(const Params& p, Smem* sc, uint8_t* epi, uint32_t rank,
   const int row0 = (int)rank * kRows + (warp % 4) * 32, col0 = ((warp - 4) / 4) * 128;
   uint8_t* rows = reinterpret_cast<uint8_t*>(tile + (size_t)row0 * kBN + col0);
   uint8_t* stage = epi + (warp - 4) * kEpiWarpBytes;
-  const bool ok = read_acc(p, sc, rank, item, [&](int cb, const uint32_t* v) {
+  const bool ok = read_acc<kNH>(p, sc, rank, item, [&](int cb, const uint32_t* v) {
     warp_store_rows<32>(stage, v, rows + cb * 256, (size_t)kBN * 4);
     warp_store_rows<32>(stage, v + 32, rows + cb * 256 + 128, (size_t)kBN * 4);
   });
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // This CTA's share of a compute task's loads.
   auto produce = [&](const Task& t, int ahead_at, auto&& ahead) {
     const Item it = item_of(g, t.arg);
-    return load_tile(p, &sc, smem_base, rank, &tm_a, it.r * g.M + it.mb * kBM + (int)rank * kRows, &tm_w,
+    return load_tile<kNH>(p, &sc, smem_base, rank, &tm_a, it.r * g.M + it.mb * kBM + (int)rank * kRows, &tm_w,
                      it.r * g.N + it.nb * kBN + (int)rank * kRows, n_k, fills, ahead_at, ahead);
   };
   if (warp == 0) {
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           t_prev = clock64();
           bool ok;
           if (t.cmd == CMD_COMPUTE) {
-            ok = produce(t, n_k > kNStage ? n_k - kNStage : 0, [&] { decide(p, &sc, next, was_reducing, true); });
+            ok = produce(t, n_k > Tile<kNH>::kNStage ? n_k - Tile<kNH>::kNStage : 0, [&] { decide(p, &sc, next, was_reducing, true); });
           } else {
             prev_tickets = t.arg1 >= 0 ? 2 : 1;
             ok = reduce_loads(p, &sc, smem_base, t.arg, rounds, fills);
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_task(&sc, k, 0);
         if (t.cmd == CMD_EXIT) break;
         if (t.cmd != CMD_COMPUTE) continue;
-        if (!mma_tile(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
+        if (!mma_tile<kNH>(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
         ++items;
       }
     }
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  drain_pair(&sc, rank, fills);
+  drain_pair<kNH>(&sc, rank, fills);
 }
 
 // ------------------------------------------------------------------------------------------------
