@@ -303,7 +303,8 @@ PSR_API int psr_ag_gemm(const psr_ag_shape* shape, const void* a, const void* w,
  *     out = sum_r A_r @ W_r^T      (fp32 partials summed in rank order, bf16 result, RNE),
  * each output tile being reduced and forwarded as soon as its partials exist.
  * On one GPU the P ranks are emulated in HBM: compute pairs (clusters of two
- * SMs) each produce one 256 x 256 fp32 partial tile of one rank with tcgen05
+ * SMs) each produce one 256 x 512 fp32 partial tile of one rank (256 x 256 for
+ * a rank's last tile when N is an odd multiple of 256) with tcgen05
  * cta_group::2 MMAs into the workspace, and the completion of an output tile's
  * P partials enqueues it; reduce CTAs (the communication role) stream the P
  * partials through shared memory with TMA bulk copies and write the owner's
@@ -321,7 +322,8 @@ typedef struct {
 /* Bytes of device workspace psr_gemm_rs needs: the control block and
  * trajectory log (the same layout as the other entries, so psr_get_stats and
  * psr_get_trajectory read it), per-tile arrival counters and the ready queue,
- * and the fp32 partial tiles ([P][M][N] fp32).  Returns 0 for an invalid shape. */
+ * and the fp32 partial tiles ([P][M][N'] fp32, N' = N rounded up to a
+ * multiple of 512).  Returns 0 for an invalid shape. */
 PSR_API size_t psr_gemm_rs_workspace_bytes(const psr_rs_shape* shape);
 
 /* GEMM + ReduceScatter.

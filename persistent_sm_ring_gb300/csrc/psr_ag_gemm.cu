@@ -40,8 +40,6 @@ namespace psr {
 namespace ag {
 
 using namespace gemm;  // the pair tile: stages, MMA issue, accumulator read-back
-constexpr int kNH = 2;  // 256 x 512 tiles
-using TileT = Tile<kNH>;
 constexpr int kCopyUnit = 32768;  // staging copy unit
 constexpr int kNCopyBuf = kStageArea / kCopyUnit;
 constexpr int kPieceMinBytes = 512 * 1024;
@@ -248,9 +246,9 @@ __device__ bool produce_tile(const Params& p, Smem* sc, uint32_t smem_base, uint
   const int n_k = g.K / kBK;
   // W rows of half h: wrow + 256h (past the rank's Ns in a half-wide tile: the next rank's rows,
   // or the tensor map's zero fill past the last one; never stored)
-  const int wrow = it.r * g.Ns + it.nb * TileT::kCols + (int)rank * kRows;
-  return load_tile<kNH>(p, sc, smem_base, rank, ma, arow, tm_w, wrow, n_k, fills,
-                        n_k > TileT::kNStage ? n_k - TileT::kNStage : 0, ahead);
+  const int wrow = it.r * g.Ns + it.nb * kCols + (int)rank * kRows;
+  return load_tile(p, sc, smem_base, rank, ma, arow, tm_w, wrow, n_k, fills,
+                        n_k > kNStage ? n_k - kNStage : 0, ahead);
 }
 
 // Epilogue warp: its 32 rows x 128 columns of each half of the tile, accumulator -> bf16 -> C_r
@@ -259,10 +257,10 @@ __device__ bool epilogue(const Params& p, Smem* sc, uint8_t* epi, uint32_t rank,
   const Geo& g = p.g;
   const int warp = threadIdx.x / 32;
   const size_t grow0 = (size_t)it.j * g.Ms + (size_t)it.mb * kBM + rank * kRows + (warp % 4) * 32;
-  const int col0 = it.nb * TileT::kCols + ((warp - 4) / 4) * 128;
+  const int col0 = it.nb * kCols + ((warp - 4) / 4) * 128;
   uint8_t* stage = epi + (warp - 4) * kEpiWarpBytes;
   uint16_t* rows = p.c + ((size_t)it.r * g.M + grow0) * g.Ns;
-  return read_acc<kNH>(p, sc, rank, item, [&](int cb, const uint32_t* v) {
+  return read_acc(p, sc, rank, item, [&](int cb, const uint32_t* v) {
     const int col = col0 + (cb / 2) * kBN + (cb % 2) * 64;
     if (col >= g.Ns) return;
     uint32_t w[32];
@@ -343,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               [&] { decide(p, &sc, next, was_staging, true); });
           } else {
             prev_pieces = t.arg1 >= 0 ? 2 : 1;
-            ok = wait_stages_free<kNH>(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg, stg_phase);
+            ok = wait_stages_free(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg, stg_phase);
           }
           if (!ok) { sc.abort = 1; break; }
         }
@@ -358,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t.cmd == CMD_COMPUTE)
             ok = produce_tile(p, &sc, smem_base, 1, item_of(p.g, t.arg), &tm_a, &tm_g, &tm_w, fills, starved, [] {});
           else if (t.arg1 >= 0)
-            ok = wait_stages_free<kNH>(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg1, stg_phase);
+            ok = wait_stages_free(p, &sc, fills) && run_staging(p, &sc, smem_base, t.arg1, stg_phase);
           if (!ok) { sc.abort = 1; break; }
         }
       }
@@ -373,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_task(&sc, k, 0);
         if (t.cmd == CMD_EXIT) break;
         if (t.cmd != CMD_COMPUTE) continue;
-        if (!mma_tile<kNH>(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
+        if (!mma_tile(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
         ++items;
       }
     }
@@ -391,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++items;
     }
   }
-  drain_pair<kNH>(&sc, rank, fills);
+  drain_pair(&sc, rank, fills);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -410,7 +408,7 @@ static int geometry(const psr_ag_shape* sh, Geo& g) {
   if (g.Ms % kBM != 0 || g.Ns % kBN != 0 || g.K % 128 != 0) return PSR_ERR_UNSUPPORTED;
   if ((long long)g.P * g.M >= (1LL << 31) || (long long)g.P * g.Ns >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   g.n_mb = g.Ms / kBM;
-  g.n_nb = (g.Ns + TileT::kCols - 1) / TileT::kCols;
+  g.n_nb = (g.Ns + kCols - 1) / kCols;
   // piece: >= 512 KiB of rows, a multiple of 128 rows dividing the shard
   const long long row_bytes = (long long)g.K * 2;
   int pr = 128;
@@ -496,7 +494,7 @@ int psr_ag_gemm(const psr_ag_shape* sh, const void* a, const void* w, void* c, v
   // (2*256*512*K flops) at ~60 % of an SM's dense bf16 rate
   const double piece_cycles = (double)g.piece_rows * g.K * 2 / 50e9 * 1.95e9;
   kp.c_s0 = (float)(piece_cycles > 6500.0 ? piece_cycles : 6500.0);
-  kp.c_p0 = (float)(2.0 * kBM * TileT::kCols * (double)g.K / (0.6 * 8192.0));
+  kp.c_p0 = (float)(2.0 * kBM * kCols * (double)g.K / (0.6 * 8192.0));
   const int hard_max = n_cta - 2;  // at least one compute pair
   int n_max = pt.n_max > 0 ? pt.n_max : n_cta / 2;
   if (n_max > hard_max) n_max = hard_max;

@@ -10,18 +10,22 @@
 // in HBM:
 //
 //  * the CTAs work in pairs (clusters of two); a pair takes either role;
-//  * a compute pair produces one 256 x 256 partial tile of one rank per task (the pair tile of
-//    psr_gemm_tile.cuh: each CTA 128 rows, tcgen05 cta_group::2, double-buffered accumulators)
-//    and writes it in fp32 to that rank's partial buffer; the epilogue warp that completes the
-//    last of an output tile's P partials enqueues the tile for reduction (a gpu-scope release,
-//    like the ring's readiness flags);
+//  * a compute pair produces one 256 x 512 partial tile of one rank per task (the pair tile of
+//    psr_gemm_tile.cuh with two accumulator halves: each CTA 128 rows x 512 columns, tcgen05
+//    cta_group::2) and writes it in fp32 to that rank's partial buffer as two 256 x 256 halves;
+//    when N is an odd multiple of 256 a rank's last tile is half wide (its second half is
+//    computed and not stored); the epilogue warp that completes the last of an output tile's
+//    P partials enqueues the tile for reduction (a gpu-scope release, like the ring's
+//    readiness flags);
 //  * each CTA of a reduce pair (the communication role) takes enqueued tiles, streams the P
-//    partials through shared memory with TMA bulk copies, sums them in rank order (fixed, so
-//    the result does not depend on timing) and writes the owner's bf16 rows;
-//  * compute tasks run window by window (up to 16 x 16 output tiles, every rank's partials of
+//    partials through shared memory with TMA bulk copies (a round carries a block of rows of one
+//    half from every rank), sums them in rank order (fixed, so the result does not depend on
+//    timing) and writes the owner's bf16 rows;
+//  * compute tasks run window by window (up to 16 x 8 output tiles, every rank's partials of
 //    the window before the next window), so reductions start one window after the launch, and a
-//    rank's A and W blocks of the window (16 + 16 of them) are read from HBM about once per
-//    window (8 x 8 windows read them twice as often: 6.1 GB of DRAM reads per launch against 4.6);
+//    rank's A and W blocks of the window are read from HBM about once per window (with
+//    256 x 256 tiles, windows of 8 x 8 instead of 16 x 16 read them twice as often: 6.1 GB of
+//    DRAM reads per launch against 4.6);
 //  * the shared controller splits the pairs between the roles with the pages' rule (a target of
 //    n reduce CTAs gives ceil(n/2) reduce pairs).  Compute feeds
 //    communication here, so the launch starts with no reduce CTA (pwwt.cn §2.4: the data
@@ -43,8 +47,7 @@ namespace psr {
 namespace rs {
 
 using namespace gemm;
-constexpr int kNH = 1;  // 256 x 256 tiles (partials reduced per tile), double-buffered accumulators
-constexpr int kTileElems = kBM * kBN;            // fp32 elements of one partial tile
+constexpr int kTileElems = kBM * kBN;            // fp32 elements of one half (256 x 256) of a partial tile
 constexpr int kRoundBytes = kStageArea / 3;      // one reduce round: P partial row blocks
 constexpr int kMaxP = kRoundBytes / (kBN * 4);   // at least one 256-column fp32 row per rank
 static_assert(kRoundBytes % 1024 == 0, "reduce round");
@@ -53,7 +56,7 @@ enum : uint32_t { SITE_FLAG = 1, SITE_REDUCE_LOAD = 8, SITE_REDUCE_FREE = 9, SIT
 
 struct Geo {
   int M, N, Ks, P, Mq;
-  int n_mb, n_nb;       // 256-row / 256-column output blocks
+  int n_mb, n_nb;       // 256-row / 512-column output blocks (the last one half wide when N % 512 = 256)
   int wm, wn;           // task window: wm x wn output tiles
   int n_out;            // output tiles
   long long n_items;    // compute tasks: P x n_out
@@ -62,7 +65,7 @@ struct Geo {
 
 struct Params {
   Geo g;
-  float* part;          // [P][n_out][256][256] fp32 partial tiles
+  float* part;          // [P][n_out][2][256][256] fp32 partial tiles (two halves each)
   uint16_t* out;        // [M][N] bf16
   uint32_t* count;      // [n_out] epilogue-warp arrivals (8 per partial tile)
   uint32_t* queue;      // [n_out] tiles ready for reduction (+1), in completion order
@@ -76,6 +79,11 @@ struct Params {
   float c_s0, c_p0;
   float update_headroom;
 };
+
+// 256-column halves of output tile column nb: 2, or 1 for a half-wide last tile
+__device__ __host__ inline int halves_of(const Geo& g, int nb) {
+  return (nb == g.n_nb - 1 && g.N % kCols != 0) ? 1 : 2;
+}
 
 // compute task index -> (rank, m-block, n-block): window by window, rank by rank inside a
 // window, W tile by W tile inside a rank (consecutive tasks share it)
@@ -167,8 +175,9 @@ __device__ void decide(const Params& p, Smem* sc, Task& t, bool& was_reducing, b
 // ------------------------------------------------------------------------------------------------
 // Reduce task (one CTA): output tile o = sum over ranks of its partial tiles, rounded to bf16
 // ------------------------------------------------------------------------------------------------
-// Round k of the task carries rows k*cr .. k*cr+cr-1 of every rank's partial (P bulk copies of
-// cr KiB into one third of the stage area); thread 0 issues the copies, the eight epilogue warps
+// Round k of the task carries rows kr*cr .. kr*cr+cr-1 of half h of every rank's partial
+// (h = k / (256/cr), kr = k % (256/cr); P bulk copies of cr KiB into one third of the stage area;
+// a half-wide tile has rounds of half 0 only); thread 0 issues the copies, the eight epilogue warps
 // sum and store.  Three rounds are in flight; stg[s] counts a round's bytes, stg[3 + s] the
 // eight consumer warps that have read it.  `rounds` is the CTA's lifetime round count, kept by
 // both sides.  `h` is the ticket's queue position (its entry is already published: the
@@ -180,12 +189,13 @@ __device__ void decide(const Params& p, Smem* sc, Task& t, bool& was_reducing, b
 __device__ bool reduce_loads(const Params& p, Smem* sc, uint32_t smem_base, int h, uint32_t& rounds, uint32_t fills) {
   const Geo& g = p.g;
   const int o = (int)ld_acquire(p.queue + h) - 1;
-  const int n_rounds = kBM / g.cr;
+  const int rb = kBM / g.cr;  // row blocks per half
+  const int n_rounds = halves_of(g, o % g.n_nb) * rb;
   const uint32_t rank_bytes = (uint32_t)g.cr * kBN * 4;
   if (p.fault == PSR_FAULT_SLOW_STAGING) nanosleep_ns(20000);
   const uint32_t r0 = rounds;
   rounds += (uint32_t)n_rounds;
-  if (!wait_stages_free<kNH>(p, sc, fills)) return false;
+  if (!wait_stages_free(p, sc, fills)) return false;
   // the partials were written by other CTAs (generic proxy) and published with a release that
   // the acquire above observed; order those writes before the bulk copies
   fence_proxy_async_global();
@@ -198,7 +208,8 @@ __device__ bool reduce_loads(const Params& p, Smem* sc, uint32_t smem_base, int 
     }
     mbar_expect_tx(&sc->stg[s], rank_bytes * (uint32_t)g.P);
     for (int r = 0; r < g.P; ++r) {
-      const float* src = p.part + ((size_t)r * g.n_out + o) * kTileElems + (size_t)k * g.cr * kBN;
+      const float* src =
+          p.part + (((size_t)r * g.n_out + o) * 2 + k / rb) * kTileElems + (size_t)(k % rb) * g.cr * kBN;
       bulk_load(smem_base + s * kRoundBytes + (uint32_t)r * rank_bytes, src, rank_bytes, &sc->stg[s]);
     }
   }
@@ -216,7 +227,8 @@ __device__ bool reduce_sums(const Params& p, Smem* sc, const uint8_t* smem, int 
   const int lane = threadIdx.x % 32;
   const int o = (int)ld_acquire(p.queue + h) - 1;
   const int mb = o / g.n_nb, nb = o % g.n_nb;
-  const int n_rounds = kBM / g.cr;
+  const int rb = kBM / g.cr;  // row blocks per half
+  const int n_rounds = halves_of(g, nb) * rb;
   const int t = threadIdx.x - 128;            // 0..255
   const int per_round = g.cr * (kBN / 4);     // float4 elements of one rank's rows in a round
   bool ok = true;
@@ -235,11 +247,12 @@ __device__ bool reduce_sums(const Params& p, Smem* sc, const uint8_t* smem, int 
           acc.z += x.z;
           acc.w += x.w;
         }
-        const int row = k * g.cr + e / (kBN / 4), col = (e % (kBN / 4)) * 4;
+        const int row = (k % rb) * g.cr + e / (kBN / 4);
+        const int col = nb * kCols + (k / rb) * kBN + (e % (kBN / 4)) * 4;
         uint2 v;
         v.x = pack_bf16x2(acc.x, acc.y);
         v.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(p.out + (size_t)(mb * kBM + row) * g.N + (size_t)nb * kBN + col) = v;
+        *reinterpret_cast<uint2*>(p.out + (size_t)(mb * kBM + row) * g.N + col) = v;
       }
     }
     __syncwarp();
@@ -253,18 +266,22 @@ __device__ bool reduce_sums(const Params& p, Smem* sc, const uint8_t* smem, int 
 // ------------------------------------------------------------------------------------------------
 // Compute task epilogue (each epilogue warp of both CTAs) -> fp32 partial tile
 // ------------------------------------------------------------------------------------------------
-// The warp's 32 rows x 128 columns of the partial tile; then its arrival on the tile's count
-// (16 warps per partial), and the last arrival of the output tile's P partials enqueues it.
+// The warp's 32 rows x 128 columns of each stored half of the partial tile; then its arrival on
+// the tile's count (16 warps per partial), and the last arrival of the output tile's P partials
+// enqueues it.
 __device__ bool epilogue(const Params& p, Smem* sc, uint8_t* epi, uint32_t rank, const Item& it, uint32_t item) {
   const Geo& g = p.g;
   const int warp = threadIdx.x / 32;
-  float* tile = p.part + ((size_t)it.r * g.n_out + it.o) * kTileElems;
+  float* tile = p.part + ((size_t)it.r * g.n_out + it.o) * 2 * kTileElems;
   const int row0 = (int)rank * kRows + (warp % 4) * 32, col0 = ((warp - 4) / 4) * 128;
-  uint8_t* rows = reinterpret_cast<uint8_t*>(tile + (size_t)row0 * kBN + col0);
+  const int halves = halves_of(g, it.nb);
   uint8_t* stage = epi + (warp - 4) * kEpiWarpBytes;
-  const bool ok = read_acc<kNH>(p, sc, rank, item, [&](int cb, const uint32_t* v) {
-    warp_store_rows<32>(stage, v, rows + cb * 256, (size_t)kBN * 4);
-    warp_store_rows<32>(stage, v + 32, rows + cb * 256 + 128, (size_t)kBN * 4);
+  const bool ok = read_acc(p, sc, rank, item, [&](int cb, const uint32_t* v) {
+    if (cb / 2 >= halves) return;
+    uint8_t* rows =
+        reinterpret_cast<uint8_t*>(tile + (size_t)(cb / 2) * kTileElems + (size_t)row0 * kBN + col0 + (cb % 2) * 64);
+    warp_store_rows<32>(stage, v, rows, (size_t)kBN * 4);
+    warp_store_rows<32>(stage, v + 32, rows + 128, (size_t)kBN * 4);
   });
   if (!ok) return false;
   // this warp's rows are written: publish them (each thread's stores before lane 0's release)
@@ -322,8 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // This CTA's share of a compute task's loads.
   auto produce = [&](const Task& t, int ahead_at, auto&& ahead) {
     const Item it = item_of(g, t.arg);
-    return load_tile<kNH>(p, &sc, smem_base, rank, &tm_a, it.r * g.M + it.mb * kBM + (int)rank * kRows, &tm_w,
-                     it.r * g.N + it.nb * kBN + (int)rank * kRows, n_k, fills, ahead_at, ahead);
+    // W rows of half h: + 256h (past N in a half-wide tile: the next rank's rows, or the
+    // tensor map's zero fill past the last one; never stored)
+    return load_tile(p, &sc, smem_base, rank, &tm_a, it.r * g.M + it.mb * kBM + (int)rank * kRows, &tm_w,
+                          it.r * g.N + it.nb * kCols + (int)rank * kRows, n_k, fills, ahead_at, ahead);
   };
   if (warp == 0) {
     if (lane == 0) {
@@ -357,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           t_prev = clock64();
           bool ok;
           if (t.cmd == CMD_COMPUTE) {
-            ok = produce(t, n_k > Tile<kNH>::kNStage ? n_k - Tile<kNH>::kNStage : 0, [&] { decide(p, &sc, next, was_reducing, true); });
+            ok = produce(t, n_k > kNStage ? n_k - kNStage : 0, [&] { decide(p, &sc, next, was_reducing, true); });
           } else {
             prev_tickets = t.arg1 >= 0 ? 2 : 1;
             ok = reduce_loads(p, &sc, smem_base, t.arg, rounds, fills);
@@ -388,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_task(&sc, k, 0);
         if (t.cmd == CMD_EXIT) break;
         if (t.cmd != CMD_COMPUTE) continue;
-        if (!mma_tile<kNH>(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
+        if (!mma_tile(p, &sc, smem_base, n_k, mfills, items)) { sc.abort = 1; break; }
         ++items;
       }
     }
@@ -419,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  drain_pair<kNH>(&sc, rank, fills);
+  drain_pair(&sc, rank, fills);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -444,9 +463,9 @@ static int geometry(const psr_rs_shape* sh, Geo& g) {
   if (g.Mq % kBM != 0 || g.N % kBN != 0 || g.Ks % kBK != 0 || g.P > kMaxP) return PSR_ERR_UNSUPPORTED;
   if ((long long)g.P * g.M >= (1LL << 31) || (long long)g.P * g.N >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   g.n_mb = g.M / kBM;
-  g.n_nb = g.N / kBN;
+  g.n_nb = (g.N + kCols - 1) / kCols;
   g.wm = largest_divisor_upto(g.n_mb, 16);
-  g.wn = largest_divisor_upto(g.n_nb, 16);
+  g.wn = largest_divisor_upto(g.n_nb, 8);
   const long long n_out = (long long)g.n_mb * g.n_nb;
   if (n_out >= (1LL << 30) || n_out * g.P >= (1LL << 31)) return PSR_ERR_UNSUPPORTED;
   g.n_out = (int)n_out;
@@ -467,7 +486,7 @@ static Layout layout(const Geo& g) {
   l.count = off; off = au(off + (size_t)g.n_out * 4);
   l.queue = off; off = au(off + (size_t)g.n_out * 4);
   l.reset_bytes = off;
-  l.part = off; off = au(off + (size_t)g.P * g.n_out * kTileElems * 4);
+  l.part = off; off = au(off + (size_t)g.P * g.n_out * 2 * kTileElems * 4);
   l.total = off;
   return l;
 }
@@ -526,9 +545,9 @@ int psr_gemm_rs(const psr_rs_shape* sh, const void* a, const void* w, void* out,
   kp.fault = pt.fault;
   kp.update_headroom = (float)kUpdateHeadroom;
   // priors (CTA-cycles): a reduction streams P partial tiles in and one bf16 tile out at
-  // ~100 GB/s per SM; a compute task (2*256*256*Ks flops) at ~60 % of an SM's dense bf16 rate
-  kp.c_s0 = (float)(((double)g.P * kTileElems * 4 + kTileElems * 2) / 100e9 * 1.95e9);
-  kp.c_p0 = (float)(2.0 * kBM * kBN * (double)g.Ks / (0.6 * 8192.0));
+  // ~100 GB/s per SM; a compute task (2*256*512*Ks flops) at ~60 % of an SM's dense bf16 rate
+  kp.c_s0 = (float)(((double)g.P * 2 * kTileElems * 4 + 2 * kTileElems * 2) / 100e9 * 1.95e9);
+  kp.c_p0 = (float)(2.0 * kBM * kCols * (double)g.Ks / (0.6 * 8192.0));
   const int hard_max = n_cta - 2;  // at least one compute pair
   int n_max = pt.n_max > 0 ? pt.n_max : n_cta / 2;
   if (n_max > hard_max) n_max = hard_max;

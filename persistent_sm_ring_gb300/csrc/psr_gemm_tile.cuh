@@ -1,19 +1,18 @@
-// The output tile of the persistent GEMM kernels (AllGather+GEMM and GEMM+ReduceScatter) on
-// sm_103a, computed by a pair of CTAs (a cluster of two SMs): 256 rows and NH halves of 256
-// columns (NH = 1 or 2, a template parameter).
+// The 256 x 512 output tile of the persistent GEMM kernels (AllGather+GEMM and
+// GEMM+ReduceScatter) on sm_103a, computed by a pair of CTAs (a cluster of two SMs) as two
+// halves of 256 columns.
 //
-//  * each CTA of the pair loads 128 of the tile's A rows and, per half, 128 of its W rows
+//  * each CTA of the pair loads 128 of the tile's A rows and, per half h, 128 of its W rows
 //    (output columns 256*h + 128*rank ..), one 64-wide K step per stage, K-major with the
-//    128-byte swizzle, into a ring of stages in 192 KiB; both CTAs' TMA loads are counted on
+//    128-byte swizzle, into a ring of four 48 KiB stages; both CTAs' TMA loads are counted on
 //    the even CTA's stage barrier;
 //  * one thread of the even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16)
-//    per half: each SM accumulates its 128 rows x 256 columns per half in fp32 tensor memory.
-//    NH = 1: two accumulator buffers (2 x 256 columns), so that a tile's epilogue runs while
-//    the next tile accumulates into the other buffer.  NH = 2: the two halves fill the 512
-//    columns, and each half is released as soon as the epilogue warps hold it in registers;
-//    the tile moves 48 KiB per SM and K step for twice the products of the 32 KiB step of
-//    NH = 1 (a measured SM lands ~56 B/clk of tile loads, short of the 64 B/clk that NH = 1
-//    needs at the tensor rate);
+//    per half: each SM accumulates its 128 rows x 256 columns per half in fp32 tensor memory,
+//    the two halves filling its 512 columns; each half is released as soon as the epilogue
+//    warps hold it in registers, and the next tile's first products into it wait only for
+//    that.  The tile moves 48 KiB per SM and K step, 48 B/clk at the tensor rate: a 256 x 256
+//    tile (double-buffered accumulators) needs 64 B/clk, above the ~56 B/clk of TMA tile loads
+//    that a GB300 SM was measured to land;
 //  * the even CTA's scheduling thread hands tasks to the roles of both CTAs through a ring of
 //    task slots in shared memory (the odd CTA's copy written with distributed stores), each
 //    slot released by an mbarrier: no role waits for another at a task boundary;
@@ -37,21 +36,15 @@ namespace psr {
 namespace gemm {
 
 constexpr int kBM = 256;    // output rows per tile (128 per CTA of the pair)
-constexpr int kBN = 256;    // output columns per accumulator half (W rows; 128 loaded by each CTA)
+constexpr int kBN = 256;    // output columns per half (W rows; 128 loaded by each CTA)
+constexpr int kHalves = 2;
+constexpr int kCols = kHalves * kBN;  // output columns per tile
 constexpr int kBK = 64;     // K per stage (one 128-byte swizzle atom of bf16)
 constexpr int kRows = 128;  // A rows, and W rows per half, one CTA loads per tile
-constexpr int kHalf = kRows * kBK * 2;  // 16 KiB
-constexpr int kStageArea = 196608;      // 192 KiB of stages; also the scratch of the comm roles
-constexpr int kMaxStages = 6;
-// NH halves of kBN columns per tile
-template <int NH>
-struct Tile {
-  static_assert(NH == 1 || NH == 2, "one or two accumulator halves");
-  static constexpr int kCols = NH * kBN;                        // output columns per tile
-  static constexpr int kStageBytes = (1 + NH) * kHalf;          // this CTA's A and W rows of one K step
-  static constexpr int kNStage = kStageArea / kStageBytes;      // 6 (NH = 1) or 4 (NH = 2)
-  static_assert(kNStage * kStageBytes == kStageArea && kNStage <= kMaxStages, "stages");
-};
+constexpr int kHalf = kRows * kBK * 2;                  // 16 KiB
+constexpr int kStageBytes = (1 + kHalves) * kHalf;      // this CTA's A rows and W rows of one K step
+constexpr int kNStage = 4;
+constexpr int kStageArea = kNStage * kStageBytes;       // 192 KiB; also the scratch of the comm roles
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarpBytes = 4096;  // one warp's store staging: 32 rows x 128 bytes
 constexpr int kEpiArea = kEpiWarps * kEpiWarpBytes;
@@ -76,8 +69,8 @@ struct Task {
 
 // Shared control state of one CTA.
 struct Smem {
-  uint64_t full[kMaxStages], empty[kMaxStages];  // stage loaded (both CTAs' bytes; even CTA) / read by the MMAs
-  uint64_t acc_full[2], acc_empty[2];  // accumulator buffer (NH = 1) or half (NH = 2) complete / read back (even CTA)
+  uint64_t full[kNStage], empty[kNStage];  // stage loaded (both CTAs' bytes; even CTA) / read by the MMAs
+  uint64_t acc_full[kHalves], acc_empty[kHalves];  // accumulator half complete / read back (even CTA)
   uint64_t task_full[kSlots], task_empty[kSlots];  // task slot written / read by every reader (even CTA)
   uint64_t stg[16];                        // the communication role's buffers (kernel-specific)
   uint64_t drain;
@@ -89,11 +82,11 @@ struct Smem {
 
 // Thread 0 of each CTA: the pipeline's barriers (the kernel initialises stg[] itself).
 __device__ __forceinline__ void init_barriers(Smem* sc) {
-  for (int s = 0; s < kMaxStages; ++s) {
+  for (int s = 0; s < kNStage; ++s) {
     mbar_init(&sc->full[s], 1);
     mbar_init(&sc->empty[s], 1);
   }
-  for (int b = 0; b < 2; ++b) {
+  for (int b = 0; b < kHalves; ++b) {
     mbar_init(&sc->acc_full[b], 1);
     mbar_init(&sc->acc_empty[b], 2 * kEpiWarps);
   }
@@ -177,21 +170,20 @@ __device__ __forceinline__ void release_task(Smem* sc, uint32_t k, uint32_t rank
 // `ahead()` runs once, after the loads of step `ahead_at` are issued (the scheduler decides its
 // next task there).  `fills` counts the stage fills this CTA has issued.  False on timeout or
 // abort.
-template <int NH, class KP, class Ahead>
+template <class KP, class Ahead>
 __device__ __forceinline__ bool load_tile(const KP& p, Smem* sc, uint32_t smem_base, uint32_t rank,
                                           const CUtensorMap* ma, int arow, const CUtensorMap* mw, int wrow, int n_k,
                                           uint32_t& fills, int ahead_at, Ahead&& ahead) {
-  using T = Tile<NH>;
   for (int ks = 0; ks < n_k; ++ks) {
     const uint32_t c = fills;
-    const uint32_t s = c % T::kNStage, use = c / T::kNStage;
+    const uint32_t s = c % kNStage, use = c / kNStage;
     if (use > 0 && !wait_bar(&sc->empty[s], (use - 1) & 1u, p, sc, SITE_EMPTY, kSlack)) return false;
-    if (rank == 0) mbar_expect_tx(&sc->full[s], 2 * T::kStageBytes);  // both CTAs' bytes
+    if (rank == 0) mbar_expect_tx(&sc->full[s], 2 * kStageBytes);  // both CTAs' bytes
     const uint32_t bar = mapa_shared(smem_u32(&sc->full[s]), 0);
-    const uint32_t base = smem_base + s * T::kStageBytes;
+    const uint32_t base = smem_base + s * kStageBytes;
     tma_load_2d_pair(base, ma, ks * kBK, arow, bar);
 #pragma unroll
-    for (int h = 0; h < NH; ++h) tma_load_2d_pair(base + (1 + h) * kHalf, mw, ks * kBK, wrow + h * kBN, bar);
+    for (int h = 0; h < kHalves; ++h) tma_load_2d_pair(base + (1 + h) * kHalf, mw, ks * kBK, wrow + h * kBN, bar);
     fills = c + 1;
     if (ks == ahead_at) ahead();
   }
@@ -200,47 +192,41 @@ __device__ __forceinline__ bool load_tile(const KP& p, Smem* sc, uint32_t smem_b
 
 // Producer, before a communication task reuses the stage area: every stage this CTA filled
 // has been read by the MMAs.  False on timeout or abort.
-template <int NH, class KP>
+template <class KP>
 __device__ __forceinline__ bool wait_stages_free(const KP& p, Smem* sc, uint32_t fills) {
-  constexpr uint32_t NS = Tile<NH>::kNStage;
-  for (uint32_t s = 0; s < NS && s < fills; ++s) {
-    const uint32_t last = s + ((fills - 1 - s) / NS) * NS;  // the stage's last fill
-    if (!wait_bar(&sc->empty[s], (last / NS) & 1u, p, sc, SITE_EMPTY, kSlack)) return false;
+  for (uint32_t s = 0; s < (uint32_t)kNStage && s < fills; ++s) {
+    const uint32_t last = s + ((fills - 1 - s) / kNStage) * kNStage;  // the stage's last fill
+    if (!wait_bar(&sc->empty[s], (last / kNStage) & 1u, p, sc, SITE_EMPTY, kSlack)) return false;
   }
   return true;
 }
 
-// MMA issuer: one tile's n_k stages.  NH = 1: into accumulator buffer (item & 1); NH = 2: into
-// both halves, each waited for (acc_empty: its previous tile read back) just before the first
-// product that overwrites it.  acc_full on both CTAs per buffer or half at the end.  `fills`
-// counts the stages consumed.  False on timeout or abort.
-template <int NH, class KP>
+// MMA issuer: one tile's n_k stages into both halves, each waited for (acc_empty: its previous
+// tile read back) just before the first product that overwrites it; acc_full on both CTAs per
+// half at the end.  `fills` counts the stages consumed.  False on timeout or abort.
+template <class KP>
 __device__ __forceinline__ bool mma_tile(const KP& p, Smem* sc, uint32_t smem_base, int n_k, uint32_t& fills,
                                          uint32_t item) {
-  using T = Tile<NH>;
   constexpr uint32_t ID = idesc_bf16_f32(2 * kRows, kBN, false);
   constexpr uint32_t kHi = sdesc_hi_sw128(1024);  // 8-row groups 1024 B apart
-  const uint32_t use = NH == 1 ? item >> 1 : item;  // earlier tiles in the same accumulator region
-  auto region = [&](int h) -> uint32_t { return NH == 1 ? (item & 1u) : (uint32_t)h; };
   auto acquire = [&](int h) -> bool {
-    if (use > 0 && !wait_bar<true>(&sc->acc_empty[region(h)], (use - 1) & 1u, p, sc, SITE_ACC_EMPTY, kSlack))
-      return false;
+    if (item > 0 && !wait_bar<true>(&sc->acc_empty[h], (item - 1) & 1u, p, sc, SITE_ACC_EMPTY, kSlack)) return false;
     tc_fence_after();
     return true;
   };
   if (!acquire(0)) return false;
   for (int ks = 0; ks < n_k; ++ks) {
     const uint32_t c = fills;
-    const uint32_t s = c % T::kNStage;
-    if (!wait_bar(&sc->full[s], (c / T::kNStage) & 1u, p, sc, SITE_FULL, kSlack)) return false;
+    const uint32_t s = c % kNStage;
+    if (!wait_bar(&sc->full[s], (c / kNStage) & 1u, p, sc, SITE_FULL, kSlack)) return false;
     tc_fence_after();
-    const uint32_t base = smem_base + s * T::kStageBytes;
+    const uint32_t base = smem_base + s * kStageBytes;
     const uint32_t a_lo = sdesc_lo(base, 16);
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
+    for (int h = 0; h < kHalves; ++h) {
       if (h > 0 && ks == 0 && !acquire(h)) return false;
       const uint32_t w_lo = sdesc_lo(base + (1 + h) * kHalf, 16);
-      const uint32_t tacc = sc->tmem_base + region(h) * kBN;
+      const uint32_t tacc = sc->tmem_base + h * kBN;
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk)
         mma_ss_cg<2>(tacc, a_lo + kk * 2, kHi, w_lo + kk * 2, kHi, ID, (ks > 0 || kk > 0) ? 1u : 0u);
@@ -249,28 +235,25 @@ __device__ __forceinline__ bool mma_tile(const KP& p, Smem* sc, uint32_t smem_ba
     fills = c + 1;
   }
 #pragma unroll
-  for (int h = 0; h < NH; ++h) mma_commit_cg<2>(&sc->acc_full[region(h)], 3);
+  for (int h = 0; h < kHalves; ++h) mma_commit_cg<2>(&sc->acc_full[h], 3);
   return true;
 }
 
-// Epilogue warp: for each accumulator region of the tile (NH = 1: buffer item & 1; NH = 2: half
-// 0, then half 1) it waits for the region, reads this warp's 32 rows x 128 columns as two
-// 64-column blocks, releases the region once both are in registers, and hands each block to
-// store(cb, v[64]).  Block cb covers the tile's columns 256*(cb/2) + 128*chalf + 64*(cb%2) ..
-// (chalf = (warp-4)/4); v holds raw fp32 bits; the thread's row inside the CTA's 128 is
-// 32*(warp%4) + lane.  False on timeout or abort.
-template <int NH, class KP, class Store>
+// Epilogue warp: for each half of the tile it waits for the half, reads this warp's 32 rows x 128
+// columns of it as two 64-column blocks, releases the half once both are in registers, and
+// hands each block to store(cb, v[64]).  Block cb covers the tile's columns
+// 256*(cb/2) + 128*chalf + 64*(cb%2) .. (chalf = (warp-4)/4); v holds raw fp32 bits; the thread's
+// row inside the CTA's 128 is 32*(warp%4) + lane.  False on timeout or abort.
+template <class KP, class Store>
 __device__ __forceinline__ bool read_acc(const KP& p, Smem* sc, uint32_t rank, uint32_t item, Store&& store) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quarter = warp % 4, chalf = (warp - 4) / 4;
-  const uint32_t use = NH == 1 ? item >> 1 : item;
 #pragma unroll 1
-  for (int h = 0; h < NH; ++h) {
-    const uint32_t b = NH == 1 ? (item & 1u) : (uint32_t)h;
-    const bool ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full[b], use & 1u, p, sc, SITE_ACC, kSlack));
+  for (int h = 0; h < kHalves; ++h) {
+    const bool ok = __all_sync(0xffffffffu, wait_bar(&sc->acc_full[h], item & 1u, p, sc, SITE_ACC, kSlack));
     if (!ok) { sc->abort = 1; return false; }
     tc_fence_after();
-    const uint32_t tacc = sc->tmem_base + ((uint32_t)(quarter * 32) << 16) + b * kBN + chalf * 128;
+    const uint32_t tacc = sc->tmem_base + ((uint32_t)(quarter * 32) << 16) + h * kBN + chalf * 128;
     uint32_t v[64];
     tmem_ld64(tacc, v);
     tmem_ld_wait();
@@ -280,8 +263,8 @@ __device__ __forceinline__ bool read_acc(const KP& p, Smem* sc, uint32_t rank, u
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-      if (rank == 0) mbar_arrive(&sc->acc_empty[b]);
-      else mbar_arrive_cluster(mapa_shared(smem_u32(&sc->acc_empty[b]), 0));
+      if (rank == 0) mbar_arrive(&sc->acc_empty[h]);
+      else mbar_arrive_cluster(mapa_shared(smem_u32(&sc->acc_empty[h]), 0));
     }
     store(2 * h + 1, v);
   }
@@ -320,9 +303,7 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t* 
 // may have issued different numbers of fills (at most one apart per stage), so the even CTA
 // completes each stage's last phase itself: it arms a phase only the odd CTA loaded, and
 // accounts for the odd CTA's bytes of a phase that only it loaded.
-template <int NH>
 __device__ __forceinline__ void drain_pair(Smem* sc, uint32_t rank, uint32_t fills) {
-  using T = Tile<NH>;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (warp == 1 && lane == 0 && rank == 0) {
     mma_commit_cg<2>(&sc->drain, 1);
@@ -337,11 +318,11 @@ __device__ __forceinline__ void drain_pair(Smem* sc, uint32_t rank, uint32_t fil
   if (threadIdx.x == 0 && rank == 0) {
     const uint32_t L = fills, Q = sc->peer_fills, F = L > Q ? L : Q;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t s = 0; s < (uint32_t)T::kNStage && s < F; ++s) {
-      const uint32_t m = s + ((F - 1 - s) / T::kNStage) * T::kNStage;  // the stage's last fill by either CTA
-      if (m >= L) mbar_expect_tx(&sc->full[s], T::kStageBytes);         // armed by no one: the odd CTA's bytes
-      else if (m >= Q) mbar_complete_tx(&sc->full[s], T::kStageBytes);  // the odd CTA's bytes will not come
-      while (!mbar_try_wait(&sc->full[s], (m / T::kNStage) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+    for (uint32_t s = 0; s < (uint32_t)kNStage && s < F; ++s) {
+      const uint32_t m = s + ((F - 1 - s) / kNStage) * kNStage;  // the stage's last fill by either CTA
+      if (m >= L) mbar_expect_tx(&sc->full[s], kStageBytes);         // armed by no one: the odd CTA's bytes
+      else if (m >= Q) mbar_complete_tx(&sc->full[s], kStageBytes);  // the odd CTA's bytes will not come
+      while (!mbar_try_wait(&sc->full[s], (m / kNStage) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
   }
