@@ -241,3 +241,34 @@ def test_controller_minimises_predicted_makespan(psr):
         best = 1 + int(np.argmin(span))
         assert abs(n - best) <= 1, (N, Rs, Cs, Rp, Cp, n, best)
         assert 1 <= n <= N - 1
+
+
+# ------------------------------------------------------------------------------------------------
+# GEMM workspaces: sizes and shape rules (host side only)
+# ------------------------------------------------------------------------------------------------
+
+def test_ag_gemm_workspace_holds_the_gather_buffers(psr):
+    for M, K, Ns, P in [(1024, 512, 256, 4), (2048, 1024, 512, 4), (512, 256, 256, 1), (8192, 8192, 3584, 8)]:
+        n = psr.ag_gemm_workspace_bytes(M, K, Ns, P)
+        assert P * M * K * 2 <= n < P * M * K * 2 + (1 << 20), (M, K, Ns, P, n)  # one gathered A per rank
+    for bad in [(1000, 512, 256, 4),   # M/P = 250, not a multiple of 256
+                (1024, 512, 384, 4),   # Ns not a multiple of 256
+                (1024, 500, 256, 4),   # K not a multiple of 128
+                (1024, 512, 256, 3)]:  # M not divisible by P
+        with pytest.raises(psr.PsrError):
+            psr.ag_gemm_workspace_bytes(*bad)
+
+
+def test_gemm_rs_workspace_holds_every_partial_tile(psr):
+    # the fp32 partials of 256 x 512 output tiles: [P][M][N'] with N' = N rounded up to 512 (a
+    # rank's last tile is half wide when N is an odd multiple of 256; its second half is not stored)
+    for M, N, Ks, P in [(1024, 512, 256, 4), (512, 768, 192, 1), (768, 256, 320, 3), (8192, 8192, 3584, 8)]:
+        n = psr.gemm_rs_workspace_bytes(M, N, Ks, P)
+        part = P * M * ((N + 511) // 512 * 512) * 4
+        assert part <= n < part + (1 << 20), (M, N, Ks, P, n)
+    for bad in [(1024, 300, 256, 4),       # N not a multiple of 256
+                (1024, 512, 100, 4),       # Ks not a multiple of 64
+                (65 * 256, 512, 64, 65),   # more ranks than a reduce round holds (64)
+                (1000, 512, 256, 4)]:      # M/P not a multiple of 256
+        with pytest.raises(psr.PsrError):
+            psr.gemm_rs_workspace_bytes(*bad)
