@@ -49,6 +49,8 @@ SMALL = [
     ri.AG_WORKLOADS["ag_small"].with_(name="ag_medium", M=2048, K=1024, Ns=512, P=4, seed=702),
     ri.AG_WORKLOADS["ag_small"].with_(name="ag_p1", M=512, K=256, Ns=256, P=1, seed=703),
     ri.AG_WORKLOADS["ag_small"].with_(name="ag_p8", M=2048, K=384, Ns=256, P=8, seed=704),
+    # a full-width 256 x 512 tile and a half-wide last tile in every rank
+    ri.AG_WORKLOADS["ag_small"].with_(name="ag_ns768", M=1024, K=384, Ns=768, P=2, seed=705),
 ]
 
 
