@@ -17,8 +17,8 @@
 //    task slots in shared memory (the odd CTA's copy written with distributed stores), each
 //    slot released by an mbarrier: no role waits for another at a task boundary;
 //  * eight epilogue warps per CTA read the accumulators back with tcgen05.ld (warp w: tensor
-//    memory lanes 32*(w%4) .., columns 128*((w-4)/4) ..) and hand 64-column blocks to a
-//    kernel-specific store.
+//    memory lanes 32*(w%4) .., columns 256*h + 128*((w-4)/4) .. of half h) and hand 64-column
+//    blocks to a kernel-specific store.
 // Each kernel adds its own task selection, data dependencies, communication role and epilogue
 // destination.
 #pragma once
